@@ -1,0 +1,581 @@
+/*
+ * CPU oracle for CSR neighbourhood aggregation -- TEST INFRASTRUCTURE ONLY.
+ *
+ * Only tests/, __graft_entry__.smoke() and bench.py's CPU-baseline / reference
+ * leg may load or call this library.  The CUDA library never does, and this
+ * file shares no code, header or constant table with it.
+ *
+ * Plain, slow, single-threaded definitions with fp64 accumulation.  Inputs
+ * are fp32, or bf16 given as raw 16-bit patterns (dtype 1), widened exactly.
+ * The source paper is "On efficient scaling of GNNs via IO-aware layer
+ * implementations" (cited below as "IO-aware GNN layers"); the reordering
+ * follows "A High-Throughput Solver for Marginalized Graph Kernels on GPU"
+ * (Section on reordering, RCM).
+ *
+ * Graph convention: CSR by destination -- row i lists the sources j of the
+ * edges j -> i, so N(i) = colidx[rowptr[i] .. rowptr[i+1]).
+ *
+ * Every function below is pinned by CPU tests (dense brute force, closed
+ * forms, invariants); none is "parity unpinned".
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_OK 0
+#define ORC_ERR 1
+
+static double widen(const void *p, int dtype, int64_t i) {
+    if (dtype == 0) return (double)((const float *)p)[i];
+    uint32_t u = (uint32_t)((const uint16_t *)p)[i] << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return (double)f;
+}
+
+static int32_t sel_row(const int32_t *rows, int32_t s) { return rows ? rows[s] : s; }
+
+/* ------------------------------------------------------------------ */
+/* degrees                                                             */
+/* ------------------------------------------------------------------ */
+
+/* d_in(i) = length of row i; d_out(j) = occurrences of j among all columns
+ * (self-loops included in both). */
+int orc_degrees(int32_t n_rows, int32_t n_cols, const int32_t *rowptr,
+                const int32_t *colidx, int32_t *d_in, int32_t *d_out) {
+    for (int32_t i = 0; i < n_rows; ++i) d_in[i] = rowptr[i + 1] - rowptr[i];
+    for (int32_t j = 0; j < n_cols; ++j) d_out[j] = 0;
+    for (int64_t e = 0; e < rowptr[n_rows]; ++e) {
+        int32_t j = colidx[e];
+        if (j < 0 || j >= n_cols) return ORC_ERR;
+        d_out[j]++;
+    }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------ */
+/* SpMM  (IO-aware GNN layers, Section 2.2 (i); Appendix D.4)          */
+/* ------------------------------------------------------------------ */
+
+/*
+ * Y[i,:] = sum_{e in row i} w_e * X[colidx[e], :]
+ * w_e = values[e] (or 1 when values is NULL) times the normalisation factor:
+ *   norm 0 none:  1
+ *   norm 1 left:  1 / d_in(i)
+ *   norm 2 right: 1 / d_out(j)
+ *   norm 3 both:  1 / sqrt(d_in(i) * d_out(j))     (GCN, Kipf & Welling)
+ * Rows with no edges give 0.  Only the selected rows are computed
+ * (rows == NULL: all rows, n_sel = n_rows); Y is [n_sel, F].
+ */
+int orc_spmm(int32_t n_rows, int32_t n_cols, const int32_t *rowptr,
+             const int32_t *colidx, const float *values, int norm,
+             const void *X, int dtype, int32_t F, const int32_t *rows,
+             int32_t n_sel, double *Y) {
+    int32_t *d_out = NULL;
+    if (norm == 2 || norm == 3) {
+        d_out = calloc((size_t)n_cols, sizeof(int32_t));
+        if (!d_out) return ORC_ERR;
+        for (int64_t e = 0; e < rowptr[n_rows]; ++e) d_out[colidx[e]]++;
+    }
+    for (int32_t s = 0; s < n_sel; ++s) {
+        int32_t i = sel_row(rows, s);
+        double *y = Y + (int64_t)s * F;
+        for (int32_t f = 0; f < F; ++f) y[f] = 0.0;
+        int64_t d_in = rowptr[i + 1] - rowptr[i];
+        for (int64_t e = rowptr[i]; e < rowptr[i + 1]; ++e) {
+            int32_t j = colidx[e];
+            double w = values ? (double)values[e] : 1.0;
+            if (norm == 1) w /= (double)d_in;
+            else if (norm == 2) w /= (double)d_out[j];
+            else if (norm == 3) w /= sqrt((double)d_in * (double)d_out[j]);
+            for (int32_t f = 0; f < F; ++f)
+                y[f] += w * widen(X, dtype, (int64_t)j * F + f);
+        }
+    }
+    free(d_out);
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------ */
+/* segment reductions (IO-aware GNN layers, Section 2.2 (ii); D.1)     */
+/* ------------------------------------------------------------------ */
+
+/* Order-preserving 32-bit key of an fp32 value (IO-aware GNN layers,
+ * Appendix D.1, order-preserving packing for atomic reductions): negative
+ * values have every bit inverted, non-negative values get the sign bit set,
+ * so unsigned comparison of keys orders the floats (and -0 < +0). */
+uint32_t orc_order_key(float v) {
+    uint32_t u;
+    memcpy(&u, &v, 4);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+/*
+ * op 0 sum, 1 mean (= sum / d_in(i)), 2 max.
+ * max: the neighbour value with the largest order key; among equal keys the
+ * smallest source node id wins; argmax[s,f] = that source node id.  A row
+ * with no edges gives 0 (and argmax -1).  Y is [n_sel, F].
+ */
+int orc_segment_reduce(int op, int32_t n_rows, const int32_t *rowptr,
+                       const int32_t *colidx, const void *X, int dtype,
+                       int32_t F, const int32_t *rows, int32_t n_sel, double *Y,
+                       int32_t *argmax) {
+    (void)n_rows;
+    for (int32_t s = 0; s < n_sel; ++s) {
+        int32_t i = sel_row(rows, s);
+        int64_t b = rowptr[i], e_end = rowptr[i + 1];
+        for (int32_t f = 0; f < F; ++f) {
+            double acc = 0.0;
+            int32_t best_j = -1;
+            uint32_t best_key = 0;
+            double best_v = 0.0;
+            for (int64_t e = b; e < e_end; ++e) {
+                int32_t j = colidx[e];
+                double v = widen(X, dtype, (int64_t)j * F + f);
+                if (op == 2) {
+                    uint32_t k = orc_order_key((float)v);
+                    if (best_j < 0 || k > best_key || (k == best_key && j < best_j)) {
+                        best_key = k;
+                        best_j = j;
+                        best_v = v;
+                    }
+                } else {
+                    acc += v;
+                }
+            }
+            double out;
+            if (op == 0) out = acc;
+            else if (op == 1) out = (e_end > b) ? acc / (double)(e_end - b) : 0.0;
+            else out = (best_j >= 0) ? best_v : 0.0;
+            Y[(int64_t)s * F + f] = out;
+            if (op == 2 && argmax) argmax[(int64_t)s * F + f] = best_j;
+        }
+    }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------ */
+/* attention (IO-aware GNN layers, Section 2.2 (iii); Appendix D.2)    */
+/* ------------------------------------------------------------------ */
+
+/* softmax over the logits e[0..deg) of one (row, head); writes alpha and
+ * returns logsumexp = m + ln sum exp(e - m) (natural log). */
+static double softmax_row(const double *e, int64_t deg, double *alpha) {
+    if (deg == 0) return -INFINITY;
+    double m = e[0];
+    for (int64_t k = 1; k < deg; ++k)
+        if (e[k] > m) m = e[k];
+    double s = 0.0;
+    for (int64_t k = 0; k < deg; ++k) s += exp(e[k] - m);
+    for (int64_t k = 0; k < deg; ++k) alpha[k] = exp(e[k] - m) / s;
+    return m + log(s);
+}
+
+/* row i of C = H * W (H [., F_in], W [F_in, HD] row-major), in fp64 */
+static void project_row(const void *H, int dtype, int32_t F_in, const void *W,
+                        int32_t HD, int32_t i, double *out) {
+    for (int32_t c = 0; c < HD; ++c) out[c] = 0.0;
+    for (int32_t k = 0; k < F_in; ++k) {
+        double h = widen(H, dtype, (int64_t)i * F_in + k);
+        for (int32_t c = 0; c < HD; ++c) out[c] += h * widen(W, dtype, (int64_t)k * HD + c);
+    }
+}
+
+/*
+ * GATv2 forward for the selected destination rows i, every head h:
+ *   l_i = H_i W_l,  r_j = H_j W_r        (W_r NULL: W_r = W_l)
+ *   e_ij = sum_d a[h,d] * LeakyReLU_slope(l_i[h,d] + r_j[h,d])
+ *   alpha_ij = softmax over j in N(i) of e_ij
+ *   out_i[h,:] = sum_j alpha_ij r_j[h,:],  lse[i,h] = ln sum_j exp(e_ij)
+ * Head h owns columns [h*D, (h+1)*D).  out [n_sel, heads*D], lse [n_sel,
+ * heads]; alpha (optional) [edges of the selected rows in order, heads].
+ */
+int orc_gatv2(int32_t n_rows, const int32_t *rowptr, const int32_t *colidx,
+              const void *H, int dtype, int32_t F_in, const void *W_l,
+              const void *W_r, const float *a, int32_t heads, int32_t D,
+              double slope, const int32_t *rows, int32_t n_sel, double *out,
+              double *lse, double *alpha) {
+    (void)n_rows;
+    int32_t HD = heads * D;
+    if (!W_r) W_r = W_l;
+    int64_t max_deg = 0;
+    for (int32_t s = 0; s < n_sel; ++s) {
+        int32_t i = sel_row(rows, s);
+        int64_t d = rowptr[i + 1] - rowptr[i];
+        if (d > max_deg) max_deg = d;
+    }
+    double *l = malloc(sizeof(double) * (size_t)HD);
+    double *R = malloc(sizeof(double) * (size_t)HD * (size_t)(max_deg > 0 ? max_deg : 1));
+    double *e = malloc(sizeof(double) * (size_t)(max_deg > 0 ? max_deg : 1));
+    double *al = malloc(sizeof(double) * (size_t)(max_deg > 0 ? max_deg : 1));
+    if (!l || !R || !e || !al) { free(l); free(R); free(e); free(al); return ORC_ERR; }
+    int64_t alpha_pos = 0;
+    for (int32_t s = 0; s < n_sel; ++s) {
+        int32_t i = sel_row(rows, s);
+        int64_t b = rowptr[i], deg = rowptr[i + 1] - b;
+        project_row(H, dtype, F_in, W_l, HD, i, l);
+        for (int64_t k = 0; k < deg; ++k)
+            project_row(H, dtype, F_in, W_r, HD, colidx[b + k], R + k * HD);
+        for (int32_t h = 0; h < heads; ++h) {
+            for (int64_t k = 0; k < deg; ++k) {
+                double acc = 0.0;
+                for (int32_t d = 0; d < D; ++d) {
+                    double x = l[h * D + d] + R[k * HD + h * D + d];
+                    double act = x > 0.0 ? x : slope * x;
+                    acc += (double)a[h * D + d] * act;
+                }
+                e[k] = acc;
+            }
+            double L = softmax_row(e, deg, al);
+            lse[(int64_t)s * heads + h] = L;
+            for (int32_t d = 0; d < D; ++d) {
+                double o = 0.0;
+                for (int64_t k = 0; k < deg; ++k) o += al[k] * R[k * HD + h * D + d];
+                out[(int64_t)s * HD + h * D + d] = o;
+            }
+            if (alpha)
+                for (int64_t k = 0; k < deg; ++k) alpha[(alpha_pos + k) * heads + h] = al[k];
+        }
+        alpha_pos += deg;
+    }
+    free(l); free(R); free(e); free(al);
+    return ORC_OK;
+}
+
+/*
+ * Graph Transformer attention for the selected destination rows i, every
+ * head h (query at the destination, key and value at the source):
+ *   e_ij = scale * sum_d Q[i,h,d] K[j,h,d]
+ *   out_i[h,:] = sum_j softmax_j(e_ij) V[j,h,:],  lse[i,h] = ln sum_j exp(e_ij)
+ * Q, K, V are [N, heads*D] row-major.
+ */
+int orc_gt(int32_t n_rows, const int32_t *rowptr, const int32_t *colidx,
+           const void *Q, const void *K, const void *V, int dtype, int32_t heads,
+           int32_t D, double scale, const int32_t *rows, int32_t n_sel,
+           double *out, double *lse, double *alpha) {
+    (void)n_rows;
+    int32_t HD = heads * D;
+    int64_t max_deg = 0;
+    for (int32_t s = 0; s < n_sel; ++s) {
+        int32_t i = sel_row(rows, s);
+        int64_t d = rowptr[i + 1] - rowptr[i];
+        if (d > max_deg) max_deg = d;
+    }
+    double *e = malloc(sizeof(double) * (size_t)(max_deg > 0 ? max_deg : 1));
+    double *al = malloc(sizeof(double) * (size_t)(max_deg > 0 ? max_deg : 1));
+    if (!e || !al) { free(e); free(al); return ORC_ERR; }
+    int64_t alpha_pos = 0;
+    for (int32_t s = 0; s < n_sel; ++s) {
+        int32_t i = sel_row(rows, s);
+        int64_t b = rowptr[i], deg = rowptr[i + 1] - b;
+        for (int32_t h = 0; h < heads; ++h) {
+            for (int64_t k = 0; k < deg; ++k) {
+                int32_t j = colidx[b + k];
+                double acc = 0.0;
+                for (int32_t d = 0; d < D; ++d)
+                    acc += widen(Q, dtype, (int64_t)i * HD + h * D + d) *
+                           widen(K, dtype, (int64_t)j * HD + h * D + d);
+                e[k] = scale * acc;
+            }
+            double L = softmax_row(e, deg, al);
+            lse[(int64_t)s * heads + h] = L;
+            for (int32_t d = 0; d < D; ++d) {
+                double o = 0.0;
+                for (int64_t k = 0; k < deg; ++k)
+                    o += al[k] * widen(V, dtype, (int64_t)colidx[b + k] * HD + h * D + d);
+                out[(int64_t)s * HD + h * D + d] = o;
+            }
+            if (alpha)
+                for (int64_t k = 0; k < deg; ++k) alpha[(alpha_pos + k) * heads + h] = al[k];
+        }
+        alpha_pos += deg;
+    }
+    free(e); free(al);
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------ */
+/* block-sparse tiles (IO-aware GNN layers, Appendix D.3, WSB format)  */
+/* ------------------------------------------------------------------ */
+
+static int cmp_i32(const void *a, const void *b) {
+    int32_t x = *(const int32_t *)a, y = *(const int32_t *)b;
+    return (x > y) - (x < y);
+}
+
+/*
+ * Rows are cut into windows of 16 and groups of 8 windows (128 rows).  For a
+ * group g, U_g = the sorted unique source columns of its rows; column block
+ * b holds U_g[16b .. 16b+16) (missing entries padded with column 0 and never
+ * masked in).  The tile (window w, block b) is 16x16 with a 256-bit mask,
+ * bit r*16+c set iff the edge U_g[16b+c] -> 16w+r exists (word (r*16+c)/64,
+ * bit (r*16+c)%64).  A tile is kept iff its popcount p >= 1 and
+ * (float)p / 256.0f >= threshold (fp32 comparison).  A block is listed iff at
+ * least one of its 8 tiles is kept; listed blocks keep ascending b.  Masks of
+ * tiles that are not kept are stored as zero.  Edges of tiles that are not
+ * kept form the residual CSR (same rows, ascending columns).
+ *
+ * counts[0..3] = {n_blocks, n_tiles_kept, nnz_tiles, nnz_residual}.
+ * Output arrays may be NULL (count only).  grp_blk_offset [n_groups+1],
+ * blk_cols [n_blocks*16], blk_mask [n_blocks*8*4], res_rowptr [n_rows+1],
+ * res_colidx [nnz_residual].
+ */
+int orc_blocksparse(int32_t n_rows, const int32_t *rowptr, const int32_t *colidx,
+                    float threshold, int64_t *counts, int32_t *grp_blk_offset,
+                    int32_t *blk_cols, uint64_t *blk_mask, int32_t *res_rowptr,
+                    int32_t *res_colidx) {
+    int32_t n_groups = (n_rows + 127) / 128;
+    int64_t n_blocks = 0, n_kept = 0, nnz_tiles = 0, nnz_res = 0;
+    int64_t max_ge = 0;
+    for (int32_t g = 0; g < n_groups; ++g) {
+        int32_t r0 = g * 128, r1 = r0 + 128 < n_rows ? r0 + 128 : n_rows;
+        int64_t ge = rowptr[r1] - rowptr[r0];
+        if (ge > max_ge) max_ge = ge;
+    }
+    int32_t *U = malloc(sizeof(int32_t) * (size_t)(max_ge > 0 ? max_ge : 1));
+    /* per group: masks[block][window][4] */
+    int64_t max_blocks = (max_ge + 15) / 16;
+    uint64_t *masks = malloc(sizeof(uint64_t) * (size_t)(max_blocks > 0 ? max_blocks : 1) * 32);
+    uint8_t *kept = malloc((size_t)(max_blocks > 0 ? max_blocks : 1) * 8);
+    if (!U || !masks || !kept) { free(U); free(masks); free(kept); return ORC_ERR; }
+    if (res_rowptr) res_rowptr[0] = 0;
+    if (grp_blk_offset) grp_blk_offset[0] = 0;
+    for (int32_t g = 0; g < n_groups; ++g) {
+        int32_t r0 = g * 128, r1 = r0 + 128 < n_rows ? r0 + 128 : n_rows;
+        int64_t ge = rowptr[r1] - rowptr[r0];
+        memcpy(U, colidx + rowptr[r0], sizeof(int32_t) * (size_t)ge);
+        qsort(U, (size_t)ge, sizeof(int32_t), cmp_i32);
+        int64_t nu = 0;
+        for (int64_t k = 0; k < ge; ++k)
+            if (nu == 0 || U[nu - 1] != U[k]) U[nu++] = U[k];
+        int64_t nb = (nu + 15) / 16;
+        memset(masks, 0, sizeof(uint64_t) * (size_t)nb * 32);
+        /* place every edge of the group */
+        for (int32_t i = r0; i < r1; ++i) {
+            int32_t w = (i - r0) / 16, r = (i - r0) % 16;
+            for (int64_t e = rowptr[i]; e < rowptr[i + 1]; ++e) {
+                int32_t j = colidx[e];
+                /* position of j in U (binary search) */
+                int64_t lo = 0, hi = nu - 1;
+                while (lo < hi) {
+                    int64_t mid = (lo + hi) / 2;
+                    if (U[mid] < j) lo = mid + 1; else hi = mid;
+                }
+                int64_t b = lo / 16, c = lo % 16, bit = r * 16 + c;
+                masks[(b * 8 + w) * 4 + bit / 64] |= 1ull << (bit % 64);
+            }
+        }
+        for (int64_t b = 0; b < nb; ++b) {
+            int any = 0;
+            for (int32_t w = 0; w < 8; ++w) {
+                int p = 0;
+                for (int q = 0; q < 4; ++q) p += __builtin_popcountll(masks[(b * 8 + w) * 4 + q]);
+                int k = (p >= 1) && ((float)p / 256.0f >= threshold);
+                kept[b * 8 + w] = (uint8_t)k;
+                if (k) { any = 1; n_kept++; nnz_tiles += p; }
+            }
+            if (any) {
+                if (blk_cols)
+                    for (int c = 0; c < 16; ++c)
+                        blk_cols[n_blocks * 16 + c] = (16 * b + c < nu) ? U[16 * b + c] : 0;
+                if (blk_mask)
+                    for (int32_t w = 0; w < 8; ++w)
+                        for (int q = 0; q < 4; ++q)
+                            blk_mask[(n_blocks * 8 + w) * 4 + q] =
+                                kept[b * 8 + w] ? masks[(b * 8 + w) * 4 + q] : 0;
+                n_blocks++;
+            }
+        }
+        if (grp_blk_offset) grp_blk_offset[g + 1] = (int32_t)n_blocks;
+        /* residual edges, in row order then ascending column */
+        for (int32_t i = r0; i < r1; ++i) {
+            int32_t w = (i - r0) / 16;
+            for (int64_t e = rowptr[i]; e < rowptr[i + 1]; ++e) {
+                int32_t j = colidx[e];
+                int64_t lo = 0, hi = nu - 1;
+                while (lo < hi) {
+                    int64_t mid = (lo + hi) / 2;
+                    if (U[mid] < j) lo = mid + 1; else hi = mid;
+                }
+                if (!kept[(lo / 16) * 8 + w]) {
+                    if (res_colidx) res_colidx[nnz_res] = j;
+                    nnz_res++;
+                }
+            }
+            if (res_rowptr) res_rowptr[i + 1] = (int32_t)nnz_res;
+        }
+    }
+    counts[0] = n_blocks;
+    counts[1] = n_kept;
+    counts[2] = nnz_tiles;
+    counts[3] = nnz_res;
+    free(U); free(masks); free(kept);
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------ */
+/* vertex orderings                                                    */
+/* ------------------------------------------------------------------ */
+
+/* SplitMix64 (Steele, Lea, Flood 2014): one step of the generator started
+ * from state x. */
+uint64_t orc_splitmix64(uint64_t x) {
+    uint64_t z = x + 0x9E3779B97F4A7C15ull;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+typedef struct { uint64_t k; int32_t id; } key_id;
+
+static int cmp_key_id(const void *a, const void *b) {
+    const key_id *x = a, *y = b;
+    if (x->k != y->k) return x->k < y->k ? -1 : 1;
+    return (x->id > y->id) - (x->id < y->id);
+}
+
+/* perm[new] = old.  Random order: ascending (splitmix64(seed ^ id), id). */
+int orc_perm_random(int32_t n, uint64_t seed, int32_t *perm) {
+    key_id *v = malloc(sizeof(key_id) * (size_t)(n > 0 ? n : 1));
+    if (!v) return ORC_ERR;
+    for (int32_t i = 0; i < n; ++i) { v[i].k = orc_splitmix64(seed ^ (uint64_t)i); v[i].id = i; }
+    qsort(v, (size_t)n, sizeof(key_id), cmp_key_id);
+    for (int32_t i = 0; i < n; ++i) perm[i] = v[i].id;
+    free(v);
+    return ORC_OK;
+}
+
+/* Degree order: descending total degree d_in + d_out (as stored, self-loops
+ * included), ties by ascending id. */
+int orc_perm_degree(int32_t n, const int32_t *rowptr, const int32_t *colidx,
+                    int32_t *perm) {
+    int64_t *deg = calloc((size_t)(n > 0 ? n : 1), sizeof(int64_t));
+    key_id *v = malloc(sizeof(key_id) * (size_t)(n > 0 ? n : 1));
+    if (!deg || !v) { free(deg); free(v); return ORC_ERR; }
+    for (int32_t i = 0; i < n; ++i) deg[i] += rowptr[i + 1] - rowptr[i];
+    for (int64_t e = 0; e < rowptr[n]; ++e) deg[colidx[e]]++;
+    for (int32_t i = 0; i < n; ++i) { v[i].k = (uint64_t)(INT64_MAX - deg[i]); v[i].id = i; }
+    qsort(v, (size_t)n, sizeof(key_id), cmp_key_id);
+    for (int32_t i = 0; i < n; ++i) perm[i] = v[i].id;
+    free(deg); free(v);
+    return ORC_OK;
+}
+
+/* symmetric adjacency S = (A + A^T) without self-loops, deduplicated */
+static int symmetrize(int32_t n, const int32_t *rowptr, const int32_t *colidx,
+                      int64_t **sp_out, int32_t **sc_out) {
+    int64_t m = rowptr[n];
+    int64_t *cnt = calloc((size_t)n + 1, sizeof(int64_t));
+    if (!cnt) return ORC_ERR;
+    for (int32_t i = 0; i < n; ++i)
+        for (int64_t e = rowptr[i]; e < rowptr[i + 1]; ++e)
+            if (colidx[e] != i) { cnt[i + 1]++; cnt[colidx[e] + 1]++; }
+    for (int32_t i = 0; i < n; ++i) cnt[i + 1] += cnt[i];
+    int32_t *adj = malloc(sizeof(int32_t) * (size_t)(cnt[n] > 0 ? cnt[n] : 1));
+    int64_t *pos = malloc(sizeof(int64_t) * (size_t)(n > 0 ? n : 1));
+    if (!adj || !pos) { free(cnt); free(adj); free(pos); return ORC_ERR; }
+    (void)m;
+    for (int32_t i = 0; i < n; ++i) pos[i] = cnt[i];
+    for (int32_t i = 0; i < n; ++i)
+        for (int64_t e = rowptr[i]; e < rowptr[i + 1]; ++e) {
+            int32_t j = colidx[e];
+            if (j == i) continue;
+            adj[pos[i]++] = j;
+            adj[pos[j]++] = i;
+        }
+    /* sort + dedupe each list, compacting */
+    int64_t w = 0;
+    int64_t prev_start = 0;
+    for (int32_t i = 0; i < n; ++i) {
+        int64_t b = cnt[i], e = cnt[i + 1];
+        qsort(adj + b, (size_t)(e - b), sizeof(int32_t), cmp_i32);
+        int64_t start = w;
+        for (int64_t k = b; k < e; ++k)
+            if (w == start || adj[w - 1] != adj[k]) adj[w++] = adj[k];
+        cnt[i] = prev_start;
+        prev_start = w;
+        (void)start;
+    }
+    cnt[n] = w;
+    /* cnt[i] now holds the compacted start of list i */
+    free(pos);
+    *sp_out = cnt;
+    *sc_out = adj;
+    return ORC_OK;
+}
+
+static int32_t *g_sdeg; /* degree table used by the comparators below */
+
+static int cmp_deg_id(const void *a, const void *b) {
+    int32_t x = *(const int32_t *)a, y = *(const int32_t *)b;
+    if (g_sdeg[x] != g_sdeg[y]) return g_sdeg[x] < g_sdeg[y] ? -1 : 1;
+    return (x > y) - (x < y);
+}
+
+/*
+ * Reverse Cuthill-McKee on S = A + A^T (self-loops dropped).  Each connected
+ * component starts at the unvisited node of smallest degree (lowest id on
+ * ties); breadth-first, each dequeued node appends its unvisited neighbours
+ * in ascending (degree, id) order; the final sequence is reversed.
+ * perm[new] = old.
+ */
+int orc_perm_rcm(int32_t n, const int32_t *rowptr, const int32_t *colidx,
+                 int32_t *perm) {
+    int64_t *sp;
+    int32_t *sc;
+    if (symmetrize(n, rowptr, colidx, &sp, &sc) != ORC_OK) return ORC_ERR;
+    int32_t *deg = malloc(sizeof(int32_t) * (size_t)(n > 0 ? n : 1));
+    int32_t *by_deg = malloc(sizeof(int32_t) * (size_t)(n > 0 ? n : 1));
+    int32_t *order = malloc(sizeof(int32_t) * (size_t)(n > 0 ? n : 1));
+    int32_t *tmp = malloc(sizeof(int32_t) * (size_t)(n > 0 ? n : 1));
+    uint8_t *vis = calloc((size_t)(n > 0 ? n : 1), 1);
+    if (!deg || !by_deg || !order || !tmp || !vis) {
+        free(sp); free(sc); free(deg); free(by_deg); free(order); free(tmp); free(vis);
+        return ORC_ERR;
+    }
+    for (int32_t i = 0; i < n; ++i) { deg[i] = (int32_t)(sp[i + 1] - sp[i]); by_deg[i] = i; }
+    g_sdeg = deg;
+    qsort(by_deg, (size_t)n, sizeof(int32_t), cmp_deg_id);
+    int32_t len = 0, scan = 0;
+    while (len < n) {
+        while (vis[by_deg[scan]]) ++scan;
+        int32_t start = by_deg[scan];
+        vis[start] = 1;
+        order[len++] = start;
+        for (int32_t head = len - 1; head < len; ++head) {
+            int32_t u = order[head];
+            int32_t t = 0;
+            for (int64_t k = sp[u]; k < sp[u + 1]; ++k)
+                if (!vis[sc[k]]) { vis[sc[k]] = 1; tmp[t++] = sc[k]; }
+            qsort(tmp, (size_t)t, sizeof(int32_t), cmp_deg_id);
+            for (int32_t k = 0; k < t; ++k) order[len++] = tmp[k];
+        }
+    }
+    for (int32_t k = 0; k < n; ++k) perm[k] = order[n - 1 - k];
+    free(sp); free(sc); free(deg); free(by_deg); free(order); free(tmp); free(vis);
+    return ORC_OK;
+}
+
+/*
+ * Relabel a square CSR by perm (perm[new] = old, inv[old] = new): new row r
+ * is old row perm[r] with every column c replaced by inv[c], columns
+ * re-sorted ascending.  Feature rows follow as X_new[r] = X[perm[r]].
+ */
+int orc_apply_perm(int32_t n, const int32_t *rowptr, const int32_t *colidx,
+                   const int32_t *perm, int32_t *rowptr_out, int32_t *colidx_out) {
+    int32_t *inv = malloc(sizeof(int32_t) * (size_t)(n > 0 ? n : 1));
+    if (!inv) return ORC_ERR;
+    for (int32_t k = 0; k < n; ++k) inv[perm[k]] = k;
+    rowptr_out[0] = 0;
+    for (int32_t r = 0; r < n; ++r) {
+        int32_t o = perm[r];
+        int32_t b = rowptr_out[r];
+        int32_t d = rowptr[o + 1] - rowptr[o];
+        for (int32_t k = 0; k < d; ++k) colidx_out[b + k] = inv[colidx[rowptr[o] + k]];
+        qsort(colidx_out + b, (size_t)d, sizeof(int32_t), cmp_i32);
+        rowptr_out[r + 1] = b + d;
+    }
+    free(inv);
+    return ORC_OK;
+}
