@@ -1,0 +1,283 @@
+/*
+ * gnn.h -- C ABI of libgnn, CSR neighbourhood aggregation for GNN layers on
+ * one NVIDIA GB300 (sm_103a).
+ *
+ * The operations follow "On efficient scaling of GNNs via IO-aware layer
+ * implementations" (cited as "IO-aware GNN layers"): SpMM convolutions
+ * (Section 2.2 (i), Appendix D.4), degree-aware segment reductions
+ * (Section 2.2 (ii), Appendix D.1) and fused CSR attention for GATv2 and the
+ * Graph Transformer (Section 2.2 (iii), Section 3.2, Appendix D.2), plus the
+ * 16x16 block-sparse tensor-core layout (Section 3.3, Appendix D.3) and
+ * vertex reordering (Section 4.1; RCM as in "A High-Throughput Solver for
+ * Marginalized Graph Kernels on GPU", graph reordering section).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Graph: CSR by destination.  Row i lists the source nodes j of the edges
+ *   j -> i in colidx[rowptr[i] .. rowptr[i+1]), ascending and without
+ *   duplicates; N(i) includes i only if the graph stores a self-loop (the
+ *   library never adds one).  Indices are int32 (nnz < 2^31).
+ * Memory: every array argument is a DEVICE pointer owned by the caller unless
+ *   the comment says "host".  The library never allocates device memory;
+ *   scratch space comes from the caller through (ws, ws_bytes), sized by
+ *   gnn_workspace_size().  A workspace must be zero-filled once before its
+ *   first use; every call leaves it zero-filled again (so one cudaMemset
+ *   after allocation suffices).  Calls that may overlap on the GPU need
+ *   separate workspaces.
+ * Features: dense row-major [rows, F].  Rows must start on 16-byte
+ *   boundaries: F % 4 == 0 for fp32, F % 8 == 0 for bf16, and every feature
+ *   pointer 16-byte aligned.
+ * Streams: `stream` is a cudaStream_t (NULL = the legacy default stream).
+ *   Calls are asynchronous on it unless the comment says "synchronous".
+ * Errors: arguments are validated on the host before any launch; a failed
+ *   check returns GNN_ERR_INVALID_ARG / GNN_ERR_UNSUPPORTED /
+ *   GNN_ERR_WORKSPACE and launches nothing.  Launch failures return
+ *   GNN_ERR_CUDA.  Device-side checks (gnn_csr_validate, bounded waits) never
+ *   trap: they record a code in a device error word, read with
+ *   gnn_last_device_error().
+ */
+#ifndef GNN_H
+#define GNN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GNN_OK = 0,
+    GNN_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned pointer */
+    GNN_ERR_UNSUPPORTED = 2,   /* valid but not implemented (dtype, width) */
+    GNN_ERR_WORKSPACE = 3,     /* ws too small */
+    GNN_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
+    GNN_ERR_DEVICE_CHECK = 5,  /* a device-side check failed (see error word) */
+    GNN_ERR_TIMEOUT = 6        /* a bounded device-side wait ran out */
+} gnn_status;
+
+typedef enum { GNN_F32 = 0, GNN_BF16 = 1 } gnn_dtype;
+
+/* SpMM normalisation (IO-aware GNN layers, Appendix D.4: none/left/right/
+ * both).  Edge weight w_ij = v_ij * f, v_ij = values[e] (or 1 if values is
+ * NULL), f = 1 (NONE), 1/d_in(i) (LEFT), 1/d_out(j) (RIGHT),
+ * 1/sqrt(d_in(i) d_out(j)) (BOTH, the GCN normalisation of Section 2.2 (i)).
+ * d_in(i) = row length, d_out(j) = occurrences of j in colidx. */
+typedef enum { GNN_NORM_NONE = 0, GNN_NORM_LEFT = 1, GNN_NORM_RIGHT = 2, GNN_NORM_BOTH = 3 } gnn_norm;
+
+/* Kernel mappings (IO-aware GNN layers, Section 4.1 and Appendix E.1, the
+ * "dot-aggr" study; Appendix D.1 degree-aware split):
+ *   AUTO  -- degree-aware: the edge list is cut into equal runs of edges, one
+ *            per warp; short rows are packed several to a warp, rows longer
+ *            than a run are split across warps and their partial results
+ *            merged (two-phase, deterministic).  Feature-parallel lanes.
+ *   FEAT  -- one warp per destination row, lanes over features (coalesced
+ *            loads), neighbours visited sequentially.
+ *   NEIGH -- one warp per destination row, lanes over neighbours (gather),
+ *            a warp reduction per 16-byte feature slice. */
+typedef enum { GNN_MAP_AUTO = 0, GNN_MAP_FEAT = 1, GNN_MAP_NEIGH = 2 } gnn_mapping;
+
+typedef struct {
+    int32_t n_rows;        /* destination nodes */
+    int32_t n_cols;        /* source nodes (== n_rows for a square graph) */
+    int64_t nnz;           /* edges = rowptr[n_rows] */
+    const int32_t *rowptr; /* device [n_rows+1], rowptr[0] = 0, non-decreasing */
+    const int32_t *colidx; /* device [nnz], each in [0, n_cols) */
+    const float *values;   /* device [nnz] edge values, or NULL */
+} gnn_csr;
+
+/* ---------------------------------------------------------------- prep */
+
+/* Bytes of the prepared-graph buffer for g (host call, no GPU work). */
+size_t gnn_graph_prepare_size(const gnn_csr *g);
+
+/* Step a0: per-graph preparation, done once and reused by every call on the
+ * same graph (IO-aware GNN layers, Appendix D.4, "normalisation as a
+ * preprocessing step" and the graph-structure cache).  Fills `prep` with
+ * d_out[n_cols] (int32), 1/sqrt(d_in)[n_rows] and 1/sqrt(d_out)[n_cols]
+ * (fp32).  prep: device buffer of gnn_graph_prepare_size(g) bytes, 256-byte
+ * aligned, owned by the caller.  Asynchronous. */
+gnn_status gnn_graph_prepare(const gnn_csr *g, void *prep, size_t prep_bytes, void *stream);
+
+/* Device-side structural check of g: rowptr[0] == 0, non-decreasing,
+ * rowptr[n_rows] == nnz, colidx in [0, n_cols), strictly ascending within a
+ * row.  A violation sets the device error word to GNN_ERR_DEVICE_CHECK (no
+ * trap).  Asynchronous; read the result with gnn_last_device_error. */
+gnn_status gnn_csr_validate(const gnn_csr *g, void *stream);
+
+/* Synchronous: waits for `stream`, returns the device error word (GNN_OK if
+ * clear) in *code and clears it. */
+gnn_status gnn_last_device_error(void *stream, int32_t *code);
+
+/* Operation ids for gnn_workspace_size. */
+typedef enum {
+    GNN_OP_SPMM = 0, GNN_OP_SUM = 1, GNN_OP_MEAN = 2, GNN_OP_MAX = 3,
+    GNN_OP_GATV2 = 4, GNN_OP_GT = 5, GNN_OP_REORDER = 6, GNN_OP_APPLY_PERM = 7,
+    GNN_OP_BLOCKSPARSE = 8
+} gnn_op;
+
+/* Workspace bytes needed by operation `op` on g with feature width F (or
+ * heads x head_dim for attention; F is then F_in for GATv2).  Host call. */
+size_t gnn_workspace_size(int32_t op, const gnn_csr *g, int32_t F, int32_t heads,
+                          int32_t head_dim);
+
+/* ------------------------------------------------------- step a1: SpMM */
+
+/* Y = A_w X  (IO-aware GNN layers, Section 2.2 (i); GCN with
+ * norm = GNN_NORM_BOTH).  X [n_cols, F] (fp32 or bf16), Y [n_rows, F] fp32,
+ * accumulation fp32.  prep from gnn_graph_prepare (required for LEFT/RIGHT/
+ * BOTH, may be NULL for NONE).  mapping: gnn_mapping.  Supported F: fp32
+ * 32..1024 and bf16 64..2048 with F / (16 bytes) a power of two. */
+gnn_status gnn_spmm(const gnn_csr *g, const void *prep, int32_t norm, const void *X,
+                    int32_t x_dtype, int32_t F, float *Y, int32_t mapping, void *ws,
+                    size_t ws_bytes, void *stream);
+
+/* ---------------------------------------- step a2: segment reductions */
+
+/* Y[i,:] = sum over j in N(i) of X[j,:]  (IO-aware GNN layers, Section
+ * 2.2 (ii)).  Empty rows give 0.  Shapes and F as gnn_spmm.  prep may be
+ * NULL; when given, the edge-run table it holds replaces a per-run search. */
+gnn_status gnn_segment_reduce_sum(const gnn_csr *g, const void *prep, const void *X,
+                                  int32_t x_dtype, int32_t F, float *Y, void *ws,
+                                  size_t ws_bytes, void *stream);
+
+/* Y[i,:] = (sum over j in N(i) of X[j,:]) / d_in(i); empty rows give 0. */
+gnn_status gnn_segment_reduce_mean(const gnn_csr *g, const void *prep, const void *X,
+                                   int32_t x_dtype, int32_t F, float *Y, void *ws,
+                                   size_t ws_bytes, void *stream);
+
+/* Y[i,f] = max over j in N(i) of X[j,f] under the order-preserving key of
+ * IO-aware GNN layers, Appendix D.1 (so -0 < +0); ties go to the smallest
+ * source id.  argmax[i,f] (int32 [n_rows, F], may be NULL) = that source
+ * node id (not an edge position).  Empty rows give Y = 0, argmax = -1.
+ * Inputs must be finite.  Bit-exact. */
+gnn_status gnn_segment_reduce_max(const gnn_csr *g, const void *prep, const void *X,
+                                  int32_t x_dtype, int32_t F, float *Y, int32_t *argmax,
+                                  void *ws, size_t ws_bytes, void *stream);
+
+/* -------------------------------------------- step a3: dense projection */
+
+/* C = H W  (IO-aware GNN layers, Section 2.2 (i), the dense GEMM of
+ * footnote 2).  H [n, F_in], W [F_in, F_out] row-major, C [n, F_out].
+ * bf16 inputs: tcgen05 tensor cores, fp32 accumulation in TMEM, C bf16;
+ * F_in % 64 == 0, F_out % 16 == 0, F_out <= 256.  fp32 inputs: fp32 FMA
+ * (no TF32), C fp32. */
+gnn_status gnn_projection(const void *H, int32_t dtype, int64_t n, int32_t F_in, const void *W,
+                          int32_t F_out, void *C, void *stream);
+
+/* ------------------------------------------------ step a4: fused GATv2 */
+
+/* GATv2 forward (IO-aware GNN layers, Section 2.2 (iii); Appendix D.2 fused
+ * CSR forward): l = H W_l, r = H W_r (W_r NULL: shared W, l = r), then per
+ * destination i and head h
+ *   e_ij = sum_d a[h,d] LeakyReLU_neg_slope(l[i,h,d] + r[j,h,d]),
+ *   out[i,h,:] = sum_j softmax_j(e_ij) r[j,h,:],
+ *   lse[i,h] = ln sum_j exp(e_ij)   (lse may be NULL).
+ * Score, online softmax and aggregation run in one pass; no per-edge tensor
+ * is written.  H [n_cols, F_in]; W [F_in, heads*head_dim]; a fp32 [heads,
+ * head_dim]; out fp32 [n_rows, heads*head_dim]; lse fp32 [n_rows, heads].
+ * dtype bf16: projections on tcgen05, l/r stored bf16 in ws.  dtype fp32:
+ * fp32 projections.  head_dim in {32, 64, 128}; heads*head_dim <= 256
+ * (bf16) or <= 1024 (fp32); square graphs only.  Empty rows give out 0,
+ * lse -inf. */
+gnn_status gnn_gatv2_fwd(const gnn_csr *g, const void *prep, const void *H, int32_t dtype,
+                         int32_t F_in, const void *W_l, const void *W_r, const float *a,
+                         int32_t heads, int32_t head_dim, float neg_slope, float *out,
+                         float *lse, void *ws, size_t ws_bytes, void *stream);
+
+/* ------------------------------------------- step a6: block-sparse tiles */
+
+/* Block-sparse tile layout (IO-aware GNN layers, Section 3.3 and Appendix
+ * D.3, weighted block-sparse format): rows are cut into 16-row windows and
+ * 128-row groups (8 windows).  U_g = sorted unique source columns of group
+ * g; column block b = U_g[16b .. 16b+16) (padding entries are column 0 and
+ * never masked in).  Tile (window w, block b) is 16x16 with a 256-bit mask,
+ * bit r*16+c (word (r*16+c)/64) set iff edge U_g[16b+c] -> 16w+r exists.
+ * A tile is kept iff popcount >= 1 and popcount/256 >= fill_threshold (fp32
+ * comparison); a block is listed iff one of its 8 tiles is kept; masks of
+ * unkept tiles are zero; edges of unkept tiles form the residual CSR. */
+typedef struct {
+    int32_t n_rows, n_groups;
+    int64_t n_blocks;        /* listed column blocks */
+    int64_t n_tiles_kept;    /* kept 16x16 tiles */
+    int64_t nnz_tiles;       /* edges inside kept tiles */
+    int64_t nnz_residual;    /* edges in the residual CSR */
+    float fill_threshold;
+    /* device pointers into the caller's buffer */
+    int32_t *grp_blk_offset; /* [n_groups+1] */
+    int32_t *blk_cols;       /* [n_blocks*16] */
+    uint64_t *blk_mask;      /* [n_blocks*8*4] */
+    int32_t *res_rowptr;     /* [n_rows+1] */
+    int32_t *res_colidx;     /* [nnz_residual] */
+} gnn_blocksparse;
+
+/* Synchronous planning pass: fills the counts of *bs (host struct; pointers
+ * left NULL) and *out_bytes, the size of the buffer gnn_blocksparse_build
+ * needs. */
+gnn_status gnn_blocksparse_plan(const gnn_csr *g, float fill_threshold, void *ws,
+                                size_t ws_bytes, gnn_blocksparse *bs, size_t *out_bytes,
+                                void *stream);
+
+/* Build the layout planned by gnn_blocksparse_plan into `out` (device,
+ * out_bytes, 256-byte aligned); sets the device pointers of *bs (host struct).
+ * Bit-exact.  Asynchronous. */
+gnn_status gnn_blocksparse_build(const gnn_csr *g, gnn_blocksparse *bs, void *out,
+                                 size_t out_bytes, void *ws, size_t ws_bytes, void *stream);
+
+/* ---------------------------- steps a5 + a7: Graph Transformer attention */
+
+/* Graph Transformer attention (IO-aware GNN layers, Section 2.2 (iii);
+ * Appendix D.2 fused CSR forward; Appendix D.3 tensor-core attention):
+ *   e_ij = scale * sum_d Q[i,h,d] K[j,h,d]  (query at the destination),
+ *   out[i,h,:] = sum_j softmax_j(e_ij) V[j,h,:], lse[i,h] = ln sum_j exp(e_ij).
+ * bs NULL: fused CSR kernel over g.  bs from gnn_blocksparse_build on g:
+ * edges in kept tiles run on tcgen05 (S = Q K^T and P V per 128-row group),
+ * residual edges on the CSR kernel, softmax states merged.  Q, K, V
+ * [n, heads*head_dim] (bf16 for the tile path; fp32 or bf16 for CSR), out
+ * fp32 [n_rows, heads*head_dim], lse fp32 [n_rows, heads] (may be NULL).
+ * head_dim in {32, 64}; square graphs. */
+gnn_status gnn_gt_attn_fwd(const gnn_csr *g, const void *prep, const gnn_blocksparse *bs,
+                           const void *Q, const void *K, const void *V, int32_t dtype,
+                           int32_t heads, int32_t head_dim, float scale, float *out,
+                           float *lse, void *ws, size_t ws_bytes, void *stream);
+
+/* --------------------------------------------------- step a8: reordering */
+
+typedef enum { GNN_PERM_IDENTITY = 0, GNN_PERM_RANDOM = 1, GNN_PERM_DEGREE = 2,
+               GNN_PERM_RCM = 3 } gnn_perm_kind;
+
+/* Vertex ordering of a square graph (IO-aware GNN layers, Section 2.4 and
+ * Section 4.1; RCM per the marginalized-graph-kernel solver's reordering
+ * section).  perm[new] = old, inv[old] = new (either may be NULL).
+ *   RANDOM: ascending (splitmix64(seed ^ id), id)
+ *   DEGREE: descending d_in + d_out (as stored), ties by ascending id
+ *   RCM:    reverse Cuthill-McKee on A + A^T without self-loops; each
+ *           component starts at its unvisited node of smallest degree
+ *           (lowest id), each visited node appends its unvisited neighbours
+ *           in ascending (degree, id).
+ * Bit-exact.  IDENTITY/RANDOM/DEGREE are asynchronous; RCM is synchronous
+ * (its number of breadth-first levels is data dependent). */
+gnn_status gnn_reorder_perm(const gnn_csr *g, int32_t kind, uint64_t seed, int32_t *perm,
+                            int32_t *inv, void *ws, size_t ws_bytes, void *stream);
+
+/* Relabel: new row r = old row perm[r] with columns mapped through inv and
+ * re-sorted; rowptr_out [n+1], colidx_out [nnz]; if X is not NULL, X_out[r]
+ * = X[perm[r]] ([n, F], x_dtype).  Bit-exact.  Asynchronous. */
+gnn_status gnn_apply_perm(const gnn_csr *g, const int32_t *perm, const int32_t *inv,
+                          int32_t *rowptr_out, int32_t *colidx_out, const void *X,
+                          int32_t x_dtype, int32_t F, void *X_out, void *ws, size_t ws_bytes,
+                          void *stream);
+
+/* ------------------------------------------------------------ utilities */
+
+const char *gnn_status_string(int32_t status);
+/* Number of kernels this library has launched in this process (host
+ * counter, incremented at every launch). */
+uint64_t gnn_launch_count(void);
+/* Library version string. */
+const char *gnn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GNN_H */

@@ -1,0 +1,233 @@
+"""Thin ctypes binding of libgnn (include/gnn.h): argument marshalling only.
+
+Every computation runs in libgnn's CUDA kernels.  PyTorch supplies device
+memory (outputs, workspaces) and the current CUDA stream.  There is no CPU
+fallback: if libgnn.so is missing or no GPU is visible, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.environ.get("GNN_LIB_PATH") or os.path.join(_HERE, "libgnn.so")
+
+GNN_OK, GNN_ERR_INVALID_ARG, GNN_ERR_UNSUPPORTED, GNN_ERR_WORKSPACE = 0, 1, 2, 3
+GNN_ERR_CUDA, GNN_ERR_DEVICE_CHECK, GNN_ERR_TIMEOUT = 4, 5, 6
+GNN_F32, GNN_BF16 = 0, 1
+GNN_NORM_NONE, GNN_NORM_LEFT, GNN_NORM_RIGHT, GNN_NORM_BOTH = 0, 1, 2, 3
+GNN_MAP_AUTO, GNN_MAP_FEAT, GNN_MAP_NEIGH = 0, 1, 2
+(GNN_OP_SPMM, GNN_OP_SUM, GNN_OP_MEAN, GNN_OP_MAX, GNN_OP_GATV2, GNN_OP_GT, GNN_OP_REORDER,
+ GNN_OP_APPLY_PERM, GNN_OP_BLOCKSPARSE) = range(9)
+GNN_PERM_IDENTITY, GNN_PERM_RANDOM, GNN_PERM_DEGREE, GNN_PERM_RCM = 0, 1, 2, 3
+
+
+class GnnError(RuntimeError):
+    def __init__(self, fn, code):
+        msg = lib().gnn_status_string(code).decode() if _lib is not None else str(code)
+        super().__init__(f"{fn} failed: {msg} ({code})")
+        self.code = code
+
+
+class gnn_csr(ctypes.Structure):
+    _fields_ = [("n_rows", ctypes.c_int32), ("n_cols", ctypes.c_int32), ("nnz", ctypes.c_int64),
+                ("rowptr", ctypes.c_void_p), ("colidx", ctypes.c_void_p),
+                ("values", ctypes.c_void_p)]
+
+
+class gnn_blocksparse(ctypes.Structure):
+    _fields_ = [("n_rows", ctypes.c_int32), ("n_groups", ctypes.c_int32),
+                ("n_blocks", ctypes.c_int64), ("n_tiles_kept", ctypes.c_int64),
+                ("nnz_tiles", ctypes.c_int64), ("nnz_residual", ctypes.c_int64),
+                ("fill_threshold", ctypes.c_float),
+                ("grp_blk_offset", ctypes.c_void_p), ("blk_cols", ctypes.c_void_p),
+                ("blk_mask", ctypes.c_void_p), ("res_rowptr", ctypes.c_void_p),
+                ("res_colidx", ctypes.c_void_p)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+_SIGS = {
+    "gnn_graph_prepare_size": (ctypes.c_size_t, ["csr"]),
+    "gnn_graph_prepare": (ctypes.c_int, ["csr", "p", "sz", "p"]),
+    "gnn_csr_validate": (ctypes.c_int, ["csr", "p"]),
+    "gnn_last_device_error": (ctypes.c_int, ["p", "p"]),
+    "gnn_workspace_size": (ctypes.c_size_t, ["i32", "csr", "i32", "i32", "i32"]),
+    "gnn_spmm": (ctypes.c_int, ["csr", "p", "i32", "p", "i32", "i32", "p", "i32", "p", "sz", "p"]),
+    "gnn_segment_reduce_sum": (ctypes.c_int, ["csr", "p", "p", "i32", "i32", "p", "p", "sz", "p"]),
+    "gnn_segment_reduce_mean": (ctypes.c_int, ["csr", "p", "p", "i32", "i32", "p", "p", "sz", "p"]),
+    "gnn_segment_reduce_max": (ctypes.c_int, ["csr", "p", "p", "i32", "i32", "p", "p", "p", "sz",
+                                              "p"]),
+    "gnn_projection": (ctypes.c_int, ["p", "i32", "i64", "i32", "p", "i32", "p", "p"]),
+    "gnn_gatv2_fwd": (ctypes.c_int, ["csr", "p", "p", "i32", "i32", "p", "p", "p", "i32", "i32",
+                                     "f32", "p", "p", "p", "sz", "p"]),
+    "gnn_blocksparse_plan": (ctypes.c_int, ["csr", "f32", "p", "sz", "bs", "p", "p"]),
+    "gnn_blocksparse_build": (ctypes.c_int, ["csr", "bs", "p", "sz", "p", "sz", "p"]),
+    "gnn_gt_attn_fwd": (ctypes.c_int, ["csr", "p", "bs", "p", "p", "p", "i32", "i32", "i32", "f32",
+                                       "p", "p", "p", "sz", "p"]),
+    "gnn_reorder_perm": (ctypes.c_int, ["csr", "i32", "u64", "p", "p", "p", "sz", "p"]),
+    "gnn_apply_perm": (ctypes.c_int, ["csr", "p", "p", "p", "p", "p", "i32", "i32", "p", "p", "sz",
+                                      "p"]),
+    "gnn_status_string": (ctypes.c_char_p, ["i32"]),
+    "gnn_launch_count": (ctypes.c_uint64, []),
+    "gnn_version": (ctypes.c_char_p, []),
+}
+
+_CT = {"csr": ctypes.POINTER(gnn_csr), "bs": ctypes.POINTER(gnn_blocksparse),
+       "p": ctypes.c_void_p, "sz": ctypes.c_size_t, "i32": ctypes.c_int32,
+       "i64": ctypes.c_int64, "u64": ctypes.c_uint64, "f32": ctypes.c_float}
+
+EXPORTED = tuple(_SIGS)
+
+
+def lib():
+    """Load libgnn.so (built by __graft_entry__.build()); raises if absent."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"libgnn.so is not built ({LIB_PATH}); "
+                                   "run __graft_entry__.build()")
+            L = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in _SIGS.items():
+                f = getattr(L, name)
+                f.restype = res
+                f.argtypes = [_CT[a] for a in args]
+            _lib = L
+    return _lib
+
+
+def _check(name, code):
+    if code != GNN_OK:
+        raise GnnError(name, code)
+
+
+def _stream(stream=None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return GNN_F32
+    if t.dtype == torch.bfloat16:
+        return GNN_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _require_cuda(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+class Graph:
+    """A CSR graph by destination on the GPU plus its prepared buffer (step
+    a0) and cached, zero-initialised workspaces."""
+
+    def __init__(self, rowptr: torch.Tensor, colidx: torch.Tensor, values=None, n_cols=None,
+                 prepare: bool = True, stream=None):
+        _require_cuda(rowptr, colidx, values)
+        if rowptr.dtype != torch.int32 or colidx.dtype != torch.int32:
+            raise TypeError("rowptr/colidx must be int32")
+        self.rowptr, self.colidx, self.values = rowptr, colidx, values
+        self.n_rows = rowptr.numel() - 1
+        self.n_cols = self.n_rows if n_cols is None else int(n_cols)
+        self.nnz = colidx.numel()
+        self.csr = gnn_csr(self.n_rows, self.n_cols, self.nnz, rowptr.data_ptr(),
+                           colidx.data_ptr() if self.nnz else None, _ptr(values))
+        self.device = rowptr.device
+        self._ws = {}
+        self.prep = None
+        if prepare:
+            n = lib().gnn_graph_prepare_size(ctypes.byref(self.csr))
+            self.prep = torch.empty(max(n, 256), dtype=torch.uint8, device=self.device)
+            _check("gnn_graph_prepare", lib().gnn_graph_prepare(
+                ctypes.byref(self.csr), self.prep.data_ptr(), self.prep.numel(), _stream(stream)))
+
+    def workspace(self, op: int, F: int = 0, heads: int = 0, head_dim: int = 0, key=None):
+        n = lib().gnn_workspace_size(op, ctypes.byref(self.csr), F, heads, head_dim)
+        k = (op, F, heads, head_dim, key)
+        ws = self._ws.get(k)
+        if ws is None or ws.numel() < n:
+            ws = torch.zeros(max(n, 256), dtype=torch.uint8, device=self.device)
+            self._ws[k] = ws
+        return ws
+
+
+def graph_prepare(rowptr, colidx, values=None, n_cols=None, stream=None) -> Graph:
+    return Graph(rowptr, colidx, values, n_cols, True, stream)
+
+
+def csr_validate(g: Graph, stream=None) -> int:
+    L = lib()
+    _check("gnn_csr_validate", L.gnn_csr_validate(ctypes.byref(g.csr), _stream(stream)))
+    code = ctypes.c_int32(0)
+    _check("gnn_last_device_error", L.gnn_last_device_error(_stream(stream), ctypes.byref(code)))
+    return code.value
+
+
+def gnn_spmm(g: Graph, X: torch.Tensor, norm: int = GNN_NORM_BOTH, mapping: int = GNN_MAP_AUTO,
+             out=None, stream=None):
+    _require_cuda(X)
+    F = X.shape[1]
+    Y = out if out is not None else torch.empty((g.n_rows, F), dtype=torch.float32,
+                                                device=X.device)
+    ws = g.workspace(GNN_OP_SPMM, F)
+    _check("gnn_spmm", lib().gnn_spmm(ctypes.byref(g.csr), _ptr(g.prep), norm, X.data_ptr(),
+                                      _dtype_code(X), F, Y.data_ptr(), mapping, ws.data_ptr(),
+                                      ws.numel(), _stream(stream)))
+    return Y
+
+
+def _reduce(name, op, g, X, out, stream):
+    _require_cuda(X)
+    F = X.shape[1]
+    Y = out if out is not None else torch.empty((g.n_rows, F), dtype=torch.float32,
+                                                device=X.device)
+    ws = g.workspace(op, F)
+    _check(name, getattr(lib(), name)(ctypes.byref(g.csr), _ptr(g.prep), X.data_ptr(),
+                                      _dtype_code(X), F, Y.data_ptr(), ws.data_ptr(), ws.numel(),
+                                      _stream(stream)))
+    return Y
+
+
+def gnn_segment_reduce_sum(g: Graph, X, out=None, stream=None):
+    return _reduce("gnn_segment_reduce_sum", GNN_OP_SUM, g, X, out, stream)
+
+
+def gnn_segment_reduce_mean(g: Graph, X, out=None, stream=None):
+    return _reduce("gnn_segment_reduce_mean", GNN_OP_MEAN, g, X, out, stream)
+
+
+def gnn_segment_reduce_max(g: Graph, X, want_argmax: bool = True, out=None, argmax=None,
+                           stream=None):
+    _require_cuda(X)
+    F = X.shape[1]
+    Y = out if out is not None else torch.empty((g.n_rows, F), dtype=torch.float32,
+                                                device=X.device)
+    am = None
+    if want_argmax:
+        am = argmax if argmax is not None else torch.empty((g.n_rows, F), dtype=torch.int32,
+                                                           device=X.device)
+    ws = g.workspace(GNN_OP_MAX, F)
+    _check("gnn_segment_reduce_max", lib().gnn_segment_reduce_max(
+        ctypes.byref(g.csr), _ptr(g.prep), X.data_ptr(), _dtype_code(X), F, Y.data_ptr(),
+        _ptr(am), ws.data_ptr(), ws.numel(), _stream(stream)))
+    return Y, am
+
+
+def launch_count() -> int:
+    return int(lib().gnn_launch_count())
+
+
+def version() -> str:
+    return lib().gnn_version().decode()

@@ -1,0 +1,1030 @@
+// Steps a1 (SpMM) and a2 (segment sum / mean / max) of CSR neighbourhood
+// aggregation.
+//
+// IO-aware GNN layers, Section 2.2 (i)-(ii), Section 3.1 and Appendix D.1
+// ("degree-aware reduction", light/heavy split, packed (value, index)
+// merge), Section 4.1 / Appendix E.1 (feature- vs neighbour-parallel
+// mappings).
+//
+// GB300 design.  All three families stream 16-byte feature chunks with
+// 128-bit loads; rows are 16-byte aligned.  The AUTO mapping cuts the edge
+// list into runs of E edges, one run per group of LPR lanes (a "worker"),
+// instead of one block per node: light rows are packed several to a worker
+// and heavy rows are split across ceil(deg/E) workers, so every worker does
+// the same number of loads.  Loads of U consecutive edges are issued before
+// any of them is accumulated, whatever row they belong to, which keeps U
+// 16-byte loads in flight per lane even through runs of degree-1 rows.  A
+// row that crosses a run boundary leaves one partial result per worker in
+// the workspace; the last worker to finish it (a ticket counter, no
+// spinning) combines the partials in edge order, so results are
+// deterministic.  For max the partials are (value, source id) pairs combined
+// under the order-preserving key with ties to the smaller id -- the same
+// result as the paper's packed 64-bit atomicMin, without atomics on the
+// feature data.
+#include <algorithm>
+
+#include "common.cuh"
+
+// Minimum resident 256-thread blocks per SM requested for the one-chunk-per-
+// lane AUTO kernels (register cap 65536 / (256 * GNN_AGG_MINB)).
+#ifndef GNN_AGG_MINB
+#define GNN_AGG_MINB 4
+#endif
+// 16-byte loads in flight per lane in the edge loops
+#ifndef GNN_AGG_U
+#define GNN_AGG_U 4
+#endif
+// 1: 32-lane AUTO workers use the shared-memory staged kernel
+#ifndef GNN_AGG_STAGED
+#define GNN_AGG_STAGED 0
+#endif
+// upper bound on the staged kernel's pipeline depth
+#ifndef GNN_AGG_STAGES
+#define GNN_AGG_STAGES 8
+#endif
+
+namespace gnn {
+
+void prep_pointers(const gnn_csr *g, const void *prep, const int32_t **d_out,
+                   const float **dinv_in, const float **dinv_out);
+gnn_status check_csr_args(const gnn_csr *g);
+const int32_t *prep_run_table(const gnn_csr *g, const void *prep);
+
+enum AggOp { AGG_WSUM = 0, AGG_MEAN = 1, AGG_MAX = 2 };
+// per-edge weight source / per-row factor source
+enum ColMode { COL_ONE = 0, COL_RSQRT = 1, COL_RECIP = 2 };
+enum RowMode { ROW_ONE = 0, ROW_RSQRT = 1, ROW_RECIP = 2 };
+
+struct AggArgs {
+    const int32_t *rowptr;
+    const int32_t *colidx;
+    const float *values;    // per-edge values or null
+    const int32_t *d_out;   // for COL_RECIP
+    const float *dinv_in;   // for ROW_RSQRT
+    const float *dinv_out;  // for COL_RSQRT
+    const uint4 *X;         // [n_cols, V] 16-byte chunks
+    float *Y;
+    int32_t *argmax;
+    float *carry;           // [n_workers, F] fp32 (max: [n_workers, F] uint64)
+    int32_t *tickets;       // [n_workers], zero on entry and on exit
+    const int32_t *run_first_row;  // [n_workers+1] from the prepared graph, or null
+    int64_t nnz;
+    int64_t n_workers;
+    int32_t n_rows;
+    int32_t F;              // features
+    int32_t V;              // 16-byte chunks per row
+    int32_t lpr;            // lanes per worker (8, 16 or 32)
+    int32_t E;              // edges per worker (multiple of 32)
+    int32_t col_mode, row_mode;
+};
+
+template <int OP, class T, int CPL>
+struct Acc {
+    static constexpr int NV = Chunk<T>::N;
+    float v[CPL][NV];
+    int32_t idx[OP == AGG_MAX ? CPL : 1][OP == AGG_MAX ? NV : 1];
+
+    // key of the current maximum (0 = nothing seen; every finite key is > 0)
+    __device__ __forceinline__ uint32_t key(int c, int k) const {
+        return idx[c][k] >= 0 ? order_key(v[c][k]) : 0u;
+    }
+    __device__ __forceinline__ void reset() {
+#pragma unroll
+        for (int c = 0; c < CPL; ++c)
+#pragma unroll
+            for (int k = 0; k < NV; ++k) {
+                v[c][k] = 0.f;
+                if (OP == AGG_MAX) idx[c][k] = -1;
+            }
+    }
+    __device__ __forceinline__ void add(const uint4 *x, float w, int32_t j) {
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+            float f[NV];
+            Chunk<T>::unpack(x[c], f);
+#pragma unroll
+            for (int k = 0; k < NV; ++k) {
+                if (OP == AGG_MAX) {
+                    uint32_t kk = order_key(f[k]);
+                    // edges arrive in ascending source id: strict > keeps the
+                    // smallest id among equal keys
+                    if (kk > key(c, k)) { idx[c][k] = j; v[c][k] = f[k]; }
+                } else {
+                    v[c][k] = fmaf(w, f[k], v[c][k]);
+                }
+            }
+        }
+    }
+};
+
+__device__ __forceinline__ float row_factor(const AggArgs &a, int32_t r, int32_t deg) {
+    if (a.row_mode == ROW_RSQRT) return a.dinv_in[r];
+    if (a.row_mode == ROW_RECIP) return deg > 0 ? 1.f / (float)deg : 0.f;
+    return 1.f;
+}
+
+__device__ __forceinline__ float edge_weight(const AggArgs &a, int64_t e, int32_t j) {
+    float w = a.values ? __ldg(a.values + e) : 1.f;
+    if (a.col_mode == COL_RSQRT) w *= __ldg(a.dinv_out + j);
+    else if (a.col_mode == COL_RECIP) w *= 1.f / (float)__ldg(a.d_out + j);
+    return w;
+}
+
+// Store a finished row (fp32 features; the lane owns chunks c*lpr + gl).
+template <int OP, class T, int CPL>
+__device__ __forceinline__ void store_row(const AggArgs &a, int32_t r, int32_t deg,
+                                          const Acc<OP, T, CPL> &acc, int gl) {
+    constexpr int NV = Chunk<T>::N;
+    float s = 1.f;
+    if (OP == AGG_WSUM) s = row_factor(a, r, deg);
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) {
+        int64_t base = (int64_t)r * a.F + (int64_t)(c * a.lpr + gl) * NV;
+        float o[NV];
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            if (OP == AGG_WSUM) o[k] = acc.v[c][k] * s;
+            else if (OP == AGG_MEAN) o[k] = deg > 0 ? acc.v[c][k] / (float)deg : 0.f;
+            else o[k] = acc.idx[c][k] >= 0 ? acc.v[c][k] : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < NV; k += 4)
+            *reinterpret_cast<float4 *>(a.Y + base + k) = make_float4(o[k], o[k + 1], o[k + 2], o[k + 3]);
+        if (OP == AGG_MAX && a.argmax) {
+#pragma unroll
+            for (int k = 0; k < NV; k += 4)
+                *reinterpret_cast<int4 *>(a.argmax + base + k) =
+                    make_int4(acc.idx[c][k], acc.idx[c][k + 1], acc.idx[c][k + 2], acc.idx[c][k + 3]);
+        }
+    }
+}
+
+template <int OP, class T, int CPL>
+__device__ __forceinline__ void store_row_f(const AggArgs &a, int32_t r, int32_t deg, float rf,
+                                            const Acc<OP, T, CPL> &acc, int gl) {
+    constexpr int NV = Chunk<T>::N;
+    float s = 1.f;
+    if (OP == AGG_WSUM)
+        s = a.row_mode == ROW_RSQRT ? rf : (a.row_mode == ROW_RECIP ? (deg > 0 ? 1.f / (float)deg : 0.f) : 1.f);
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) {
+        int64_t base = (int64_t)r * a.F + (int64_t)(c * a.lpr + gl) * NV;
+        float o[NV];
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            if (OP == AGG_WSUM) o[k] = acc.v[c][k] * s;
+            else if (OP == AGG_MEAN) o[k] = deg > 0 ? acc.v[c][k] / (float)deg : 0.f;
+            else o[k] = acc.idx[c][k] >= 0 ? acc.v[c][k] : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < NV; k += 4)
+            *reinterpret_cast<float4 *>(a.Y + base + k) = make_float4(o[k], o[k + 1], o[k + 2], o[k + 3]);
+        if (OP == AGG_MAX && a.argmax) {
+#pragma unroll
+            for (int k = 0; k < NV; k += 4)
+                *reinterpret_cast<int4 *>(a.argmax + base + k) =
+                    make_int4(acc.idx[c][k], acc.idx[c][k + 1], acc.idx[c][k + 2], acc.idx[c][k + 3]);
+        }
+    }
+}
+
+// Partial row of a heavy row r (degree > E).  Every run that holds a piece of
+// r folds it into the row's accumulation slot -- slot wa, the run the row
+// starts in -- with vector fp32 atomics (sum-like ops) or, for max, with a
+// 64-bit atomicMax on (key << 32) | ~source_id, the packed (value, index)
+// merge of IO-aware GNN layers, Appendix D.1 (ties resolve to the smallest
+// id).  A ticket counter per slot tells the last piece to arrive, which
+// finalises the row and leaves the slot and ticket at zero again.
+template <int OP, class T, int CPL>
+__device__ __forceinline__ void flush_partial(const AggArgs &a, int64_t w, int slot, int32_t r,
+                                              Acc<OP, T, CPL> &acc, int gl, unsigned gmask) {
+    (void)w;
+    (void)slot;
+    constexpr int NV = Chunk<T>::N;
+    const int64_t F = a.F;
+    const int32_t rb = __ldg(a.rowptr + r), re = __ldg(a.rowptr + r + 1);
+    const int64_t wa = (int64_t)rb / a.E, wb = ((int64_t)re - 1) / a.E;
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) {
+        const int64_t off = wa * F + (int64_t)(c * a.lpr + gl) * NV;
+#pragma unroll
+        for (int k = 0; k < NV; k += 4) {
+            if (OP == AGG_MAX) {
+                unsigned long long *dst = reinterpret_cast<unsigned long long *>(a.carry) + off + k;
+#pragma unroll
+                for (int z = 0; z < 4; ++z) {
+                    const uint32_t key = acc.key(c, k + z);
+                    const unsigned long long packed =
+                        ((unsigned long long)key << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)acc.idx[c][k + z]);
+                    atomicMax(dst + z, packed);
+                }
+            } else {
+                atomicAdd(reinterpret_cast<float4 *>(a.carry + off + k),
+                          make_float4(acc.v[c][k], acc.v[c][k + 1], acc.v[c][k + 2], acc.v[c][k + 3]));
+            }
+        }
+    }
+    __threadfence();
+    __syncwarp(gmask);
+    int t = 0;
+    if (gl == 0) t = atomicAdd(a.tickets + wa, 1);
+    t = __shfl_sync(gmask, t, 0, a.lpr);
+    if (t != (int)(wb - wa)) return;
+    __threadfence();
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) {
+        const int64_t off = wa * F + (int64_t)(c * a.lpr + gl) * NV;
+#pragma unroll
+        for (int k = 0; k < NV; k += 4) {
+            if (OP == AGG_MAX) {
+                unsigned long long *src = reinterpret_cast<unsigned long long *>(a.carry) + off + k;
+#pragma unroll
+                for (int z = 0; z < 4; ++z) {
+                    const unsigned long long p = __ldcg(src + z);
+                    const uint32_t key = (uint32_t)(p >> 32);
+                    const uint32_t u = (key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key;
+                    acc.v[c][k + z] = __uint_as_float(u);
+                    acc.idx[c][k + z] = (int32_t)(0xFFFFFFFFu - (uint32_t)p);
+                    src[z] = 0ull;
+                }
+            } else {
+                float4 *src = reinterpret_cast<float4 *>(a.carry + off + k);
+                const float4 pv = __ldcg(src);
+                acc.v[c][k] = pv.x;
+                acc.v[c][k + 1] = pv.y;
+                acc.v[c][k + 2] = pv.z;
+                acc.v[c][k + 3] = pv.w;
+                *src = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+    }
+    store_row<OP, T, CPL>(a, r, re - rb, acc, gl);
+    __syncwarp(gmask);
+    if (gl == 0) a.tickets[wa] = 0;
+}
+
+// First row r with rowptr[r] >= e (rowptr[n_rows] >= e assumed), found by the
+// lpr lanes of a group together: each round every lane probes one position
+// of the current interval and a ballot narrows it by a factor of lpr.
+__device__ __forceinline__ int32_t group_lower_bound(const int32_t *__restrict__ rowptr,
+                                                     int32_t n_rows, int32_t e, int gl, int lpr,
+                                                     unsigned gmask) {
+    int32_t lo = 0, hi = n_rows;  // answer in [lo, hi]
+    while (hi - lo > 1) {
+        int32_t span = hi - lo;
+        int32_t step = (span + lpr - 1) / lpr;
+        int32_t pos = lo + gl * step;            // probe rowptr[pos] < e ?
+        bool below = pos < hi && __ldg(rowptr + pos) < e;
+        unsigned b = __ballot_sync(gmask, below);
+        if (lpr < 32) b = (b >> ((threadIdx.x & 31) & ~(lpr - 1))) & ((1u << lpr) - 1u);
+        int nb = __popc(b);                       // probes 0..nb-1 are below e
+        if (nb == 0) { hi = lo; break; }
+        int32_t new_lo = lo + (nb - 1) * step + 1;  // first index not known below
+        int32_t new_hi = min(hi, lo + nb * step);
+        lo = new_lo;
+        hi = new_hi;
+        if (lo >= hi) break;
+    }
+    // lo is the answer unless rowptr[lo] < e (possible when hi - lo == 1)
+    if (lo < n_rows && __ldg(rowptr + lo) < e) ++lo;
+    return lo;
+}
+
+// Accumulate the edges [b, end) of one row into acc (no row changes).
+template <int OP, class T, int CPL>
+__device__ __forceinline__ void run_segment(const AggArgs &a, int32_t b, int32_t end,
+                                            Acc<OP, T, CPL> &acc, int gl, unsigned gmask,
+                                            bool weighted) {
+    constexpr int U = CPL >= GNN_AGG_U ? 1 : GNN_AGG_U / CPL;
+    const int lpr = a.lpr;
+    for (int32_t cb = b; cb < end; cb += lpr) {
+        int32_t cj = (cb + gl < end) ? __ldg(a.colidx + cb + gl) : 0;
+        float cw = (weighted && cb + gl < end) ? edge_weight(a, cb + gl, cj) : 1.f;
+        const int n = min(lpr, end - cb);
+        for (int u0 = 0; u0 < n; u0 += U) {
+            uint4 xv[U][CPL];
+            int32_t jv[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                jv[u] = __shfl_sync(gmask, cj, u0 + u, lpr);
+                if (u0 + u < n) {
+                    const uint4 *src = a.X + (size_t)jv[u] * a.V + gl;
+#pragma unroll
+                    for (int c = 0; c < CPL; ++c) xv[u][c] = ldg16(src + c * lpr);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                float wt = weighted ? __shfl_sync(gmask, cw, u0 + u, lpr) : 1.f;
+                if (u0 + u < n) acc.add(xv[u], wt, jv[u]);
+            }
+        }
+    }
+}
+
+// AUTO mapping.  Run w covers edges [w*E, (w+1)*E).  A light row (degree
+// <= E) belongs whole to the run its first edge falls in, so a run may read
+// up to 2E-1 edges; a heavy row (degree > E) is cut at run boundaries and
+// each run leaves a partial result that the row's last run merges.
+template <int OP, class T, int CPL, int LPR>
+__global__ void __launch_bounds__(256, (CPL <= 4 ? GNN_AGG_MINB : 2)) k_agg_auto(AggArgs a) {
+    constexpr int U = CPL >= GNN_AGG_U ? 1 : GNN_AGG_U / CPL;
+    // LPR > 0: lanes per worker known at compile time (32); 0: a.lpr
+    const int lpr = LPR > 0 ? LPR : a.lpr;
+    const int lane = threadIdx.x & 31;
+    const int gl = lane & (lpr - 1);
+    const unsigned gmask = lpr == 32 ? 0xffffffffu : (((1u << lpr) - 1u) << (lane & ~(lpr - 1)));
+    const int32_t w = (int32_t)(((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / lpr);
+    if (w >= a.n_workers) return;
+    const int32_t nnz = (int32_t)a.nnz;
+    const int32_t E = a.E;
+    const int32_t e0 = w * E;
+    const int32_t e1 = min(e0 + E, nnz);
+    const int32_t *__restrict__ rowptr = a.rowptr;
+    const int32_t n_rows = a.n_rows;
+    const bool weighted = (OP == AGG_WSUM) && (a.values || a.col_mode != COL_ONE);
+
+    // rows owned by this run: [lo, lo_end)
+    int32_t lo, lo_end;
+    if (a.run_first_row) {
+        lo = __ldg(a.run_first_row + w);
+        lo_end = __ldg(a.run_first_row + w + 1);
+    } else {
+        lo = group_lower_bound(rowptr, n_rows, e0, gl, lpr, gmask);
+        lo_end = (w + 1 == a.n_workers) ? n_rows : group_lower_bound(rowptr, n_rows, e1, gl, lpr, gmask);
+    }
+
+    Acc<OP, T, CPL> acc;
+    acc.reset();
+
+    // a heavy row that started in an earlier run and reaches into this one
+    if (lo > 0 && e0 < nnz) {
+        const int32_t lo_beg = __ldg(rowptr + lo);
+        if (lo_beg > e0) {
+            const int32_t h = lo - 1;
+            const int32_t hb = __ldg(rowptr + h);
+            if (lo_beg - hb > E) {
+                run_segment<OP, T, CPL>(a, e0, min(lo_beg, e1), acc, gl, gmask, weighted);
+                flush_partial<OP, T, CPL>(a, w, 0, h, acc, gl, gmask);
+                acc.reset();
+            }
+        }
+    }
+    if (lo >= lo_end) return;
+
+    // stream [s0, s1) over the owned rows lo .. rl
+    const int32_t rl = lo_end - 1;
+    const int32_t rl_beg = __ldg(rowptr + rl), rl_end = __ldg(rowptr + rl + 1);
+    const bool heavy_tail = rl_end - rl_beg > E;
+    const int32_t s0 = __ldg(rowptr + lo);
+    const int32_t s1 = heavy_tail ? e1 : rl_end;
+
+    // row-end (and row-factor) cache: lane k holds data of row rb + k
+    int32_t r = lo, rb = lo;
+    const bool rsq = OP == AGG_WSUM && a.row_mode == ROW_RSQRT;
+    int32_t rp_cur = (rb + gl < n_rows) ? __ldg(rowptr + rb + gl + 1) : INT32_MAX;
+    int32_t rp_nxt = (rb + lpr + gl < n_rows) ? __ldg(rowptr + rb + lpr + gl + 1) : INT32_MAX;
+    float rf_cur = (rsq && rb + gl < n_rows) ? __ldg(a.dinv_in + rb + gl) : 1.f;
+    float rf_nxt = (rsq && rb + lpr + gl < n_rows) ? __ldg(a.dinv_in + rb + lpr + gl) : 1.f;
+    int32_t row_beg = s0;
+    int32_t row_end = __shfl_sync(gmask, rp_cur, 0, lpr);
+
+    auto finish_row = [&]() {
+        float rf = __shfl_sync(gmask, rf_cur, r - rb, lpr);
+        store_row_f<OP, T, CPL>(a, r, row_end - row_beg, rf, acc, gl);
+        acc.reset();
+    };
+    auto advance = [&]() {
+        ++r;
+        if (r - rb == lpr) {
+            rb = r;
+            rp_cur = rp_nxt;
+            rf_cur = rf_nxt;
+            rp_nxt = (rb + lpr + gl < n_rows) ? __ldg(rowptr + rb + lpr + gl + 1) : INT32_MAX;
+            if (rsq) rf_nxt = (rb + lpr + gl < n_rows) ? __ldg(a.dinv_in + rb + lpr + gl) : 1.f;
+        }
+        row_beg = row_end;
+        row_end = __shfl_sync(gmask, rp_cur, r - rb, lpr);
+    };
+
+    // column / weight cache for edges [cb, cb+lpr); next window prefetched
+    int32_t cb = s0;
+    int32_t c_cur = (cb + gl < s1) ? __ldg(a.colidx + cb + gl) : 0;
+    int32_t c_nxt = (cb + lpr + gl < s1) ? __ldg(a.colidx + cb + lpr + gl) : 0;
+    float w_cur = 1.f, w_nxt = 1.f;
+    if (weighted) {
+        if (cb + gl < s1) w_cur = edge_weight(a, cb + gl, c_cur);
+        if (cb + lpr + gl < s1) w_nxt = edge_weight(a, cb + lpr + gl, c_nxt);
+    }
+    const uint4 *__restrict__ X = a.X;
+    const int32_t V = LPR > 0 ? LPR * CPL : a.V;
+    for (int32_t eb = s0; eb < s1; eb += U) {
+        if (eb - cb == lpr) {
+            cb = eb;
+            c_cur = c_nxt;
+            w_cur = w_nxt;
+            const int32_t en = cb + lpr + gl;
+            c_nxt = en < s1 ? __ldg(a.colidx + en) : 0;
+            if (weighted && en < s1) w_nxt = edge_weight(a, en, c_nxt);
+        }
+        uint4 xv[U][CPL];
+        int32_t jv[U];
+        const bool full = eb + U <= s1;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            jv[u] = __shfl_sync(gmask, c_cur, (eb - cb) + u, lpr);
+            if (full || eb + u < s1) {
+                const uint4 *src = X + (size_t)jv[u] * V + gl;
+#pragma unroll
+                for (int c = 0; c < CPL; ++c) xv[u][c] = ldg16(src + c * lpr);
+            }
+        }
+        if (full && row_end >= eb + U) {
+            // fast path: the whole batch lies inside the current row
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const float wt = weighted ? __shfl_sync(gmask, w_cur, (eb - cb) + u, lpr) : 1.f;
+                acc.add(xv[u], wt, jv[u]);
+            }
+        } else {
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int32_t e = eb + u;
+                if (e < s1) {
+                    while (e == row_end) {
+                        finish_row();
+                        advance();
+                    }
+                    const float wt = weighted ? __shfl_sync(gmask, w_cur, (eb - cb) + u, lpr) : 1.f;
+                    acc.add(xv[u], wt, jv[u]);
+                }
+            }
+        }
+    }
+    // the row holding the last streamed edge, then empty rows up to rl
+    if (r == rl && heavy_tail) {
+        flush_partial<OP, T, CPL>(a, w, 1, r, acc, gl, gmask);
+        return;
+    }
+    finish_row();
+    while (r < rl) {
+        advance();
+        finish_row();
+    }
+}
+
+// ---------------------------------------------------------------------------
+// AUTO mapping, staged: the same edge-run schedule as k_agg_auto for 32-lane
+// workers, but the feature chunks are moved from L2 into a per-warp ring of
+// shared memory with cp.async (16 B per lane per edge) S-1 batches ahead of
+// their use.  The data in flight occupies shared memory instead of
+// registers, so each warp keeps (S-1)*U rows in flight while it accumulates.
+// Per-edge scalars (source id for max, edge value and column factor for
+// SpMM) travel through the same ring.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+    const uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(sa), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void *smem, const void *gmem) {
+    const uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(sa), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+// wait until at most n groups (0..7) are still pending
+__device__ __forceinline__ void cp_async_wait_n(int n) {
+    switch (n) {
+        case 0: cp_async_wait<0>(); break;
+        case 1: cp_async_wait<1>(); break;
+        case 2: cp_async_wait<2>(); break;
+        case 3: cp_async_wait<3>(); break;
+        case 4: cp_async_wait<4>(); break;
+        case 5: cp_async_wait<5>(); break;
+        case 6: cp_async_wait<6>(); break;
+        default: cp_async_wait<7>(); break;
+    }
+}
+
+struct StageLayout {
+    int32_t stages;        // S
+    int32_t stage_bytes;   // per warp per stage
+    int32_t off_wv;        // edge values [U][32] fp32, or -1
+    int32_t off_wc;        // column factor source [U][32] (fp32 or int32), or -1
+    int32_t off_j;         // source ids [U][32] int32, or -1
+};
+
+template <int OP, class T, int CPL>
+__global__ void __launch_bounds__(128) k_agg_staged(AggArgs a, StageLayout L) {
+    constexpr int U = CPL >= 8 ? 1 : 8 / CPL;
+    constexpr int LPR = 32;
+    constexpr int V = LPR * CPL;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const unsigned FULL = 0xffffffffu;
+    const int32_t w = blockIdx.x * 4 + warp;
+    if (w >= a.n_workers) return;
+    unsigned char *ring = smem_raw + (size_t)warp * L.stages * L.stage_bytes;
+    const int S = L.stages;
+
+    const int32_t nnz = (int32_t)a.nnz;
+    const int32_t E = a.E;
+    const int32_t e0 = w * E;
+    const int32_t e1 = min(e0 + E, nnz);
+    const int32_t *__restrict__ rowptr = a.rowptr;
+    const int32_t n_rows = a.n_rows;
+    const bool has_vals = OP == AGG_WSUM && a.values != nullptr;
+    const bool has_colf = OP == AGG_WSUM && a.col_mode != COL_ONE;
+
+    int32_t lo, lo_end;
+    if (a.run_first_row) {
+        lo = __ldg(a.run_first_row + w);
+        lo_end = __ldg(a.run_first_row + w + 1);
+    } else {
+        lo = group_lower_bound(rowptr, n_rows, e0, lane, LPR, FULL);
+        lo_end = (w + 1 == a.n_workers) ? n_rows : group_lower_bound(rowptr, n_rows, e1, lane, LPR, FULL);
+    }
+    // heavy head piece?
+    bool in_head = false;
+    int32_t h = -1, lo_beg = 0;
+    if (lo > 0 && e0 < nnz) {
+        lo_beg = __ldg(rowptr + lo);
+        if (lo_beg > e0) {
+            h = lo - 1;
+            in_head = (lo_beg - __ldg(rowptr + h)) > E;
+        }
+    }
+    const bool owns = lo < lo_end;
+    if (!in_head && !owns) return;
+    int32_t rl = 0, s1 = 0;
+    bool heavy_tail = false;
+    if (owns) {
+        rl = lo_end - 1;
+        const int32_t rl_beg = __ldg(rowptr + rl), rl_end = __ldg(rowptr + rl + 1);
+        heavy_tail = rl_end - rl_beg > E;
+        s1 = heavy_tail ? e1 : rl_end;
+    }
+    const int32_t sb = in_head ? e0 : __ldg(rowptr + lo);
+    const int32_t se = owns ? s1 : min(lo_beg, e1);
+
+    // row tracking (owned rows through a lane cache of row ends / factors)
+    int32_t r = lo, rb = lo;
+    const bool rsq = OP == AGG_WSUM && a.row_mode == ROW_RSQRT;
+    int32_t rp_cur = (owns && rb + lane < n_rows) ? __ldg(rowptr + rb + lane + 1) : INT32_MAX;
+    int32_t rp_nxt = (owns && rb + LPR + lane < n_rows) ? __ldg(rowptr + rb + LPR + lane + 1) : INT32_MAX;
+    float rf_cur = (rsq && owns && rb + lane < n_rows) ? __ldg(a.dinv_in + rb + lane) : 1.f;
+    float rf_nxt = (rsq && owns && rb + LPR + lane < n_rows) ? __ldg(a.dinv_in + rb + LPR + lane) : 1.f;
+    int32_t row_beg = sb;
+    int32_t row_end = in_head ? min(lo_beg, e1) : __shfl_sync(FULL, rp_cur, 0);
+
+    Acc<OP, T, CPL> acc;
+    acc.reset();
+
+    auto finish_row = [&]() {
+        const float rf = __shfl_sync(FULL, rf_cur, r - rb);
+        store_row_f<OP, T, CPL>(a, r, row_end - row_beg, rf, acc, lane);
+        acc.reset();
+    };
+    auto advance = [&]() {
+        ++r;
+        if (r - rb == LPR) {
+            rb = r;
+            rp_cur = rp_nxt;
+            rf_cur = rf_nxt;
+            rp_nxt = (rb + LPR + lane < n_rows) ? __ldg(rowptr + rb + LPR + lane + 1) : INT32_MAX;
+            if (rsq) rf_nxt = (rb + LPR + lane < n_rows) ? __ldg(a.dinv_in + rb + LPR + lane) : 1.f;
+        }
+        row_beg = row_end;
+        row_end = __shfl_sync(FULL, rp_cur, r - rb);
+    };
+    auto leave_head = [&]() {
+        flush_partial<OP, T, CPL>(a, w, 0, h, acc, lane, FULL);
+        acc.reset();
+        in_head = false;
+        row_beg = row_end;
+        row_end = __shfl_sync(FULL, rp_cur, 0);
+    };
+
+    // producer: colidx window of 32 edges (lane k holds edge pcb + k), next
+    // window prefetched
+    const int32_t nb = (se - sb + U - 1) / U;
+    int32_t pcb = sb;
+    int32_t pc_cur = (pcb + lane < se) ? __ldg(a.colidx + pcb + lane) : 0;
+    int32_t pc_nxt = (pcb + LPR + lane < se) ? __ldg(a.colidx + pcb + LPR + lane) : 0;
+    const uint4 *__restrict__ X = a.X;
+    auto produce = [&](int32_t p) {
+        const int32_t pb = sb + p * U;
+        if (pb - pcb == LPR) {
+            pcb = pb;
+            pc_cur = pc_nxt;
+            pc_nxt = (pcb + LPR + lane < se) ? __ldg(a.colidx + pcb + LPR + lane) : 0;
+        }
+        unsigned char *st = ring + (size_t)(p % S) * L.stage_bytes;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int32_t j = __shfl_sync(FULL, pc_cur, (pb - pcb) + u);
+            const int32_t e = pb + u;
+            if (e < se) {
+                uint4 *dst = reinterpret_cast<uint4 *>(st) + (u * LPR + lane) * CPL;
+                const uint4 *src = X + (size_t)j * V + lane;
+#pragma unroll
+                for (int c = 0; c < CPL; ++c) cp_async16(dst + c, src + c * LPR);
+                if (has_vals) cp_async4(st + L.off_wv + (u * LPR + lane) * 4, a.values + e);
+                if (has_colf)
+                    cp_async4(st + L.off_wc + (u * LPR + lane) * 4,
+                              a.col_mode == COL_RSQRT ? (const void *)(a.dinv_out + j) : (const void *)(a.d_out + j));
+                if (OP == AGG_MAX) *reinterpret_cast<int32_t *>(st + L.off_j + (u * LPR + lane) * 4) = j;
+            }
+        }
+    };
+    auto edge_w = [&](const unsigned char *st, int u) -> float {
+        float wv = 1.f;
+        if (has_vals) wv = *reinterpret_cast<const float *>(st + L.off_wv + (u * LPR + lane) * 4);
+        if (has_colf) {
+            if (a.col_mode == COL_RSQRT) wv *= *reinterpret_cast<const float *>(st + L.off_wc + (u * LPR + lane) * 4);
+            else wv *= 1.f / (float)*reinterpret_cast<const int32_t *>(st + L.off_wc + (u * LPR + lane) * 4);
+        }
+        return wv;
+    };
+
+    for (int32_t p = 0; p < S - 1; ++p) {
+        if (p < nb) produce(p);
+        cp_async_commit();
+    }
+    for (int32_t k = 0; k < nb; ++k) {
+        cp_async_wait_n(S - 2);
+        const unsigned char *st = ring + (size_t)(k % S) * L.stage_bytes;
+        const int32_t eb = sb + k * U;
+        const bool full = eb + U <= se;
+        uint4 xv[U][CPL];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+            for (int c = 0; c < CPL; ++c)
+                xv[u][c] = reinterpret_cast<const uint4 *>(st)[(u * LPR + lane) * CPL + c];
+        if (full && row_end >= eb + U) {
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int32_t j = OP == AGG_MAX ? *reinterpret_cast<const int32_t *>(st + L.off_j + (u * LPR + lane) * 4) : 0;
+                acc.add(xv[u], edge_w(st, u), j);
+            }
+        } else {
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int32_t e = eb + u;
+                if (e < se) {
+                    while (e == row_end) {
+                        if (in_head) leave_head();
+                        else { finish_row(); advance(); }
+                    }
+                    const int32_t j = OP == AGG_MAX ? *reinterpret_cast<const int32_t *>(st + L.off_j + (u * LPR + lane) * 4) : 0;
+                    acc.add(xv[u], edge_w(st, u), j);
+                }
+            }
+        }
+        // refill the stage consumed one iteration ago
+        if (k + S - 1 < nb) produce(k + S - 1);
+        cp_async_commit();
+    }
+    cp_async_wait<0>();
+    if (in_head) {
+        flush_partial<OP, T, CPL>(a, w, 0, h, acc, lane, FULL);
+        acc.reset();
+        if (!owns) return;
+        row_beg = row_end;
+        row_end = __shfl_sync(FULL, rp_cur, 0);
+    }
+    if (r == rl && heavy_tail) {
+        flush_partial<OP, T, CPL>(a, w, 1, r, acc, lane, FULL);
+        return;
+    }
+    finish_row();
+    while (r < rl) {
+        advance();
+        finish_row();
+    }
+}
+
+// FEAT mapping: one group of lpr lanes per destination row, lanes over
+// feature chunks, neighbours in sequence (IO-aware GNN layers, Section 4.1,
+// feature-parallel "dot-aggr" mapping).
+template <class T, int CPL>
+__global__ void __launch_bounds__(256) k_agg_feat(AggArgs a) {
+    constexpr int U = CPL >= GNN_AGG_U ? 1 : GNN_AGG_U / CPL;
+    const int lpr = a.lpr;
+    const int lane = threadIdx.x & 31;
+    const int gl = lane & (lpr - 1);
+    const unsigned gmask = lpr == 32 ? 0xffffffffu : (((1u << lpr) - 1u) << (lane & ~(lpr - 1)));
+    const int64_t r64 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / lpr;
+    if (r64 >= a.n_rows) return;
+    const int32_t r = (int32_t)r64;
+    const int64_t b = __ldg(a.rowptr + r), e1 = __ldg(a.rowptr + r + 1);
+    const bool weighted = a.values || a.col_mode != COL_ONE;
+    Acc<AGG_WSUM, T, CPL> acc;
+    acc.reset();
+    for (int64_t cb = b; cb < e1; cb += lpr) {
+        int32_t cj = (cb + gl < e1) ? __ldg(a.colidx + cb + gl) : 0;
+        float cw = (weighted && cb + gl < e1) ? edge_weight(a, cb + gl, cj) : 1.f;
+        int n = (int)((e1 - cb) < (int64_t)lpr ? (e1 - cb) : (int64_t)lpr);
+        for (int u0 = 0; u0 < n; u0 += U) {
+            uint4 xv[U][CPL];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                int32_t j = __shfl_sync(gmask, cj, u0 + u, lpr);
+                if (u0 + u < n) {
+                    const uint4 *src = a.X + (int64_t)j * a.V + gl;
+#pragma unroll
+                    for (int c = 0; c < CPL; ++c) xv[u][c] = ldg16(src + c * lpr);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                float wt = __shfl_sync(gmask, cw, u0 + u, lpr);
+                if (u0 + u < n) acc.add(xv[u], wt, 0);
+            }
+        }
+    }
+    store_row<AGG_WSUM, T, CPL>(a, r, (int32_t)(e1 - b), acc, gl);
+}
+
+// NEIGH mapping: one warp per destination row, lanes over neighbours
+// (gather); each lane reads UC consecutive 16-byte chunks of its neighbour,
+// then a butterfly reduction across the warp per chunk (IO-aware GNN
+// layers, Section 4.1, neighbour-parallel "dot-aggr" mapping).
+template <class T>
+__global__ void __launch_bounds__(256) k_agg_neigh(AggArgs a) {
+    constexpr int NV = Chunk<T>::N;
+    constexpr int UC = 4;
+    const int lane = threadIdx.x & 31;
+    const int64_t r64 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (r64 >= a.n_rows) return;
+    const int32_t r = (int32_t)r64;
+    const int64_t b = __ldg(a.rowptr + r), e1 = __ldg(a.rowptr + r + 1);
+    const bool weighted = a.values || a.col_mode != COL_ONE;
+    const float s = row_factor(a, r, (int32_t)(e1 - b));
+    for (int c0 = 0; c0 < a.V; c0 += UC) {
+        float acc[UC][NV];
+#pragma unroll
+        for (int u = 0; u < UC; ++u)
+#pragma unroll
+            for (int k = 0; k < NV; ++k) acc[u][k] = 0.f;
+        for (int64_t e = b + lane; e < e1; e += 32) {
+            int32_t j = __ldg(a.colidx + e);
+            float wt = weighted ? edge_weight(a, e, j) : 1.f;
+            const uint4 *src = a.X + (int64_t)j * a.V + c0;
+            uint4 xv[UC];
+#pragma unroll
+            for (int u = 0; u < UC; ++u)
+                if (c0 + u < a.V) xv[u] = ldg16(src + u);
+#pragma unroll
+            for (int u = 0; u < UC; ++u) {
+                if (c0 + u >= a.V) break;
+                float f[NV];
+                Chunk<T>::unpack(xv[u], f);
+#pragma unroll
+                for (int k = 0; k < NV; ++k) acc[u][k] = fmaf(wt, f[k], acc[u][k]);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < UC; ++u)
+#pragma unroll
+            for (int k = 0; k < NV; ++k) {
+                float v = acc[u][k];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                acc[u][k] = v * s;
+            }
+        // lane u writes chunk c0+u
+#pragma unroll
+        for (int u = 0; u < UC; ++u) {
+            if (lane == u && c0 + u < a.V) {
+                float *dst = a.Y + (int64_t)r * a.F + (int64_t)(c0 + u) * NV;
+#pragma unroll
+                for (int k = 0; k < NV; k += 4)
+                    *reinterpret_cast<float4 *>(dst + k) =
+                        make_float4(acc[u][k], acc[u][k + 1], acc[u][k + 2], acc[u][k + 3]);
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------- host side
+
+struct AggShape {
+    int32_t V, lpr, cpl, E;
+};
+
+static bool agg_shape(int32_t x_dtype, int32_t F, AggShape *s) {
+    int nv = x_dtype == GNN_F32 ? 4 : 8;
+    if (F <= 0 || F % nv) return false;
+    int32_t V = F / nv;
+    if (V < 8 || V > 256 || (V & (V - 1))) return false;
+    s->V = V;
+    s->lpr = V < 32 ? V : 32;
+    s->cpl = V / s->lpr;
+    s->E = kRunEdges;
+    return true;
+}
+
+static int64_t n_workers_for(const gnn_csr *g, int32_t E) {
+    int64_t n = (g->nnz + E - 1) / E;
+    return n > 0 ? n : 1;
+}
+
+size_t agg_workspace_bytes(const gnn_csr *g, int32_t op, int32_t x_dtype_unused, int32_t F) {
+    (void)x_dtype_unused;
+    int64_t nw = n_workers_for(g, kRunEdges);
+    size_t word = op == GNN_OP_MAX ? sizeof(unsigned long long) : sizeof(float);
+    size_t b = round_up(word * (size_t)nw * (size_t)F, 256);
+    b += round_up(sizeof(int32_t) * (size_t)nw, 256);
+    return b;
+}
+
+template <int OP, class T, int CPL>
+static cudaError_t launch_staged_cpl(const AggArgs &a, cudaStream_t s) {
+    constexpr int U = CPL >= 8 ? 1 : 8 / CPL;
+    StageLayout L;
+    int32_t off = U * 32 * CPL * 16;
+    L.off_wv = (OP == AGG_WSUM && a.values) ? off : -1;
+    if (L.off_wv >= 0) off += U * 32 * 4;
+    L.off_wc = (OP == AGG_WSUM && a.col_mode != COL_ONE) ? off : -1;
+    if (L.off_wc >= 0) off += U * 32 * 4;
+    L.off_j = OP == AGG_MAX ? off : -1;
+    if (L.off_j >= 0) off += U * 32 * 4;
+    L.stage_bytes = (int32_t)round_up((size_t)off, 16);
+    // ~112 KB per 4-warp block (two blocks per SM), 3..8 stages
+    int S = (int)((112 * 1024) / (4 * L.stage_bytes));
+    L.stages = S < 3 ? 3 : (S > GNN_AGG_STAGES ? GNN_AGG_STAGES : S);
+    size_t smem = (size_t)4 * L.stages * L.stage_bytes;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(k_agg_staged<OP, T, CPL>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    int blocks = (int)((a.n_workers + 3) / 4);
+    k_agg_staged<OP, T, CPL><<<blocks, 128, smem, s>>>(a, L);
+    return cudaGetLastError();
+}
+
+template <int OP, class T>
+static cudaError_t launch_staged(const AggArgs &a, int cpl, cudaStream_t s) {
+    switch (cpl) {
+        case 1: return launch_staged_cpl<OP, T, 1>(a, s);
+        case 2: return launch_staged_cpl<OP, T, 2>(a, s);
+        case 4: return launch_staged_cpl<OP, T, 4>(a, s);
+        default: return launch_staged_cpl<OP, T, 8>(a, s);
+    }
+}
+
+template <int OP, class T>
+static void launch_auto(const AggArgs &a, int cpl, cudaStream_t s) {
+    if (a.lpr == 32 && GNN_AGG_STAGED) {
+        launch_staged<OP, T>(a, cpl, s);
+        return;
+    }
+    int64_t threads = a.n_workers * a.lpr;
+    int blocks = (int)((threads + 255) / 256);
+    if (a.lpr == 32) {
+        switch (cpl) {
+            case 1: k_agg_auto<OP, T, 1, 32><<<blocks, 256, 0, s>>>(a); break;
+            case 2: k_agg_auto<OP, T, 2, 32><<<blocks, 256, 0, s>>>(a); break;
+            case 4: k_agg_auto<OP, T, 4, 32><<<blocks, 256, 0, s>>>(a); break;
+            default: k_agg_auto<OP, T, 8, 32><<<blocks, 256, 0, s>>>(a); break;
+        }
+    } else {
+        k_agg_auto<OP, T, 1, 0><<<blocks, 256, 0, s>>>(a);
+    }
+}
+
+template <class T>
+static void launch_feat(const AggArgs &a, int cpl, cudaStream_t s) {
+    int64_t threads = (int64_t)a.n_rows * a.lpr;
+    int blocks = (int)((threads + 255) / 256);
+    switch (cpl) {
+        case 1: k_agg_feat<T, 1><<<blocks, 256, 0, s>>>(a); break;
+        case 2: k_agg_feat<T, 2><<<blocks, 256, 0, s>>>(a); break;
+        case 4: k_agg_feat<T, 4><<<blocks, 256, 0, s>>>(a); break;
+        default: k_agg_feat<T, 8><<<blocks, 256, 0, s>>>(a); break;
+    }
+}
+
+gnn_status run_aggregate(const gnn_csr *g, const void *prep, int32_t op, int32_t norm,
+                         const void *X, int32_t x_dtype, int32_t F, float *Y, int32_t *argmax,
+                         int32_t mapping, void *ws, size_t ws_bytes, void *stream) {
+    gnn_status st = check_csr_args(g);
+    if (st != GNN_OK) return st;
+    if (!Y || (!X && g->n_cols > 0)) return GNN_ERR_INVALID_ARG;
+    if (x_dtype != GNN_F32 && x_dtype != GNN_BF16) return GNN_ERR_UNSUPPORTED;
+    if (norm < GNN_NORM_NONE || norm > GNN_NORM_BOTH) return GNN_ERR_INVALID_ARG;
+    if (mapping < GNN_MAP_AUTO || mapping > GNN_MAP_NEIGH) return GNN_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(Y) || (argmax && !aligned16(argmax))) return GNN_ERR_INVALID_ARG;
+    AggShape sh;
+    if (!agg_shape(x_dtype, F, &sh)) return GNN_ERR_UNSUPPORTED;
+    if (norm != GNN_NORM_NONE && !prep) return GNN_ERR_INVALID_ARG;
+    if (g->n_rows == 0) return GNN_OK;
+
+    AggArgs a{};
+    a.rowptr = g->rowptr;
+    a.colidx = g->colidx;
+    a.values = (op == GNN_OP_SPMM) ? g->values : nullptr;
+    a.X = static_cast<const uint4 *>(X);
+    a.Y = Y;
+    a.argmax = argmax;
+    a.nnz = g->nnz;
+    a.n_rows = g->n_rows;
+    a.F = F;
+    a.V = sh.V;
+    a.lpr = sh.lpr;
+    a.E = sh.E;
+    a.n_workers = n_workers_for(g, sh.E);
+    a.col_mode = COL_ONE;
+    a.row_mode = ROW_ONE;
+    if (prep) {
+        prep_pointers(g, prep, &a.d_out, &a.dinv_in, &a.dinv_out);
+        a.run_first_row = prep_run_table(g, prep);
+    }
+    if (op == GNN_OP_SPMM) {
+        if (norm == GNN_NORM_LEFT) a.row_mode = ROW_RECIP;
+        if (norm == GNN_NORM_RIGHT) a.col_mode = COL_RECIP;
+        if (norm == GNN_NORM_BOTH) { a.row_mode = ROW_RSQRT; a.col_mode = COL_RSQRT; }
+    }
+    cudaStream_t s = as_stream(stream);
+    const bool bf = x_dtype == GNN_BF16;
+
+    if (op == GNN_OP_SPMM && mapping == GNN_MAP_FEAT) {
+        if (bf) launch_feat<__nv_bfloat16>(a, sh.cpl, s); else launch_feat<float>(a, sh.cpl, s);
+        note_launch();
+        GNN_LAUNCH_CHECK();
+        return GNN_OK;
+    }
+    if (op == GNN_OP_SPMM && mapping == GNN_MAP_NEIGH) {
+        int blocks = (int)(((int64_t)g->n_rows * 32 + 255) / 256);
+        if (bf) k_agg_neigh<__nv_bfloat16><<<blocks, 256, 0, s>>>(a);
+        else k_agg_neigh<float><<<blocks, 256, 0, s>>>(a);
+        note_launch();
+        GNN_LAUNCH_CHECK();
+        return GNN_OK;
+    }
+
+    size_t need = agg_workspace_bytes(g, op, x_dtype, F);
+    if (!ws || ws_bytes < need) return GNN_ERR_WORKSPACE;
+    if (!aligned256(ws)) return GNN_ERR_INVALID_ARG;
+    Carver cv(ws);
+    a.carry = cv.take<float>((size_t)a.n_workers * F * (op == GNN_OP_MAX ? 2 : 1));
+    a.tickets = cv.take<int32_t>((size_t)a.n_workers);
+
+    if (op == GNN_OP_MAX) {
+        if (bf) launch_auto<AGG_MAX, __nv_bfloat16>(a, sh.cpl, s);
+        else launch_auto<AGG_MAX, float>(a, sh.cpl, s);
+    } else if (op == GNN_OP_MEAN) {
+        if (bf) launch_auto<AGG_MEAN, __nv_bfloat16>(a, sh.cpl, s);
+        else launch_auto<AGG_MEAN, float>(a, sh.cpl, s);
+    } else {
+        if (bf) launch_auto<AGG_WSUM, __nv_bfloat16>(a, sh.cpl, s);
+        else launch_auto<AGG_WSUM, float>(a, sh.cpl, s);
+    }
+    note_launch();
+    GNN_LAUNCH_CHECK();
+    return GNN_OK;
+}
+
+}  // namespace gnn
+
+using namespace gnn;
+
+extern "C" {
+
+gnn_status gnn_spmm(const gnn_csr *g, const void *prep, int32_t norm, const void *X,
+                    int32_t x_dtype, int32_t F, float *Y, int32_t mapping, void *ws,
+                    size_t ws_bytes, void *stream) {
+    return run_aggregate(g, prep, GNN_OP_SPMM, norm, X, x_dtype, F, Y, nullptr, mapping, ws,
+                         ws_bytes, stream);
+}
+
+gnn_status gnn_segment_reduce_sum(const gnn_csr *g, const void *prep, const void *X,
+                                  int32_t x_dtype, int32_t F, float *Y, void *ws,
+                                  size_t ws_bytes, void *stream) {
+    return run_aggregate(g, prep, GNN_OP_SUM, GNN_NORM_NONE, X, x_dtype, F, Y, nullptr,
+                         GNN_MAP_AUTO, ws, ws_bytes, stream);
+}
+
+gnn_status gnn_segment_reduce_mean(const gnn_csr *g, const void *prep, const void *X,
+                                   int32_t x_dtype, int32_t F, float *Y, void *ws,
+                                   size_t ws_bytes, void *stream) {
+    return run_aggregate(g, prep, GNN_OP_MEAN, GNN_NORM_NONE, X, x_dtype, F, Y, nullptr,
+                         GNN_MAP_AUTO, ws, ws_bytes, stream);
+}
+
+gnn_status gnn_segment_reduce_max(const gnn_csr *g, const void *prep, const void *X,
+                                  int32_t x_dtype, int32_t F, float *Y, int32_t *argmax,
+                                  void *ws, size_t ws_bytes, void *stream) {
+    return run_aggregate(g, prep, GNN_OP_MAX, GNN_NORM_NONE, X, x_dtype, F, Y, argmax,
+                         GNN_MAP_AUTO, ws, ws_bytes, stream);
+}
+
+}  // extern "C"

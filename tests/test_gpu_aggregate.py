@@ -1,0 +1,174 @@
+"""GPU parity of steps a0-a2 (prep, SpMM, segment sum/mean/max) against the
+CPU oracle, through the C ABI.  Marked gpu."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from tests import graphs as G
+from tests.tolerance import TOL_BF16, TOL_F32, assert_rowwise_close
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def gnn():
+    if not torch.cuda.is_available():
+        pytest.fail("a GPU test was selected but torch sees no CUDA device")
+    import sparse_neighbourhood_aggregation_gb300 as m
+    m.lib()
+    return m
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def feats_to_dev(X):
+    """numpy fp32 or bf16 bits (uint16) -> CUDA tensor of the same dtype."""
+    if X.dtype == np.uint16:
+        return dev(X.view(np.int16)).view(torch.bfloat16)
+    return dev(X)
+
+
+def check_exact_max(y, am, ref_y, ref_am):
+    ref32 = ref_y.astype(np.float32)
+    assert np.array_equal(y.view(np.uint32), ref32.view(np.uint32)), "max values differ"
+    assert np.array_equal(am, ref_am), "argmax differs"
+
+
+def run_all(gnn, rp, ci, X, rows=None, tol=TOL_F32, mappings=(0, 1, 2), norms=(0, 1, 2, 3),
+            values=None):
+    g = gnn.graph_prepare(dev(rp), dev(ci), None if values is None else dev(values))
+    Xd = feats_to_dev(X)
+    sel = slice(None) if rows is None else rows
+    for norm in norms:
+        ref = oracle.spmm(rp, ci, X, norm=norm, values=values, rows=rows)
+        for mp in mappings:
+            Y = gnn.gnn_spmm(g, Xd, norm=norm, mapping=mp).cpu().numpy()
+            assert_rowwise_close(Y[sel], ref, tol, f"spmm norm={norm} map={mp}")
+    if values is not None:
+        return
+    ys = gnn.gnn_segment_reduce_sum(g, Xd).cpu().numpy()
+    assert_rowwise_close(ys[sel], oracle.segment_reduce(oracle.OP_SUM, rp, ci, X, rows=rows), tol,
+                         "sum")
+    ym = gnn.gnn_segment_reduce_mean(g, Xd).cpu().numpy()
+    assert_rowwise_close(ym[sel], oracle.segment_reduce(oracle.OP_MEAN, rp, ci, X, rows=rows), tol,
+                         "mean")
+    yx, am = gnn.gnn_segment_reduce_max(g, Xd)
+    ry, ram = oracle.segment_reduce(oracle.OP_MAX, rp, ci, X, rows=rows)
+    check_exact_max(yx.cpu().numpy()[sel], am.cpu().numpy()[sel], ry, ram)
+    return g
+
+
+def _hub_graph(n=3000, hubs=(0, 17, 2999), deg=2500, seed=0):
+    rng = np.random.default_rng(seed)
+    edges = [(int(s), h) for h in hubs for s in rng.choice(n, deg, replace=False)]
+    edges += [(int(rng.integers(n)), int(rng.integers(n))) for _ in range(4 * n)]
+    return G.from_edges(n, edges)
+
+
+@pytest.mark.parametrize("F", [32, 64, 128, 256])
+def test_tiny_graphs_fp32(gnn, F):
+    rng = np.random.default_rng(F)
+    for k, (rp, ci) in enumerate([G.random_graph(7, 0.3, 0), G.random_graph(40, 0.1, 2, False),
+                                  G.star(17), G.from_edges(9, [], self_loops=False),
+                                  G.from_edges(12, [(a, b) for a in range(12) for b in range(12)]),
+                                  G.from_edges(5, [(0, 1)], self_loops=False)]):
+        n = len(rp) - 1
+        X = rng.standard_normal((n, F)).astype(np.float32)
+        run_all(gnn, rp, ci, X)
+
+
+def test_ties_and_signed_zero_max_exact(gnn):
+    rng = np.random.default_rng(3)
+    rp, ci = _hub_graph(600, hubs=(5, 300), deg=550)
+    X = rng.integers(-3, 4, (600, 32)).astype(np.float32)
+    X[rng.random(X.shape) < 0.2] = -0.0
+    g = gnn.graph_prepare(dev(rp), dev(ci))
+    yx, am = gnn.gnn_segment_reduce_max(g, dev(X))
+    ry, ram = oracle.segment_reduce(oracle.OP_MAX, rp, ci, X)
+    check_exact_max(yx.cpu().numpy(), am.cpu().numpy(), ry, ram)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_heavy_rows_split_across_workers(gnn, dtype):
+    rp, ci = _hub_graph()
+    n = len(rp) - 1
+    if dtype == "f32":
+        X, tol = synth.normal_f32((n, 128), 1.0, 11), TOL_F32
+    else:
+        X, tol = synth.normal_bf16((n, 256), 1.0, 11), TOL_BF16
+    run_all(gnn, rp, ci, X, tol=tol)
+
+
+def test_edge_values_and_wide_features(gnn):
+    rp, ci = _hub_graph(1500, hubs=(3,), deg=1400, seed=4)
+    n = len(rp) - 1
+    vals = synth.uniform_f32(len(ci), 0.5, 2.0, 9)
+    X = synth.normal_f32((n, 512), 1.0, 12)
+    run_all(gnn, rp, ci, X, values=vals)
+    run_all(gnn, rp, ci, X, mappings=(0,), norms=(3,))
+
+
+def test_empty_graph_and_trailing_empty_rows(gnn):
+    X = np.ones((10, 32), np.float32)
+    run_all(gnn, *G.from_edges(10, [], self_loops=False), X)
+    rp, ci = G.from_edges(300, [(i, 3) for i in range(1, 290)], self_loops=False)
+    run_all(gnn, rp, ci, np.random.default_rng(0).standard_normal((300, 32)).astype(np.float32))
+
+
+def test_config1_er(gnn):
+    w = synth.workload("c1_er1k")
+    run_all(gnn, w["rowptr"], w["colidx"], w["X"])
+
+
+def test_config2_rmat17_sampled(gnn):
+    w = synth.workload("c2_rmat17")
+    rp, ci, X = w["rowptr"], w["colidx"], w["X"]
+    deg = np.diff(rp)
+    rng = np.random.default_rng(0)
+    # the heaviest rows, rows whose edges cross run boundaries, random rows
+    heavy = np.argsort(-deg, kind="stable")[:24]
+    bnd = np.searchsorted(rp, np.arange(256, len(ci), 256 * 97), side="right") - 1
+    rows = np.unique(np.concatenate([heavy, bnd, rng.choice(len(deg), 400, replace=False),
+                                     [0, len(deg) - 1]])).astype(np.int32)
+    run_all(gnn, rp, ci, X, rows=rows)
+
+
+def test_repeat_calls_reuse_the_workspace(gnn):
+    # max is bit-identical run to run; sums of heavy rows are folded with fp32
+    # atomics, so repeats agree to rounding; both show the workspace slots and
+    # tickets are left zeroed for the next call
+    w = synth.workload("c2_rmat17")
+    g = gnn.graph_prepare(dev(w["rowptr"]), dev(w["colidx"]))
+    Xd = dev(w["X"])
+    a = gnn.gnn_spmm(g, Xd).cpu().numpy()
+    b = gnn.gnn_spmm(g, Xd).cpu().numpy()
+    assert_rowwise_close(b, a, 1e-6, "spmm repeat")
+    m1, i1 = gnn.gnn_segment_reduce_max(g, Xd)
+    m2, i2 = gnn.gnn_segment_reduce_max(g, Xd)
+    assert torch.equal(m1, m2) and torch.equal(i1, i2)
+
+
+def test_validate_flags_bad_csr(gnn):
+    rp = np.array([0, 2, 3], np.int32)
+    ci = np.array([1, 0, 5], np.int32)  # column 5 out of range, row 0 unsorted
+    g = gnn.Graph(dev(rp), dev(ci), prepare=False)
+    assert gnn.csr_validate(g) == gnn.GNN_ERR_DEVICE_CHECK
+    rp2, ci2 = G.random_graph(30, 0.2, 1)
+    assert gnn.csr_validate(gnn.Graph(dev(rp2), dev(ci2), prepare=False)) == 0
+
+
+def test_host_validation_rejects_bad_arguments(gnn):
+    rp, ci = G.random_graph(30, 0.2, 1)
+    g = gnn.graph_prepare(dev(rp), dev(ci))
+    with pytest.raises(gnn.GnnError) as e:
+        gnn.gnn_spmm(g, dev(np.ones((30, 12), np.float32)))      # F=12: 3 chunks
+    assert e.value.code == gnn.GNN_ERR_UNSUPPORTED
+    X = torch.ones(30 * 32 + 1, device="cuda")[1:].view(30, 32)  # misaligned rows
+    with pytest.raises(gnn.GnnError) as e:
+        gnn.gnn_segment_reduce_sum(g, X)
+    assert e.value.code == gnn.GNN_ERR_INVALID_ARG
