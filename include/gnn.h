@@ -141,6 +141,38 @@ gnn_status gnn_segment_reduce_sum(const gnn_csr *g, const void *prep, const void
                                   int32_t x_dtype, int32_t F, float *Y, void *ws,
                                   size_t ws_bytes, void *stream);
 
+/* Segment sum without a caller workspace.  The paper has no counterpart to
+ * this entry point; it exists for callers that cannot allocate device
+ * memory themselves: a plugin inside a host framework that owns every device
+ * allocation and hands the plugin only its input and output buffers, or a
+ * latency-critical loop that must not pay for cudaMalloc's implicit device
+ * synchronisation.
+ *
+ * Computes exactly what gnn_segment_reduce_sum computes, through the same
+ * kernel, but its scratch space (heavy-row partial sums and their arrival
+ * counters) is a fixed library-owned device array of
+ * GNN_NOALLOC_SCRATCH_BYTES bytes.  Every GPU that loads the library holds
+ * that array until the process exits.  The call allocates nothing: no
+ * cudaMalloc, no cudaFree, no allocating library routine.
+ *
+ * Size limit: the problem must satisfy
+ *   gnn_workspace_size(GNN_OP_SUM, g, F, 0, 0) <= GNN_NOALLOC_SCRATCH_BYTES
+ * (roughly nnz / 64 * (4 F + 4) bytes; about one million edges at F = 128
+ * fp32); larger problems are rejected with GNN_ERR_WORKSPACE before any
+ * launch.  Other arguments, validation and errors are as for
+ * gnn_segment_reduce_sum.
+ *
+ * The first call on a device, with that device current, looks up the
+ * array's device address (cudaGetSymbolAddress) and caches it; make that
+ * first call before any stream capture.  Each call clears the part of the
+ * array it uses (cudaMemsetAsync on `stream`) before its kernel runs.  All
+ * calls on a device share the one array, which keeps the last call's
+ * contents: calls that may overlap on the GPU (different streams without
+ * ordering between them) race on it and give wrong results. */
+#define GNN_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+gnn_status gnn_segment_reduce_sum_noalloc(const gnn_csr *g, const void *prep, const void *X,
+                                          int32_t x_dtype, int32_t F, float *Y, void *stream);
+
 /* Y[i,:] = (sum over j in N(i) of X[j,:]) / d_in(i); empty rows give 0. */
 gnn_status gnn_segment_reduce_mean(const gnn_csr *g, const void *prep, const void *X,
                                    int32_t x_dtype, int32_t F, float *Y, void *ws,

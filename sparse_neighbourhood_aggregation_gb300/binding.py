@@ -59,6 +59,7 @@ _SIGS = {
     "gnn_workspace_size": (ctypes.c_size_t, ["i32", "csr", "i32", "i32", "i32"]),
     "gnn_spmm": (ctypes.c_int, ["csr", "p", "i32", "p", "i32", "i32", "p", "i32", "p", "sz", "p"]),
     "gnn_segment_reduce_sum": (ctypes.c_int, ["csr", "p", "p", "i32", "i32", "p", "p", "sz", "p"]),
+    "gnn_segment_reduce_sum_noalloc": (ctypes.c_int, ["csr", "p", "p", "i32", "i32", "p", "p"]),
     "gnn_segment_reduce_mean": (ctypes.c_int, ["csr", "p", "p", "i32", "i32", "p", "p", "sz", "p"]),
     "gnn_segment_reduce_max": (ctypes.c_int, ["csr", "p", "p", "i32", "i32", "p", "p", "p", "sz",
                                               "p"]),
@@ -202,6 +203,20 @@ def _reduce(name, op, g, X, out, stream):
 
 def gnn_segment_reduce_sum(g: Graph, X, out=None, stream=None):
     return _reduce("gnn_segment_reduce_sum", GNN_OP_SUM, g, X, out, stream)
+
+
+def gnn_segment_reduce_sum_noalloc(g: Graph, X, out=None, stream=None):
+    """Segment sum whose scratch is the library's fixed device array instead
+    of a workspace (no device allocation by the library; the output is still
+    allocated here unless `out` is given)."""
+    _require_cuda(X)
+    F = X.shape[1]
+    Y = out if out is not None else torch.empty((g.n_rows, F), dtype=torch.float32,
+                                                device=X.device)
+    _check("gnn_segment_reduce_sum_noalloc", lib().gnn_segment_reduce_sum_noalloc(
+        ctypes.byref(g.csr), _ptr(g.prep), X.data_ptr(), _dtype_code(X), F, Y.data_ptr(),
+        _stream(stream)))
+    return Y
 
 
 def gnn_segment_reduce_mean(g: Graph, X, out=None, stream=None):
