@@ -116,6 +116,11 @@ typedef enum {
     GNN_OP_BLOCKSPARSE = 8
 } gnn_op;
 
+/* OR-ed into `op` of gnn_workspace_size: size the workspace for bf16 inputs
+ * (the attention ops keep their projected features in the input dtype);
+ * without it attention workspaces are sized for fp32 inputs. */
+#define GNN_OP_FLAG_BF16 0x100
+
 /* Workspace bytes needed by operation `op` on g with feature width F (or
  * heads x head_dim for attention; F is then F_in for GATv2).  Host call. */
 size_t gnn_workspace_size(int32_t op, const gnn_csr *g, int32_t F, int32_t heads,

@@ -246,3 +246,69 @@ def launch_count() -> int:
 
 def version() -> str:
     return lib().gnn_version().decode()
+
+
+GNN_OP_FLAG_BF16 = 0x100
+
+
+def _ws_op(op: int, t: torch.Tensor) -> int:
+    return op | (GNN_OP_FLAG_BF16 if t.dtype == torch.bfloat16 else 0)
+
+
+def gnn_projection(H: torch.Tensor, W: torch.Tensor, out=None, stream=None):
+    """C = H W (bf16: tcgen05 tensor cores, fp32 accumulation, bf16 out;
+    fp32: fp32 FMA)."""
+    _require_cuda(H, W)
+    n, F_in = H.shape
+    F_out = W.shape[1]
+    C = out if out is not None else torch.empty((n, F_out), dtype=H.dtype, device=H.device)
+    _check("gnn_projection", lib().gnn_projection(H.data_ptr(), _dtype_code(H), n, F_in,
+                                                  W.data_ptr(), F_out, C.data_ptr(),
+                                                  _stream(stream)))
+    return C
+
+
+def gnn_gatv2_fwd(g: Graph, H: torch.Tensor, W_l: torch.Tensor, a: torch.Tensor, heads: int,
+                  head_dim: int, neg_slope: float = 0.2, W_r=None, want_lse: bool = True,
+                  out=None, lse=None, stream=None):
+    """Fused GATv2 forward: returns (out [n, heads*head_dim] fp32, lse [n,
+    heads] fp32 or None)."""
+    _require_cuda(H, W_l, W_r, a)
+    if a.dtype != torch.float32:
+        raise TypeError("a must be fp32")
+    HD = heads * head_dim
+    o = out if out is not None else torch.empty((g.n_rows, HD), dtype=torch.float32,
+                                                device=H.device)
+    L = None
+    if want_lse:
+        L = lse if lse is not None else torch.empty((g.n_rows, heads), dtype=torch.float32,
+                                                    device=H.device)
+    ws = g.workspace(_ws_op(GNN_OP_GATV2, H), H.shape[1], heads, head_dim)
+    _check("gnn_gatv2_fwd", lib().gnn_gatv2_fwd(
+        ctypes.byref(g.csr), _ptr(g.prep), H.data_ptr(), _dtype_code(H), H.shape[1],
+        W_l.data_ptr(), _ptr(W_r), a.data_ptr(), heads, head_dim, float(neg_slope),
+        o.data_ptr(), _ptr(L), ws.data_ptr(), ws.numel(), _stream(stream)))
+    return o, L
+
+
+def gnn_gt_attn_fwd(g: Graph, Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, heads: int,
+                    head_dim: int, scale: float, bs=None, want_lse: bool = True, out=None,
+                    lse=None, stream=None):
+    """Graph Transformer attention: returns (out fp32 [n, heads*head_dim],
+    lse fp32 [n, heads] or None).  bs: a BlockSparse from
+    gnn_blocksparse_build for the tensor-core tile path, or None (CSR)."""
+    _require_cuda(Q, K, V)
+    HD = heads * head_dim
+    o = out if out is not None else torch.empty((g.n_rows, HD), dtype=torch.float32,
+                                                device=Q.device)
+    L = None
+    if want_lse:
+        L = lse if lse is not None else torch.empty((g.n_rows, heads), dtype=torch.float32,
+                                                    device=Q.device)
+    ws = g.workspace(_ws_op(GNN_OP_GT, Q), 0, heads, head_dim, key="bs" if bs is not None else None)
+    bsp = ctypes.byref(bs.meta) if bs is not None else None
+    _check("gnn_gt_attn_fwd", lib().gnn_gt_attn_fwd(
+        ctypes.byref(g.csr), _ptr(g.prep), bsp, Q.data_ptr(), K.data_ptr(), V.data_ptr(),
+        _dtype_code(Q), heads, head_dim, float(scale), o.data_ptr(), _ptr(L), ws.data_ptr(),
+        ws.numel(), _stream(stream)))
+    return o, L

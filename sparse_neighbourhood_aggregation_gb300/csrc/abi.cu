@@ -4,7 +4,8 @@
 
 namespace gnn {
 size_t agg_workspace_bytes(const gnn_csr *g, int32_t op, int32_t x_dtype, int32_t F);
-size_t gatv2_workspace_bytes(const gnn_csr *g, int32_t F_in, int32_t heads, int32_t head_dim);
+size_t gatv2_workspace_bytes(const gnn_csr *g, int32_t F_in, int32_t heads, int32_t head_dim,
+                             int32_t esize);
 size_t gt_workspace_bytes(const gnn_csr *g, int32_t heads, int32_t head_dim);
 size_t reorder_workspace_bytes(const gnn_csr *g);
 size_t apply_perm_workspace_bytes(const gnn_csr *g);
@@ -17,14 +18,15 @@ using namespace gnn;
 extern "C" size_t gnn_workspace_size(int32_t op, const gnn_csr *g, int32_t F, int32_t heads,
                                      int32_t head_dim) {
     if (check_csr_args(g) != GNN_OK) return 0;
-    switch (op) {
+    const int32_t esize = (op & GNN_OP_FLAG_BF16) ? 2 : 4;
+    switch (op & ~GNN_OP_FLAG_BF16) {
         case GNN_OP_SPMM:
         case GNN_OP_SUM:
         case GNN_OP_MEAN:
         case GNN_OP_MAX:
             return agg_workspace_bytes(g, op, GNN_F32, F);
         case GNN_OP_GATV2:
-            return gatv2_workspace_bytes(g, F, heads, head_dim);
+            return gatv2_workspace_bytes(g, F, heads, head_dim, esize);
         case GNN_OP_GT:
             return gt_workspace_bytes(g, heads, head_dim);
         case GNN_OP_REORDER:

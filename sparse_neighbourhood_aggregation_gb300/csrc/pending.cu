@@ -3,25 +3,18 @@
 #include "common.cuh"
 
 namespace gnn {
-size_t gatv2_workspace_bytes(const gnn_csr *, int32_t, int32_t, int32_t) { return 0; }
-size_t gt_workspace_bytes(const gnn_csr *, int32_t, int32_t) { return 0; }
 size_t reorder_workspace_bytes(const gnn_csr *) { return 0; }
 size_t apply_perm_workspace_bytes(const gnn_csr *) { return 0; }
 size_t blocksparse_workspace_bytes(const gnn_csr *) { return 0; }
+
+gnn_status gt_attn_tiles(const gnn_csr *, const gnn_blocksparse *, const void *, const void *,
+                         const void *, int32_t, int32_t, float, float *, float *, void *, size_t,
+                         cudaStream_t) {
+    return GNN_ERR_UNSUPPORTED;
+}
 }  // namespace gnn
 
 extern "C" {
-
-gnn_status gnn_projection(const void *, int32_t, int64_t, int32_t, const void *, int32_t, void *,
-                          void *) {
-    return GNN_ERR_UNSUPPORTED;
-}
-
-gnn_status gnn_gatv2_fwd(const gnn_csr *, const void *, const void *, int32_t, int32_t,
-                         const void *, const void *, const float *, int32_t, int32_t, float,
-                         float *, float *, void *, size_t, void *) {
-    return GNN_ERR_UNSUPPORTED;
-}
 
 gnn_status gnn_blocksparse_plan(const gnn_csr *, float, void *, size_t, gnn_blocksparse *,
                                 size_t *, void *) {
@@ -30,12 +23,6 @@ gnn_status gnn_blocksparse_plan(const gnn_csr *, float, void *, size_t, gnn_bloc
 
 gnn_status gnn_blocksparse_build(const gnn_csr *, gnn_blocksparse *, void *, size_t, void *,
                                  size_t, void *) {
-    return GNN_ERR_UNSUPPORTED;
-}
-
-gnn_status gnn_gt_attn_fwd(const gnn_csr *, const void *, const gnn_blocksparse *, const void *,
-                           const void *, const void *, int32_t, int32_t, int32_t, float, float *,
-                           float *, void *, size_t, void *) {
     return GNN_ERR_UNSUPPORTED;
 }
 

@@ -51,7 +51,8 @@ def assert_lse_close(got, ref, tol, what="lse"):
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
     both_inf = np.isneginf(got) & np.isneginf(ref)
-    d = np.where(both_inf, 0.0, np.abs(got - ref))
+    with np.errstate(invalid="ignore"):
+        d = np.where(both_inf, 0.0, np.abs(got - ref))
     d = np.where(np.isnan(d), np.inf, d)
     if np.max(d, initial=0.0) > tol:
         i = np.unravel_index(int(np.argmax(d)), d.shape)
