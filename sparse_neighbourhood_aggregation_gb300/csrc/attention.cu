@@ -401,10 +401,15 @@ __global__ void __launch_bounds__(256) k_gatv2_linear(const T *__restrict__ C, i
     }
 }
 
-// coef[c] = (1-s)/2 * a[c] * log2e
-__global__ void k_gatv2_coef(const float *__restrict__ a, int32_t HD, float half_1ms, float *__restrict__ coef) {
+// coef[c] = (1-s)/2 a[c] log2e (the |.| part), lin[c] = (1+s)/2 a[c] log2e
+// (the linear part)
+__global__ void k_gatv2_coef(const float *__restrict__ a, int32_t HD, float half_1ms, float half_1ps,
+                             float *__restrict__ coef, float *__restrict__ lin) {
     const int32_t c = blockIdx.x * blockDim.x + threadIdx.x;
-    if (c < HD) coef[c] = a[c] * half_1ms * kLog2e;
+    if (c < HD) {
+        coef[c] = a[c] * half_1ms * kLog2e;
+        lin[c] = a[c] * half_1ps * kLog2e;
+    }
 }
 
 // ---------------------------------------------------------------- SIMT GEMM
@@ -468,6 +473,8 @@ __global__ void __launch_bounds__(256) k_proj_simt(const T *__restrict__ H, cons
 // GNN_ERR_UNSUPPORTED for shapes it does not cover.
 gnn_status projection_tc(const void *H, int64_t n, int32_t F_in, const void *W, int32_t F_out,
                          void *C, cudaStream_t s);
+gnn_status projection_tc_lin(const void *H, int64_t n, int32_t Fi, const void *W, int32_t Fo, void *C,
+                             const float *lin_coef, int32_t heads, int32_t D, float *lin_out, cudaStream_t s);
 
 static gnn_status projection_any(const void *H, int32_t dtype, int64_t n, int32_t F_in, const void *W,
                                  int32_t F_out, void *C, cudaStream_t s) {
@@ -499,7 +506,7 @@ static size_t attn_slot_bytes(const gnn_csr *g, int32_t heads, int32_t head_dim)
 
 struct GatLayout {
     void *l, *r;
-    float *Al, *Ar, *coef, *slots;
+    float *Al, *Ar, *coef, *lin, *slots;
     int32_t *tickets;
     size_t bytes;
 };
@@ -515,6 +522,7 @@ static GatLayout gat_layout(const gnn_csr *g, void *base, int32_t esize, bool se
     L.Al = c.take<float>((size_t)g->n_cols * heads);
     L.Ar = separate ? c.take<float>((size_t)g->n_cols * heads) : L.Al;
     L.coef = c.take<float>(HD);
+    L.lin = c.take<float>(HD);
     L.slots = c.take<float>((size_t)2 * nw * (size_t)slot_stride((int32_t)HD, heads));
     L.tickets = c.take<int32_t>((size_t)nw);
     L.bytes = c.used;
@@ -606,33 +614,35 @@ gnn_status gnn_gatv2_fwd(const gnn_csr *g, const void *prep, const void *H, int3
     const int32_t HD = heads * head_dim;
     const int64_t n = g->n_cols;
 
-    // a3: projections l = H W_l (and r = H W_r)
-    st = projection_any(H, dtype, n, F_in, W_l, HD, WL.l, s);
-    if (st != GNN_OK) return st;
-    if (separate) {
-        st = projection_any(H, dtype, n, F_in, W_r, HD, WL.r, s);
-        if (st != GNN_OK) return st;
-    }
-    // per-node linear parts and per-channel |.| coefficients
+    // coefficients of the |.| part and of the per-node linear parts
     const float half_1ps = 0.5f * (1.f + neg_slope), half_1ms = 0.5f * (1.f - neg_slope);
-    const int lin_blocks = (int)((n * 32 + 255) / 256);
-    if (dtype == GNN_F32) {
-        k_gatv2_linear<float><<<lin_blocks, 256, 0, s>>>(static_cast<const float *>(WL.l), n, heads, head_dim, a,
-                                                          half_1ps, WL.Al);
-        if (separate)
-            k_gatv2_linear<float><<<lin_blocks, 256, 0, s>>>(static_cast<const float *>(WL.r), n, heads, head_dim,
-                                                              a, half_1ps, WL.Ar);
-    } else {
-        k_gatv2_linear<__nv_bfloat16><<<lin_blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(WL.l), n,
-                                                                  heads, head_dim, a, half_1ps, WL.Al);
-        if (separate)
-            k_gatv2_linear<__nv_bfloat16><<<lin_blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(WL.r), n,
-                                                                      heads, head_dim, a, half_1ps, WL.Ar);
-    }
-    note_launch(separate ? 2 : 1);
-    k_gatv2_coef<<<(HD + 255) / 256, 256, 0, s>>>(a, HD, half_1ms, WL.coef);
+    k_gatv2_coef<<<(HD + 255) / 256, 256, 0, s>>>(a, HD, half_1ms, half_1ps, WL.coef, WL.lin);
     note_launch();
     GNN_LAUNCH_CHECK();
+    // a3: projections l = H W_l (and r = H W_r) with the linear parts A_l, A_r
+    const void *Ws[2] = {W_l, W_r};
+    void *Cs[2] = {WL.l, WL.r};
+    float *As[2] = {WL.Al, WL.Ar};
+    for (int k = 0; k < (separate ? 2 : 1); ++k) {
+        st = GNN_ERR_UNSUPPORTED;
+        if (dtype == GNN_BF16)
+            st = projection_tc_lin(H, n, F_in, Ws[k], HD, Cs[k], WL.lin, heads, head_dim, As[k], s);
+        if (st == GNN_ERR_UNSUPPORTED) {
+            st = projection_any(H, dtype, n, F_in, Ws[k], HD, Cs[k], s);
+            if (st != GNN_OK) return st;
+            const int lin_blocks = (int)((n * 32 + 255) / 256);
+            if (dtype == GNN_F32)
+                k_gatv2_linear<float><<<lin_blocks, 256, 0, s>>>(static_cast<const float *>(Cs[k]), n, heads,
+                                                                  head_dim, a, half_1ps, As[k]);
+            else
+                k_gatv2_linear<__nv_bfloat16><<<lin_blocks, 256, 0, s>>>(
+                    static_cast<const __nv_bfloat16 *>(Cs[k]), n, heads, head_dim, a, half_1ps, As[k]);
+            note_launch();
+            GNN_LAUNCH_CHECK();
+        } else if (st != GNN_OK) {
+            return st;
+        }
+    }
 
     AttnArgs A{};
     A.rowptr = g->rowptr;
