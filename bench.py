@@ -1,20 +1,30 @@
 #!/usr/bin/env python3
 """Benchmark of the CSR neighbourhood-aggregation hot path on GB300.
 
-Default workload (one "step" = one pass of the layer set over one synthetic
-input, all kernels through the C ABI):
-  c2_rmat17: R-MAT scale 17 (131,072 nodes, edge factor 16, duplicates
-  removed, self-loops added), X fp32 N(0,1) [N,128]; GCN SpMM (symmetric
-  normalisation) + segment sum + mean + max(+argmax).
-Other workloads (--workload): c3_rmat20_gatv2, c4_clustered_gt, c5_rmat22.
+A "step" is one pass of a workload's layers over one synthetic input, every
+kernel launched through the C ABI (include/gnn.h) by the Python binding:
+
+  c2_rmat17 (default): R-MAT scale 17 (131,072 nodes, edge factor 16,
+      a,b,c,d = .57,.19,.19,.05, duplicates removed, self-loops added),
+      X fp32 N(0,1) [N,128]; GCN SpMM (symmetric normalisation), segment
+      sum, mean and max (+argmax), degree-aware edge-run mapping.
+  c3_rmat20_gatv2: R-MAT scale 20, H bf16 [N,256], W bf16 [256,256],
+      4 heads x 64; one fused GATv2 forward (tcgen05 projection + fused
+      score / online softmax / aggregate).
+  c4_clustered_gt: clustered graph 1024 x 256 nodes (p = 0.3, 1% rewired),
+      Q, K, V bf16 [N, 8x32]; Graph Transformer attention, CSR path.
+  c5_rmat22: R-MAT scale 22, X bf16 [N,256]; GCN SpMM.
 
 Prints ONE JSON line (rank 0).  Metric: aggregation Gedge*feat/s = edges x
-features aggregated per second, summed over the step's layers.  Timing:
-CUDA events on the launching stream around each step, L2 flushed (256 MB
-write) between timed steps outside the events; max over ranks.
+features aggregated per second, summed over the step's layers (attention:
+edges x heads x head_dim).  Timing: CUDA events on the launching stream;
+an L2 flush (a 512 MB write) precedes every timed step outside the events;
+max over ranks.  The roofline object describes the step's dominant kernel:
+achieved = its compulsory bytes (indices read once, every feature row read
+once, every output written once) / its mean event-timed duration.
 
---impl reference times the CPU oracle (the plain single-threaded C
-definition) on the host cores on a bounded row sample of the same workload.
+--impl reference times the CPU oracle (plain single-threaded C, fp64) on a
+bounded sample of destination rows of the same workload.
 """
 from __future__ import annotations
 
@@ -33,6 +43,8 @@ sys.path.insert(0, ROOT)
 
 FALLBACK_HBM_GBS = 6800.0
 NORTH_STAR_HBM_GBS = 8000.0
+METRIC = "aggregation Gedge*feat/s"
+UNIT = "Gedge*feat/s"
 
 
 def measured_peaks():
@@ -103,65 +115,187 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- workloads
 
-def c2_setup(torch, gnn, w):
-    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
-    g = gnn.graph_prepare(dev(w["rowptr"]), dev(w["colidx"]))
-    X = dev(w["X"])
+class Layer:
+    """One API call of the step: fn(inputs) launches it; units = edge x
+    feature products it aggregates; bcomp = its compulsory bytes."""
+
+    def __init__(self, name, fn, units, bcomp, bound="hbm"):
+        self.name, self.fn, self.units, self.bcomp, self.bound = name, fn, units, bcomp, bound
+
+
+class Workload:
+    def __init__(self, name, layers, inputs, outputs, config, dtype, oracle_step, sample_rows,
+                 extra=None):
+        self.name = name
+        self.layers = layers
+        self.inputs = inputs        # device tensors a step reads (copied from host in e2e)
+        self.outputs = outputs      # device tensors a step writes (read back in e2e)
+        self.config = config
+        self.dtype = dtype
+        self.oracle_step = oracle_step
+        self.sample_rows = sample_rows
+        self.extra = extra or {}
+
+    def step(self, ins=None, events=None):
+        ins = self.inputs if ins is None else ins
+        for L in self.layers:
+            if events is not None:
+                events[L.name][0].record()
+            L.fn(ins)
+            if events is not None:
+                events[L.name][1].record()
+
+
+def _dev(torch, a):
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).cuda().view(torch.bfloat16)
+    return torch.from_numpy(a).cuda()
+
+
+def _sample_by_edges(rp, target_edges, seed=0):
+    """Destination rows in a fixed random order until ~target_edges edges."""
+    n = len(rp) - 1
+    order = np.random.default_rng(seed).permutation(n)
+    cum = np.cumsum(np.diff(rp)[order])
+    k = int(np.searchsorted(cum, target_edges)) + 1
+    rows = np.sort(order[:k]).astype(np.int32)
+    return rows, int(np.sum(rp[rows + 1] - rp[rows]))
+
+
+def setup_c2(torch, gnn, w):
+    g = gnn.graph_prepare(_dev(torch, w["rowptr"]), _dev(torch, w["colidx"]))
+    X = _dev(torch, w["X"])
     n, F = X.shape
     M = len(w["colidx"])
     outs = {k: torch.empty((n, F), dtype=torch.float32, device="cuda")
             for k in ("spmm", "sum", "mean", "max")}
     am = torch.empty((n, F), dtype=torch.int32, device="cuda")
-
-    def step(Xin=None, events=None):
-        Xs = X if Xin is None else Xin
-        if events is not None:
-            events["spmm"][0].record()
-        gnn.gnn_spmm(g, Xs, norm=gnn.GNN_NORM_BOTH, out=outs["spmm"])
-        if events is not None:
-            events["spmm"][1].record()
-            events["sum"][0].record()
-        gnn.gnn_segment_reduce_sum(g, Xs, out=outs["sum"])
-        if events is not None:
-            events["sum"][1].record()
-            events["mean"][0].record()
-        gnn.gnn_segment_reduce_mean(g, Xs, out=outs["mean"])
-        if events is not None:
-            events["mean"][1].record()
-            events["max"][0].record()
-        gnn.gnn_segment_reduce_max(g, Xs, out=outs["max"], argmax=am)
-        if events is not None:
-            events["max"][1].record()
-
     idx = 4 * (n + 1) + 4 * M
-    xb = X.numel() * X.element_size()
-    yb = n * F * 4
-    bcomp = {"spmm": idx + xb + yb + 8 * n, "sum": idx + xb + yb, "mean": idx + xb + yb,
-             "max": idx + xb + yb + n * F * 4}
-    info = {"units_per_step": 4 * M * F, "unit": "Gedge*feat/s", "dtype": "f32",
-            "bcomp": bcomp, "n": n, "nnz": M, "F": F, "X": X, "outputs": list(outs.values()) + [am],
-            "config": {"workload": "c2_rmat17", "graph": "R-MAT scale 17, edge factor 16, "
-                       "a,b,c,d=.57,.19,.19,.05, dedup + self-loops", "nodes": n, "edges": M,
-                       "features": F, "layers": ["gcn_spmm", "segment_sum", "segment_mean",
-                                                 "segment_max+argmax"],
-                       "mapping": "auto (degree-aware edge runs)", "l2": "flushed between steps"}}
-    return step, info
+    xb, yb = X.numel() * X.element_size(), n * F * 4
+    layers = [
+        Layer("spmm", lambda ins: gnn.gnn_spmm(g, ins[0], norm=gnn.GNN_NORM_BOTH,
+                                               out=outs["spmm"]), M * F, idx + xb + yb + 8 * n),
+        Layer("sum", lambda ins: gnn.gnn_segment_reduce_sum(g, ins[0], out=outs["sum"]), M * F,
+              idx + xb + yb),
+        Layer("mean", lambda ins: gnn.gnn_segment_reduce_mean(g, ins[0], out=outs["mean"]), M * F,
+              idx + xb + yb),
+        Layer("max", lambda ins: gnn.gnn_segment_reduce_max(g, ins[0], out=outs["max"],
+                                                            argmax=am), M * F,
+              idx + xb + yb + n * F * 4),
+    ]
+
+    def oracle_step(rows):
+        import oracle
+        rp, ci, Xh = w["rowptr"], w["colidx"], w["X"]
+        oracle.spmm(rp, ci, Xh, norm=oracle.NORM_BOTH, rows=rows)
+        oracle.segment_reduce(oracle.OP_SUM, rp, ci, Xh, rows=rows)
+        oracle.segment_reduce(oracle.OP_MEAN, rp, ci, Xh, rows=rows)
+        oracle.segment_reduce(oracle.OP_MAX, rp, ci, Xh, rows=rows)
+
+    cfg = {"workload": "c2_rmat17", "graph": "R-MAT scale 17, edge factor 16, "
+           "a,b,c,d=.57,.19,.19,.05, dedup + self-loops", "nodes": n, "edges": M, "features": F,
+           "x_dtype": "fp32", "layers": ["gcn_spmm", "segment_sum", "segment_mean",
+                                         "segment_max+argmax"],
+           "mapping": "auto (degree-aware edge runs)"}
+    # ~4 x 8.3M edge-rows of oracle work (all rows): ~10 s on one core
+    rows = np.arange(n, dtype=np.int32)
+    return Workload("c2_rmat17", layers, [X], list(outs.values()) + [am], cfg, "f32",
+                    oracle_step, (rows, M))
 
 
-def oracle_step_c2(w, rows):
-    import oracle
-    rp, ci, X = w["rowptr"], w["colidx"], w["X"]
-    oracle.spmm(rp, ci, X, norm=oracle.NORM_BOTH, rows=rows)
-    oracle.segment_reduce(oracle.OP_SUM, rp, ci, X, rows=rows)
-    oracle.segment_reduce(oracle.OP_MEAN, rp, ci, X, rows=rows)
-    oracle.segment_reduce(oracle.OP_MAX, rp, ci, X, rows=rows)
+def setup_c3(torch, gnn, w):
+    g = gnn.graph_prepare(_dev(torch, w["rowptr"]), _dev(torch, w["colidx"]))
+    H = _dev(torch, w["H"])
+    W = _dev(torch, w["W"])
+    a = _dev(torch, w["a"])
+    n = H.shape[0]
+    M = len(w["colidx"])
+    heads, D = w["heads"], w["head_dim"]
+    HD = heads * D
+    out = torch.empty((n, HD), dtype=torch.float32, device="cuda")
+    lse = torch.empty((n, heads), dtype=torch.float32, device="cuda")
+    C = torch.empty((n, HD), dtype=torch.bfloat16, device="cuda")
+    idx = 4 * (n + 1) + 4 * M
+    # fused layer: H read, C written then read once, out + lse written, indices read
+    b_proj = n * 256 * 2 + n * HD * 2 + 256 * HD * 2 + n * heads * 4
+    b_attn = idx + n * HD * 2 + n * HD * 4 + n * heads * 4 + 2 * n * heads * 4
+    layers = [Layer("gatv2_fwd", lambda ins: gnn.gnn_gatv2_fwd(g, ins[0], W, a, heads, D,
+                                                               w["slope"], out=out, lse=lse),
+                    M * HD, b_proj + b_attn, "alu")]
+
+    def proj_only():
+        gnn.gnn_projection(H, W, out=C)
+
+    def oracle_step(rows):
+        import oracle
+        oracle.gatv2(w["rowptr"], w["colidx"], w["H"], w["W"], w["a"], heads, D, w["slope"],
+                     rows=rows)
+
+    cfg = {"workload": "c3_rmat20_gatv2", "graph": "R-MAT scale 20, edge factor 16, dedup + "
+           "self-loops", "nodes": n, "edges": M, "heads": heads, "head_dim": D, "f_in": 256,
+           "dtype": "bf16 H, W and C; fp32 softmax and accumulation; fp32 out",
+           "layers": ["tcgen05 projection + fused GATv2 (score, online softmax, aggregate)"]}
+    rows = _sample_by_edges(w["rowptr"], 40000)
+    return Workload("c3_rmat20_gatv2", layers, [H], [out, lse], cfg, "bf16", oracle_step, rows,
+                    extra={"proj_only": (proj_only, b_proj), "b_attn": b_attn,
+                           "unfused": (g, H, W, a, heads, D, w["slope"])})
 
 
-def sample_rows(w, frac_den=8):
-    n = len(w["rowptr"]) - 1
-    rows = np.arange(0, n, frac_den, dtype=np.int32)
-    ne = int(np.sum(w["rowptr"][rows + 1] - w["rowptr"][rows]))
-    return rows, ne
+def setup_c4(torch, gnn, w):
+    g = gnn.graph_prepare(_dev(torch, w["rowptr"]), _dev(torch, w["colidx"]))
+    Q, K, V = (_dev(torch, w[k]) for k in ("Q", "K", "V"))
+    n = Q.shape[0]
+    M = len(w["colidx"])
+    heads, D = w["heads"], w["head_dim"]
+    HD = heads * D
+    out = torch.empty((n, HD), dtype=torch.float32, device="cuda")
+    lse = torch.empty((n, heads), dtype=torch.float32, device="cuda")
+    idx = 4 * (n + 1) + 4 * M
+    bcomp = idx + 3 * n * HD * 2 + n * HD * 4 + n * heads * 4
+    layers = [Layer("gt_csr", lambda ins: gnn.gnn_gt_attn_fwd(g, ins[0], ins[1], ins[2], heads, D,
+                                                              w["scale"], out=out, lse=lse),
+                    M * HD, bcomp, "alu")]
+
+    def oracle_step(rows):
+        import oracle
+        oracle.gt(w["rowptr"], w["colidx"], w["Q"], w["K"], w["V"], heads, D, w["scale"],
+                  rows=rows)
+
+    cfg = {"workload": "c4_clustered_gt", "graph": "1024 clusters x 256 nodes, p=0.3, 1% of "
+           "sources rewired, dedup + self-loops", "nodes": n, "edges": M, "heads": heads,
+           "head_dim": D, "dtype": "bf16 Q, K, V; fp32 softmax and accumulation; fp32 out",
+           "layers": ["fused GT attention, CSR path"]}
+    rows = _sample_by_edges(w["rowptr"], 400000)
+    return Workload("c4_clustered_gt", layers, [Q, K, V], [out, lse], cfg, "bf16", oracle_step,
+                    rows)
+
+
+def setup_c5(torch, gnn, w, mapping="auto"):
+    g = gnn.graph_prepare(_dev(torch, w["rowptr"]), _dev(torch, w["colidx"]))
+    X = _dev(torch, w["X"])
+    n, F = X.shape
+    M = len(w["colidx"])
+    Y = torch.empty((n, F), dtype=torch.float32, device="cuda")
+    mp = {"auto": gnn.GNN_MAP_AUTO, "feat": gnn.GNN_MAP_FEAT, "neigh": gnn.GNN_MAP_NEIGH}[mapping]
+    idx = 4 * (n + 1) + 4 * M
+    bcomp = idx + n * F * 2 + n * F * 4 + 8 * n
+    layers = [Layer("spmm", lambda ins: gnn.gnn_spmm(g, ins[0], norm=gnn.GNN_NORM_BOTH,
+                                                     mapping=mp, out=Y), M * F, bcomp)]
+
+    def oracle_step(rows):
+        import oracle
+        oracle.spmm(w["rowptr"], w["colidx"], w["X"], norm=oracle.NORM_BOTH, rows=rows)
+
+    cfg = {"workload": "c5_rmat22", "graph": "R-MAT scale 22, edge factor 16, dedup + "
+           "self-loops", "nodes": n, "edges": M, "features": F, "x_dtype": "bf16",
+           "ordering": "original ids", "mapping": mapping, "layers": ["gcn_spmm"]}
+    rows = _sample_by_edges(w["rowptr"], 2000000)
+    return Workload("c5_rmat22", layers, [X], [Y], cfg, "bf16", oracle_step, rows)
+
+
+SETUPS = {"c2_rmat17": setup_c2, "c3_rmat20_gatv2": setup_c3, "c4_clustered_gt": setup_c4,
+          "c5_rmat22": setup_c5}
 
 
 # ---------------------------------------------------------------- main
@@ -179,26 +313,126 @@ def run_reference(args):
     if rank != 0:
         return
     w = synth.workload(args.workload)
-    rows, ne = sample_rows(w, 8)
-    F = w["X"].shape[1]
+    wl_meta = REF_META[args.workload](w)
+    rows, ne, per_edge, fn = wl_meta
     for _ in range(args.warmup):
-        oracle_step_c2(w, rows)
+        fn(rows)
     t = time.perf_counter()
     for _ in range(args.steps):
-        oracle_step_c2(w, rows)
+        fn(rows)
     dt = (time.perf_counter() - t) / args.steps
-    v = 4 * ne * F / dt / 1e9
-    line = {"impl": "reference", "metric": "aggregation Gedge*feat/s", "value": v,
-            "unit": "Gedge*feat/s", "n_gpus": args.gpus, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload, "sample": f"every 8th destination row "
-                       f"({len(rows)} rows, {ne} edges) per step"},
-            "cpu_baseline": {"value": v, "unit": "Gedge*feat/s", "cores": 1, "kind": "oracle",
-                             "sample": f"every 8th row of {args.workload}"},
-            "e2e": {"value": v, "unit": "Gedge*feat/s", "h2d_bytes_per_step": 0,
+    v = ne * per_edge / dt / 1e9
+    sample = f"{len(rows)} destination rows ({ne} edges) of {args.workload} per step"
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "sample": sample},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def _ref_c2(w):
+    import oracle
+    rp, ci, X = w["rowptr"], w["colidx"], w["X"]
+    rows = np.arange(0, len(rp) - 1, 16, dtype=np.int32)
+    ne = int(np.sum(rp[rows + 1] - rp[rows]))
+
+    def fn(r):
+        oracle.spmm(rp, ci, X, norm=oracle.NORM_BOTH, rows=r)
+        oracle.segment_reduce(oracle.OP_SUM, rp, ci, X, rows=r)
+        oracle.segment_reduce(oracle.OP_MEAN, rp, ci, X, rows=r)
+        oracle.segment_reduce(oracle.OP_MAX, rp, ci, X, rows=r)
+    return rows, ne, 4 * X.shape[1], fn
+
+
+def _ref_c3(w):
+    import oracle
+    rows, ne = _sample_by_edges(w["rowptr"], 4000)
+    HD = w["heads"] * w["head_dim"]
+
+    def fn(r):
+        oracle.gatv2(w["rowptr"], w["colidx"], w["H"], w["W"], w["a"], w["heads"], w["head_dim"],
+                     w["slope"], rows=r)
+    return rows, ne, HD, fn
+
+
+def _ref_c4(w):
+    import oracle
+    rows, ne = _sample_by_edges(w["rowptr"], 100000)
+    HD = w["heads"] * w["head_dim"]
+
+    def fn(r):
+        oracle.gt(w["rowptr"], w["colidx"], w["Q"], w["K"], w["V"], w["heads"], w["head_dim"],
+                  w["scale"], rows=r)
+    return rows, ne, HD, fn
+
+
+def _ref_c5(w):
+    import oracle
+    rows, ne = _sample_by_edges(w["rowptr"], 500000)
+
+    def fn(r):
+        oracle.spmm(w["rowptr"], w["colidx"], w["X"], norm=oracle.NORM_BOTH, rows=r)
+    return rows, ne, w["X"].shape[1], fn
+
+
+REF_META = {"c2_rmat17": _ref_c2, "c3_rmat20_gatv2": _ref_c3, "c4_clustered_gt": _ref_c4,
+            "c5_rmat22": _ref_c5}
+
+
+def time_layers(torch, W, steps, flush, stream):
+    names = [L.name for L in W.layers]
+    ev = [{k: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for k in names} for _ in range(steps)]
+    st = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for k in range(steps):
+        flush.fill_(float(k))
+        st[k][0].record(stream)
+        W.step(events=ev[k])
+        st[k][1].record(stream)
+    torch.cuda.synchronize()
+    step_ms = [a.elapsed_time(b) for a, b in st]
+    per = {k: float(np.mean([e[k][0].elapsed_time(e[k][1]) for e in ev])) for k in names}
+    return step_ms, per
+
+
+def unfused_gatv2_peak(torch, gnn, args_tuple):
+    """Edge-materialising comparator (plain PyTorch ops): the per-edge
+    scores, weights and messages of an unfused GATv2 layer are written to
+    device memory, as message-passing frameworks do.  Returns (ms, peak
+    bytes above the inputs)."""
+    g, H, W, a, heads, D, slope = args_tuple
+    rp = g.rowptr.long()
+    ci = g.colidx.long()
+    n = H.shape[0]
+    dst = torch.repeat_interleave(torch.arange(n, device="cuda"), rp[1:] - rp[:-1])
+    torch.cuda.synchronize()
+    torch.cuda.reset_peak_memory_stats()
+    base = torch.cuda.memory_allocated()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    C = (H.float() @ W.float()).view(n, heads, D)
+    x = C[dst] + C[ci]                                        # [M, heads, D]
+    e = (torch.nn.functional.leaky_relu(x, slope) * a.view(1, heads, D)).sum(-1)  # [M, heads]
+    del x
+    m = torch.full((n, heads), -float("inf"), device="cuda").index_reduce_(0, dst, e, "amax")
+    p = torch.exp(e - m[dst])
+    s = torch.zeros((n, heads), device="cuda").index_add_(0, dst, p)
+    alpha = p / s[dst]
+    msg = alpha.unsqueeze(-1) * C[ci]                          # [M, heads, D]
+    out = torch.zeros((n, heads, D), device="cuda").index_add_(0, dst, msg)
+    t1.record()
+    torch.cuda.synchronize()
+    peak = torch.cuda.max_memory_allocated() - base
+    del C, e, m, p, s, alpha, msg, out
+    torch.cuda.empty_cache()
+    return t0.elapsed_time(t1), peak
 
 
 def main():
@@ -207,8 +441,13 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="c2_rmat17")
+    ap.add_argument("--workload", default="c2_rmat17", choices=sorted(SETUPS))
+    ap.add_argument("--mapping", default="auto", choices=["auto", "feat", "neigh"],
+                    help="SpMM kernel mapping (c5_rmat22)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-comparator", action="store_true",
+                    help="skip the unfused GATv2 comparator (c3_rmat20_gatv2)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -227,102 +466,130 @@ def main():
     gnn.lib()
 
     w = synth.workload(args.workload)
-    if args.workload != "c2_rmat17":
-        raise SystemExit("only c2_rmat17 is wired into bench.py so far")
-    step, info = c2_setup(torch, gnn, w)
+    if args.workload == "c5_rmat22":
+        W = setup_c5(torch, gnn, w, args.mapping)
+    else:
+        W = SETUPS[args.workload](torch, gnn, w)
     stream = torch.cuda.current_stream()
-    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
 
+    torch.cuda.reset_peak_memory_stats()
     for _ in range(args.warmup):
-        step()
+        W.step()
     torch.cuda.synchronize()
+    peak_mem = torch.cuda.max_memory_allocated() - flush.numel() * 4
 
     def barrier():
         if world > 1:
             torch.distributed.barrier()
         torch.cuda.synchronize()
 
-    names = ["spmm", "sum", "mean", "max"]
-    ev = [{k: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for k in names} for _ in range(args.steps)]
-    st = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
     clocks = ClockSampler(local)
     barrier()
     clocks.start()
     launches0 = gnn.launch_count()
-    for k in range(args.steps):
-        flush.fill_(float(k))
-        st[k][0].record(stream)
-        step(events=ev[k])
-        st[k][1].record(stream)
-    torch.cuda.synchronize()
+    step_ms, per = time_layers(torch, W, args.steps, flush, stream)
     launches = gnn.launch_count() - launches0
     clk = clocks.stop()
-    step_ms = [a.elapsed_time(b) for a, b in st]
     total_ms = float(np.sum(step_ms))
     if world > 1:
         t = torch.tensor([total_ms], device="cuda")
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         total_ms = float(t.item())
     ms = total_ms / args.steps
-    value = world * info["units_per_step"] * args.steps / (total_ms * 1e-3) / 1e9
+    units = sum(L.units for L in W.layers)
+    value = world * units * args.steps / (total_ms * 1e-3) / 1e9
 
-    # per-kernel times and roofline of the dominant kernel
-    hbm, _, peak_kind = measured_peaks()
-    per = {k: float(np.mean([e[k][0].elapsed_time(e[k][1]) for e in ev])) for k in names}
-    dom = max(per, key=per.get)
-    achieved = info["bcomp"][dom] / (per[dom] * 1e-3) / 1e9
-    layers = {k: {"ms": per[k], "gedge_feat_s": info["units_per_step"] / 4 / (per[k] * 1e-3) / 1e9,
-                  "bcomp_bytes": info["bcomp"][k],
-                  "hbm_gbs": info["bcomp"][k] / (per[k] * 1e-3) / 1e9,
-                  "frac_of_measured": info["bcomp"][k] / (per[k] * 1e-3) / 1e9 / hbm,
-                  "frac_of_8tbs": info["bcomp"][k] / (per[k] * 1e-3) / 1e9 / NORTH_STAR_HBM_GBS}
-              for k in names}
+    hbm, bf16_tf, peak_kind = measured_peaks()
+    layers = {}
+    for L in W.layers:
+        gbs = L.bcomp / (per[L.name] * 1e-3) / 1e9
+        layers[L.name] = {"ms": per[L.name], "gedge_feat_s": L.units / (per[L.name] * 1e-3) / 1e9,
+                          "bcomp_bytes": L.bcomp, "hbm_gbs": gbs, "frac_of_measured": gbs / hbm,
+                          "frac_of_8tbs": gbs / NORTH_STAR_HBM_GBS, "bound": L.bound}
+    extra = {}
+    if "proj_only" in W.extra:
+        fn, b_proj = W.extra["proj_only"]
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for k, (e0, e1) in enumerate(evs):
+            flush.fill_(float(k))
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        pms = float(np.mean([e0.elapsed_time(e1) for e0, e1 in evs]))
+        gat = layers["gatv2_fwd"]["ms"]
+        extra["projection_alone"] = {"ms": pms, "bytes": b_proj,
+                                     "hbm_gbs": b_proj / (pms * 1e-3) / 1e9,
+                                     "frac_of_measured": b_proj / (pms * 1e-3) / 1e9 / hbm,
+                                     "tflops": 2 * W.inputs[0].shape[0] * 256 * 256 / (pms * 1e-3) / 1e12}
+        att_ms = max(gat - pms, 1e-6)
+        extra["attention_by_difference"] = {
+            "ms": att_ms, "bytes": W.extra["b_attn"],
+            "hbm_gbs": W.extra["b_attn"] / (att_ms * 1e-3) / 1e9,
+            "frac_of_measured": W.extra["b_attn"] / (att_ms * 1e-3) / 1e9 / hbm}
+        if not args.no_comparator:
+            ums, upeak = unfused_gatv2_peak(torch, gnn, W.extra["unfused"])
+            extra["unfused_torch_comparator"] = {"ms": ums, "peak_bytes_above_inputs": upeak,
+                                                 "fused_peak_bytes": peak_mem,
+                                                 "peak_memory_ratio": upeak / max(peak_mem, 1),
+                                                 "speedup": ums / gat}
 
-    # end to end through the public API with host buffers
-    Xh = info["X"].cpu().pin_memory()
-    outs_h = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in info["outputs"]]
-    Xdev = torch.empty_like(info["X"])
-    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(max(3, args.steps // 4))]
-    for k, (a, b) in enumerate(e2e_ev):
-        flush.fill_(float(k))
-        a.record(stream)
-        Xdev.copy_(Xh, non_blocking=True)
-        step(Xin=Xdev)
-        for oh, od in zip(outs_h, info["outputs"]):
-            oh.copy_(od, non_blocking=True)
-        b.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = float(np.mean([a.elapsed_time(b) for a, b in e2e_ev]))
-    h2d = Xh.numel() * Xh.element_size()
-    d2h = sum(o.numel() * o.element_size() for o in outs_h)
+    dom = max(W.layers, key=lambda L: per[L.name])
+    achieved = dom.bcomp / (per[dom.name] * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": dom.name, "achieved": achieved, "peak": hbm,
+                "unit": "GB/s", "frac": achieved / hbm, "peak_kind": peak_kind,
+                "frac_of_8tbs": achieved / NORTH_STAR_HBM_GBS, "traffic": None,
+                "bcomp_bytes": dom.bcomp}
+    if dom.bound == "alu":
+        roofline["note"] = ("kernel is FP32-ALU heavy; frac is its compulsory-byte rate "
+                            "against the HBM peak")
 
-    line = {"metric": "aggregation Gedge*feat/s", "value": value, "unit": info["unit"],
-            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": info["dtype"], "data": "synthetic", "config": info["config"],
-            "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm,
-                         "unit": "GB/s", "frac": achieved / hbm, "peak_kind": peak_kind,
-                         "frac_of_8tbs": achieved / NORTH_STAR_HBM_GBS, "traffic": None,
-                         "bcomp_bytes": info["bcomp"][dom]},
-            "layers": layers,
-            "e2e": {"value": world * info["units_per_step"] / (e2e_ms * 1e-3) / 1e9,
-                    "unit": info["unit"], "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "ms_per_step": e2e_ms},
-            "gpu_launches": int(launches), "clocks": clk}
+    e2e = None
+    if not args.no_e2e:
+        ins_h = [x.cpu().pin_memory() for x in W.inputs]
+        outs_h = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in W.outputs]
+        ins_d = [torch.empty_like(x) for x in W.inputs]
+        e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(max(3, args.steps // 4))]
+        for k, (a, b) in enumerate(e2e_ev):
+            flush.fill_(float(k))
+            a.record(stream)
+            for xd, xh in zip(ins_d, ins_h):
+                xd.copy_(xh, non_blocking=True)
+            W.step(ins=ins_d)
+            for oh, od in zip(outs_h, W.outputs):
+                oh.copy_(od, non_blocking=True)
+            b.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = float(np.mean([a.elapsed_time(b) for a, b in e2e_ev]))
+        e2e = {"value": world * units / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
+               "h2d_bytes_per_step": sum(x.numel() * x.element_size() for x in ins_h),
+               "d2h_bytes_per_step": sum(o.numel() * o.element_size() for o in outs_h),
+               "ms_per_step": e2e_ms}
+
+    cfg = dict(W.config)
+    cfg["l2"] = "512 MB flush write before every timed step"
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": W.dtype, "data": "synthetic",
+            "config": cfg, "roofline": roofline, "layers": layers, "e2e": e2e,
+            "gpu_launches": int(launches), "clocks": clk,
+            "peak_memory_bytes": peak_mem}
+    if extra:
+        line["extra"] = extra
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        import oracle  # noqa: F401  (bench's CPU-baseline leg)
-        rows, ne = sample_rows(w, 8)
+        rows, ne = W.sample_rows
         t = time.perf_counter()
-        oracle_step_c2(w, rows)
+        W.oracle_step(rows)
         dt = time.perf_counter() - t
-        line["cpu_baseline"] = {"value": 4 * ne * info["F"] / dt / 1e9, "unit": info["unit"],
-                                "cores": 1, "kind": "oracle",
-                                "sample": f"every 8th destination row ({len(rows)} rows, "
-                                          f"{ne} edges), one step, {dt:.2f} s"}
+        per_edge = units / max(len(w["colidx"]), 1)
+        line["cpu_baseline"] = {"value": ne * per_edge / dt / 1e9, "unit": UNIT, "cores": 1,
+                                "kind": "oracle",
+                                "sample": f"{len(rows)} destination rows ({ne} edges) of "
+                                          f"{args.workload}, one step, {dt:.2f} s"}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -1,38 +1,49 @@
 // Steps a4 (fused GATv2 forward) and a5 (fused Graph Transformer attention,
-// CSR path), plus the SIMT projection used for fp32 inputs.
+// CSR path), plus the SIMT projection used where the tensor-core path does
+// not apply.
 //
 // IO-aware GNN layers, Section 2.2 (iii) (GATv2 and GT scores), Section 3.2
 // and Appendix D.2 (fused CSR forward: score, online softmax and weighted
 // aggregate in one pass over the destination's adjacency list, logsumexp kept
 // for the backward pass; no per-edge score, weight or message reaches HBM).
 //
-// GB300 design.  One warp is one worker.  The edge list is cut into runs of
-// E edges (the prepared graph's run table, read at a stride); a warp owns the
-// rows whose first edge lies in its run and processes each of them whole
-// (light rows), so short rows of a power-law graph are packed many to a
-// warp.  A row longer than E (heavy) is cut at run boundaries; every piece
-// leaves its softmax state (running max, running sum, unnormalised
-// accumulator) in a workspace slot, and the last piece to finish (ticket
-// counter, no spinning) merges the pieces in edge order, so the result does
-// not depend on scheduling.  A run can hold the last piece of one heavy row
-// and the first piece of the next, so each run has two slots: 2w for a piece
-// continued from an earlier run, 2w+1 for the first piece of a row it owns.
-//
-// Lane layout: lane l owns CPL consecutive 16-byte chunks of a feature row
-// (8 bf16 or 4 fp32 channels per chunk); a head's channels sit on
-// D / (CPL * chunk) adjacent lanes, whose partial scores are summed with
-// xor-shuffles.  Scores are kept in base-2 units (scaled by log2 e) so each
-// softmax weight is a single exp2.
+// GB300 design.
+// * Schedule: one warp is one worker.  The edge list is cut into runs of E
+//   edges (the prepared graph's run table, read at a stride); a warp owns the
+//   rows whose first edge lies in its run and processes each of them whole,
+//   so short rows of a power-law graph are packed many to a warp.  A row
+//   longer than E (heavy) is cut at run boundaries; every piece leaves its
+//   softmax state (running max, running sum, unnormalised accumulator) in a
+//   workspace slot, and the last piece to finish (ticket counter, no
+//   spinning) merges the pieces in edge order, so the result does not depend
+//   on scheduling.  A run can hold the last piece of one heavy row and the
+//   first piece of the next, so each run has two slots: 2w for a piece
+//   continued from an earlier run, 2w+1 for the first piece of a row it owns.
+// * Gathers: the warp's edges (one contiguous span) stream through a ring of
+//   S shared-memory stages of U neighbour records.  Lane u of the warp
+//   fetches the record of edge u of a batch with one bulk copy
+//   (cp.async.bulk, completing on the stage's mbarrier), S batches ahead of
+//   their use, with the column ids of the next batch prefetched.  The data in
+//   flight sits in shared memory, not registers, and the TMA engine does the
+//   address work.  A GATv2 record is the projected row r_j followed by its
+//   per-head linear parts A_r[j] (one copy); a GT record is K_j then V_j.
+// * Lanes: lane l owns CPL consecutive 16-byte chunks of a feature row (8
+//   bf16 or 4 fp32 channels per chunk); a head's channels sit on
+//   D / (CPL * chunk) adjacent lanes, whose partial scores are summed with
+//   xor-shuffles.  Scores are kept in base-2 units (scaled by log2 e) so each
+//   softmax weight is a single exp2.  Edges are scored four at a time where a
+//   row allows, so the shuffle chains of four edges overlap.
 //
 // GATv2 score.  With LeakyReLU slope s, LReLU(x) = (1+s)/2 x + (1-s)/2 |x|,
 // so  e_ij = A_l[i] + A_r[j] + sum_d a''_d |l_id + r_jd|  with
 // A_l[i,h] = sum_d a'_hd l_id, A_r[j,h] = sum_d a'_hd r_jd, a' = (1+s)/2 a,
-// a'' = (1-s)/2 a.  A_l and A_r are per-node scalars computed once after the
-// projection; per edge and channel only an add and an |.| multiply-add
-// remain (the plain definition would need add, multiply, max and
-// multiply-add).
+// a'' = (1-s)/2 a.  A_l and A_r are per-node scalars formed once with the
+// projection; per edge and channel only an add and an |.| multiply-add remain
+// (the plain definition needs add, multiply, max and multiply-add).
 #include <algorithm>
+#include <mutex>
 
+#include "async.cuh"
 #include "common.cuh"
 
 namespace gnn {
@@ -47,12 +58,8 @@ constexpr float kLn2 = 0.6931471805599453f;
 // attention run = kAttnRunMul runs of the prepared graph's run table
 constexpr int kAttnRunMul = 4;
 constexpr int kAttnE = kRunEdges * kAttnRunMul;
-// edges whose rows are loaded before any of them is used (fewer when a lane
-// holds more channels, to stay within registers)
-template <int CPL>
-struct AttnU {
-    static constexpr int value = CPL == 1 ? 4 : (CPL == 2 ? 2 : 1);
-};
+constexpr int kAttnWarps = 4;  // warps per block
+constexpr int kGroup = 4;      // edges scored together
 
 enum AttnKind { ATT_GATV2 = 0, ATT_GT = 1 };
 
@@ -62,21 +69,32 @@ __host__ __device__ __forceinline__ int64_t slot_stride(int32_t HD, int32_t head
     return ((int64_t)HD + 2 * heads + 3) & ~(int64_t)3;
 }
 
+// bytes of a projected GATv2 row: HD channels then A[heads] fp32, padded
+// to 16 bytes (rows are bulk-copied whole)
+__host__ __device__ __forceinline__ int64_t gat_row_bytes(int32_t HD, int32_t heads, int32_t esize) {
+    return (int64_t)HD * esize + (((int64_t)heads * 4 + 15) & ~(int64_t)15);
+}
+
 struct AttnArgs {
     const int32_t *rowptr;
     const int32_t *colidx;
     const int32_t *run_table;  // prepared graph's run table (E = kRunEdges) or null
-    const uint4 *Sg;           // gathered score rows: GATv2 r = H W_r, GT K
-    const uint4 *Vg;           // gathered value rows: GATv2 r, GT V
-    const uint4 *Qd;           // destination rows: GATv2 l = H W_l, GT Q
-    const float *Al;           // GATv2 [n, heads] base-2 linear part at the destination
-    const float *Ar;           // GATv2 [n, heads] base-2 linear part at the source
-    const float *coef;         // GATv2 [HD] (1-s)/2 a log2e; GT unused
+    const char *Sg;            // gathered rows: GATv2 padded r rows, GT K
+    const char *Vg;            // GT V (GATv2 unused)
+    const char *Qd;            // destination rows: GATv2 padded l rows, GT Q
+    int64_t sg_stride, vg_stride, qd_stride;  // bytes between rows
+    int32_t s_bytes, v_bytes;  // bytes copied per edge from Sg and Vg
+    int32_t rec;               // bytes of one edge record in the ring
+    int32_t ar_off;            // GATv2: offset of A within a padded row
+    int32_t U, S;              // edges per stage, stages
+    int32_t ring_bytes;        // per warp: S*U*rec + S mbarriers
+    const float *coef;         // GATv2 [HD] (1-s)/2 a log2e
     float qscale;              // GT: scale * log2e
     float *out;                // [n_rows, HD]
     float *lse;                // [n_rows, heads] or null
-    float *slots;              // [2 n_workers, HD + 2 heads]
+    float *slots;              // [2 n_workers, slot_stride]
     int32_t *tickets;          // [n_workers], zero on entry and on exit
+    int32_t *err;              // device error word
     int64_t nnz;
     int64_t n_workers;
     int32_t n_rows;
@@ -110,28 +128,47 @@ struct SmState {
     }
 };
 
-template <int KIND, class T, int CPL>
-struct AttnLane {
+template <int KIND, class T, int CPL, int LPH>
+struct Lane {
     static constexpr int NV = Elt<T>::N;
     static constexpr int NC = CPL * NV;  // channels per lane
     int lane;
-    bool active;    // owns channels
-    int head;       // head of the lane's channels
-    int lph;        // lanes per head
+    bool active;  // owns channels
+    int head;     // head of the lane's channels
+    int lph;      // lanes per head (when LPH == 0)
     float coef[KIND == ATT_GATV2 ? NC : 1];
-
-    __device__ __forceinline__ float head_sum(float v) const {
-        for (int o = lph >> 1; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        return v;
-    }
+    // lanes per head: the template constant, or the runtime value if 0
+    __device__ __forceinline__ int lphv() const { return LPH > 0 ? LPH : lph; }
+    // a compile-time LPH is used only when every lane owns channels
+    __device__ __forceinline__ bool act() const { return LPH > 0 ? true : active; }
 };
 
-template <class T, int CPL>
-__device__ __forceinline__ void load_row(const uint4 *base, int64_t row, int nch, int lane, bool active,
-                                         uint4 *v) {
-    const uint4 *p = base + row * nch + lane * CPL;
-#pragma unroll
-    for (int c = 0; c < CPL; ++c) v[c] = active ? ldg16(p + c) : make_uint4(0u, 0u, 0u, 0u);
+// 2^x by the hardware approximation (ex2.approx.ftz; 2^-inf = +0)
+__device__ __forceinline__ float exp2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Packed fp32 pairs (Blackwell f32x2 instructions): d += a * b and a + b on
+// two lanes of a 64-bit register pair.
+__device__ __forceinline__ uint64_t pk2(float x, float y) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
+    return r;
+}
+__device__ __forceinline__ void upk2(uint64_t r, float &x, float &y) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(r));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
 }
 
 template <class T, int CPL>
@@ -140,132 +177,140 @@ __device__ __forceinline__ void unpack_row(const uint4 *v, float *f) {
     for (int c = 0; c < CPL; ++c) Chunk<T>::unpack(v[c], f + c * Elt<T>::N);
 }
 
-// Accumulate the edges [b, e) of destination row r into st.  dq: the
-// destination's channels (l for GATv2, Q pre-scaled for GT); al: A_l[r,head].
-template <int KIND, class T, int CPL>
-__device__ __forceinline__ void attend_range(const AttnArgs &a, const AttnLane<KIND, T, CPL> &L,
-                                             int32_t b, int32_t e, const float *dq, float al,
-                                             SmState<CPL * Elt<T>::N> &st) {
+// Score NG edges held in ring records rec0[0..NG) and fold them into st.
+// dq: the destination's channels (l for GATv2, Q pre-scaled for GT);
+// al: A_l[row, head] (GATv2).
+template <int KIND, class T, int CPL, int LPH, int NG>
+__device__ __forceinline__ void fold_edges(const AttnArgs &a, const Lane<KIND, T, CPL, LPH> &L,
+                                           const unsigned char *rec0, const float *dq, float al,
+                                           SmState<CPL * Elt<T>::N> &st) {
     constexpr int NC = CPL * Elt<T>::N;
-    constexpr int U = AttnU<CPL>::value;
-    const int lane = L.lane;
-    for (int32_t wb = b; wb < e; wb += 32) {
-        // column ids of the next (up to) 32 edges, one per lane
-        const int32_t cj = (wb + lane < e) ? __ldg(a.colidx + wb + lane) : 0;
-        const int nw = min(32, e - wb);
-        for (int u0 = 0; u0 < nw; u0 += U) {
-            uint4 sv[U][CPL];
-            uint4 vv[KIND == ATT_GT ? U : 1][CPL];
-            float ar[U];
+    float sf[NG][NC];
+    float part[NG];
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int32_t j = __shfl_sync(0xffffffffu, cj, (u0 + u) & 31);
-                const bool ok = u0 + u < nw;
-                if (ok) {
-                    load_row<T, CPL>(a.Sg, j, a.nch, lane, L.active, sv[u]);
-                    if (KIND == ATT_GT) load_row<T, CPL>(a.Vg, j, a.nch, lane, L.active, vv[u]);
-                    ar[u] = (KIND == ATT_GATV2 && L.active) ? __ldg(a.Ar + (int64_t)j * a.heads + L.head) : 0.f;
-                }
+    for (int g = 0; g < NG; ++g) {
+        const unsigned char *rec = rec0 + g * a.rec;
+        uint4 sv[CPL];
+#pragma unroll
+        for (int c = 0; c < CPL; ++c)
+            sv[c] = L.act() ? *reinterpret_cast<const uint4 *>(rec + (L.lane * CPL + c) * 16)
+                             : make_uint4(0u, 0u, 0u, 0u);
+        unpack_row<T, CPL>(sv, sf[g]);
+        float p0 = 0.f, p1 = 0.f;  // two chains: half the dependent-FMA latency
+        if (KIND == ATT_GATV2) {
+#pragma unroll
+            for (int k = 0; k < NC; k += 2) {
+                float x0, x1;
+                upk2(add2(pk2(dq[k], dq[k + 1]), pk2(sf[g][k], sf[g][k + 1])), x0, x1);
+                p0 = fmaf(L.coef[k], fabsf(x0), p0);
+                p1 = fmaf(L.coef[k + 1], fabsf(x1), p1);
             }
-            float e2[U];
-            float sf[U][KIND == ATT_GATV2 ? NC : 1];
+        } else {
+            uint64_t pp = pk2(0.f, 0.f);
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                float part = 0.f;
-                if (KIND == ATT_GATV2) {
-                    unpack_row<T, CPL>(sv[u], sf[u]);
+            for (int k = 0; k < NC; k += 2) pp = fma2(pk2(dq[k], dq[k + 1]), pk2(sf[g][k], sf[g][k + 1]), pp);
+            upk2(pp, p0, p1);
+        }
+        part[g] = p0 + p1;
+    }
+    for (int o = L.lphv() >> 1; o > 0; o >>= 1) {
 #pragma unroll
-                    for (int k = 0; k < NC; ++k) part = fmaf(L.coef[k], fabsf(dq[k] + sf[u][k]), part);
-                } else {
-                    float kf[NC];
-                    unpack_row<T, CPL>(sv[u], kf);
+        for (int g = 0; g < NG; ++g) part[g] += __shfl_xor_sync(0xffffffffu, part[g], o);
+    }
+    float mx = st.m;
 #pragma unroll
-                    for (int k = 0; k < NC; ++k) part = fmaf(dq[k], kf[k], part);
-                }
-                part = L.head_sum(part);
-                e2[u] = (u0 + u < nw) ? (KIND == ATT_GATV2 ? part + al + ar[u] : part) : -INFINITY;
-            }
-            float mx = st.m;
+    for (int g = 0; g < NG; ++g) {
+        if (KIND == ATT_GATV2)
+            part[g] += al + (L.act() ? *reinterpret_cast<const float *>(rec0 + g * a.rec + a.ar_off + 4 * L.head)
+                                      : 0.f);
+        mx = fmaxf(mx, part[g]);
+    }
+    if (__any_sync(0xffffffffu, mx > st.m)) {
+        const float sc = (mx > st.m) ? exp2_approx(st.m - mx) : 1.f;
+        st.s *= sc;
 #pragma unroll
-            for (int u = 0; u < U; ++u) mx = fmaxf(mx, e2[u]);
-            if (__any_sync(0xffffffffu, mx > st.m)) {
-                const float sc = (mx > st.m) ? exp2f(st.m - mx) : 1.f;
-                st.s *= sc;
+        for (int k = 0; k < NC; ++k) st.acc[k] *= sc;
+        st.m = mx;
+    }
 #pragma unroll
-                for (int k = 0; k < NC; ++k) st.acc[k] *= sc;
-                st.m = mx;
-            }
+    for (int g = 0; g < NG; ++g) {
+        const float p = exp2_approx(part[g] - st.m);
+        st.s += p;
+        const uint64_t pp = pk2(p, p);
+        if (KIND == ATT_GATV2) {
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                if (u0 + u < nw) {
-                    const float p = exp2f(e2[u] - st.m);
-                    st.s += p;
-                    if (KIND == ATT_GATV2) {
+            for (int k = 0; k < NC; k += 2)
+                upk2(fma2(pp, pk2(sf[g][k], sf[g][k + 1]), pk2(st.acc[k], st.acc[k + 1])), st.acc[k], st.acc[k + 1]);
+        } else {
+            const unsigned char *rec = rec0 + g * a.rec + a.s_bytes;
+            uint4 vv[CPL];
 #pragma unroll
-                        for (int k = 0; k < NC; ++k) st.acc[k] = fmaf(p, sf[u][k], st.acc[k]);
-                    } else {
-                        float vf[NC];
-                        unpack_row<T, CPL>(vv[u], vf);
+            for (int c = 0; c < CPL; ++c)
+                vv[c] = L.act() ? *reinterpret_cast<const uint4 *>(rec + (L.lane * CPL + c) * 16)
+                                 : make_uint4(0u, 0u, 0u, 0u);
+            float vf[NC];
+            unpack_row<T, CPL>(vv, vf);
 #pragma unroll
-                        for (int k = 0; k < NC; ++k) st.acc[k] = fmaf(p, vf[k], st.acc[k]);
-                    }
-                }
-            }
+            for (int k = 0; k < NC; k += 2)
+                upk2(fma2(pp, pk2(vf[k], vf[k + 1]), pk2(st.acc[k], st.acc[k + 1])), st.acc[k], st.acc[k + 1]);
         }
     }
 }
 
-template <int KIND, class T, int CPL>
-__device__ __forceinline__ void store_final(const AttnArgs &a, const AttnLane<KIND, T, CPL> &L,
-                                            int32_t r, const SmState<CPL * Elt<T>::N> &st) {
+template <int KIND, class T, int CPL, int LPH>
+__device__ __forceinline__ void store_final(const AttnArgs &a, const Lane<KIND, T, CPL, LPH> &L, int32_t r,
+                                            const SmState<CPL * Elt<T>::N> &st) {
     constexpr int NC = CPL * Elt<T>::N;
-    if (!L.active) return;
+    if (!L.act()) return;
     const float inv = st.s > 0.f ? 1.f / st.s : 0.f;
     float *o = a.out + (int64_t)r * a.HD + (int64_t)L.lane * NC;
 #pragma unroll
     for (int k = 0; k < NC; k += 4)
         *reinterpret_cast<float4 *>(o + k) =
             make_float4(st.acc[k] * inv, st.acc[k + 1] * inv, st.acc[k + 2] * inv, st.acc[k + 3] * inv);
-    if (a.lse && (L.lane % L.lph) == 0)
+    if (a.lse && (L.lane % L.lphv()) == 0)
         a.lse[(int64_t)r * a.heads + L.head] = st.s > 0.f ? (st.m + log2f(st.s)) * kLn2 : -INFINITY;
 }
 
-// Load the destination-side data of row r: GATv2 l_r (unpacked) and A_l;
+// Destination-side data of row r: GATv2 l_r (unpacked) and A_l[r, head];
 // GT Q_r pre-scaled by scale * log2 e.
-template <int KIND, class T, int CPL>
-__device__ __forceinline__ void load_dest(const AttnArgs &a, const AttnLane<KIND, T, CPL> &L,
-                                          int32_t r, float *dq, float *al) {
+template <int KIND, class T, int CPL, int LPH>
+__device__ __forceinline__ void load_dest(const AttnArgs &a, const Lane<KIND, T, CPL, LPH> &L, int32_t r,
+                                          float *dq, float *al) {
     constexpr int NC = CPL * Elt<T>::N;
+    const char *row = a.Qd + (int64_t)r * a.qd_stride;
     uint4 v[CPL];
-    load_row<T, CPL>(a.Qd, r, a.nch, L.lane, L.active, v);
+#pragma unroll
+    for (int c = 0; c < CPL; ++c)
+        v[c] = L.act() ? ldg16(row + (L.lane * CPL + c) * 16) : make_uint4(0u, 0u, 0u, 0u);
     unpack_row<T, CPL>(v, dq);
     if (KIND == ATT_GT) {
 #pragma unroll
         for (int k = 0; k < NC; ++k) dq[k] *= a.qscale;
         *al = 0.f;
     } else {
-        *al = L.active ? __ldg(a.Al + (int64_t)r * a.heads + L.head) : 0.f;
+        *al = L.act() ? __ldg(reinterpret_cast<const float *>(row + a.ar_off) + L.head) : 0.f;
     }
 }
 
 // A piece of heavy row r (edges of run w) leaves its state in slot 2w+1 (the
 // row's first piece) or 2w (a later piece); the last piece to arrive merges
 // the pieces of runs wa..wb in order and writes the row.
-template <int KIND, class T, int CPL>
-__device__ __forceinline__ void flush_piece(const AttnArgs &a, const AttnLane<KIND, T, CPL> &L,
-                                            int64_t w, int32_t r, const SmState<CPL * Elt<T>::N> &st) {
+template <int KIND, class T, int CPL, int LPH>
+__device__ __forceinline__ void flush_piece(const AttnArgs &a, const Lane<KIND, T, CPL, LPH> &L, int64_t w,
+                                            int32_t r, const SmState<CPL * Elt<T>::N> &st) {
     constexpr int NC = CPL * Elt<T>::N;
     const int64_t stride = slot_stride(a.HD, a.heads);
     const int32_t rb = __ldg(a.rowptr + r), re = __ldg(a.rowptr + r + 1);
     const int64_t E = kAttnE;
     const int64_t wa = rb / E, wb = ((int64_t)re - 1) / E;
     float *slot = a.slots + (2 * w + (w == wa ? 1 : 0)) * stride;
-    if (L.active) {
+    if (L.act()) {
 #pragma unroll
         for (int k = 0; k < NC; k += 4)
             __stcg(reinterpret_cast<float4 *>(slot + L.lane * NC + k),
                    make_float4(st.acc[k], st.acc[k + 1], st.acc[k + 2], st.acc[k + 3]));
-        if ((L.lane % L.lph) == 0) {
+        if ((L.lane % L.lphv()) == 0) {
             __stcg(slot + a.HD + 2 * L.head, st.m);
             __stcg(slot + a.HD + 2 * L.head + 1, st.s);
         }
@@ -281,13 +326,13 @@ __device__ __forceinline__ void flush_piece(const AttnArgs &a, const AttnLane<KI
     m.reset();
     for (int64_t k = wa; k <= wb; ++k) {
         const float *sk = a.slots + (2 * k + (k == wa ? 1 : 0)) * stride;
-        const float mk = L.active ? __ldcg(sk + a.HD + 2 * L.head) : -INFINITY;
-        const float sk_s = L.active ? __ldcg(sk + a.HD + 2 * L.head + 1) : 0.f;
+        const float mk = L.act() ? __ldcg(sk + a.HD + 2 * L.head) : -INFINITY;
+        const float sk_s = L.act() ? __ldcg(sk + a.HD + 2 * L.head + 1) : 0.f;
         const float mx = fmaxf(m.m, mk);
         const float c_old = (m.m == -INFINITY) ? 0.f : exp2f(m.m - mx);
         const float c_new = (mk == -INFINITY) ? 0.f : exp2f(mk - mx);
         m.s = m.s * c_old + sk_s * c_new;
-        if (L.active) {
+        if (L.act()) {
 #pragma unroll
             for (int q = 0; q < NC; q += 4) {
                 const float4 v = __ldcg(reinterpret_cast<const float4 *>(sk + L.lane * NC + q));
@@ -299,7 +344,7 @@ __device__ __forceinline__ void flush_piece(const AttnArgs &a, const AttnLane<KI
         }
         m.m = mx;
     }
-    store_final<KIND, T, CPL>(a, L, r, m);
+    store_final<KIND, T, CPL, LPH>(a, L, r, m);
     __syncwarp();
     if (L.lane == 0) a.tickets[wa] = 0;
 }
@@ -318,19 +363,95 @@ __device__ __forceinline__ int32_t warp_lower_bound(const int32_t *__restrict__ 
     return __shfl_sync(0xffffffffu, lo, 0);
 }
 
-template <int KIND, class T, int CPL>
-__global__ void __launch_bounds__(256) k_attn(AttnArgs a) {
+// The warp's edge stream: edges [sb, se) in batches of U through S stages.
+struct Ring {
+    unsigned char *stages;  // S * U * rec bytes
+    uint64_t *bars;         // S mbarriers
+    int32_t sb, se, nb;     // span and its batch count
+    int32_t k_issue;        // next batch to issue
+    int32_t kc;             // batch of the next edge to consume
+    int32_t cs;             // its stage (kc mod S)
+    uint32_t cph;           // its mbarrier phase parity ((kc / S) mod 2)
+    int32_t u;              // position of that edge in its batch
+    bool ready;             // batch kc has been waited for
+    int32_t pcol;           // prefetched column id of lane's edge in batch k_issue
+    bool bail;
+};
+
+// Issue batch R.k_issue into stage st (the stage batch k_issue - S used).
+__device__ __forceinline__ void ring_issue(const AttnArgs &a, Ring &R, int lane, int32_t st) {
+    const int32_t k = R.k_issue;
+    const int32_t base = R.sb + k * a.U;
+    const int32_t cnt = min(a.U, R.se - base);
+    uint64_t *bar = R.bars + st;
+    if (lane == 0) mbar_expect_tx(bar, (uint32_t)(cnt * (a.s_bytes + a.v_bytes)));
+    __syncwarp();
+    if (lane < cnt) {
+        unsigned char *dst = R.stages + ((size_t)st * a.U + lane) * a.rec;
+        const int64_t j = R.pcol;
+        bulk_g2s(dst, a.Sg + j * a.sg_stride, (uint32_t)a.s_bytes, bar);
+        if (a.v_bytes) bulk_g2s(dst + a.s_bytes, a.Vg + j * a.vg_stride, (uint32_t)a.v_bytes, bar);
+    }
+    const int32_t nxt = base + a.U + lane;
+    R.pcol = (lane < a.U && nxt < R.se) ? __ldg(a.colidx + nxt) : 0;
+    ++R.k_issue;
+}
+
+// Fold the edges [b, end) of the span (consecutive with what was consumed
+// before) into st.
+template <int KIND, class T, int CPL, int LPH>
+__device__ __forceinline__ void consume(const AttnArgs &a, const Lane<KIND, T, CPL, LPH> &L, Ring &R, int32_t b,
+                                        int32_t end, const float *dq, float al, SmState<CPL * Elt<T>::N> &st) {
+    int32_t e = b;
+    while (e < end && !R.bail) {
+        if (!R.ready) {
+            const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(R.bars + R.cs, R.cph));
+            if (!ok) {
+                set_device_error(a.err, GNN_ERR_TIMEOUT);
+                R.bail = true;
+                return;
+            }
+            R.ready = true;
+        }
+        const unsigned char *stage = R.stages + (size_t)R.cs * a.U * a.rec;
+        const int32_t n = min(a.U - R.u, end - e);
+        int32_t g = 0;
+        for (; g + kGroup <= n; g += kGroup)
+            fold_edges<KIND, T, CPL, LPH, kGroup>(a, L, stage + (size_t)(R.u + g) * a.rec, dq, al, st);
+        for (; g < n; ++g) fold_edges<KIND, T, CPL, LPH, 1>(a, L, stage + (size_t)(R.u + g) * a.rec, dq, al, st);
+        e += n;
+        R.u += n;
+        if (R.u == a.U || e == R.se) {
+            // batch consumed: its stage takes the batch S ahead
+            __syncwarp();
+            fence_proxy_async_smem();
+            if (R.k_issue < R.nb) ring_issue(a, R, L.lane, R.cs);
+            ++R.kc;
+            if (++R.cs == a.S) {
+                R.cs = 0;
+                R.cph ^= 1u;
+            }
+            R.u = 0;
+            R.ready = false;
+        }
+    }
+}
+
+template <int KIND, class T, int CPL, int LPH>
+__global__ void __launch_bounds__(kAttnWarps * 32) k_attn(AttnArgs a) {
     constexpr int NC = CPL * Elt<T>::N;
-    const int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int warp = threadIdx.x >> 5;
+    const int64_t w = (int64_t)blockIdx.x * kAttnWarps + warp;
     if (w >= a.n_workers) return;
-    AttnLane<KIND, T, CPL> L;
+    Lane<KIND, T, CPL, LPH> L;
     L.lane = threadIdx.x & 31;
     L.active = L.lane * CPL < a.nch;
     L.lph = a.D / NC;
-    L.head = L.active ? (L.lane * NC) / a.D : 0;
+    L.head = L.act() ? (L.lane * NC) / a.D : 0;
     if (KIND == ATT_GATV2) {
 #pragma unroll
-        for (int k = 0; k < NC; ++k) L.coef[k] = L.active ? __ldg(a.coef + L.lane * NC + k) : 0.f;
+        for (int k = 0; k < NC; ++k) L.coef[k] = L.act() ? __ldg(a.coef + L.lane * NC + k) : 0.f;
     }
     const int64_t E = kAttnE;
     const int64_t e0 = w * E;
@@ -344,60 +465,95 @@ __global__ void __launch_bounds__(256) k_attn(AttnArgs a) {
         lo = warp_lower_bound(rowptr, a.n_rows, e0);
         lo_end = (w + 1 == a.n_workers) ? a.n_rows : warp_lower_bound(rowptr, a.n_rows, e1);
     }
+    // a heavy row that started in an earlier run and reaches into this one
+    int32_t h = -1, lo_beg = 0;
+    if (lo > 0 && e0 < a.nnz) {
+        lo_beg = __ldg(rowptr + lo);
+        if (lo_beg > e0 && lo_beg - __ldg(rowptr + lo - 1) > E) h = lo - 1;
+    }
+    // the span of edges this warp folds
+    Ring R;
+    R.sb = h >= 0 ? (int32_t)e0 : (lo < lo_end ? __ldg(rowptr + lo) : 0);
+    if (lo < lo_end) {
+        const int32_t rl = lo_end - 1;
+        const int32_t rlb = __ldg(rowptr + rl), rle = __ldg(rowptr + rl + 1);
+        R.se = (rle - rlb > E) ? (int32_t)e1 : rle;
+    } else {
+        R.se = h >= 0 ? (int32_t)min((int64_t)lo_beg, e1) : R.sb;
+    }
+    R.nb = (R.se - R.sb + a.U - 1) / a.U;
+    R.stages = smem + (size_t)warp * a.ring_bytes;
+    R.bars = reinterpret_cast<uint64_t *>(R.stages + (size_t)a.S * a.U * a.rec);
+    R.k_issue = 0;
+    R.kc = 0;
+    R.cs = 0;
+    R.cph = 0;
+    R.u = 0;
+    R.ready = false;
+    R.bail = false;
+    R.pcol = 0;
+    if (R.nb > 0) {
+        if (L.lane == 0) {
+            for (int s = 0; s < a.S; ++s) mbar_init(R.bars + s, 1);
+            mbar_init_fence();
+        }
+        __syncwarp();
+        R.pcol = (L.lane < a.U && R.sb + L.lane < R.se) ? __ldg(a.colidx + R.sb + L.lane) : 0;
+        for (int s = 0; s < a.S && R.k_issue < R.nb; ++s) ring_issue(a, R, L.lane, s);
+    }
+
     float dq[NC];
     float al;
     SmState<NC> st;
-    // a heavy row that started in an earlier run and reaches into this one
-    if (lo > 0 && e0 < a.nnz) {
-        const int32_t lo_beg = __ldg(rowptr + lo);
-        if (lo_beg > e0) {
-            const int32_t h = lo - 1;
-            if (lo_beg - __ldg(rowptr + h) > E) {
-                load_dest<KIND, T, CPL>(a, L, h, dq, &al);
-                st.reset();
-                attend_range<KIND, T, CPL>(a, L, (int32_t)e0, (int32_t)min((int64_t)lo_beg, e1), dq, al, st);
-                flush_piece<KIND, T, CPL>(a, L, w, h, st);
-            }
-        }
+    if (h >= 0) {
+        load_dest<KIND, T, CPL, LPH>(a, L, h, dq, &al);
+        st.reset();
+        consume<KIND, T, CPL, LPH>(a, L, R, R.sb, (int32_t)min((int64_t)lo_beg, e1), dq, al, st);
+        if (!R.bail) flush_piece<KIND, T, CPL, LPH>(a, L, w, h, st);
     }
-    for (int32_t r = lo; r < lo_end; ++r) {
+    for (int32_t r = lo; r < lo_end && !R.bail; ++r) {
         const int32_t rb = __ldg(rowptr + r), re = __ldg(rowptr + r + 1);
         st.reset();
         if (re == rb) {
-            store_final<KIND, T, CPL>(a, L, r, st);
+            store_final<KIND, T, CPL, LPH>(a, L, r, st);
             continue;
         }
-        load_dest<KIND, T, CPL>(a, L, r, dq, &al);
+        load_dest<KIND, T, CPL, LPH>(a, L, r, dq, &al);
         if (re - rb > E) {  // heavy: this run holds its first piece (and it is the last owned row)
-            attend_range<KIND, T, CPL>(a, L, rb, (int32_t)e1, dq, al, st);
-            flush_piece<KIND, T, CPL>(a, L, w, r, st);
+            consume<KIND, T, CPL, LPH>(a, L, R, rb, (int32_t)e1, dq, al, st);
+            if (!R.bail) flush_piece<KIND, T, CPL, LPH>(a, L, w, r, st);
         } else {
-            attend_range<KIND, T, CPL>(a, L, rb, re, dq, al, st);
-            store_final<KIND, T, CPL>(a, L, r, st);
+            consume<KIND, T, CPL, LPH>(a, L, R, rb, re, dq, al, st);
+            store_final<KIND, T, CPL, LPH>(a, L, r, st);
         }
+    }
+    if (R.bail) {
+        // let the copies still in flight land before the warp leaves
+        for (int32_t k = R.kc; k < R.k_issue; ++k) mbar_wait_bounded(R.bars + (k % a.S), (uint32_t)((k / a.S) & 1u));
     }
 }
 
-// GATv2 per-node linear parts: A[i,h] = log2e * sum_d a'_hd C[i, hD+d] with
-// a' = (1+s)/2 a.  One warp per node; lanes stride over the channels.
+// GATv2 per-node linear parts: A[i,h] = sum_d lin[hD+d] C[i, hD+d], written
+// into the padding of the projected row.  One warp per node.
 template <class T>
-__global__ void __launch_bounds__(256) k_gatv2_linear(const T *__restrict__ C, int64_t n, int32_t heads,
-                                                      int32_t D, const float *__restrict__ a,
-                                                      float half_1ps, float *__restrict__ A) {
+__global__ void __launch_bounds__(256) k_gatv2_linear(char *__restrict__ C, int64_t row_bytes, int64_t n,
+                                                      int32_t heads, int32_t D, const float *__restrict__ lin) {
     const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (i >= n) return;
+    const T *row = reinterpret_cast<const T *>(C + i * row_bytes);
+    float *A = reinterpret_cast<float *>(C + i * row_bytes + (int64_t)heads * D * sizeof(T));
     for (int32_t h = 0; h < heads; ++h) {
         float s = 0.f;
         for (int32_t d = lane; d < D; d += 32) {
             float c;
-            if constexpr (sizeof(T) == 4) c = (float)C[i * heads * D + h * D + d];
-            else c = __bfloat162float(C[i * heads * D + h * D + d]);
-            s = fmaf(__ldg(a + h * D + d), c, s);
+            if constexpr (sizeof(T) == 4) c = (float)row[h * D + d];
+            else c = __bfloat162float(row[h * D + d]);
+            s = fmaf(__ldg(lin + h * D + d), c, s);
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        if (lane == 0) A[i * heads + h] = s * half_1ps * kLog2e;
+        if (lane == 0) A[h] = s;
     }
 }
 
@@ -413,12 +569,13 @@ __global__ void k_gatv2_coef(const float *__restrict__ a, int32_t HD, float half
 }
 
 // ---------------------------------------------------------------- SIMT GEMM
-// C[n, Fo] = H[n, Fi] W[Fi, Fo], fp32 FMA (no TF32), output in T (bf16 by
-// round-to-nearest-even).  64x64 tile per 256-thread block, 4x4 per thread.
+// C[n, Fo] = H[n, Fi] W[Fi, Fo] (C rows ldc elements apart), fp32 FMA (no
+// TF32), output in T (bf16 by round-to-nearest-even).  64x64 tile per
+// 256-thread block, 4x4 per thread.
 template <class T>
 __global__ void __launch_bounds__(256) k_proj_simt(const T *__restrict__ H, const T *__restrict__ W,
-                                                   T *__restrict__ C, int64_t n, int32_t Fi,
-                                                   int32_t Fo) {
+                                                   T *__restrict__ C, int64_t n, int32_t Fi, int32_t Fo,
+                                                   int64_t ldc) {
     __shared__ float sH[16][64 + 4];
     __shared__ float sW[16][64 + 4];
     const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
@@ -461,8 +618,8 @@ __global__ void __launch_bounds__(256) k_proj_simt(const T *__restrict__ H, cons
         for (int q = 0; q < 4; ++q) {
             const int32_t gc = col0 + tx * 4 + q;
             if (gc >= Fo) continue;
-            if constexpr (sizeof(T) == 4) C[gr * Fo + gc] = acc[p][q];
-            else C[gr * Fo + gc] = __float2bfloat16_rn(acc[p][q]);
+            if constexpr (sizeof(T) == 4) C[gr * ldc + gc] = acc[p][q];
+            else C[gr * ldc + gc] = __float2bfloat16_rn(acc[p][q]);
         }
     }
 }
@@ -470,27 +627,24 @@ __global__ void __launch_bounds__(256) k_proj_simt(const T *__restrict__ H, cons
 }  // namespace
 
 // tcgen05 projection (bf16), defined in projection.cu; returns
-// GNN_ERR_UNSUPPORTED for shapes it does not cover.
-gnn_status projection_tc(const void *H, int64_t n, int32_t F_in, const void *W, int32_t F_out,
-                         void *C, cudaStream_t s);
+// GNN_ERR_UNSUPPORTED for shapes it does not cover.  ldc: C row stride in
+// elements; lin_out/lin_ld: per-node linear parts and their row stride in
+// floats.
 gnn_status projection_tc_lin(const void *H, int64_t n, int32_t Fi, const void *W, int32_t Fo, void *C,
-                             const float *lin_coef, int32_t heads, int32_t D, float *lin_out, cudaStream_t s);
+                             int64_t ldc, const float *lin_coef, int32_t heads, int32_t D, float *lin_out,
+                             int64_t lin_ld, cudaStream_t s);
 
-static gnn_status projection_any(const void *H, int32_t dtype, int64_t n, int32_t F_in, const void *W,
-                                 int32_t F_out, void *C, cudaStream_t s) {
+static gnn_status projection_simt(const void *H, int32_t dtype, int64_t n, int32_t F_in, const void *W,
+                                  int32_t F_out, void *C, int64_t ldc, cudaStream_t s) {
     if (n == 0) return GNN_OK;
-    if (dtype == GNN_BF16) {
-        gnn_status st = projection_tc(H, n, F_in, W, F_out, C, s);
-        if (st != GNN_ERR_UNSUPPORTED) return st;
-    }
     dim3 grid((unsigned)((n + 63) / 64), (unsigned)((F_out + 63) / 64));
     if (dtype == GNN_F32)
         k_proj_simt<float><<<grid, 256, 0, s>>>(static_cast<const float *>(H), static_cast<const float *>(W),
-                                                 static_cast<float *>(C), n, F_in, F_out);
+                                                 static_cast<float *>(C), n, F_in, F_out, ldc);
     else
         k_proj_simt<__nv_bfloat16><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(H),
                                                          static_cast<const __nv_bfloat16 *>(W),
-                                                         static_cast<__nv_bfloat16 *>(C), n, F_in, F_out);
+                                                         static_cast<__nv_bfloat16 *>(C), n, F_in, F_out, ldc);
     note_launch();
     GNN_LAUNCH_CHECK();
     return GNN_OK;
@@ -505,9 +659,10 @@ static size_t attn_slot_bytes(const gnn_csr *g, int32_t heads, int32_t head_dim)
 }
 
 struct GatLayout {
-    void *l, *r;
-    float *Al, *Ar, *coef, *lin, *slots;
+    char *l, *r;  // padded projected rows [n, gat_row_bytes]
+    float *coef, *lin, *slots;
     int32_t *tickets;
+    int64_t row_bytes;
     size_t bytes;
 };
 
@@ -515,15 +670,14 @@ static GatLayout gat_layout(const gnn_csr *g, void *base, int32_t esize, bool se
                             int32_t head_dim) {
     Carver c(base);
     GatLayout L;
-    const size_t HD = (size_t)heads * head_dim;
+    const int32_t HD = heads * head_dim;
     const int64_t nw = attn_workers(g);
-    L.l = c.take<char>((size_t)g->n_cols * HD * esize);
-    L.r = separate ? c.take<char>((size_t)g->n_cols * HD * esize) : L.l;
-    L.Al = c.take<float>((size_t)g->n_cols * heads);
-    L.Ar = separate ? c.take<float>((size_t)g->n_cols * heads) : L.Al;
+    L.row_bytes = gat_row_bytes(HD, heads, esize);
+    L.l = c.take<char>((size_t)g->n_cols * L.row_bytes);
+    L.r = separate ? c.take<char>((size_t)g->n_cols * L.row_bytes) : L.l;
     L.coef = c.take<float>(HD);
     L.lin = c.take<float>(HD);
-    L.slots = c.take<float>((size_t)2 * nw * (size_t)slot_stride((int32_t)HD, heads));
+    L.slots = c.take<float>((size_t)2 * nw * (size_t)slot_stride(HD, heads));
     L.tickets = c.take<int32_t>((size_t)nw);
     L.bytes = c.used;
     return L;
@@ -540,18 +694,49 @@ size_t gt_workspace_bytes(const gnn_csr *g, int32_t heads, int32_t head_dim) {
     return attn_slot_bytes(g, heads, head_dim);
 }
 
+// Ring geometry: two stages of U records per warp.  Measured on GB300 (GT,
+// 1 KB records: U = 4; GATv2, 528-byte records: U = 8): deeper rings cost
+// more shared memory per warp than they gain, since fewer warps fit.
+static void ring_shape(AttnArgs &a) {
+    a.rec = a.s_bytes + a.v_bytes;
+    a.U = a.rec <= 640 ? 8 : 4;
+    a.S = 2;
+    a.ring_bytes = (int32_t)round_up((size_t)a.S * a.U * a.rec + (size_t)a.S * 8, 128);
+}
+
+template <int KIND, class T, int CPL, int LPH>
+static cudaError_t launch_attn_lph(const AttnArgs &a, cudaStream_t s) {
+    static std::once_flag once;
+    static cudaError_t attr = cudaSuccess;
+    std::call_once(once, [] {
+        attr = cudaFuncSetAttribute(k_attn<KIND, T, CPL, LPH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    227 * 1024);
+    });
+    if (attr != cudaSuccess) return attr;
+    const size_t smem = (size_t)kAttnWarps * a.ring_bytes;
+    if (smem > 227 * 1024) return cudaErrorInvalidValue;
+    const int blocks = (int)((a.n_workers + kAttnWarps - 1) / kAttnWarps);
+    k_attn<KIND, T, CPL, LPH><<<blocks, kAttnWarps * 32, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
 template <int KIND, class T>
-static void launch_attn(const AttnArgs &a, int cpl, cudaStream_t s) {
-    const int64_t threads = a.n_workers * 32;
-    const int blocks = (int)((threads + 255) / 256);
+static cudaError_t launch_attn(const AttnArgs &a, int cpl, cudaStream_t s) {
     if constexpr (sizeof(T) == 2) {
-        k_attn<KIND, T, 1><<<blocks, 256, 0, s>>>(a);  // bf16: at most 256 channels
+        // bf16: at most 256 channels, one chunk per lane; a compile-time
+        // lanes-per-head (D/8) when all 32 lanes own channels
+        if (a.nch != 32) return launch_attn_lph<KIND, T, 1, 0>(a, s);
+        switch (a.D / 8) {
+            case 4: return launch_attn_lph<KIND, T, 1, 4>(a, s);
+            case 8: return launch_attn_lph<KIND, T, 1, 8>(a, s);
+            default: return launch_attn_lph<KIND, T, 1, 16>(a, s);
+        }
     } else {
         switch (cpl) {
-            case 1: k_attn<KIND, T, 1><<<blocks, 256, 0, s>>>(a); break;
-            case 2: k_attn<KIND, T, 2><<<blocks, 256, 0, s>>>(a); break;
-            case 4: k_attn<KIND, T, 4><<<blocks, 256, 0, s>>>(a); break;
-            default: k_attn<KIND, T, 8><<<blocks, 256, 0, s>>>(a); break;
+            case 1: return launch_attn_lph<KIND, T, 1, 0>(a, s);
+            case 2: return launch_attn_lph<KIND, T, 2, 0>(a, s);
+            case 4: return launch_attn_lph<KIND, T, 4, 0>(a, s);
+            default: return launch_attn_lph<KIND, T, 8, 0>(a, s);
         }
     }
 }
@@ -588,7 +773,13 @@ gnn_status gnn_projection(const void *H, int32_t dtype, int64_t n, int32_t F_in,
     if (n < 0 || F_in <= 0 || F_out <= 0) return GNN_ERR_INVALID_ARG;
     if (dtype != GNN_F32 && dtype != GNN_BF16) return GNN_ERR_UNSUPPORTED;
     if (n > 0 && (!H || !W || !C)) return GNN_ERR_INVALID_ARG;
-    return projection_any(H, dtype, n, F_in, W, F_out, C, as_stream(stream));
+    if (n == 0) return GNN_OK;
+    cudaStream_t s = as_stream(stream);
+    if (dtype == GNN_BF16) {
+        gnn_status st = projection_tc_lin(H, n, F_in, W, F_out, C, F_out, nullptr, 0, 0, nullptr, 0, s);
+        if (st != GNN_ERR_UNSUPPORTED) return st;
+    }
+    return projection_simt(H, dtype, n, F_in, W, F_out, C, F_out, s);
 }
 
 gnn_status gnn_gatv2_fwd(const gnn_csr *g, const void *prep, const void *H, int32_t dtype,
@@ -610,6 +801,8 @@ gnn_status gnn_gatv2_fwd(const gnn_csr *g, const void *prep, const void *H, int3
     GatLayout WL = gat_layout(g, ws, esize, separate, heads, head_dim);
     if (!ws || ws_bytes < WL.bytes) return GNN_ERR_WORKSPACE;
     if (!aligned256(ws)) return GNN_ERR_INVALID_ARG;
+    int32_t *err = device_error_word();
+    if (!err) return GNN_ERR_CUDA;
     cudaStream_t s = as_stream(stream);
     const int32_t HD = heads * head_dim;
     const int64_t n = g->n_cols;
@@ -619,24 +812,26 @@ gnn_status gnn_gatv2_fwd(const gnn_csr *g, const void *prep, const void *H, int3
     k_gatv2_coef<<<(HD + 255) / 256, 256, 0, s>>>(a, HD, half_1ms, half_1ps, WL.coef, WL.lin);
     note_launch();
     GNN_LAUNCH_CHECK();
-    // a3: projections l = H W_l (and r = H W_r) with the linear parts A_l, A_r
+    // a3: projections l = H W_l (and r = H W_r) into padded rows, with the
+    // linear parts A_l, A_r in the padding
     const void *Ws[2] = {W_l, W_r};
-    void *Cs[2] = {WL.l, WL.r};
-    float *As[2] = {WL.Al, WL.Ar};
+    char *Cs[2] = {WL.l, WL.r};
+    const int64_t ldc = WL.row_bytes / esize;
     for (int k = 0; k < (separate ? 2 : 1); ++k) {
+        float *A = reinterpret_cast<float *>(Cs[k] + (int64_t)HD * esize);
         st = GNN_ERR_UNSUPPORTED;
         if (dtype == GNN_BF16)
-            st = projection_tc_lin(H, n, F_in, Ws[k], HD, Cs[k], WL.lin, heads, head_dim, As[k], s);
+            st = projection_tc_lin(H, n, F_in, Ws[k], HD, Cs[k], ldc, WL.lin, heads, head_dim, A,
+                                   WL.row_bytes / 4, s);
         if (st == GNN_ERR_UNSUPPORTED) {
-            st = projection_any(H, dtype, n, F_in, Ws[k], HD, Cs[k], s);
+            st = projection_simt(H, dtype, n, F_in, Ws[k], HD, Cs[k], ldc, s);
             if (st != GNN_OK) return st;
             const int lin_blocks = (int)((n * 32 + 255) / 256);
             if (dtype == GNN_F32)
-                k_gatv2_linear<float><<<lin_blocks, 256, 0, s>>>(static_cast<const float *>(Cs[k]), n, heads,
-                                                                  head_dim, a, half_1ps, As[k]);
+                k_gatv2_linear<float><<<lin_blocks, 256, 0, s>>>(Cs[k], WL.row_bytes, n, heads, head_dim, WL.lin);
             else
-                k_gatv2_linear<__nv_bfloat16><<<lin_blocks, 256, 0, s>>>(
-                    static_cast<const __nv_bfloat16 *>(Cs[k]), n, heads, head_dim, a, half_1ps, As[k]);
+                k_gatv2_linear<__nv_bfloat16><<<lin_blocks, 256, 0, s>>>(Cs[k], WL.row_bytes, n, heads, head_dim,
+                                                                          WL.lin);
             note_launch();
             GNN_LAUNCH_CHECK();
         } else if (st != GNN_OK) {
@@ -648,16 +843,20 @@ gnn_status gnn_gatv2_fwd(const gnn_csr *g, const void *prep, const void *H, int3
     A.rowptr = g->rowptr;
     A.colidx = g->colidx;
     A.run_table = prep ? prep_run_table(g, prep) : nullptr;
-    A.Sg = static_cast<const uint4 *>(WL.r);
-    A.Vg = A.Sg;
-    A.Qd = static_cast<const uint4 *>(WL.l);
-    A.Al = WL.Al;
-    A.Ar = WL.Ar;
+    A.Sg = WL.r;
+    A.Vg = nullptr;
+    A.Qd = WL.l;
+    A.sg_stride = A.qd_stride = WL.row_bytes;
+    A.vg_stride = 0;
+    A.s_bytes = (int32_t)WL.row_bytes;
+    A.v_bytes = 0;
+    A.ar_off = HD * esize;
     A.coef = WL.coef;
     A.out = out;
     A.lse = lse;
     A.slots = WL.slots;
     A.tickets = WL.tickets;
+    A.err = err;
     A.nnz = g->nnz;
     A.n_workers = attn_workers(g);
     A.n_rows = g->n_rows;
@@ -665,10 +864,11 @@ gnn_status gnn_gatv2_fwd(const gnn_csr *g, const void *prep, const void *H, int3
     A.heads = heads;
     A.D = head_dim;
     A.nch = nch;
-    if (dtype == GNN_F32) launch_attn<ATT_GATV2, float>(A, cpl, s);
-    else launch_attn<ATT_GATV2, __nv_bfloat16>(A, cpl, s);
+    ring_shape(A);
+    cudaError_t e = dtype == GNN_F32 ? launch_attn<ATT_GATV2, float>(A, cpl, s)
+                                     : launch_attn<ATT_GATV2, __nv_bfloat16>(A, cpl, s);
     note_launch();
-    GNN_LAUNCH_CHECK();
+    if (e != cudaSuccess) return cuda_status(e);
     return GNN_OK;
 }
 
@@ -693,17 +893,24 @@ gnn_status gnn_gt_attn_fwd(const gnn_csr *g, const void *prep, const gnn_blocksp
     const size_t need = attn_slot_bytes(g, heads, head_dim);
     if (!ws || ws_bytes < need) return GNN_ERR_WORKSPACE;
     if (!aligned256(ws)) return GNN_ERR_INVALID_ARG;
+    int32_t *err = device_error_word();
+    if (!err) return GNN_ERR_CUDA;
+    const int32_t esize = dtype == GNN_F32 ? 4 : 2;
     Carver cv(ws);
     AttnArgs A{};
     A.rowptr = g->rowptr;
     A.colidx = g->colidx;
     A.run_table = prep ? prep_run_table(g, prep) : nullptr;
-    A.Sg = static_cast<const uint4 *>(K);
-    A.Vg = static_cast<const uint4 *>(V);
-    A.Qd = static_cast<const uint4 *>(Q);
+    A.Sg = static_cast<const char *>(K);
+    A.Vg = static_cast<const char *>(V);
+    A.Qd = static_cast<const char *>(Q);
+    A.sg_stride = A.vg_stride = A.qd_stride = (int64_t)heads * head_dim * esize;
+    A.s_bytes = A.v_bytes = heads * head_dim * esize;
+    A.ar_off = 0;
     A.qscale = scale * kLog2e;
     A.out = out;
     A.lse = lse;
+    A.err = err;
     A.n_workers = attn_workers(g);
     A.slots = cv.take<float>((size_t)2 * A.n_workers * (size_t)slot_stride(heads * head_dim, heads));
     A.tickets = cv.take<int32_t>((size_t)A.n_workers);
@@ -713,10 +920,11 @@ gnn_status gnn_gt_attn_fwd(const gnn_csr *g, const void *prep, const gnn_blocksp
     A.heads = heads;
     A.D = head_dim;
     A.nch = nch;
-    if (dtype == GNN_F32) launch_attn<ATT_GT, float>(A, cpl, s);
-    else launch_attn<ATT_GT, __nv_bfloat16>(A, cpl, s);
+    ring_shape(A);
+    cudaError_t e = dtype == GNN_F32 ? launch_attn<ATT_GT, float>(A, cpl, s)
+                                     : launch_attn<ATT_GT, __nv_bfloat16>(A, cpl, s);
     note_launch();
-    GNN_LAUNCH_CHECK();
+    if (e != cudaSuccess) return cuda_status(e);
     return GNN_OK;
 }
 

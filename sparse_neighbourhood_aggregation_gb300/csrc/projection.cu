@@ -28,6 +28,7 @@
 
 #include <mutex>
 
+#include "async.cuh"
 #include "common.cuh"
 
 namespace gnn {
@@ -39,7 +40,6 @@ constexpr int kBK = 64;                     // K per stage: 128 bytes of bf16
 constexpr int kStageBytes = kBM * kBK * 2;  // 16 KB
 constexpr int kMaxStages = 8;
 constexpr int kThreads = 192;               // 6 warps
-constexpr uint64_t kWaitNs = 2000000000ull; // 2 s per wait
 
 struct Bars {
     uint64_t full[kMaxStages];
@@ -51,41 +51,6 @@ struct Bars {
     int32_t bail;
 };
 
-__device__ __forceinline__ uint32_t su32(const void *p) {
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ uint64_t globaltimer() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t *b, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t *b, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(b)), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t *b) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_test(uint64_t *b, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(su32(b)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
 // Wait for the phase of parity `parity` of barrier b; false if the CTA is
 // bailing out or the wait ran out of time (then the CTA bails out).
 __device__ __noinline__ bool mbar_wait(uint64_t *b, uint32_t parity, Bars *bars, int32_t *err) {
@@ -94,9 +59,9 @@ __device__ __noinline__ bool mbar_wait(uint64_t *b, uint32_t parity, Bars *bars,
         if (mbar_test(b, parity)) return true;
         if ((i & 255) == 255) {
             if (*reinterpret_cast<volatile int32_t *>(&bars->bail)) return false;
-            const uint64_t t = globaltimer();
+            const uint64_t t = globaltimer_ns();
             if (t0 == 0) t0 = t;
-            else if (t - t0 > kWaitNs) {
+            else if (t - t0 > kWaitLimitNs) {
                 atomicExch(&bars->bail, 1);
                 set_device_error(err, GNN_ERR_TIMEOUT);
                 return false;
@@ -171,7 +136,9 @@ struct ProjArgs {
     const __nv_bfloat16 *W;  // [Fi, Fo]
     __nv_bfloat16 *C;        // [n, Fo]
     const float *lin_coef;   // [Fo] or null: per-node linear parts
-    float *lin_out;          // [n, heads]
+    float *lin_out;          // [n, lin_ld] (first `heads` columns written)
+    int64_t ldc;             // C row stride (elements)
+    int64_t lin_ld;          // lin_out row stride (floats)
     int64_t n;
     int32_t Fi, Fo;
     int32_t heads, D;
@@ -266,8 +233,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_proj_tc(const __grid_constant__
                 for (int64_t k = k0; k < issued; ++k) {
                     const int s = (int)(k % p.stages);
                     const uint32_t ph = (uint32_t)((k / p.stages) & 1);
-                    const uint64_t t0 = globaltimer();
-                    while (!mbar_test(&bars->full[s], ph) && globaltimer() - t0 < kWaitNs) {
+                    const uint64_t t0 = globaltimer_ns();
+                    while (!mbar_test(&bars->full[s], ph) && globaltimer_ns() - t0 < kWaitLimitNs) {
                     }
                 }
             }
@@ -303,8 +270,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_proj_tc(const __grid_constant__
             }
             // every MMA issued has completed before TMEM is released
             umma_commit(&bars->drain);
-            const uint64_t t0 = globaltimer();
-            while (!mbar_test(&bars->drain, 0) && globaltimer() - t0 < kWaitNs) {
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_test(&bars->drain, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
             }
         }
     } else {
@@ -333,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_proj_tc(const __grid_constant__
                 }
                 if (in) {
                     // F_out may end half way through the 32-column chunk
-                    uint4 *dst = reinterpret_cast<uint4 *>(p.C + row * p.Fo + c0);
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.C + row * p.ldc + c0);
                     const int nq = min(32, p.Fo - c0) / 8;
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
@@ -346,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_proj_tc(const __grid_constant__
                         lin = fmaf(__ldg(p.lin_coef + c0 + 2 * k + 1), bf16hi(pk[k]), lin);
                     }
                     if (((c0 + 32) % p.D) == 0) {
-                        if (in) p.lin_out[row * p.heads + (c0 + 32) / p.D - 1] = lin;
+                        if (in) p.lin_out[row * p.lin_ld + (c0 + 32) / p.D - 1] = lin;
                         lin = 0.f;
                     }
                 }
@@ -386,14 +353,16 @@ bool projection_tc_supported(int64_t n, int32_t Fi, int32_t Fo) {
            n < ((int64_t)1 << 31);
 }
 
-// C = H W (bf16) on tcgen05.  lin_coef (device [Fo], may be null): also
-// write lin_out[i, h] = sum_{d < D} lin_coef[hD + d] C[i, hD + d] (C as
-// rounded to bf16), D % 32 == 0.
+// C = H W (bf16) on tcgen05, C rows ldc elements apart.  lin_coef (device
+// [Fo], may be null): also write lin_out[i * lin_ld + h] =
+// sum_{d < D} lin_coef[hD + d] C[i, hD + d] (C as rounded to bf16),
+// D % 32 == 0.
 gnn_status projection_tc_lin(const void *H, int64_t n, int32_t Fi, const void *W, int32_t Fo, void *C,
-                             const float *lin_coef, int32_t heads, int32_t D, float *lin_out, cudaStream_t s) {
+                             int64_t ldc, const float *lin_coef, int32_t heads, int32_t D, float *lin_out,
+                             int64_t lin_ld, cudaStream_t s) {
     if (!projection_tc_supported(n, Fi, Fo)) return GNN_ERR_UNSUPPORTED;
     if (lin_coef && (D % 32 || heads * D != Fo || !lin_out)) return GNN_ERR_UNSUPPORTED;
-    if (!aligned16(H) || !aligned16(W) || !aligned16(C)) return GNN_ERR_UNSUPPORTED;
+    if (!aligned16(H) || !aligned16(W) || !aligned16(C) || ldc < Fo || ldc % 8) return GNN_ERR_UNSUPPORTED;
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return GNN_ERR_UNSUPPORTED;
     int32_t *err = device_error_word();
@@ -414,6 +383,8 @@ gnn_status projection_tc_lin(const void *H, int64_t n, int32_t Fi, const void *W
     p.C = static_cast<__nv_bfloat16 *>(C);
     p.lin_coef = lin_coef;
     p.lin_out = lin_out;
+    p.ldc = ldc;
+    p.lin_ld = lin_ld;
     p.n = n;
     p.Fi = Fi;
     p.Fo = Fo;
@@ -447,9 +418,5 @@ gnn_status projection_tc_lin(const void *H, int64_t n, int32_t Fi, const void *W
     return GNN_OK;
 }
 
-gnn_status projection_tc(const void *H, int64_t n, int32_t Fi, const void *W, int32_t Fo, void *C,
-                         cudaStream_t s) {
-    return projection_tc_lin(H, n, Fi, W, Fo, C, nullptr, 0, 0, nullptr, s);
-}
 
 }  // namespace gnn
