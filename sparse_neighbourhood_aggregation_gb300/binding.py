@@ -312,3 +312,33 @@ def gnn_gt_attn_fwd(g: Graph, Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor,
         _dtype_code(Q), heads, head_dim, float(scale), o.data_ptr(), _ptr(L), ws.data_ptr(),
         ws.numel(), _stream(stream)))
     return o, L
+
+
+def gnn_reorder_perm(g: Graph, kind: int, seed: int = 7, stream=None):
+    """Vertex order of a square graph: returns (perm, inv) int32 tensors,
+    perm[new] = old, inv[old] = new.  RCM is synchronous."""
+    perm = torch.empty(g.n_rows, dtype=torch.int32, device=g.device)
+    inv = torch.empty(g.n_rows, dtype=torch.int32, device=g.device)
+    ws = g.workspace(GNN_OP_REORDER)
+    _check("gnn_reorder_perm", lib().gnn_reorder_perm(ctypes.byref(g.csr), int(kind), int(seed),
+                                                      perm.data_ptr(), inv.data_ptr(),
+                                                      ws.data_ptr(), ws.numel(), _stream(stream)))
+    return perm, inv
+
+
+def gnn_apply_perm(g: Graph, perm: torch.Tensor, inv=None, X=None, stream=None):
+    """Relabel g by perm (perm[new] = old): returns (rowptr, colidx, X_out)
+    with columns re-sorted within rows and X_out[r] = X[perm[r]] (None if X
+    is None)."""
+    _require_cuda(perm, inv, X)
+    rp = torch.empty(g.n_rows + 1, dtype=torch.int32, device=g.device)
+    ci = torch.empty(max(g.nnz, 1), dtype=torch.int32, device=g.device)
+    Xo = None
+    if X is not None:
+        Xo = torch.empty_like(X)
+    ws = g.workspace(GNN_OP_APPLY_PERM)
+    _check("gnn_apply_perm", lib().gnn_apply_perm(
+        ctypes.byref(g.csr), perm.data_ptr(), _ptr(inv), rp.data_ptr(), ci.data_ptr(), _ptr(X),
+        _dtype_code(X) if X is not None else 0, X.shape[1] if X is not None else 0, _ptr(Xo),
+        ws.data_ptr(), ws.numel(), _stream(stream)))
+    return rp, ci[:g.nnz], Xo

@@ -3,8 +3,6 @@
 #include "common.cuh"
 
 namespace gnn {
-size_t reorder_workspace_bytes(const gnn_csr *) { return 0; }
-size_t apply_perm_workspace_bytes(const gnn_csr *) { return 0; }
 size_t blocksparse_workspace_bytes(const gnn_csr *) { return 0; }
 
 gnn_status gt_attn_tiles(const gnn_csr *, const gnn_blocksparse *, const void *, const void *,
@@ -23,16 +21,6 @@ gnn_status gnn_blocksparse_plan(const gnn_csr *, float, void *, size_t, gnn_bloc
 
 gnn_status gnn_blocksparse_build(const gnn_csr *, gnn_blocksparse *, void *, size_t, void *,
                                  size_t, void *) {
-    return GNN_ERR_UNSUPPORTED;
-}
-
-gnn_status gnn_reorder_perm(const gnn_csr *, int32_t, uint64_t, int32_t *, int32_t *, void *,
-                            size_t, void *) {
-    return GNN_ERR_UNSUPPORTED;
-}
-
-gnn_status gnn_apply_perm(const gnn_csr *, const int32_t *, const int32_t *, int32_t *, int32_t *,
-                          const void *, int32_t, int32_t, void *, void *, size_t, void *) {
     return GNN_ERR_UNSUPPORTED;
 }
 
