@@ -271,11 +271,27 @@ def setup_c4(torch, gnn, w):
                     rows)
 
 
-def setup_c5(torch, gnn, w, mapping="auto"):
-    g = gnn.graph_prepare(_dev(torch, w["rowptr"]), _dev(torch, w["colidx"]))
+def setup_c5(torch, gnn, w, mapping="auto", ordering="original"):
+    rp, ci = _dev(torch, w["rowptr"]), _dev(torch, w["colidx"])
     X = _dev(torch, w["X"])
     n, F = X.shape
     M = len(w["colidx"])
+    prep = {}
+    if ordering != "original":
+        kind = {"random": gnn.GNN_PERM_RANDOM, "degree": gnn.GNN_PERM_DEGREE,
+                "rcm": gnn.GNN_PERM_RCM}[ordering]
+        g0 = gnn.Graph(rp, ci, prepare=False)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        perm, inv = gnn.gnn_reorder_perm(g0, kind, 7)
+        torch.cuda.synchronize()
+        t1 = time.perf_counter()
+        rp, ci, X = gnn.gnn_apply_perm(g0, perm, inv, X=X)
+        torch.cuda.synchronize()
+        t2 = time.perf_counter()
+        prep = {"order_ms": (t1 - t0) * 1e3, "relabel_ms": (t2 - t1) * 1e3}
+        del g0, perm, inv
+    g = gnn.graph_prepare(rp, ci)
     Y = torch.empty((n, F), dtype=torch.float32, device="cuda")
     mp = {"auto": gnn.GNN_MAP_AUTO, "feat": gnn.GNN_MAP_FEAT, "neigh": gnn.GNN_MAP_NEIGH}[mapping]
     idx = 4 * (n + 1) + 4 * M
@@ -289,9 +305,10 @@ def setup_c5(torch, gnn, w, mapping="auto"):
 
     cfg = {"workload": "c5_rmat22", "graph": "R-MAT scale 22, edge factor 16, dedup + "
            "self-loops", "nodes": n, "edges": M, "features": F, "x_dtype": "bf16",
-           "ordering": "original ids", "mapping": mapping, "layers": ["gcn_spmm"]}
+           "ordering": ordering, "mapping": mapping, "layers": ["gcn_spmm"]}
     rows = _sample_by_edges(w["rowptr"], 2000000)
-    return Workload("c5_rmat22", layers, [X], [Y], cfg, "bf16", oracle_step, rows)
+    return Workload("c5_rmat22", layers, [X], [Y], cfg, "bf16", oracle_step, rows,
+                    extra={"reorder_prep": prep} if prep else None)
 
 
 SETUPS = {"c2_rmat17": setup_c2, "c3_rmat20_gatv2": setup_c3, "c4_clustered_gt": setup_c4,
@@ -444,6 +461,9 @@ def main():
     ap.add_argument("--workload", default="c2_rmat17", choices=sorted(SETUPS))
     ap.add_argument("--mapping", default="auto", choices=["auto", "feat", "neigh"],
                     help="SpMM kernel mapping (c5_rmat22)")
+    ap.add_argument("--ordering", default="original",
+                    choices=["original", "random", "degree", "rcm"],
+                    help="vertex ordering applied before timing (c5_rmat22; prep timed apart)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-comparator", action="store_true",
@@ -467,7 +487,7 @@ def main():
 
     w = synth.workload(args.workload)
     if args.workload == "c5_rmat22":
-        W = setup_c5(torch, gnn, w, args.mapping)
+        W = setup_c5(torch, gnn, w, args.mapping, args.ordering)
     else:
         W = SETUPS[args.workload](torch, gnn, w)
     stream = torch.cuda.current_stream()
@@ -508,6 +528,8 @@ def main():
                           "bcomp_bytes": L.bcomp, "hbm_gbs": gbs, "frac_of_measured": gbs / hbm,
                           "frac_of_8tbs": gbs / NORTH_STAR_HBM_GBS, "bound": L.bound}
     extra = {}
+    if "reorder_prep" in W.extra:
+        extra["reorder_prep"] = W.extra["reorder_prep"]
     if "proj_only" in W.extra:
         fn, b_proj = W.extra["proj_only"]
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))

@@ -30,17 +30,15 @@
 #ifndef GNN_AGG_MINB
 #define GNN_AGG_MINB 4
 #endif
+// AUTO runs are GNN_AGG_RUNMUL runs of the prepared graph's run table
+// (kRunEdges edges each): longer runs amortise each worker's start-up chain
+// of dependent loads (run table -> row pointers -> column ids -> rows)
+#ifndef GNN_AGG_RUNMUL
+#define GNN_AGG_RUNMUL 1
+#endif
 // 16-byte loads in flight per lane in the edge loops
 #ifndef GNN_AGG_U
 #define GNN_AGG_U 4
-#endif
-// 1: 32-lane AUTO workers use the shared-memory staged kernel
-#ifndef GNN_AGG_STAGED
-#define GNN_AGG_STAGED 0
-#endif
-// upper bound on the staged kernel's pipeline depth
-#ifndef GNN_AGG_STAGES
-#define GNN_AGG_STAGES 8
 #endif
 
 namespace gnn {
@@ -347,8 +345,8 @@ __global__ void __launch_bounds__(256, (CPL <= 4 ? GNN_AGG_MINB : 2)) k_agg_auto
     // rows owned by this run: [lo, lo_end)
     int32_t lo, lo_end;
     if (a.run_first_row) {
-        lo = __ldg(a.run_first_row + w);
-        lo_end = __ldg(a.run_first_row + w + 1);
+        lo = __ldg(a.run_first_row + (int64_t)w * GNN_AGG_RUNMUL);
+        lo_end = (w + 1 == a.n_workers) ? n_rows : __ldg(a.run_first_row + (int64_t)(w + 1) * GNN_AGG_RUNMUL);
     } else {
         lo = group_lower_bound(rowptr, n_rows, e0, gl, lpr, gmask);
         lo_end = (w + 1 == a.n_workers) ? n_rows : group_lower_bound(rowptr, n_rows, e1, gl, lpr, gmask);
@@ -464,241 +462,6 @@ __global__ void __launch_bounds__(256, (CPL <= 4 ? GNN_AGG_MINB : 2)) k_agg_auto
     // the row holding the last streamed edge, then empty rows up to rl
     if (r == rl && heavy_tail) {
         flush_partial<OP, T, CPL>(a, w, 1, r, acc, gl, gmask);
-        return;
-    }
-    finish_row();
-    while (r < rl) {
-        advance();
-        finish_row();
-    }
-}
-
-// ---------------------------------------------------------------------------
-// AUTO mapping, staged: the same edge-run schedule as k_agg_auto for 32-lane
-// workers, but the feature chunks are moved from L2 into a per-warp ring of
-// shared memory with cp.async (16 B per lane per edge) S-1 batches ahead of
-// their use.  The data in flight occupies shared memory instead of
-// registers, so each warp keeps (S-1)*U rows in flight while it accumulates.
-// Per-edge scalars (source id for max, edge value and column factor for
-// SpMM) travel through the same ring.
-// ---------------------------------------------------------------------------
-
-__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
-    const uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(sa), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async4(void *smem, const void *gmem) {
-    const uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(sa), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
-// wait until at most n groups (0..7) are still pending
-__device__ __forceinline__ void cp_async_wait_n(int n) {
-    switch (n) {
-        case 0: cp_async_wait<0>(); break;
-        case 1: cp_async_wait<1>(); break;
-        case 2: cp_async_wait<2>(); break;
-        case 3: cp_async_wait<3>(); break;
-        case 4: cp_async_wait<4>(); break;
-        case 5: cp_async_wait<5>(); break;
-        case 6: cp_async_wait<6>(); break;
-        default: cp_async_wait<7>(); break;
-    }
-}
-
-struct StageLayout {
-    int32_t stages;        // S
-    int32_t stage_bytes;   // per warp per stage
-    int32_t off_wv;        // edge values [U][32] fp32, or -1
-    int32_t off_wc;        // column factor source [U][32] (fp32 or int32), or -1
-    int32_t off_j;         // source ids [U][32] int32, or -1
-};
-
-template <int OP, class T, int CPL>
-__global__ void __launch_bounds__(128) k_agg_staged(AggArgs a, StageLayout L) {
-    constexpr int U = CPL >= 8 ? 1 : 8 / CPL;
-    constexpr int LPR = 32;
-    constexpr int V = LPR * CPL;
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
-    const unsigned FULL = 0xffffffffu;
-    const int32_t w = blockIdx.x * 4 + warp;
-    if (w >= a.n_workers) return;
-    unsigned char *ring = smem_raw + (size_t)warp * L.stages * L.stage_bytes;
-    const int S = L.stages;
-
-    const int32_t nnz = (int32_t)a.nnz;
-    const int32_t E = a.E;
-    const int32_t e0 = w * E;
-    const int32_t e1 = min(e0 + E, nnz);
-    const int32_t *__restrict__ rowptr = a.rowptr;
-    const int32_t n_rows = a.n_rows;
-    const bool has_vals = OP == AGG_WSUM && a.values != nullptr;
-    const bool has_colf = OP == AGG_WSUM && a.col_mode != COL_ONE;
-
-    int32_t lo, lo_end;
-    if (a.run_first_row) {
-        lo = __ldg(a.run_first_row + w);
-        lo_end = __ldg(a.run_first_row + w + 1);
-    } else {
-        lo = group_lower_bound(rowptr, n_rows, e0, lane, LPR, FULL);
-        lo_end = (w + 1 == a.n_workers) ? n_rows : group_lower_bound(rowptr, n_rows, e1, lane, LPR, FULL);
-    }
-    // heavy head piece?
-    bool in_head = false;
-    int32_t h = -1, lo_beg = 0;
-    if (lo > 0 && e0 < nnz) {
-        lo_beg = __ldg(rowptr + lo);
-        if (lo_beg > e0) {
-            h = lo - 1;
-            in_head = (lo_beg - __ldg(rowptr + h)) > E;
-        }
-    }
-    const bool owns = lo < lo_end;
-    if (!in_head && !owns) return;
-    int32_t rl = 0, s1 = 0;
-    bool heavy_tail = false;
-    if (owns) {
-        rl = lo_end - 1;
-        const int32_t rl_beg = __ldg(rowptr + rl), rl_end = __ldg(rowptr + rl + 1);
-        heavy_tail = rl_end - rl_beg > E;
-        s1 = heavy_tail ? e1 : rl_end;
-    }
-    const int32_t sb = in_head ? e0 : __ldg(rowptr + lo);
-    const int32_t se = owns ? s1 : min(lo_beg, e1);
-
-    // row tracking (owned rows through a lane cache of row ends / factors)
-    int32_t r = lo, rb = lo;
-    const bool rsq = OP == AGG_WSUM && a.row_mode == ROW_RSQRT;
-    int32_t rp_cur = (owns && rb + lane < n_rows) ? __ldg(rowptr + rb + lane + 1) : INT32_MAX;
-    int32_t rp_nxt = (owns && rb + LPR + lane < n_rows) ? __ldg(rowptr + rb + LPR + lane + 1) : INT32_MAX;
-    float rf_cur = (rsq && owns && rb + lane < n_rows) ? __ldg(a.dinv_in + rb + lane) : 1.f;
-    float rf_nxt = (rsq && owns && rb + LPR + lane < n_rows) ? __ldg(a.dinv_in + rb + LPR + lane) : 1.f;
-    int32_t row_beg = sb;
-    int32_t row_end = in_head ? min(lo_beg, e1) : __shfl_sync(FULL, rp_cur, 0);
-
-    Acc<OP, T, CPL> acc;
-    acc.reset();
-
-    auto finish_row = [&]() {
-        const float rf = __shfl_sync(FULL, rf_cur, r - rb);
-        store_row_f<OP, T, CPL>(a, r, row_end - row_beg, rf, acc, lane);
-        acc.reset();
-    };
-    auto advance = [&]() {
-        ++r;
-        if (r - rb == LPR) {
-            rb = r;
-            rp_cur = rp_nxt;
-            rf_cur = rf_nxt;
-            rp_nxt = (rb + LPR + lane < n_rows) ? __ldg(rowptr + rb + LPR + lane + 1) : INT32_MAX;
-            if (rsq) rf_nxt = (rb + LPR + lane < n_rows) ? __ldg(a.dinv_in + rb + LPR + lane) : 1.f;
-        }
-        row_beg = row_end;
-        row_end = __shfl_sync(FULL, rp_cur, r - rb);
-    };
-    auto leave_head = [&]() {
-        flush_partial<OP, T, CPL>(a, w, 0, h, acc, lane, FULL);
-        acc.reset();
-        in_head = false;
-        row_beg = row_end;
-        row_end = __shfl_sync(FULL, rp_cur, 0);
-    };
-
-    // producer: colidx window of 32 edges (lane k holds edge pcb + k), next
-    // window prefetched
-    const int32_t nb = (se - sb + U - 1) / U;
-    int32_t pcb = sb;
-    int32_t pc_cur = (pcb + lane < se) ? __ldg(a.colidx + pcb + lane) : 0;
-    int32_t pc_nxt = (pcb + LPR + lane < se) ? __ldg(a.colidx + pcb + LPR + lane) : 0;
-    const uint4 *__restrict__ X = a.X;
-    auto produce = [&](int32_t p) {
-        const int32_t pb = sb + p * U;
-        if (pb - pcb == LPR) {
-            pcb = pb;
-            pc_cur = pc_nxt;
-            pc_nxt = (pcb + LPR + lane < se) ? __ldg(a.colidx + pcb + LPR + lane) : 0;
-        }
-        unsigned char *st = ring + (size_t)(p % S) * L.stage_bytes;
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int32_t j = __shfl_sync(FULL, pc_cur, (pb - pcb) + u);
-            const int32_t e = pb + u;
-            if (e < se) {
-                uint4 *dst = reinterpret_cast<uint4 *>(st) + (u * LPR + lane) * CPL;
-                const uint4 *src = X + (size_t)j * V + lane;
-#pragma unroll
-                for (int c = 0; c < CPL; ++c) cp_async16(dst + c, src + c * LPR);
-                if (has_vals) cp_async4(st + L.off_wv + (u * LPR + lane) * 4, a.values + e);
-                if (has_colf)
-                    cp_async4(st + L.off_wc + (u * LPR + lane) * 4,
-                              a.col_mode == COL_RSQRT ? (const void *)(a.dinv_out + j) : (const void *)(a.d_out + j));
-                if (OP == AGG_MAX) *reinterpret_cast<int32_t *>(st + L.off_j + (u * LPR + lane) * 4) = j;
-            }
-        }
-    };
-    auto edge_w = [&](const unsigned char *st, int u) -> float {
-        float wv = 1.f;
-        if (has_vals) wv = *reinterpret_cast<const float *>(st + L.off_wv + (u * LPR + lane) * 4);
-        if (has_colf) {
-            if (a.col_mode == COL_RSQRT) wv *= *reinterpret_cast<const float *>(st + L.off_wc + (u * LPR + lane) * 4);
-            else wv *= 1.f / (float)*reinterpret_cast<const int32_t *>(st + L.off_wc + (u * LPR + lane) * 4);
-        }
-        return wv;
-    };
-
-    for (int32_t p = 0; p < S - 1; ++p) {
-        if (p < nb) produce(p);
-        cp_async_commit();
-    }
-    for (int32_t k = 0; k < nb; ++k) {
-        cp_async_wait_n(S - 2);
-        const unsigned char *st = ring + (size_t)(k % S) * L.stage_bytes;
-        const int32_t eb = sb + k * U;
-        const bool full = eb + U <= se;
-        uint4 xv[U][CPL];
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-#pragma unroll
-            for (int c = 0; c < CPL; ++c)
-                xv[u][c] = reinterpret_cast<const uint4 *>(st)[(u * LPR + lane) * CPL + c];
-        if (full && row_end >= eb + U) {
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int32_t j = OP == AGG_MAX ? *reinterpret_cast<const int32_t *>(st + L.off_j + (u * LPR + lane) * 4) : 0;
-                acc.add(xv[u], edge_w(st, u), j);
-            }
-        } else {
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int32_t e = eb + u;
-                if (e < se) {
-                    while (e == row_end) {
-                        if (in_head) leave_head();
-                        else { finish_row(); advance(); }
-                    }
-                    const int32_t j = OP == AGG_MAX ? *reinterpret_cast<const int32_t *>(st + L.off_j + (u * LPR + lane) * 4) : 0;
-                    acc.add(xv[u], edge_w(st, u), j);
-                }
-            }
-        }
-        // refill the stage consumed one iteration ago
-        if (k + S - 1 < nb) produce(k + S - 1);
-        cp_async_commit();
-    }
-    cp_async_wait<0>();
-    if (in_head) {
-        flush_partial<OP, T, CPL>(a, w, 0, h, acc, lane, FULL);
-        acc.reset();
-        if (!owns) return;
-        row_beg = row_end;
-        row_end = __shfl_sync(FULL, rp_cur, 0);
-    }
-    if (r == rl && heavy_tail) {
-        flush_partial<OP, T, CPL>(a, w, 1, r, acc, lane, FULL);
         return;
     }
     finish_row();
@@ -843,50 +606,8 @@ size_t agg_workspace_bytes(const gnn_csr *g, int32_t op, int32_t x_dtype_unused,
     return b;
 }
 
-template <int OP, class T, int CPL>
-static cudaError_t launch_staged_cpl(const AggArgs &a, cudaStream_t s) {
-    constexpr int U = CPL >= 8 ? 1 : 8 / CPL;
-    StageLayout L;
-    int32_t off = U * 32 * CPL * 16;
-    L.off_wv = (OP == AGG_WSUM && a.values) ? off : -1;
-    if (L.off_wv >= 0) off += U * 32 * 4;
-    L.off_wc = (OP == AGG_WSUM && a.col_mode != COL_ONE) ? off : -1;
-    if (L.off_wc >= 0) off += U * 32 * 4;
-    L.off_j = OP == AGG_MAX ? off : -1;
-    if (L.off_j >= 0) off += U * 32 * 4;
-    L.stage_bytes = (int32_t)round_up((size_t)off, 16);
-    // ~112 KB per 4-warp block (two blocks per SM), 3..8 stages
-    int S = (int)((112 * 1024) / (4 * L.stage_bytes));
-    L.stages = S < 3 ? 3 : (S > GNN_AGG_STAGES ? GNN_AGG_STAGES : S);
-    size_t smem = (size_t)4 * L.stages * L.stage_bytes;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(k_agg_staged<OP, T, CPL>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
-    int blocks = (int)((a.n_workers + 3) / 4);
-    k_agg_staged<OP, T, CPL><<<blocks, 128, smem, s>>>(a, L);
-    return cudaGetLastError();
-}
-
-template <int OP, class T>
-static cudaError_t launch_staged(const AggArgs &a, int cpl, cudaStream_t s) {
-    switch (cpl) {
-        case 1: return launch_staged_cpl<OP, T, 1>(a, s);
-        case 2: return launch_staged_cpl<OP, T, 2>(a, s);
-        case 4: return launch_staged_cpl<OP, T, 4>(a, s);
-        default: return launch_staged_cpl<OP, T, 8>(a, s);
-    }
-}
-
 template <int OP, class T>
 static void launch_auto(const AggArgs &a, int cpl, cudaStream_t s) {
-    if (a.lpr == 32 && GNN_AGG_STAGED) {
-        launch_staged<OP, T>(a, cpl, s);
-        return;
-    }
     int64_t threads = a.n_workers * a.lpr;
     int blocks = (int)((threads + 255) / 256);
     if (a.lpr == 32) {
@@ -940,8 +661,8 @@ gnn_status run_aggregate(const gnn_csr *g, const void *prep, int32_t op, int32_t
     a.F = F;
     a.V = sh.V;
     a.lpr = sh.lpr;
-    a.E = sh.E;
-    a.n_workers = n_workers_for(g, sh.E);
+    a.E = kRunEdges * GNN_AGG_RUNMUL;
+    a.n_workers = n_workers_for(g, a.E);
     a.col_mode = COL_ONE;
     a.row_mode = ROW_ONE;
     if (prep) {
