@@ -250,14 +250,16 @@ typedef struct {
 
 /* Synchronous planning pass: fills the counts of *bs (host struct; pointers
  * left NULL) and *out_bytes, the size of the buffer gnn_blocksparse_build
- * needs. */
+ * needs.  fill_threshold in [0, 1]. */
 gnn_status gnn_blocksparse_plan(const gnn_csr *g, float fill_threshold, void *ws,
                                 size_t ws_bytes, gnn_blocksparse *bs, size_t *out_bytes,
                                 void *stream);
 
 /* Build the layout planned by gnn_blocksparse_plan into `out` (device,
  * out_bytes, 256-byte aligned); sets the device pointers of *bs (host struct).
- * Bit-exact.  Asynchronous. */
+ * If the graph's counts differ from the plan's, returns GNN_ERR_INVALID_ARG
+ * and writes nothing to `out`.  Bit-exact.  Synchronous.  ws: as for the
+ * plan, gnn_workspace_size(GNN_OP_BLOCKSPARSE, g, 0, 0, 0) bytes. */
 gnn_status gnn_blocksparse_build(const gnn_csr *g, gnn_blocksparse *bs, void *out,
                                  size_t out_bytes, void *ws, size_t ws_bytes, void *stream);
 

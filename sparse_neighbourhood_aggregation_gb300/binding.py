@@ -342,3 +342,42 @@ def gnn_apply_perm(g: Graph, perm: torch.Tensor, inv=None, X=None, stream=None):
         _dtype_code(X) if X is not None else 0, X.shape[1] if X is not None else 0, _ptr(Xo),
         ws.data_ptr(), ws.numel(), _stream(stream)))
     return rp, ci[:g.nnz], Xo
+
+
+class BlockSparse:
+    """A built block-sparse layout (step a6): the host descriptor `meta`
+    (gnn_blocksparse) and the device buffer that holds its arrays."""
+
+    def __init__(self, meta: gnn_blocksparse, buf: torch.Tensor):
+        self.meta, self.buf = meta, buf
+
+    def _view(self, ptr, count, dtype):
+        if count == 0:
+            return torch.empty(0, dtype=dtype, device=self.buf.device)
+        off = ptr - self.buf.data_ptr()
+        nbytes = count * torch.empty(0, dtype=dtype).element_size()
+        return self.buf[off:off + nbytes].view(dtype)
+
+    def arrays(self):
+        m = self.meta
+        return {"grp_blk_offset": self._view(m.grp_blk_offset, m.n_groups + 1, torch.int32),
+                "blk_cols": self._view(m.blk_cols, m.n_blocks * 16, torch.int32).view(-1, 16),
+                "blk_mask": self._view(m.blk_mask, m.n_blocks * 32, torch.int64).view(-1, 8, 4),
+                "res_rowptr": self._view(m.res_rowptr, m.n_rows + 1, torch.int32),
+                "res_colidx": self._view(m.res_colidx, m.nnz_residual, torch.int32)}
+
+
+def gnn_blocksparse_build(g: Graph, fill_threshold: float, stream=None) -> BlockSparse:
+    """Plan and build the 16x16 block-sparse tile layout of g (synchronous)."""
+    ws = g.workspace(GNN_OP_BLOCKSPARSE)
+    meta = gnn_blocksparse()
+    nbytes = ctypes.c_size_t(0)
+    L = lib()
+    _check("gnn_blocksparse_plan", L.gnn_blocksparse_plan(
+        ctypes.byref(g.csr), float(fill_threshold), ws.data_ptr(), ws.numel(), ctypes.byref(meta),
+        ctypes.byref(nbytes), _stream(stream)))
+    buf = torch.empty(max(nbytes.value, 256), dtype=torch.uint8, device=g.device)
+    _check("gnn_blocksparse_build", L.gnn_blocksparse_build(
+        ctypes.byref(g.csr), ctypes.byref(meta), buf.data_ptr(), buf.numel(), ws.data_ptr(),
+        ws.numel(), _stream(stream)))
+    return BlockSparse(meta, buf)
