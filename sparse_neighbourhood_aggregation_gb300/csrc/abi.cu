@@ -6,7 +6,7 @@ namespace gnn {
 size_t agg_workspace_bytes(const gnn_csr *g, int32_t op, int32_t x_dtype, int32_t F);
 size_t gatv2_workspace_bytes(const gnn_csr *g, int32_t F_in, int32_t heads, int32_t head_dim,
                              int32_t esize);
-size_t gt_workspace_bytes(const gnn_csr *g, int32_t heads, int32_t head_dim);
+size_t gt_tiles_workspace_bytes(const gnn_csr *g, int32_t heads, int32_t head_dim);
 size_t reorder_workspace_bytes(const gnn_csr *g);
 size_t apply_perm_workspace_bytes(const gnn_csr *g);
 size_t blocksparse_workspace_bytes(const gnn_csr *g);
@@ -28,7 +28,7 @@ extern "C" size_t gnn_workspace_size(int32_t op, const gnn_csr *g, int32_t F, in
         case GNN_OP_GATV2:
             return gatv2_workspace_bytes(g, F, heads, head_dim, esize);
         case GNN_OP_GT:
-            return gt_workspace_bytes(g, heads, head_dim);
+            return gt_tiles_workspace_bytes(g, heads, head_dim);  // covers the CSR path too
         case GNN_OP_REORDER:
             return reorder_workspace_bytes(g);
         case GNN_OP_APPLY_PERM:

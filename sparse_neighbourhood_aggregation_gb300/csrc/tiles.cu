@@ -1,0 +1,337 @@
+// Step a7: Graph Transformer attention over the kept 16x16 tiles of a
+// block-sparse layout on the 5th-generation tensor cores, merged with the
+// fused CSR attention over the residual edges.
+//
+// IO-aware GNN layers, Section 3.3 and Appendix D.3 (tensor-core attention on
+// the weighted block-sparse format: per row window, scores against the packed
+// column tiles, the tile bitmaps masking absent edges, softmax and the
+// weighted sum of values; the edges left out of the tiles go through the CSR
+// kernel and the two softmax states are merged).
+//
+// GB300 design.  One CTA (4 warps, one thread per row) per 128-row group and
+// head.  The group's listed column blocks are taken in chunks of up to 12
+// blocks (192 columns):
+//   1. the chunk's K rows and V rows (head h) are gathered into shared memory
+//      in the no-swizzle core-matrix layout of tcgen05 operands (8 rows x 16
+//      bytes per core matrix); V is written transposed so that both operands
+//      of the second product are K-major;
+//   2. one thread issues S = Q K^T (M = 128, N = 16 x blocks, K = head_dim)
+//      into TMEM;
+//   3. each thread reads its row of S (tcgen05.ld), masks it with the tile
+//      bitmaps, updates its online-softmax state (running max, running sum,
+//      rescale of its output row) and writes P = exp(S - m) in bf16 to
+//      shared memory;
+//   4. one thread issues O_chunk = P V (M = 128, N = head_dim, K = columns);
+//      each thread adds its row of O_chunk to its output row in registers.
+// The residual edges run first on the CSR kernel, which writes (out, lse);
+// the tile state is then merged with it through the logsumexp.  MMA
+// completion is tracked with an mbarrier; every wait is bounded.
+#include <algorithm>
+#include <mutex>
+
+#include "async.cuh"
+#include "common.cuh"
+#include "tcgen05.cuh"
+
+extern "C" gnn_status gnn_gt_attn_fwd(const gnn_csr *g, const void *prep, const gnn_blocksparse *bs,
+                                      const void *Q, const void *K, const void *V, int32_t dtype,
+                                      int32_t heads, int32_t head_dim, float scale, float *out, float *lse,
+                                      void *ws, size_t ws_bytes, void *stream);
+
+namespace gnn {
+
+size_t gt_workspace_bytes(const gnn_csr *g, int32_t heads, int32_t head_dim);
+
+namespace {
+
+constexpr int kRows = 128;          // rows per group (MMA M)
+constexpr int kChunkBlocks = 12;    // column blocks per chunk (192 columns)
+constexpr int kTmemCols = 256;      // S: [0, 192), O: [192, 192 + D)
+constexpr int kOCol = 192;
+constexpr float kLog2eT = 1.4426950408889634f;
+constexpr float kLn2T = 0.6931471805599453f;
+
+struct TileArgs {
+    const int32_t *grp_blk_offset;
+    const int32_t *blk_cols;
+    const unsigned long long *blk_mask;
+    const __nv_bfloat16 *Q, *K, *V;
+    float *out;        // holds the residual result on entry
+    float *lse;        // [n, heads]: the residual logsumexp on entry, the merged one on exit
+    int32_t n_rows, heads, D;
+    float qscale;      // scale * log2 e
+    int32_t *err;
+};
+
+__device__ __forceinline__ void st16s(void *p, uint4 v) { *reinterpret_cast<uint4 *>(p) = v; }
+
+template <int D>
+__global__ void __launch_bounds__(kRows) k_gt_tiles(TileArgs t) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *base = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                            ~(uintptr_t)1023);
+    constexpr int NCMAX = kChunkBlocks * 16;
+    unsigned char *sQ = base;                         // [16][D/8] core matrices
+    unsigned char *sK = sQ + kRows * D * 2;           // [NC/8][D/8]
+    unsigned char *sV = sK + NCMAX * D * 2;           // [D/8][NC/8] (V transposed)
+    unsigned char *sP = sV + NCMAX * D * 2;           // [16][NC/8]
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sP + kRows * NCMAX * 2);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 1);
+
+    const int g = blockIdx.x, h = blockIdx.y;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int b0 = __ldg(t.grp_blk_offset + g), b1 = __ldg(t.grp_blk_offset + g + 1);
+    if (b0 == b1) return;  // no tiles: the residual result stands
+    const int64_t HD = (int64_t)t.heads * D;
+    const int32_t row = g * kRows + tid;
+    const bool valid = row < t.n_rows;
+
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
+                     "r"(kTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        mbar_init_fence();
+    }
+    // Q tile: row tid, dims [8k, 8k+8) -> core matrix (tid/8, k)
+#pragma unroll
+    for (int k = 0; k < D / 8; ++k) {
+        const uint4 v = valid ? ldg16(t.Q + row * HD + h * D + 8 * k) : make_uint4(0u, 0u, 0u, 0u);
+        st16s(sQ + ((tid / 8) * (D / 8) + k) * 128 + (tid % 8) * 16, v);
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t idesc_o = bf16_idesc(kRows, D);
+
+    float m = -INFINITY, l = 0.f;
+    float o[D];
+#pragma unroll
+    for (int d = 0; d < D; ++d) o[d] = 0.f;
+    uint32_t phase = 0;
+    bool ok = true;
+    const int w = (tid % kRows) / 16, r = tid % 16;  // window and row within it
+
+    for (int c0 = b0; c0 < b1 && ok; c0 += kChunkBlocks) {
+        const int nbk = min(kChunkBlocks, b1 - c0);
+        const int NC = nbk * 16;
+        // gather K (as rows) and V (transposed) of the chunk's columns
+        for (int idx = tid; idx < NC * (D / 8); idx += kRows) {
+            const int c = idx / (D / 8), k = idx % (D / 8);
+            const int32_t col = __ldg(t.blk_cols + (int64_t)c0 * 16 + c);
+            const uint4 kv = ldg16(t.K + (int64_t)col * HD + h * D + 8 * k);
+            st16s(sK + ((c / 8) * (D / 8) + k) * 128 + (c % 8) * 16, kv);
+            const uint4 vv = ldg16(t.V + (int64_t)col * HD + h * D + 8 * k);
+            const uint16_t *ve = reinterpret_cast<const uint16_t *>(&vv);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const int d = 8 * k + q;
+                *reinterpret_cast<uint16_t *>(sV + ((d / 8) * (NC / 8) + c / 8) * 128 + (d % 8) * 16 + (c % 8) * 2) =
+                    ve[q];
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        // S = Q K^T
+        if (tid == 0) {
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks)
+                umma_bf16(tmem, plain_desc(su32(sQ) + ks * 256, 128, (D / 8) * 128),
+                          plain_desc(su32(sK) + ks * 256, 128, (D / 8) * 128), bf16_idesc(kRows, NC), ks > 0);
+            umma_commit(bar);
+        }
+        if (!__syncthreads_and(mbar_wait_bounded(bar, phase))) {
+            ok = false;
+            break;
+        }
+        phase ^= 1u;
+        tc_fence_after();
+        // pass 1: masked row maximum of this chunk (scores in base-2 units)
+        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        float cm = -INFINITY;
+        for (int cc = 0; cc < NC; cc += 32) {
+            uint32_t v[32];
+            tmem_ld32(lane_base + (uint32_t)cc, v);
+            const unsigned long long w0 = __ldg(t.blk_mask + ((int64_t)(c0 + cc / 16) * 8 + w) * 4 + (r * 16) / 64);
+            const uint32_t m0 = (uint32_t)(w0 >> ((r * 16) % 64)) & 0xFFFFu;
+            uint32_t m1 = 0;
+            if (cc + 16 < NC) {
+                const unsigned long long w1 =
+                    __ldg(t.blk_mask + ((int64_t)(c0 + cc / 16 + 1) * 8 + w) * 4 + (r * 16) / 64);
+                m1 = (uint32_t)(w1 >> ((r * 16) % 64)) & 0xFFFFu;
+            }
+            const uint32_t mk = m0 | (m1 << 16);
+#pragma unroll
+            for (int q = 0; q < 32; ++q)
+                if ((mk >> q) & 1u) cm = fmaxf(cm, __uint_as_float(v[q]) * t.qscale);
+        }
+        const float mn = fmaxf(m, cm);
+        const float sc = (m == -INFINITY) ? 0.f : exp2f(m - mn);
+        l *= sc;
+#pragma unroll
+        for (int d = 0; d < D; ++d) o[d] *= sc;
+        m = mn;
+        // pass 2: P = exp2(s - m) (0 where masked), into shared memory
+        for (int cc = 0; cc < NC; cc += 32) {
+            uint32_t v[32];
+            tmem_ld32(lane_base + (uint32_t)cc, v);
+            const unsigned long long w0 = __ldg(t.blk_mask + ((int64_t)(c0 + cc / 16) * 8 + w) * 4 + (r * 16) / 64);
+            const uint32_t m0 = (uint32_t)(w0 >> ((r * 16) % 64)) & 0xFFFFu;
+            uint32_t m1 = 0;
+            if (cc + 16 < NC) {
+                const unsigned long long w1 =
+                    __ldg(t.blk_mask + ((int64_t)(c0 + cc / 16 + 1) * 8 + w) * 4 + (r * 16) / 64);
+                m1 = (uint32_t)(w1 >> ((r * 16) % 64)) & 0xFFFFu;
+            }
+            const uint32_t mk = m0 | (m1 << 16);
+            const int nq = min(32, NC - cc);
+#pragma unroll
+            for (int g8 = 0; g8 < 4; ++g8) {
+                if (g8 * 8 >= nq) break;
+                uint32_t pk[4];
+#pragma unroll
+                for (int q2 = 0; q2 < 4; ++q2) {
+                    const int q = g8 * 8 + 2 * q2;
+                    const float p0 = ((mk >> q) & 1u) ? exp2f(__uint_as_float(v[q]) * t.qscale - m) : 0.f;
+                    const float p1 = ((mk >> (q + 1)) & 1u) ? exp2f(__uint_as_float(v[q + 1]) * t.qscale - m) : 0.f;
+                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
+                    // the sum uses the rounded weights, the ones the product uses
+                    l += __low2float(b2) + __high2float(b2);
+                    pk[q2] = *reinterpret_cast<const uint32_t *>(&b2);
+                }
+                const int c = cc + g8 * 8;
+                st16s(sP + ((tid / 8) * (NC / 8) + c / 8) * 128 + (tid % 8) * 16, make_uint4(pk[0], pk[1], pk[2], pk[3]));
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        // O_chunk = P V
+        if (tid == 0) {
+            for (int ks = 0; ks < NC / 16; ++ks)
+                umma_bf16(tmem + kOCol, plain_desc(su32(sP) + ks * 256, 128, (NC / 8) * 128),
+                          plain_desc(su32(sV) + ks * 256, 128, (NC / 8) * 128), idesc_o, ks > 0);
+            umma_commit(bar);
+        }
+        if (!__syncthreads_and(mbar_wait_bounded(bar, phase))) {
+            ok = false;
+            break;
+        }
+        phase ^= 1u;
+        tc_fence_after();
+#pragma unroll
+        for (int d0 = 0; d0 < D; d0 += 32) {
+            uint32_t v[32];
+            tmem_ld32(lane_base + (uint32_t)(kOCol + d0), v);
+#pragma unroll
+            for (int q = 0; q < 32; ++q) o[d0 + q] += __uint_as_float(v[q]);
+        }
+        tc_fence_before();
+        __syncthreads();  // the next chunk overwrites sK, sV, sP and S
+        tc_fence_after();
+    }
+    if (!ok) {
+        set_device_error(t.err, GNN_ERR_TIMEOUT);
+        // an MMA still in flight completes before TMEM is released
+        mbar_wait_bounded(bar, phase);
+    }
+    // merge with the residual CSR result (out, lse_res) through the logsumexp
+    if (ok && valid && l > 0.f) {
+        const float lse_t = (m + log2f(l)) * kLn2T;
+        const float lse_r = t.lse[(int64_t)row * t.heads + h];
+        const float L = lse_r == -INFINITY ? lse_t : fmaxf(lse_r, lse_t) + log1pf(expf(-fabsf(lse_r - lse_t)));
+        const float cr = lse_r == -INFINITY ? 0.f : expf(lse_r - L);
+        const float ct = expf(lse_t - L) / l;
+        float *orow = t.out + (int64_t)row * HD + h * D;
+#pragma unroll
+        for (int d = 0; d < D; d += 4) {
+            const float4 rv = *reinterpret_cast<const float4 *>(orow + d);
+            *reinterpret_cast<float4 *>(orow + d) = make_float4(rv.x * cr + o[d] * ct, rv.y * cr + o[d + 1] * ct,
+                                                                rv.z * cr + o[d + 2] * ct, rv.w * cr + o[d + 3] * ct);
+        }
+        t.lse[(int64_t)row * t.heads + h] = L;
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+    }
+}
+
+template <int D>
+size_t tile_smem_bytes() {
+    return 1024 + (size_t)kRows * D * 2 + 2 * (size_t)kChunkBlocks * 16 * D * 2 + (size_t)kRows * kChunkBlocks * 16 * 2 +
+           64;
+}
+
+template <int D>
+cudaError_t launch_tiles(const TileArgs &t, int32_t n_groups, cudaStream_t s) {
+    static std::once_flag once;
+    static cudaError_t attr = cudaSuccess;
+    std::call_once(once, [] {
+        attr = cudaFuncSetAttribute(k_gt_tiles<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    });
+    if (attr != cudaSuccess) return attr;
+    dim3 grid((unsigned)n_groups, (unsigned)t.heads);
+    k_gt_tiles<D><<<grid, kRows, tile_smem_bytes<D>(), s>>>(t);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+// Workspace of the tile path: residual logsumexp, then the CSR workspace.
+size_t gt_tiles_workspace_bytes(const gnn_csr *g, int32_t heads, int32_t head_dim) {
+    return round_up(sizeof(float) * (size_t)g->n_rows * heads, 256) + gt_workspace_bytes(g, heads, head_dim);
+}
+
+gnn_status gt_attn_tiles(const gnn_csr *g, const gnn_blocksparse *bs, const void *Q, const void *K, const void *V,
+                         int32_t heads, int32_t head_dim, float scale, float *out, float *lse, void *ws,
+                         size_t ws_bytes, cudaStream_t s) {
+    if (head_dim != 32 && head_dim != 64) return GNN_ERR_UNSUPPORTED;
+    if (!bs->grp_blk_offset || !bs->res_rowptr || bs->n_rows != g->n_rows) return GNN_ERR_INVALID_ARG;
+    if (bs->n_groups != (g->n_rows + kRows - 1) / kRows) return GNN_ERR_INVALID_ARG;
+    const size_t need = gt_tiles_workspace_bytes(g, heads, head_dim);
+    if (!ws || ws_bytes < need) return GNN_ERR_WORKSPACE;
+    int32_t *err = device_error_word();
+    if (!err) return GNN_ERR_CUDA;
+    // the residual logsumexp goes to the caller's lse (or the workspace) and
+    // is merged there in place; rows without tiles keep it
+    Carver cv(ws);
+    float *lse_ws = cv.take<float>((size_t)g->n_rows * heads);
+    float *lse_res = lse ? lse : lse_ws;
+    void *csr_ws = static_cast<char *>(ws) + cv.used;
+    // residual edges: fused CSR kernel, writing (out, lse_res)
+    gnn_csr res{g->n_rows, g->n_cols, bs->nnz_residual, bs->res_rowptr, bs->res_colidx, nullptr};
+    gnn_status st = gnn_gt_attn_fwd(&res, nullptr, nullptr, Q, K, V, GNN_BF16, heads, head_dim, scale, out, lse_res,
+                                    csr_ws, ws_bytes - cv.used, s);
+    if (st != GNN_OK) return st;
+    if (bs->n_blocks == 0) return GNN_OK;
+    TileArgs t{};
+    t.grp_blk_offset = bs->grp_blk_offset;
+    t.blk_cols = bs->blk_cols;
+    t.blk_mask = reinterpret_cast<const unsigned long long *>(bs->blk_mask);
+    t.Q = static_cast<const __nv_bfloat16 *>(Q);
+    t.K = static_cast<const __nv_bfloat16 *>(K);
+    t.V = static_cast<const __nv_bfloat16 *>(V);
+    t.out = out;
+    t.lse = lse_res;
+    t.n_rows = g->n_rows;
+    t.heads = heads;
+    t.D = head_dim;
+    t.qscale = scale * kLog2eT;
+    t.err = err;
+    cudaError_t e = head_dim == 32 ? launch_tiles<32>(t, bs->n_groups, s) : launch_tiles<64>(t, bs->n_groups, s);
+    note_launch();
+    if (e != cudaSuccess) return cuda_status(e);
+    return GNN_OK;
+}
+
+}  // namespace gnn

@@ -164,3 +164,64 @@ def test_gt_config4_sampled(gnn):
                                      [0, len(deg) - 1]])).astype(np.int32)
     check_gt(gnn, rp, ci, w["Q"], w["K"], w["V"], 8, 32, w["scale"], rows=rows, tol=TOL_BF16,
              lse_tol=TOL_BF16)
+
+
+# ------------------------------------------------------- GT, tensor-core tiles
+
+def clustered_small(n_clusters, size=256, p=0.3, seed=2, n_extra=None):
+    rng = np.random.default_rng(seed)
+    edges = []
+    for c in range(n_clusters):
+        base = c * size
+        m = rng.random((size, size)) < p
+        d, s = np.nonzero(m)
+        edges += [(base + int(b), base + int(a)) for a, b in zip(d, s)]
+    n = n_clusters * size
+    for _ in range(n // 2 if n_extra is None else n_extra):
+        edges.append((int(rng.integers(n)), int(rng.integers(n))))
+    return G.from_edges(n, edges)
+
+
+def check_gt_tiles(gnn, rp, ci, Q, K, V, heads, D, scale, thr, rows=None):
+    g = gnn.graph_prepare(dev(rp), dev(ci))
+    bs = gnn.gnn_blocksparse_build(g, thr)
+    out, lse = gnn.gnn_gt_attn_fwd(g, dev(Q), dev(K), dev(V), heads, D, scale, bs=bs)
+    ro, rl = oracle.gt(rp, ci, Q, K, V, heads, D, scale, rows=rows)
+    sel = slice(None) if rows is None else rows
+    assert_rowwise_close(out.cpu().numpy()[sel], ro, TOL_BF16, f"gt tiles out thr={thr}")
+    assert_lse_close(lse.cpu().numpy()[sel], rl, TOL_BF16, f"gt tiles lse thr={thr}")
+    return bs
+
+
+@pytest.mark.parametrize("thr", [0.0, 0.25, 0.35, 1.0])
+@pytest.mark.parametrize("heads,D", [(8, 32), (2, 64)])
+def test_gt_tiles_small_clustered(gnn, thr, heads, D):
+    # 5 clusters of 256 nodes (10 row groups, one of them ragged by the extra
+    # 40 nodes), cross-cluster edges that land in sparse tiles
+    rp, ci = clustered_small(5, p=0.3, seed=heads)
+    n = len(rp) - 1
+    Q, K, V = (synth.normal_bf16((n, heads * D), 1.0, 80 + k) for k in range(3))
+    check_gt_tiles(gnn, rp, ci, Q, K, V, heads, D, 1.0 / math.sqrt(D), thr)
+
+
+def test_gt_tiles_ragged_group_and_dense_block(gnn):
+    # 300 nodes: the last 128-row group is partial; a 60-node clique gives
+    # full tiles, a sparse rest gives residual edges
+    rp, ci = G.from_edges(300, [(a, b) for a in range(60) for b in range(60)] +
+                          [(i, (7 * i + 3) % 300) for i in range(300)])
+    n = len(rp) - 1
+    Q, K, V = (synth.normal_bf16((n, 256), 1.0, 90 + k) for k in range(3))
+    for thr in (0.0, 0.5):
+        check_gt_tiles(gnn, rp, ci, Q, K, V, 8, 32, 1.0 / math.sqrt(32), thr)
+
+
+def test_gt_tiles_config4_sampled(gnn):
+    w = synth.workload("c4_clustered_gt")
+    rp, ci = w["rowptr"], w["colidx"]
+    rng = np.random.default_rng(3)
+    rows = np.unique(np.concatenate([rng.choice(len(rp) - 1, 300, replace=False),
+                                     [0, 127, 128, len(rp) - 2]])).astype(np.int32)
+    for thr in (0.0, 0.5):
+        bs = check_gt_tiles(gnn, rp, ci, w["Q"], w["K"], w["V"], 8, 32, w["scale"], thr, rows=rows)
+        if thr == 0.0:
+            assert bs.meta.nnz_residual == 0 and bs.meta.n_tiles_kept > 0
