@@ -242,7 +242,7 @@ def setup_c3(torch, gnn, w):
                            "unfused": (g, H, W, a, heads, D, w["slope"])})
 
 
-def setup_c4(torch, gnn, w):
+def setup_c4(torch, gnn, w, tiles=None):
     g = gnn.graph_prepare(_dev(torch, w["rowptr"]), _dev(torch, w["colidx"]))
     Q, K, V = (_dev(torch, w[k]) for k in ("Q", "K", "V"))
     n = Q.shape[0]
@@ -253,9 +253,23 @@ def setup_c4(torch, gnn, w):
     lse = torch.empty((n, heads), dtype=torch.float32, device="cuda")
     idx = 4 * (n + 1) + 4 * M
     bcomp = idx + 3 * n * HD * 2 + n * HD * 4 + n * heads * 4
-    layers = [Layer("gt_csr", lambda ins: gnn.gnn_gt_attn_fwd(g, ins[0], ins[1], ins[2], heads, D,
-                                                              w["scale"], out=out, lse=lse),
-                    M * HD, bcomp, "alu")]
+    extra = {}
+    bs = None
+    if tiles is not None:
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        bs = gnn.gnn_blocksparse_build(g, tiles)
+        torch.cuda.synchronize()
+        m = bs.meta
+        extra["blocksparse"] = {"threshold": tiles, "build_ms": (time.perf_counter() - t0) * 1e3,
+                                "listed_blocks": m.n_blocks, "kept_tiles": m.n_tiles_kept,
+                                "tile_edges": m.nnz_tiles, "residual_edges": m.nnz_residual,
+                                # S = Q K^T and O = P V over every listed block's 16 columns
+                                "tile_mma_flop": 4.0 * 128 * D * 16 * m.n_blocks * heads}
+    name = "gt_tiles" if bs is not None else "gt_csr"
+    layers = [Layer(name, lambda ins: gnn.gnn_gt_attn_fwd(g, ins[0], ins[1], ins[2], heads, D,
+                                                          w["scale"], bs=bs, out=out, lse=lse),
+                    M * HD, bcomp, "alu" if bs is None else "tensor")]
 
     def oracle_step(rows):
         import oracle
@@ -265,10 +279,11 @@ def setup_c4(torch, gnn, w):
     cfg = {"workload": "c4_clustered_gt", "graph": "1024 clusters x 256 nodes, p=0.3, 1% of "
            "sources rewired, dedup + self-loops", "nodes": n, "edges": M, "heads": heads,
            "head_dim": D, "dtype": "bf16 Q, K, V; fp32 softmax and accumulation; fp32 out",
-           "layers": ["fused GT attention, CSR path"]}
+           "layers": ["fused GT attention, CSR path" if bs is None else
+                      f"GT attention: tcgen05 16x16 tiles (fill >= {tiles}) + CSR residual"]}
     rows = _sample_by_edges(w["rowptr"], 400000)
     return Workload("c4_clustered_gt", layers, [Q, K, V], [out, lse], cfg, "bf16", oracle_step,
-                    rows)
+                    rows, extra=extra)
 
 
 def setup_c5(torch, gnn, w, mapping="auto", ordering="original"):
@@ -464,6 +479,8 @@ def main():
     ap.add_argument("--ordering", default="original",
                     choices=["original", "random", "degree", "rcm"],
                     help="vertex ordering applied before timing (c5_rmat22; prep timed apart)")
+    ap.add_argument("--tiles", type=float, default=None,
+                    help="c4_clustered_gt: tensor-core tile path at this fill threshold")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-comparator", action="store_true",
@@ -488,6 +505,8 @@ def main():
     w = synth.workload(args.workload)
     if args.workload == "c5_rmat22":
         W = setup_c5(torch, gnn, w, args.mapping, args.ordering)
+    elif args.workload == "c4_clustered_gt":
+        W = setup_c4(torch, gnn, w, args.tiles)
     else:
         W = SETUPS[args.workload](torch, gnn, w)
     stream = torch.cuda.current_stream()
@@ -530,6 +549,11 @@ def main():
     extra = {}
     if "reorder_prep" in W.extra:
         extra["reorder_prep"] = W.extra["reorder_prep"]
+    if "blocksparse" in W.extra:
+        bsx = dict(W.extra["blocksparse"])
+        ms_t = per[W.layers[0].name]
+        bsx["tile_mma_tflops"] = bsx["tile_mma_flop"] / (ms_t * 1e-3) / 1e12
+        extra["blocksparse"] = bsx
     if "proj_only" in W.extra:
         fn, b_proj = W.extra["proj_only"]
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))

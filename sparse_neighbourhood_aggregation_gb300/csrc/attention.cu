@@ -511,26 +511,49 @@ __global__ void __launch_bounds__(kAttnWarps * 32) k_attn(AttnArgs a) {
         consume<KIND, T, CPL, LPH>(a, L, R, R.sb, (int32_t)min((int64_t)lo_beg, e1), dq, al, st);
         if (!R.bail) flush_piece<KIND, T, CPL, LPH>(a, L, w, h, st);
     }
-    for (int32_t r = lo; r < lo_end && !R.bail; ++r) {
-        const int32_t rb = __ldg(rowptr + r), re = __ldg(rowptr + r + 1);
-        st.reset();
-        if (re == rb) {
-            store_final<KIND, T, CPL, LPH>(a, L, r, st);
-            continue;
+    // owned rows, 32 at a time: lanes read the bounds of 32 rows and only the
+    // non-empty ones are visited (empty rows are written by k_attn_empty_rows)
+    for (int32_t rbase = lo; rbase < lo_end && !R.bail; rbase += 32) {
+        const int32_t rr = rbase + L.lane;
+        int32_t my_b = 0, my_e = 0;
+        if (rr < lo_end) {
+            my_b = __ldg(rowptr + rr);
+            my_e = __ldg(rowptr + rr + 1);
         }
-        load_dest<KIND, T, CPL, LPH>(a, L, r, dq, &al);
-        if (re - rb > E) {  // heavy: this run holds its first piece (and it is the last owned row)
-            consume<KIND, T, CPL, LPH>(a, L, R, rb, (int32_t)e1, dq, al, st);
-            if (!R.bail) flush_piece<KIND, T, CPL, LPH>(a, L, w, r, st);
-        } else {
-            consume<KIND, T, CPL, LPH>(a, L, R, rb, re, dq, al, st);
-            store_final<KIND, T, CPL, LPH>(a, L, r, st);
+        unsigned todo = __ballot_sync(0xffffffffu, my_e > my_b);
+        while (todo && !R.bail) {
+            const int k = __ffs(todo) - 1;
+            todo &= todo - 1;
+            const int32_t r = rbase + k;
+            const int32_t rb = __shfl_sync(0xffffffffu, my_b, k), re = __shfl_sync(0xffffffffu, my_e, k);
+            st.reset();
+            load_dest<KIND, T, CPL, LPH>(a, L, r, dq, &al);
+            if (re - rb > E) {  // heavy: this run holds its first piece (and it is the last owned row)
+                consume<KIND, T, CPL, LPH>(a, L, R, rb, (int32_t)e1, dq, al, st);
+                if (!R.bail) flush_piece<KIND, T, CPL, LPH>(a, L, w, r, st);
+            } else {
+                consume<KIND, T, CPL, LPH>(a, L, R, rb, re, dq, al, st);
+                store_final<KIND, T, CPL, LPH>(a, L, r, st);
+            }
         }
     }
     if (R.bail) {
         // let the copies still in flight land before the warp leaves
         for (int32_t k = R.kc; k < R.k_issue; ++k) mbar_wait_bounded(R.bars + (k % a.S), (uint32_t)((k / a.S) & 1u));
     }
+}
+
+// Rows without edges: out = 0, lse = -inf (one thread per row and head).
+__global__ void k_attn_empty_rows(const int32_t *__restrict__ rowptr, int32_t n_rows, int32_t HD, int32_t heads,
+                                  float *__restrict__ out, float *__restrict__ lse) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (int64_t)n_rows * heads) return;
+    const int32_t r = (int32_t)(i / heads), h = (int32_t)(i % heads);
+    if (rowptr[r + 1] != rowptr[r]) return;
+    const int32_t D = HD / heads;
+    float *o = out + (int64_t)r * HD + (int64_t)h * D;
+    for (int32_t d = 0; d < D; d += 4) *reinterpret_cast<float4 *>(o + d) = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (lse) lse[i] = -INFINITY;
 }
 
 // GATv2 per-node linear parts: A[i,h] = sum_d lin[hD+d] C[i, hD+d], written
@@ -865,6 +888,13 @@ gnn_status gnn_gatv2_fwd(const gnn_csr *g, const void *prep, const void *H, int3
     A.D = head_dim;
     A.nch = nch;
     ring_shape(A);
+    k_attn_empty_rows<<<(int)(((int64_t)g->n_rows * heads + 255) / 256), 256, 0, s>>>(g->rowptr, g->n_rows, HD,
+                                                                                      heads, out, lse);
+    note_launch();
+    if (g->nnz == 0) {
+        GNN_LAUNCH_CHECK();
+        return GNN_OK;
+    }
     cudaError_t e = dtype == GNN_F32 ? launch_attn<ATT_GATV2, float>(A, cpl, s)
                                      : launch_attn<ATT_GATV2, __nv_bfloat16>(A, cpl, s);
     note_launch();
@@ -921,6 +951,13 @@ gnn_status gnn_gt_attn_fwd(const gnn_csr *g, const void *prep, const gnn_blocksp
     A.D = head_dim;
     A.nch = nch;
     ring_shape(A);
+    k_attn_empty_rows<<<(int)(((int64_t)g->n_rows * heads + 255) / 256), 256, 0, s>>>(g->rowptr, g->n_rows,
+                                                                                      A.HD, heads, out, lse);
+    note_launch();
+    if (g->nnz == 0) {
+        GNN_LAUNCH_CHECK();
+        return GNN_OK;
+    }
     cudaError_t e = dtype == GNN_F32 ? launch_attn<ATT_GT, float>(A, cpl, s)
                                      : launch_attn<ATT_GT, __nv_bfloat16>(A, cpl, s);
     note_launch();
