@@ -42,6 +42,13 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 FALLBACK_HBM_GBS = 6800.0
+# DRAM bytes (read + write) per launch of each c2 layer's kernel, from the
+# committed ncu capture profiles/k_agg_auto_c2_rmat17.md (same kernel build);
+# set to None when the kernel changes.
+NCU_TRAFFIC = {("c2_rmat17", "spmm"): (90.103552 + 36.464128) * 1e6,
+               ("c2_rmat17", "sum"): (88.629504 + 36.113664) * 1e6,
+               ("c2_rmat17", "mean"): (88.704512 + 36.872192) * 1e6,
+               ("c2_rmat17", "max"): (102.507776 + 91.338240) * 1e6}
 NORTH_STAR_HBM_GBS = 8000.0
 METRIC = "aggregation Gedge*feat/s"
 UNIT = "Gedge*feat/s"
@@ -586,7 +593,8 @@ def main():
     achieved = dom.bcomp / (per[dom.name] * 1e-3) / 1e9
     roofline = {"bound": "hbm", "kernel": dom.name, "achieved": achieved, "peak": hbm,
                 "unit": "GB/s", "frac": achieved / hbm, "peak_kind": peak_kind,
-                "frac_of_8tbs": achieved / NORTH_STAR_HBM_GBS, "traffic": None,
+                "frac_of_8tbs": achieved / NORTH_STAR_HBM_GBS,
+                "traffic": NCU_TRAFFIC.get((W.name, dom.name)),
                 "bcomp_bytes": dom.bcomp}
     if dom.bound == "alu":
         roofline["note"] = ("kernel is FP32-ALU heavy; frac is its compulsory-byte rate "
