@@ -172,3 +172,31 @@ def test_host_validation_rejects_bad_arguments(gnn):
     with pytest.raises(gnn.GnnError) as e:
         gnn.gnn_segment_reduce_sum(g, X)
     assert e.value.code == gnn.GNN_ERR_INVALID_ARG
+
+
+def test_config5_rmat22_sampled_original_and_degree_order(gnn):
+    """GCN SpMM at full size (R-MAT scale 22, X bf16 [N,256]) in the launch
+    configuration the benchmark times, on sampled rows, with the original ids
+    and after a degree-order relabel done on the GPU."""
+    w = synth.workload("c5_rmat22")
+    rp, ci, X = w["rowptr"], w["colidx"], w["X"]
+    deg = np.diff(rp)
+    rng = np.random.default_rng(5)
+    rows = np.unique(np.concatenate([np.argsort(-deg, kind="stable")[:3],
+                                     rng.choice(len(deg), 200, replace=False),
+                                     [0, len(deg) - 1]])).astype(np.int32)
+    g = gnn.graph_prepare(dev(rp), dev(ci))
+    Xd = feats_to_dev(X)
+    Y = gnn.gnn_spmm(g, Xd, norm=gnn.GNN_NORM_BOTH).cpu().numpy()
+    assert_rowwise_close(Y[rows], oracle.spmm(rp, ci, X, norm=oracle.NORM_BOTH, rows=rows),
+                         TOL_BF16, "c5 spmm")
+    perm, inv = gnn.gnn_reorder_perm(g, gnn.GNN_PERM_DEGREE)
+    rp2, ci2, X2 = gnn.gnn_apply_perm(g, perm, inv, X=Xd)
+    g2 = gnn.graph_prepare(rp2, ci2)
+    Y2 = gnn.gnn_spmm(g2, X2, norm=gnn.GNN_NORM_BOTH).cpu().numpy()
+    p = perm.cpu().numpy()
+    inv_h = inv.cpu().numpy()
+    # row r of the relabelled result is row p[r] of the original one
+    assert_rowwise_close(Y2[inv_h[rows]], oracle.spmm(rp, ci, X, norm=oracle.NORM_BOTH, rows=rows),
+                         TOL_BF16, "c5 spmm, degree order")
+    assert np.array_equal(p[inv_h[rows]], rows)
