@@ -42,13 +42,14 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 FALLBACK_HBM_GBS = 6800.0
-# DRAM bytes (read + write) per launch of each c2 layer's kernel, from the
-# committed ncu capture profiles/k_agg_auto_c2_rmat17.md (same kernel build);
-# set to None when the kernel changes.
-NCU_TRAFFIC = {("c2_rmat17", "spmm"): (90.103552 + 36.464128) * 1e6,
-               ("c2_rmat17", "sum"): (88.629504 + 36.113664) * 1e6,
-               ("c2_rmat17", "mean"): (88.704512 + 36.872192) * 1e6,
-               ("c2_rmat17", "max"): (102.507776 + 91.338240) * 1e6}
+# DRAM bytes (read + write) per c2 layer (edge-span kernel + heavy-row
+# finalising kernel), from the committed ncu capture
+# profiles/k_agg_span_c2_rmat17.md (same kernel build); set to None when the
+# kernels change.
+NCU_TRAFFIC = {("c2_rmat17", "spmm"): (90.888704 + 33.767424 + 3.152128) * 1e6,
+               ("c2_rmat17", "sum"): (89.338624 + 30.829056 + 3.012096 + 0.001024) * 1e6,
+               ("c2_rmat17", "mean"): (89.171712 + 30.574080 + 3.008000) * 1e6,
+               ("c2_rmat17", "max"): (102.442240 + 82.603776 + 5.842944 + 0.001792) * 1e6}
 NORTH_STAR_HBM_GBS = 8000.0
 METRIC = "aggregation Gedge*feat/s"
 UNIT = "Gedge*feat/s"

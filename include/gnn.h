@@ -95,7 +95,13 @@ size_t gnn_graph_prepare_size(const gnn_csr *g);
  * same graph (IO-aware GNN layers, Appendix D.4, "normalisation as a
  * preprocessing step" and the graph-structure cache).  Fills `prep` with
  * d_out[n_cols] (int32), 1/sqrt(d_in)[n_rows] and 1/sqrt(d_out)[n_cols]
- * (fp32).  prep: device buffer of gnn_graph_prepare_size(g) bytes, 256-byte
+ * (fp32), and the schedule tables of the aggregation and attention kernels:
+ * the first row of every 64-edge run; one row-end bit per edge (a 32-bit
+ * word per 32 edges) with, per word, the rank among non-empty rows of the
+ * row holding its first edge and that row's first edge; the non-empty rows
+ * in order; the first edge of every 64-edge span once a row of degree <= 64
+ * is kept whole in the span it starts in; and the rows of degree > 64.
+ * prep: device buffer of gnn_graph_prepare_size(g) bytes, 256-byte
  * aligned, owned by the caller.  Asynchronous. */
 gnn_status gnn_graph_prepare(const gnn_csr *g, void *prep, size_t prep_bytes, void *stream);
 
@@ -141,7 +147,10 @@ gnn_status gnn_spmm(const gnn_csr *g, const void *prep, int32_t norm, const void
 
 /* Y[i,:] = sum over j in N(i) of X[j,:]  (IO-aware GNN layers, Section
  * 2.2 (ii)).  Empty rows give 0.  Shapes and F as gnn_spmm.  prep may be
- * NULL; when given, the edge-run table it holds replaces a per-run search. */
+ * NULL; when given, rows of 32 16-byte chunks (fp32 F = 128, bf16 F = 256)
+ * run on the edge-span schedule it holds (two launches: the edge stream,
+ * then the rows of degree > 64), and other widths use its edge-run table
+ * instead of a per-run search. */
 gnn_status gnn_segment_reduce_sum(const gnn_csr *g, const void *prep, const void *X,
                                   int32_t x_dtype, int32_t F, float *Y, void *ws,
                                   size_t ws_bytes, void *stream);

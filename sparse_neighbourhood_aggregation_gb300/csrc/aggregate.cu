@@ -7,20 +7,26 @@
 // mappings).
 //
 // GB300 design.  All three families stream 16-byte feature chunks with
-// 128-bit loads; rows are 16-byte aligned.  The AUTO mapping cuts the edge
-// list into runs of E edges, one run per group of LPR lanes (a "worker"),
-// instead of one block per node: light rows are packed several to a worker
-// and heavy rows are split across ceil(deg/E) workers, so every worker does
-// the same number of loads.  Loads of U consecutive edges are issued before
-// any of them is accumulated, whatever row they belong to, which keeps U
-// 16-byte loads in flight per lane even through runs of degree-1 rows.  A
-// row that crosses a run boundary leaves one partial result per worker in
-// the workspace; the last worker to finish it (a ticket counter, no
-// spinning) combines the partials in edge order, so results are
-// deterministic.  For max the partials are (value, source id) pairs combined
-// under the order-preserving key with ties to the smaller id -- the same
-// result as the paper's packed 64-bit atomicMin, without atomics on the
-// feature data.
+// 128-bit loads; rows are 16-byte aligned.  Two AUTO schedules split the
+// edge list, instead of one block per node, so every warp does about the
+// same number of loads:
+//  - k_agg_span (rows of 32 chunks, prepared graph given): spans of 64 edges
+//    from the prepared graph, light rows kept whole, heavy rows cut, row
+//    closes read from prepared row-end bits; heavy-row pieces are folded by
+//    fire-and-forget reductions and finalised by k_agg_span_fix.
+//  - k_agg_auto (any width, with or without the prepared graph): runs of E
+//    edges per group of LPR lanes (a "worker"); light rows packed several to
+//    a worker, heavy rows split across ceil(deg/E) workers; a row that
+//    crosses a run boundary leaves one partial result per worker, folded by
+//    atomics into the slot of its first run, and the last worker to arrive
+//    (a ticket counter, no spinning) finalises it.
+// Loads of U consecutive edges are issued before any of them is accumulated,
+// whatever row they belong to, which keeps U 16-byte loads in flight per lane
+// even through runs of degree-1 rows.  Sums of a row cut into three or more
+// pieces are fp32-order dependent (the pieces arrive in any order); max
+// merges (value, source id) pairs under the order-preserving key with ties
+// to the smaller id -- the paper's packed 64-bit atomic merge -- and is
+// exact and deterministic.
 #include <algorithm>
 
 #include "common.cuh"
@@ -47,6 +53,10 @@ void prep_pointers(const gnn_csr *g, const void *prep, const int32_t **d_out,
                    const float **dinv_in, const float **dinv_out);
 gnn_status check_csr_args(const gnn_csr *g);
 const int32_t *prep_run_table(const gnn_csr *g, const void *prep);
+void prep_span_tables(const gnn_csr *g, const void *prep, const uint32_t **win_flags,
+                      const int32_t **win_rowbase, const int32_t **ne_rows,
+                      const int32_t **win_rowstart, const int32_t **sp_begin,
+                      const int32_t **heavy);
 
 enum AggOp { AGG_WSUM = 0, AGG_MEAN = 1, AGG_MAX = 2 };
 // per-edge weight source / per-row factor source
@@ -66,6 +76,13 @@ struct AggArgs {
     float *carry;           // [n_workers, F] fp32 (max: [n_workers, F] uint64)
     int32_t *tickets;       // [n_workers], zero on entry and on exit
     const int32_t *run_first_row;  // [n_workers+1] from the prepared graph, or null
+    const uint32_t *win_flags;     // prepared row-end bits, one word per 32 edges
+    const int32_t *win_rowbase;    // prepared rank of the row holding edge 32*win
+    const int32_t *ne_rows;        // prepared non-empty rows, ascending
+    const int32_t *win_rowstart;   // prepared first edge of the row holding edge 32*win
+    const int32_t *sp_begin;       // prepared first edge of each edge span
+    const int32_t *heavy;          // prepared rows of degree > kSpanEdges, count at [n_rows]
+    int32_t n_spans;               // edge-span kernel: spans of kSpanEdges edges
     int64_t nnz;
     int64_t n_workers;
     int32_t n_rows;
@@ -100,16 +117,20 @@ struct Acc {
         for (int c = 0; c < CPL; ++c) {
             float f[NV];
             Chunk<T>::unpack(x[c], f);
+            if (OP == AGG_MAX) {
 #pragma unroll
-            for (int k = 0; k < NV; ++k) {
-                if (OP == AGG_MAX) {
+                for (int k = 0; k < NV; ++k) {
                     uint32_t kk = order_key(f[k]);
                     // edges arrive in ascending source id: strict > keeps the
                     // smallest id among equal keys
                     if (kk > key(c, k)) { idx[c][k] = j; v[c][k] = f[k]; }
-                } else {
-                    v[c][k] = fmaf(w, f[k], v[c][k]);
                 }
+            } else {
+                // v += w * f on pairs of features (one rounding each, as fmaf)
+                const uint64_t ww = pk2(w, w);
+#pragma unroll
+                for (int k = 0; k < NV; k += 2)
+                    upk2(fma2(ww, pk2(f[k], f[k + 1]), pk2(v[c][k], v[c][k + 1])), v[c][k], v[c][k + 1]);
             }
         }
     }
@@ -117,14 +138,14 @@ struct Acc {
 
 __device__ __forceinline__ float row_factor(const AggArgs &a, int32_t r, int32_t deg) {
     if (a.row_mode == ROW_RSQRT) return a.dinv_in[r];
-    if (a.row_mode == ROW_RECIP) return deg > 0 ? 1.f / (float)deg : 0.f;
+    if (a.row_mode == ROW_RECIP) return deg > 0 ? __frcp_rn((float)deg) : 0.f;
     return 1.f;
 }
 
 __device__ __forceinline__ float edge_weight(const AggArgs &a, int64_t e, int32_t j) {
     float w = a.values ? __ldg(a.values + e) : 1.f;
     if (a.col_mode == COL_RSQRT) w *= __ldg(a.dinv_out + j);
-    else if (a.col_mode == COL_RECIP) w *= 1.f / (float)__ldg(a.d_out + j);
+    else if (a.col_mode == COL_RECIP) w *= __frcp_rn((float)__ldg(a.d_out + j));
     return w;
 }
 
@@ -135,6 +156,7 @@ __device__ __forceinline__ void store_row(const AggArgs &a, int32_t r, int32_t d
     constexpr int NV = Chunk<T>::N;
     float s = 1.f;
     if (OP == AGG_WSUM) s = row_factor(a, r, deg);
+    const float inv_deg = (OP == AGG_MEAN && deg > 0) ? __frcp_rn((float)deg) : 0.f;
 #pragma unroll
     for (int c = 0; c < CPL; ++c) {
         int64_t base = (int64_t)r * a.F + (int64_t)(c * a.lpr + gl) * NV;
@@ -142,7 +164,7 @@ __device__ __forceinline__ void store_row(const AggArgs &a, int32_t r, int32_t d
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
             if (OP == AGG_WSUM) o[k] = acc.v[c][k] * s;
-            else if (OP == AGG_MEAN) o[k] = deg > 0 ? acc.v[c][k] / (float)deg : 0.f;
+            else if (OP == AGG_MEAN) o[k] = acc.v[c][k] * inv_deg;
             else o[k] = acc.idx[c][k] >= 0 ? acc.v[c][k] : 0.f;
         }
 #pragma unroll
@@ -163,7 +185,9 @@ __device__ __forceinline__ void store_row_f(const AggArgs &a, int32_t r, int32_t
     constexpr int NV = Chunk<T>::N;
     float s = 1.f;
     if (OP == AGG_WSUM)
-        s = a.row_mode == ROW_RSQRT ? rf : (a.row_mode == ROW_RECIP ? (deg > 0 ? 1.f / (float)deg : 0.f) : 1.f);
+        s = a.row_mode == ROW_RSQRT ? rf : (a.row_mode == ROW_RECIP ? (deg > 0 ? __frcp_rn((float)deg) : 0.f) : 1.f);
+    // mean: one correctly rounded reciprocal per row, then a product per feature
+    const float inv_deg = (OP == AGG_MEAN && deg > 0) ? __frcp_rn((float)deg) : 0.f;
 #pragma unroll
     for (int c = 0; c < CPL; ++c) {
         int64_t base = (int64_t)r * a.F + (int64_t)(c * a.lpr + gl) * NV;
@@ -171,7 +195,7 @@ __device__ __forceinline__ void store_row_f(const AggArgs &a, int32_t r, int32_t
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
             if (OP == AGG_WSUM) o[k] = acc.v[c][k] * s;
-            else if (OP == AGG_MEAN) o[k] = deg > 0 ? acc.v[c][k] / (float)deg : 0.f;
+            else if (OP == AGG_MEAN) o[k] = acc.v[c][k] * inv_deg;
             else o[k] = acc.idx[c][k] >= 0 ? acc.v[c][k] : 0.f;
         }
 #pragma unroll
@@ -471,6 +495,298 @@ __global__ void __launch_bounds__(256, (CPL <= 4 ? GNN_AGG_MINB : 2)) k_agg_auto
     }
 }
 
+// Edge-span AUTO kernel for rows of 32 16-byte chunks (fp32 F = 128, bf16
+// F = 256), used when the prepared graph is given.  The prepared graph cuts
+// the edge list into spans of about S = kSpanEdges edges: a row of degree
+// <= S belongs whole to the span it starts in (so a span reads fewer than 2S
+// edges), and a heavier row is cut at every multiple of S.  Its row-end bits
+// (one 32-bit word per 32 edges) say where rows close, its window ranks and
+// list of non-empty rows turn a close into a row id, so the edge loop reads
+// no row pointers and searches for no row, and a row's degree is the distance
+// between two closes.  Each piece of a heavy row is folded with
+// fire-and-forget reductions into the workspace slot of the span the row
+// starts in (fp32 vector adds for sum-like ops; a 64-bit max of
+// (key << 32) | ~source_id for max -- the packed (value, index) merge of
+// IO-aware GNN layers, Appendix D.1, ties to the smaller id); nothing on the
+// edge path waits on another warp, and k_agg_span_fix finalises heavy rows
+// once this grid has finished.  Warps past the last span write the empty
+// rows.
+#ifndef GNN_SPAN_U
+#define GNN_SPAN_U 4
+#endif
+// minimum resident warps per SM / 8, and threads per block
+#ifndef GNN_SPAN_MINB
+#define GNN_SPAN_MINB 4
+#endif
+#ifndef GNN_SPAN_BLOCK
+#define GNN_SPAN_BLOCK 64
+#endif
+constexpr int kSpanBlock = GNN_SPAN_BLOCK;
+constexpr int32_t kEmptyRowsPerWarp = 256;
+
+// arr[i] for a run-time i without local memory (a chain of selects)
+template <int N, class V>
+__device__ __forceinline__ V pick(const V (&arr)[N], int i) {
+    V r = arr[0];
+#pragma unroll
+    for (int k = 1; k < N; ++k)
+        if (i == k) r = arr[k];
+    return r;
+}
+
+// Row-end bits of edges [e, e+32) (bit i for edge e+i), e not necessarily
+// a multiple of 32.
+__device__ __forceinline__ uint32_t end_bits(const uint32_t *__restrict__ flags, int32_t n_win,
+                                             int32_t e) {
+    const int32_t lo = e >> 5, sh = e & 31;
+    const uint32_t w0 = __ldg(flags + lo);
+    if (sh == 0) return w0;
+    const uint32_t w1 = lo + 1 < n_win ? __ldg(flags + lo + 1) : 0u;
+    return __funnelshift_r(w0, w1, sh);
+}
+
+// Zero rows (argmax -1) for the empty rows among [q*256, (q+1)*256).
+template <int OP>
+__device__ __forceinline__ void write_empty_rows(const AggArgs &a, int32_t q, int lane) {
+    const unsigned FULL = 0xffffffffu;
+    constexpr int NB = kEmptyRowsPerWarp / 32;
+    const int32_t r0 = q * kEmptyRowsPerWarp;
+    bool empty[NB];
+#pragma unroll
+    for (int i = 0; i < NB; ++i) {
+        const int32_t r = r0 + 32 * i + lane;
+        empty[i] = r < a.n_rows && __ldg(a.rowptr + r + 1) == __ldg(a.rowptr + r);
+    }
+    const int32_t n4 = a.F / 4;
+#pragma unroll
+    for (int i = 0; i < NB; ++i) {
+        unsigned m = __ballot_sync(FULL, empty[i]);
+        while (m) {
+            const int32_t r = r0 + 32 * i + __ffs(m) - 1;
+            m &= m - 1;
+            float4 *y = reinterpret_cast<float4 *>(a.Y + (size_t)r * a.F);
+            for (int32_t c = lane; c < n4; c += 32) y[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (OP == AGG_MAX && a.argmax) {
+                int4 *am = reinterpret_cast<int4 *>(a.argmax + (size_t)r * a.F);
+                for (int32_t c = lane; c < n4; c += 32) am[c] = make_int4(-1, -1, -1, -1);
+            }
+        }
+    }
+}
+
+// Fold one piece of a heavy row into workspace slot `slot` (no return value
+// is used, so these compile to reductions that the warp does not wait for).
+template <int OP, class T>
+__device__ __forceinline__ void fold_piece(const AggArgs &a, int32_t slot, const Acc<OP, T, 1> &acc,
+                                           int lane) {
+    constexpr int NV = Chunk<T>::N;
+    const int64_t off = (int64_t)slot * a.F + (int64_t)lane * NV;
+#pragma unroll
+    for (int k = 0; k < NV; k += 4) {
+        if (OP == AGG_MAX) {
+            unsigned long long *dst = reinterpret_cast<unsigned long long *>(a.carry) + off + k;
+#pragma unroll
+            for (int z = 0; z < 4; ++z) {
+                const unsigned long long packed =
+                    ((unsigned long long)acc.key(0, k + z) << 32) |
+                    (unsigned long long)(0xFFFFFFFFu - (uint32_t)acc.idx[0][k + z]);
+                atomicMax(dst + z, packed);
+            }
+        } else {
+            atomicAdd(reinterpret_cast<float4 *>(a.carry + off + k),
+                      make_float4(acc.v[0][k], acc.v[0][k + 1], acc.v[0][k + 2], acc.v[0][k + 3]));
+        }
+    }
+}
+
+// WT = false: unit edge weights and row factor 1 (segment sum / mean / max);
+// WT = true: the SpMM's per-edge weights and row factors.
+template <int OP, class T, bool WT>
+__global__ void __launch_bounds__(kSpanBlock, ((OP != AGG_MAX && sizeof(T) == 4) ? GNN_SPAN_MINB : GNN_SPAN_MINB - 1) * 256 / kSpanBlock)
+k_agg_span(AggArgs a) {
+    constexpr int U = GNN_SPAN_U;
+    const unsigned FULL = 0xffffffffu;
+    // let the finalising kernel start its launch while this grid drains
+    asm volatile("griddepcontrol.launch_dependents;");
+    const int lane = threadIdx.x & 31;
+    const int32_t w = (int32_t)(((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+    if (w >= a.n_spans) {
+        if (w - a.n_spans < (a.n_rows + kEmptyRowsPerWarp - 1) / kEmptyRowsPerWarp)
+            write_empty_rows<OP>(a, w - a.n_spans, lane);
+        return;
+    }
+    const int32_t b0 = __ldg(a.sp_begin + w), b1 = __ldg(a.sp_begin + w + 1);
+    if (b0 >= b1) return;
+    const int32_t n_win = (int32_t)((a.nnz + 31) >> 5);
+    const bool weighted = WT && (a.values || a.col_mode != COL_ONE);
+    const bool rsq = WT && a.row_mode == ROW_RSQRT;
+
+    // first window's column ids (the next window's are fetched one ahead)
+    int32_t c_cur = b0 + lane < b1 ? __ldg(a.colidx + b0 + lane) : 0;
+    int32_t c_nxt = b0 + 32 + lane < b1 ? __ldg(a.colidx + b0 + 32 + lane) : 0;
+    // rank of the row holding b0 = row ends before b0
+    const uint32_t wb0 = __ldg(a.win_flags + (b0 >> 5));
+    const int32_t k0 = __ldg(a.win_rowbase + (b0 >> 5)) + __popc(wb0 & ((1u << (b0 & 31)) - 1u));
+    // a span that starts inside a row starts inside a heavy row
+    const bool head0 = b0 > 0 && !((__ldg(a.win_flags + ((b0 - 1) >> 5)) >> ((b0 - 1) & 31)) & 1u);
+    bool head = head0;
+    const int32_t head_slot = head0 ? __ldg(a.win_rowstart + (b0 >> 5)) / kSpanEdges : 0;
+    // lane l holds the id (and row factor) of the row of rank k0 + kofs + l
+    int32_t kofs = 0;
+    int32_t rid = k0 + lane < a.n_rows ? __ldg(a.ne_rows + k0 + lane) : 0;
+    float w_cur = (weighted && b0 + lane < b1) ? edge_weight(a, b0 + lane, c_cur) : 1.f;
+    float rf = rsq ? __ldg(a.dinv_in + rid) : 1.f;
+
+    Acc<OP, T, 1> acc;
+    acc.reset();
+    int32_t k = 0;     // rows closed so far in this span
+    int32_t rs = b0;   // first edge of the open row
+    uint32_t last_closed = 1u;
+#pragma unroll 1
+    for (int32_t cb = b0; cb < b1; cb += 32) {
+        const int n = min(32, b1 - cb);
+        const uint32_t bits_all = end_bits(a.win_flags, n_win, cb);
+        last_closed = (bits_all >> (n - 1)) & 1u;
+        const uint32_t bits = n == 32 ? bits_all : bits_all & ((1u << n) - 1u);
+#pragma unroll 1
+        for (int u0 = 0; u0 < n; u0 += U) {
+            uint4 xv[U];
+            int32_t jv[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                jv[u] = __shfl_sync(FULL, c_cur, (u0 + u) & 31);
+                if (u0 + u < n) xv[u] = ldg16(a.X + (size_t)jv[u] * 32 + lane);
+            }
+            const uint32_t gb = (bits >> u0) & ((1u << U) - 1u);
+            if (gb == 0 && u0 + U <= n) {
+                // no row closes inside this group
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const float ww = weighted ? __shfl_sync(FULL, w_cur, (u0 + u) & 31) : 1.f;
+                    acc.add(&xv[u], ww, jv[u]);
+                }
+                continue;
+            }
+            if (!head) {
+                // rows close here, all of them whole rows of this span: keep
+                // the ids of the next U ranks in the lane window
+                if (k - kofs > 32 - U) {
+                    kofs = k;
+                    rid = k0 + kofs + lane < a.n_rows ? __ldg(a.ne_rows + k0 + kofs + lane) : 0;
+                    if (rsq) rf = __ldg(a.dinv_in + rid);
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    if (u0 + u < n) {
+                        const float ww = weighted ? __shfl_sync(FULL, w_cur, (u0 + u) & 31) : 1.f;
+                        acc.add(&xv[u], ww, jv[u]);
+                        if ((gb >> u) & 1u) {
+                            const int32_t e = cb + u0 + u;
+                            const int32_t r = __shfl_sync(FULL, rid, k - kofs);
+                            const float f = rsq ? __shfl_sync(FULL, rf, k - kofs) : 1.f;
+                            store_row_f<OP, T, 1>(a, r, e - rs + 1, f, acc, lane);
+                            acc.reset();
+                            ++k;
+                            rs = e + 1;
+                        }
+                    }
+                }
+                continue;
+            }
+            // the group where the heavy row this span started inside closes
+#pragma unroll 1
+            for (int u = 0; u < U && u0 + u < n; ++u) {
+                const float ww = weighted ? __shfl_sync(FULL, w_cur, (u0 + u) & 31) : 1.f;
+                const uint4 x = pick(xv, u);
+                acc.add(&x, ww, pick(jv, u));
+                if ((gb >> u) & 1u) {
+                    const int32_t e = cb + u0 + u;
+                    if (head) {
+                        fold_piece<OP, T>(a, head_slot, acc, lane);
+                        head = false;
+                    } else {
+                        if (k - kofs == 32) {
+                            kofs += 32;
+                            rid = k0 + kofs + lane < a.n_rows ? __ldg(a.ne_rows + k0 + kofs + lane) : 0;
+                            if (rsq) rf = __ldg(a.dinv_in + rid);
+                        }
+                        const int32_t r = __shfl_sync(FULL, rid, k - kofs);
+                        const float f = rsq ? __shfl_sync(FULL, rf, k - kofs) : 1.f;
+                        store_row_f<OP, T, 1>(a, r, e - rs + 1, f, acc, lane);
+                    }
+                    acc.reset();
+                    ++k;
+                    rs = e + 1;
+                }
+            }
+        }
+        // advance the column window
+        c_cur = c_nxt;
+        const int32_t en = cb + 64 + lane;
+        c_nxt = en < b1 ? __ldg(a.colidx + en) : 0;
+        if (weighted) w_cur = cb + 32 + lane < b1 ? edge_weight(a, cb + 32 + lane, c_cur) : 1.f;
+    }
+    // a heavy row reaches past this span: leave its piece in the slot of the
+    // span it starts in (an earlier one if it never closed here)
+    if (!last_closed) fold_piece<OP, T>(a, head ? head_slot : w, acc, lane);
+}
+
+// Finalise heavy rows (degree > S, every one of them cut by at least one
+// span boundary): a persistent grid of warps strides over the prepared list
+// of heavy rows; for each, the warp reads the row's slot (the span its first
+// edge falls in), clears it and stores the row.
+template <int OP, class T>
+__global__ void __launch_bounds__(256) k_agg_span_fix(AggArgs a) {
+    constexpr int NV = Chunk<T>::N;
+    const int lane = threadIdx.x & 31;
+    const int32_t nw = (int32_t)((gridDim.x * blockDim.x) >> 5);
+    int32_t q = (int32_t)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+    // the list is prep data: read it before waiting for the span kernel
+    const int32_t n_heavy = __ldg(a.heavy + a.n_rows);
+    int32_t row = q < n_heavy ? __ldg(a.heavy + q) : 0;
+    int32_t rb = q < n_heavy ? __ldg(a.rowptr + row) : 0;
+    int32_t re = q < n_heavy ? __ldg(a.rowptr + row + 1) : 0;
+    // wait for the span kernel (its whole grid, memory included)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    for (; q < n_heavy; q += nw) {
+        const int32_t slot = rb / kSpanEdges;
+        Acc<OP, T, 1> acc;
+        const int64_t off = (int64_t)slot * a.F + (int64_t)lane * NV;
+#pragma unroll
+        for (int k = 0; k < NV; k += 4) {
+            if (OP == AGG_MAX) {
+                unsigned long long *p = reinterpret_cast<unsigned long long *>(a.carry) + off + k;
+#pragma unroll
+                for (int z = 0; z < 4; ++z) {
+                    const unsigned long long v = __ldcg(p + z);
+                    const uint32_t key = (uint32_t)(v >> 32);
+                    const uint32_t u = (key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key;
+                    acc.v[0][k + z] = __uint_as_float(u);
+                    acc.idx[0][k + z] = (int32_t)(0xFFFFFFFFu - (uint32_t)v);
+                    p[z] = 0ull;
+                }
+            } else {
+                float4 *p = reinterpret_cast<float4 *>(a.carry + off + k);
+                const float4 v = __ldcg(p);
+                acc.v[0][k] = v.x;
+                acc.v[0][k + 1] = v.y;
+                acc.v[0][k + 2] = v.z;
+                acc.v[0][k + 3] = v.w;
+                *p = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+        const int32_t cur = row, deg = re - rb;
+        // next row's list entry and pointers while this one is stored
+        const int32_t qn = q + nw;
+        if (qn < n_heavy) {
+            row = __ldg(a.heavy + qn);
+            rb = __ldg(a.rowptr + row);
+            re = __ldg(a.rowptr + row + 1);
+        }
+        store_row<OP, T, 1>(a, cur, deg, acc, lane);
+    }
+}
+
 // FEAT mapping: one group of lpr lanes per destination row, lanes over
 // feature chunks, neighbours in sequence (IO-aware GNN layers, Section 4.1,
 // feature-parallel "dot-aggr" mapping).
@@ -599,7 +915,7 @@ static int64_t n_workers_for(const gnn_csr *g, int32_t E) {
 
 size_t agg_workspace_bytes(const gnn_csr *g, int32_t op, int32_t x_dtype_unused, int32_t F) {
     (void)x_dtype_unused;
-    int64_t nw = n_workers_for(g, kRunEdges);
+    int64_t nw = n_workers_for(g, std::min(kRunEdges, kSpanEdges));
     size_t word = op == GNN_OP_MAX ? sizeof(unsigned long long) : sizeof(float);
     size_t b = round_up(word * (size_t)nw * (size_t)F, 256);
     b += round_up(sizeof(int32_t) * (size_t)nw, 256);
@@ -632,6 +948,36 @@ static void launch_feat(const AggArgs &a, int cpl, cudaStream_t s) {
         case 4: k_agg_feat<T, 4><<<blocks, 256, 0, s>>>(a); break;
         default: k_agg_feat<T, 8><<<blocks, 256, 0, s>>>(a); break;
     }
+}
+
+// The span kernel, then (if any span boundary exists) the kernel that
+// finalises cut rows, launched as a programmatic dependent of the first so
+// its launch overlaps the span kernel's last wave.
+template <int OP, class T, bool WT>
+static cudaError_t launch_span(const AggArgs &a, cudaStream_t s) {
+    const int64_t warps =
+        (int64_t)a.n_spans + ((int64_t)a.n_rows + kEmptyRowsPerWarp - 1) / kEmptyRowsPerWarp;
+    k_agg_span<OP, T, WT><<<(int)((warps * 32 + kSpanBlock - 1) / kSpanBlock), kSpanBlock, 0, s>>>(a);
+    note_launch();
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || a.n_spans <= 1) return e;
+    // heavy rows number at most nnz / (S + 1); a few blocks per SM stride over them
+    const int64_t max_heavy = a.nnz / (kSpanEdges + 1);
+    const int64_t fix_blocks = std::min<int64_t>((max_heavy * 32 + 255) / 256, (int64_t)sm_count() * 4);
+    if (fix_blocks <= 0) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)fix_blocks);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, k_agg_span_fix<OP, T>, a);
+    note_launch();
+    return e;
 }
 
 gnn_status run_aggregate(const gnn_csr *g, const void *prep, int32_t op, int32_t norm,
@@ -696,8 +1042,29 @@ gnn_status run_aggregate(const gnn_csr *g, const void *prep, int32_t op, int32_t
     if (!ws || ws_bytes < need) return GNN_ERR_WORKSPACE;
     if (!aligned256(ws)) return GNN_ERR_INVALID_ARG;
     Carver cv(ws);
-    a.carry = cv.take<float>((size_t)a.n_workers * F * (op == GNN_OP_MAX ? 2 : 1));
-    a.tickets = cv.take<int32_t>((size_t)a.n_workers);
+    const int64_t n_slots = n_workers_for(g, std::min(kRunEdges, kSpanEdges));
+    a.carry = cv.take<float>((size_t)n_slots * F * (op == GNN_OP_MAX ? 2 : 1));
+    a.tickets = cv.take<int32_t>((size_t)n_slots);
+
+    if (prep && sh.V == 32) {
+        prep_span_tables(g, prep, &a.win_flags, &a.win_rowbase, &a.ne_rows, &a.win_rowstart,
+                         &a.sp_begin, &a.heavy);
+        a.E = kSpanEdges;
+        a.n_spans = (int32_t)((g->nnz + kSpanEdges - 1) / kSpanEdges);
+        const bool wt = a.values || a.col_mode != COL_ONE || a.row_mode != ROW_ONE;
+        cudaError_t e;
+        if (op == GNN_OP_MAX) e = bf ? launch_span<AGG_MAX, __nv_bfloat16, false>(a, s)
+                                     : launch_span<AGG_MAX, float, false>(a, s);
+        else if (op == GNN_OP_MEAN) e = bf ? launch_span<AGG_MEAN, __nv_bfloat16, false>(a, s)
+                                           : launch_span<AGG_MEAN, float, false>(a, s);
+        else if (wt) e = bf ? launch_span<AGG_WSUM, __nv_bfloat16, true>(a, s)
+                            : launch_span<AGG_WSUM, float, true>(a, s);
+        else e = bf ? launch_span<AGG_WSUM, __nv_bfloat16, false>(a, s)
+                    : launch_span<AGG_WSUM, float, false>(a, s);
+        if (e != cudaSuccess) return cuda_status(e);
+        GNN_LAUNCH_CHECK();
+        return GNN_OK;
+    }
 
     if (op == GNN_OP_MAX) {
         if (bf) launch_auto<AGG_MAX, __nv_bfloat16>(a, sh.cpl, s);

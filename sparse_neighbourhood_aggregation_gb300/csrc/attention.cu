@@ -150,27 +150,6 @@ __device__ __forceinline__ float exp2_approx(float x) {
     return y;
 }
 
-// Packed fp32 pairs (Blackwell f32x2 instructions): d += a * b and a + b on
-// two lanes of a 64-bit register pair.
-__device__ __forceinline__ uint64_t pk2(float x, float y) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
-    return r;
-}
-__device__ __forceinline__ void upk2(uint64_t r, float &x, float &y) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(r));
-}
-__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-
 template <class T, int CPL>
 __device__ __forceinline__ void unpack_row(const uint4 *v, float *f) {
 #pragma unroll

@@ -31,6 +31,13 @@ inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 #define GNN_RUN_EDGES 64
 #endif
 constexpr int32_t kRunEdges = GNN_RUN_EDGES;
+// Edges per span of the edge-span aggregation kernel (a multiple of 32); the
+// prepared graph stores each span's first edge.
+#ifndef GNN_SPAN_EDGES
+#define GNN_SPAN_EDGES 64
+#endif
+constexpr int32_t kSpanEdges = GNN_SPAN_EDGES;
+static_assert(kSpanEdges % 32 == 0, "spans are whole 32-edge windows");
 inline int64_t n_runs(int64_t nnz, int32_t E) {
     int64_t n = (nnz + E - 1) / E;
     return n > 0 ? n : 1;
@@ -116,5 +123,27 @@ __device__ __forceinline__ uint32_t order_key(float v) {
 }
 
 __device__ __forceinline__ int lane_id() { return threadIdx.x & 31; }
+
+// Packed fp32 pairs (Blackwell f32x2 instructions): d += a * b and a + b on
+// two lanes of a 64-bit register pair.
+__device__ __forceinline__ uint64_t pk2(float x, float y) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
+    return r;
+}
+__device__ __forceinline__ void upk2(uint64_t r, float &x, float &y) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(r));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 
 }  // namespace gnn

@@ -3,6 +3,8 @@
 #include <atomic>
 #include <mutex>
 
+#include <cub/device/device_scan.cuh>
+
 #include "common.cuh"
 
 namespace gnn {
@@ -94,6 +96,82 @@ __global__ void k_validate_csr(const int32_t *__restrict__ rowptr, const int32_t
     }
 }
 
+// Row-end bits of the edge list: bit (e & 31) of word e >> 5 is set when
+// edge e is the last edge of its row.  Rows are independent, so the ORs
+// commute and the result is exact.
+__global__ void k_row_end_flags(const int32_t *__restrict__ rowptr, int32_t n_rows, int64_t nnz,
+                                uint32_t *__restrict__ flags, int32_t *err) {
+    int32_t stride = gridDim.x * blockDim.x;
+    for (int32_t r = blockIdx.x * blockDim.x + threadIdx.x; r < n_rows; r += stride) {
+        int32_t b = rowptr[r], e = rowptr[r + 1];
+        if (e <= b) continue;
+        if (b < 0 || (int64_t)e > nnz) { set_device_error(err, GNN_ERR_DEVICE_CHECK); continue; }
+        atomicOr(flags + ((e - 1) >> 5), 1u << ((e - 1) & 31));
+    }
+}
+
+__global__ void k_popc_words(const uint32_t *__restrict__ flags, int32_t n, int32_t *__restrict__ cnt) {
+    int32_t stride = gridDim.x * blockDim.x;
+    for (int32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) cnt[i] = __popc(flags[i]);
+}
+
+// ne_rows[k] = the k-th non-empty row: its rank is the number of row ends
+// before its own last edge, read from the scanned window counts.
+__global__ void k_nonempty_rows(const int32_t *__restrict__ rowptr, int32_t n_rows, int64_t nnz,
+                                const uint32_t *__restrict__ flags,
+                                const int32_t *__restrict__ win_rowbase,
+                                int32_t *__restrict__ ne_rows) {
+    int32_t stride = gridDim.x * blockDim.x;
+    for (int32_t r = blockIdx.x * blockDim.x + threadIdx.x; r < n_rows; r += stride) {
+        int32_t b = rowptr[r], e = rowptr[r + 1];
+        if (e <= b || b < 0 || (int64_t)e > nnz) continue;
+        int32_t last = e - 1;
+        int32_t k = win_rowbase[last >> 5] + __popc(flags[last >> 5] & ((1u << (last & 31)) - 1u));
+        if ((uint32_t)k < (uint32_t)n_rows) ne_rows[k] = r;
+    }
+}
+
+// win_rowstart[win] = first edge of the row holding edge 32*win.
+__global__ void k_win_rowstart(const int32_t *__restrict__ rowptr, int32_t n_rows, int32_t n_win,
+                               const int32_t *__restrict__ win_rowbase,
+                               const int32_t *__restrict__ ne_rows, int32_t *__restrict__ out) {
+    int32_t stride = gridDim.x * blockDim.x;
+    for (int32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < n_win; i += stride) {
+        const int32_t k = win_rowbase[i];
+        const int32_t r = (uint32_t)k < (uint32_t)n_rows ? ne_rows[k] : 0;
+        out[i] = rowptr[r];
+    }
+}
+
+// sp_begin[w] = first edge of span w.  The nominal span is [w*S, (w+1)*S);
+// a row of degree <= S that crosses w*S belongs whole to span w-1, so span w
+// starts after it; a heavier row is cut at w*S.  sp_begin[n_spans] = nnz.
+__global__ void k_span_begin(const int32_t *__restrict__ rowptr, int64_t nnz, int32_t n_spans,
+                             const uint32_t *__restrict__ flags,
+                             const int32_t *__restrict__ win_rowbase,
+                             const int32_t *__restrict__ ne_rows, int32_t n_rows,
+                             int32_t *__restrict__ out) {
+    int32_t stride = gridDim.x * blockDim.x;
+    for (int32_t w = blockIdx.x * blockDim.x + threadIdx.x; w <= n_spans; w += stride) {
+        if (w == n_spans) { out[w] = (int32_t)nnz; continue; }
+        const int32_t e = w * kSpanEdges;
+        if (e == 0 || ((flags[(e - 1) >> 5] >> ((e - 1) & 31)) & 1u)) { out[w] = e; continue; }
+        const int32_t k = win_rowbase[e >> 5];
+        const int32_t r = (uint32_t)k < (uint32_t)n_rows ? ne_rows[k] : 0;
+        const int32_t s = rowptr[r], t = rowptr[r + 1];
+        out[w] = (t - s > kSpanEdges) ? e : t;
+    }
+}
+
+// Rows of degree > S (the ones the edge-span kernel cuts), appended in any
+// order; heavy[n_rows] holds their count.
+__global__ void k_heavy_rows(const int32_t *__restrict__ rowptr, int32_t n_rows,
+                             int32_t *__restrict__ heavy) {
+    int32_t stride = gridDim.x * blockDim.x;
+    for (int32_t r = blockIdx.x * blockDim.x + threadIdx.x; r < n_rows; r += stride)
+        if (rowptr[r + 1] - rowptr[r] > kSpanEdges) heavy[atomicAdd(heavy + n_rows, 1)] = r;
+}
+
 }  // namespace gnn
 
 using namespace gnn;
@@ -104,6 +182,17 @@ struct PrepLayout {
     float *dinv_in;
     float *dinv_out;
     int32_t *run_first_row;  // [n_runs(kRunEdges) + 1]
+    uint32_t *win_flags;     // [n_win] row-end bits per 32-edge window
+    int32_t *win_count;      // [n_win] popcounts (scan input)
+    int32_t *win_rowbase;    // [n_win] rank among non-empty rows of the row holding edge 32*win
+    int32_t *ne_rows;        // [n_rows] non-empty rows, ascending (first n_nonempty entries)
+    int32_t *win_rowstart;   // [n_win] first edge of the row holding edge 32*win
+    int32_t *sp_begin;       // [n_spans + 1] first edge of each edge span
+    int32_t *heavy;          // [n_rows + 1] rows of degree > kSpanEdges, then their count
+    int32_t n_spans;
+    void *scan_tmp;
+    size_t scan_tmp_bytes;
+    int32_t n_win;
     size_t bytes;
 };
 
@@ -114,6 +203,20 @@ PrepLayout prep_layout(const gnn_csr *g, void *base) {
     L.dinv_in = c.take<float>((size_t)g->n_rows);
     L.dinv_out = c.take<float>((size_t)g->n_cols);
     L.run_first_row = c.take<int32_t>((size_t)n_runs(g->nnz, kRunEdges) + 1);
+    L.n_win = (int32_t)((g->nnz + 31) / 32);
+    L.win_flags = c.take<uint32_t>((size_t)L.n_win);
+    L.win_count = c.take<int32_t>((size_t)L.n_win);
+    L.win_rowbase = c.take<int32_t>((size_t)L.n_win);
+    L.ne_rows = c.take<int32_t>((size_t)g->n_rows);
+    L.win_rowstart = c.take<int32_t>((size_t)L.n_win);
+    L.n_spans = (int32_t)((g->nnz + kSpanEdges - 1) / kSpanEdges);
+    L.sp_begin = c.take<int32_t>((size_t)L.n_spans + 1);
+    L.heavy = c.take<int32_t>((size_t)g->n_rows + 1);
+    L.scan_tmp_bytes = 0;
+    if (L.n_win > 0)
+        cub::DeviceScan::ExclusiveSum(nullptr, L.scan_tmp_bytes, (const int32_t *)nullptr,
+                                      (int32_t *)nullptr, L.n_win);
+    L.scan_tmp = c.take<uint8_t>(L.scan_tmp_bytes);
     L.bytes = c.used;
     return L;
 }
@@ -147,6 +250,19 @@ void prep_pointers(const gnn_csr *g, const void *prep, const int32_t **d_out,
 
 const int32_t *prep_run_table(const gnn_csr *g, const void *prep) {
     return prep_layout(g, const_cast<void *>(prep)).run_first_row;
+}
+
+void prep_span_tables(const gnn_csr *g, const void *prep, const uint32_t **win_flags,
+                      const int32_t **win_rowbase, const int32_t **ne_rows,
+                      const int32_t **win_rowstart, const int32_t **sp_begin,
+                      const int32_t **heavy) {
+    PrepLayout L = prep_layout(g, const_cast<void *>(prep));
+    *sp_begin = L.sp_begin;
+    *heavy = L.heavy;
+    *win_flags = L.win_flags;
+    *win_rowbase = L.win_rowbase;
+    *ne_rows = L.ne_rows;
+    *win_rowstart = L.win_rowstart;
 }
 
 gnn_status check_csr_args(const gnn_csr *g) {
@@ -198,6 +314,35 @@ gnn_status gnn_graph_prepare(const gnn_csr *g, void *prep, size_t prep_bytes, vo
                                                          L.run_first_row);
     note_launch();
     GNN_LAUNCH_CHECK();
+    // edge-span tables: row-end bits, their window ranks and the non-empty rows
+    if (L.n_win > 0 && g->n_rows > 0) {
+        cudaError_t e = cudaMemsetAsync(L.win_flags, 0, sizeof(uint32_t) * (size_t)L.n_win, s);
+        if (e != cudaSuccess) return cuda_status(e);
+        // ranks past the last non-empty row read row 0, a valid index
+        e = cudaMemsetAsync(L.ne_rows, 0, sizeof(int32_t) * (size_t)g->n_rows, s);
+        if (e != cudaSuccess) return cuda_status(e);
+        int rb = (int)std::min<int64_t>((g->n_rows + 255) / 256, (int64_t)sms * 8);
+        int wb = (int)std::min<int64_t>((L.n_win + 255) / 256, (int64_t)sms * 8);
+        k_row_end_flags<<<rb, 256, 0, s>>>(g->rowptr, g->n_rows, g->nnz, L.win_flags, err);
+        k_popc_words<<<wb, 256, 0, s>>>(L.win_flags, L.n_win, L.win_count);
+        note_launch(2);
+        GNN_LAUNCH_CHECK();
+        size_t tb = L.scan_tmp_bytes;
+        e = cub::DeviceScan::ExclusiveSum(L.scan_tmp, tb, L.win_count, L.win_rowbase, L.n_win, s);
+        if (e != cudaSuccess) return cuda_status(e);
+        k_nonempty_rows<<<rb, 256, 0, s>>>(g->rowptr, g->n_rows, g->nnz, L.win_flags,
+                                           L.win_rowbase, L.ne_rows);
+        k_win_rowstart<<<wb, 256, 0, s>>>(g->rowptr, g->n_rows, L.n_win, L.win_rowbase, L.ne_rows,
+                                          L.win_rowstart);
+        const int sb = (int)std::min<int64_t>((L.n_spans + 1 + 255) / 256, (int64_t)sms * 8);
+        k_span_begin<<<sb, 256, 0, s>>>(g->rowptr, g->nnz, L.n_spans, L.win_flags, L.win_rowbase,
+                                        L.ne_rows, g->n_rows, L.sp_begin);
+        e = cudaMemsetAsync(L.heavy + g->n_rows, 0, sizeof(int32_t), s);
+        if (e != cudaSuccess) return cuda_status(e);
+        k_heavy_rows<<<rb, 256, 0, s>>>(g->rowptr, g->n_rows, L.heavy);
+        note_launch(4);
+        GNN_LAUNCH_CHECK();
+    }
     return GNN_OK;
 }
 

@@ -120,6 +120,50 @@ def test_empty_graph_and_trailing_empty_rows(gnn):
     run_all(gnn, rp, ci, np.random.default_rng(0).standard_normal((300, 32)).astype(np.float32))
 
 
+def _short_rows_graph(n=6000, seed=7):
+    """Rows of degree 0, 1 and 2 in random order (so one 64-edge span holds
+    more than 32 rows), a run of 700 empty rows, 300 trailing empty rows and
+    two heavy rows."""
+    rng = np.random.default_rng(seed)
+    deg = rng.choice([0, 1, 1, 2], n)
+    deg[2000:2700] = 0
+    deg[n - 300:] = 0
+    deg[[100, 4000]] = [900, 2100]
+    rp = np.zeros(n + 1, np.int32)
+    rp[1:] = np.cumsum(deg)
+    ci = np.concatenate([np.sort(rng.choice(n, d, replace=False)) for d in deg]).astype(np.int32)
+    return rp, ci
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_short_rows_and_empty_runs(gnn, dtype):
+    rp, ci = _short_rows_graph()
+    n = len(rp) - 1
+    if dtype == "f32":
+        X, tol = synth.normal_f32((n, 128), 1.0, 21), TOL_F32
+    else:
+        X, tol = synth.normal_bf16((n, 256), 1.0, 21), TOL_BF16
+    run_all(gnn, rp, ci, X, tol=tol)
+
+
+def test_unprepared_graph(gnn):
+    """Without the prepared graph each run finds its rows by search."""
+    rp, ci = _hub_graph(2000, hubs=(1, 1999), deg=1500, seed=6)
+    n = len(rp) - 1
+    X = synth.normal_f32((n, 128), 1.0, 13)
+    g = gnn.Graph(dev(rp), dev(ci), prepare=False)
+    Xd = dev(X)
+    assert_rowwise_close(gnn.gnn_spmm(g, Xd, norm=gnn.GNN_NORM_NONE).cpu().numpy(),
+                         oracle.spmm(rp, ci, X, norm=oracle.NORM_NONE), TOL_F32, "spmm, no prep")
+    assert_rowwise_close(gnn.gnn_segment_reduce_sum(g, Xd).cpu().numpy(),
+                         oracle.segment_reduce(oracle.OP_SUM, rp, ci, X), TOL_F32, "sum, no prep")
+    assert_rowwise_close(gnn.gnn_segment_reduce_mean(g, Xd).cpu().numpy(),
+                         oracle.segment_reduce(oracle.OP_MEAN, rp, ci, X), TOL_F32, "mean, no prep")
+    yx, am = gnn.gnn_segment_reduce_max(g, Xd)
+    ry, ram = oracle.segment_reduce(oracle.OP_MAX, rp, ci, X)
+    check_exact_max(yx.cpu().numpy(), am.cpu().numpy(), ry, ram)
+
+
 def test_config1_er(gnn):
     w = synth.workload("c1_er1k")
     run_all(gnn, w["rowptr"], w["colidx"], w["X"])
