@@ -96,20 +96,23 @@ struct AggArgs {
 template <int OP, class T, int CPL>
 struct Acc {
     static constexpr int NV = Chunk<T>::N;
-    float v[CPL][NV];
-    int32_t idx[OP == AGG_MAX ? CPL : 1][OP == AGG_MAX ? NV : 1];
+    static constexpr bool MX = OP == AGG_MAX;
+    float v[MX ? 1 : CPL][MX ? 1 : NV];      // sums
+    uint32_t km[MX ? CPL : 1][MX ? NV : 1];  // max: order_key of the maximum, 0 = nothing seen
+    int32_t idx[MX ? CPL : 1][MX ? NV : 1];  // max: its source id, -1 = nothing seen
 
-    // key of the current maximum (0 = nothing seen; every finite key is > 0)
-    __device__ __forceinline__ uint32_t key(int c, int k) const {
-        return idx[c][k] >= 0 ? order_key(v[c][k]) : 0u;
+    // every finite value's key is > 0, so a key of 0 means "no edge yet"
+    __device__ __forceinline__ uint32_t key(int c, int k) const { return km[c][k]; }
+    __device__ __forceinline__ float max_value(int c, int k) const {
+        return km[c][k] ? key_value(km[c][k]) : 0.f;
     }
     __device__ __forceinline__ void reset() {
 #pragma unroll
         for (int c = 0; c < CPL; ++c)
 #pragma unroll
             for (int k = 0; k < NV; ++k) {
-                v[c][k] = 0.f;
-                if (OP == AGG_MAX) idx[c][k] = -1;
+                if (MX) { km[c][k] = 0u; idx[c][k] = -1; }
+                else v[c][k] = 0.f;
             }
     }
     __device__ __forceinline__ void add(const uint4 *x, float w, int32_t j) {
@@ -117,13 +120,13 @@ struct Acc {
         for (int c = 0; c < CPL; ++c) {
             float f[NV];
             Chunk<T>::unpack(x[c], f);
-            if (OP == AGG_MAX) {
+            if (MX) {
 #pragma unroll
                 for (int k = 0; k < NV; ++k) {
-                    uint32_t kk = order_key(f[k]);
+                    const uint32_t kk = order_key(f[k]);
                     // edges arrive in ascending source id: strict > keeps the
                     // smallest id among equal keys
-                    if (kk > key(c, k)) { idx[c][k] = j; v[c][k] = f[k]; }
+                    if (kk > km[c][k]) { km[c][k] = kk; idx[c][k] = j; }
                 }
             } else {
                 // v += w * f on pairs of features (one rounding each, as fmaf)
@@ -133,6 +136,11 @@ struct Acc {
                     upk2(fma2(ww, pk2(f[k], f[k + 1]), pk2(v[c][k], v[c][k + 1])), v[c][k], v[c][k + 1]);
             }
         }
+    }
+    // merged state from a packed (key << 32) | ~id word
+    __device__ __forceinline__ void set_packed(int c, int k, unsigned long long p) {
+        km[c][k] = (uint32_t)(p >> 32);
+        idx[c][k] = (int32_t)(0xFFFFFFFFu - (uint32_t)p);
     }
 };
 
@@ -165,7 +173,7 @@ __device__ __forceinline__ void store_row(const AggArgs &a, int32_t r, int32_t d
         for (int k = 0; k < NV; ++k) {
             if (OP == AGG_WSUM) o[k] = acc.v[c][k] * s;
             else if (OP == AGG_MEAN) o[k] = acc.v[c][k] * inv_deg;
-            else o[k] = acc.idx[c][k] >= 0 ? acc.v[c][k] : 0.f;
+            else o[k] = acc.max_value(c, k);
         }
 #pragma unroll
         for (int k = 0; k < NV; k += 4)
@@ -196,7 +204,7 @@ __device__ __forceinline__ void store_row_f(const AggArgs &a, int32_t r, int32_t
         for (int k = 0; k < NV; ++k) {
             if (OP == AGG_WSUM) o[k] = acc.v[c][k] * s;
             else if (OP == AGG_MEAN) o[k] = acc.v[c][k] * inv_deg;
-            else o[k] = acc.idx[c][k] >= 0 ? acc.v[c][k] : 0.f;
+            else o[k] = acc.max_value(c, k);
         }
 #pragma unroll
         for (int k = 0; k < NV; k += 4)
@@ -262,11 +270,7 @@ __device__ __forceinline__ void flush_partial(const AggArgs &a, int64_t w, int s
                 unsigned long long *src = reinterpret_cast<unsigned long long *>(a.carry) + off + k;
 #pragma unroll
                 for (int z = 0; z < 4; ++z) {
-                    const unsigned long long p = __ldcg(src + z);
-                    const uint32_t key = (uint32_t)(p >> 32);
-                    const uint32_t u = (key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key;
-                    acc.v[c][k + z] = __uint_as_float(u);
-                    acc.idx[c][k + z] = (int32_t)(0xFFFFFFFFu - (uint32_t)p);
+                    acc.set_packed(c, k + z, __ldcg(src + z));
                     src[z] = 0ull;
                 }
             } else {
@@ -758,11 +762,7 @@ __global__ void __launch_bounds__(256) k_agg_span_fix(AggArgs a) {
                 unsigned long long *p = reinterpret_cast<unsigned long long *>(a.carry) + off + k;
 #pragma unroll
                 for (int z = 0; z < 4; ++z) {
-                    const unsigned long long v = __ldcg(p + z);
-                    const uint32_t key = (uint32_t)(v >> 32);
-                    const uint32_t u = (key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key;
-                    acc.v[0][k + z] = __uint_as_float(u);
-                    acc.idx[0][k + z] = (int32_t)(0xFFFFFFFFu - (uint32_t)v);
+                    acc.set_packed(0, k + z, __ldcg(p + z));
                     p[z] = 0ull;
                 }
             } else {

@@ -121,6 +121,10 @@ __device__ __forceinline__ uint32_t order_key(float v) {
     uint32_t u = __float_as_uint(v);
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
+// Inverse of order_key.
+__device__ __forceinline__ float key_value(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
 
 __device__ __forceinline__ int lane_id() { return threadIdx.x & 31; }
 
