@@ -46,10 +46,10 @@ FALLBACK_HBM_GBS = 6800.0
 # finalising kernel), from the committed ncu capture
 # profiles/k_agg_span_c2_rmat17.md (same kernel build); set to None when the
 # kernels change.
-NCU_TRAFFIC = {("c2_rmat17", "spmm"): (90.888704 + 33.767424 + 3.152128) * 1e6,
-               ("c2_rmat17", "sum"): (89.338624 + 30.829056 + 3.012096 + 0.001024) * 1e6,
-               ("c2_rmat17", "mean"): (89.171712 + 30.574080 + 3.008000) * 1e6,
-               ("c2_rmat17", "max"): (102.442240 + 82.603776 + 5.842944 + 0.001792) * 1e6}
+NCU_TRAFFIC = {("c2_rmat17", "spmm"): (89.525248 + 43.183872 + 13.461760) * 1e6,
+               ("c2_rmat17", "sum"): (88.022784 + 39.964928 + 13.320960) * 1e6,
+               ("c2_rmat17", "mean"): (87.809280 + 39.904256 + 13.320448) * 1e6,
+               ("c2_rmat17", "max"): (102.362112 + 82.384384 + 5.767424 + 0.000256) * 1e6}
 NORTH_STAR_HBM_GBS = 8000.0
 METRIC = "aggregation Gedge*feat/s"
 UNIT = "Gedge*feat/s"

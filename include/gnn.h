@@ -20,10 +20,13 @@
  * Memory: every array argument is a DEVICE pointer owned by the caller unless
  *   the comment says "host".  The library never allocates device memory;
  *   scratch space comes from the caller through (ws, ws_bytes), sized by
- *   gnn_workspace_size().  A workspace must be zero-filled once before its
- *   first use; every call leaves it zero-filled again (so one cudaMemset
- *   after allocation suffices).  Calls that may overlap on the GPU need
- *   separate workspaces.
+ *   gnn_workspace_size().  A workspace must be zero-filled before its first
+ *   use; every call leaves the parts that the next call of the same
+ *   operation on the same graph and feature width needs at zero, so
+ *   repeated calls need no further cudaMemset.  Other parts keep scratch
+ *   (projected rows, partial sums): a buffer moved to another operation,
+ *   graph or width needs a fresh zero-fill.  Calls that may overlap on the
+ *   GPU need separate workspaces.
  * Features: dense row-major [rows, F].  Rows must start on 16-byte
  *   boundaries: F % 4 == 0 for fp32, F % 8 == 0 for bf16, and every feature
  *   pointer 16-byte aligned.
@@ -171,9 +174,9 @@ gnn_status gnn_segment_reduce_sum(const gnn_csr *g, const void *prep, const void
  *
  * Size limit: the problem must satisfy
  *   gnn_workspace_size(GNN_OP_SUM, g, F, 0, 0) <= GNN_NOALLOC_SCRATCH_BYTES
- * (roughly nnz / 64 * (4 F + 4) bytes; about one million edges at F = 128
- * fp32); larger problems are rejected with GNN_ERR_WORKSPACE before any
- * launch.  Other arguments, validation and errors are as for
+ * (roughly nnz / 64 * (12 F + 12) bytes; about 340 thousand edges at
+ * F = 128 fp32); larger problems are rejected with GNN_ERR_WORKSPACE before
+ * any launch.  Other arguments, validation and errors are as for
  * gnn_segment_reduce_sum.
  *
  * The first call on a device, with that device current, looks up the

@@ -12,8 +12,9 @@
 // same number of loads:
 //  - k_agg_span (rows of 32 chunks, prepared graph given): spans of 64 edges
 //    from the prepared graph, light rows kept whole, heavy rows cut, row
-//    closes read from prepared row-end bits; heavy-row pieces are folded by
-//    fire-and-forget reductions and finalised by k_agg_span_fix.
+//    closes read from prepared row-end bits; heavy-row pieces are stored
+//    with plain stores (max: folded by 64-bit max reductions) and finalised,
+//    in edge order, by k_agg_span_fix.
 //  - k_agg_auto (any width, with or without the prepared graph): runs of E
 //    edges per group of LPR lanes (a "worker"); light rows packed several to
 //    a worker, heavy rows split across ceil(deg/E) workers; a row that
@@ -23,7 +24,8 @@
 // Loads of U consecutive edges are issued before any of them is accumulated,
 // whatever row they belong to, which keeps U 16-byte loads in flight per lane
 // even through runs of degree-1 rows.  Sums of a row cut into three or more
-// pieces are fp32-order dependent (the pieces arrive in any order); max
+// pieces are fp32-order dependent in k_agg_auto (the pieces arrive in any
+// order; k_agg_span adds them in edge order); max
 // merges (value, source id) pairs under the order-preserving key with ties
 // to the smaller id -- the paper's packed 64-bit atomic merge -- and is
 // exact and deterministic.
@@ -55,8 +57,8 @@ gnn_status check_csr_args(const gnn_csr *g);
 const int32_t *prep_run_table(const gnn_csr *g, const void *prep);
 void prep_span_tables(const gnn_csr *g, const void *prep, const uint32_t **win_flags,
                       const int32_t **win_rowbase, const int32_t **ne_rows,
-                      const int32_t **win_rowstart, const int32_t **sp_begin,
-                      const int32_t **heavy);
+                      const int32_t **sp_begin, const int4 **items, const int32_t **items_count,
+                      const int32_t **win_rowstart);
 
 enum AggOp { AGG_WSUM = 0, AGG_MEAN = 1, AGG_MAX = 2 };
 // per-edge weight source / per-row factor source
@@ -79,9 +81,10 @@ struct AggArgs {
     const uint32_t *win_flags;     // prepared row-end bits, one word per 32 edges
     const int32_t *win_rowbase;    // prepared rank of the row holding edge 32*win
     const int32_t *ne_rows;        // prepared non-empty rows, ascending
-    const int32_t *win_rowstart;   // prepared first edge of the row holding edge 32*win
     const int32_t *sp_begin;       // prepared first edge of each edge span
-    const int32_t *heavy;          // prepared rows of degree > kSpanEdges, count at [n_rows]
+    const int32_t *win_rowstart;   // prepared first edge of the row holding edge 32*win
+    const int4 *items;             // prepared heavy-row chunks {row, begin, end, chunk}
+    const int32_t *items_count;    // prepared number of items
     int32_t n_spans;               // edge-span kernel: spans of kSpanEdges edges
     int64_t nnz;
     int64_t n_workers;
@@ -507,14 +510,14 @@ __global__ void __launch_bounds__(256, (CPL <= 4 ? GNN_AGG_MINB : 2)) k_agg_auto
 // (one 32-bit word per 32 edges) say where rows close, its window ranks and
 // list of non-empty rows turn a close into a row id, so the edge loop reads
 // no row pointers and searches for no row, and a row's degree is the distance
-// between two closes.  Each piece of a heavy row is folded with
-// fire-and-forget reductions into the workspace slot of the span the row
-// starts in (fp32 vector adds for sum-like ops; a 64-bit max of
-// (key << 32) | ~source_id for max -- the packed (value, index) merge of
-// IO-aware GNN layers, Appendix D.1, ties to the smaller id); nothing on the
-// edge path waits on another warp, and k_agg_span_fix finalises heavy rows
-// once this grid has finished.  Warps past the last span write the empty
-// rows.
+// between two closes.  A span stores the pieces of heavy rows that it holds
+// with plain stores -- at most two: the end of one that started earlier
+// (slot 2w) and the start of one that runs on (slot 2w+1) -- so nothing on
+// the edge path waits on another warp or on an atomic unit, and
+// k_agg_span_fix sums every heavy row's pieces in edge order once this grid
+// has finished.  Max, whose merge is exact in any order, instead folds all of
+// a row's pieces into the tail slot of its first span with 64-bit max
+// reductions.  Warps past the last span write the empty rows.
 #ifndef GNN_SPAN_U
 #define GNN_SPAN_U 4
 #endif
@@ -578,30 +581,92 @@ __device__ __forceinline__ void write_empty_rows(const AggArgs &a, int32_t q, in
     }
 }
 
-// Fold one piece of a heavy row into workspace slot `slot` (no return value
-// is used, so these compile to reductions that the warp does not wait for).
+// Piece (or chunk) records of the edge-span path: per lane NV fp32 partial
+// sums, or for max NV 64-bit words (key << 32) | ~source_id, whose unsigned
+// maximum is the packed (value, index) merge of IO-aware GNN layers,
+// Appendix D.1 (ties to the smaller id).
 template <int OP, class T>
-__device__ __forceinline__ void fold_piece(const AggArgs &a, int32_t slot, const Acc<OP, T, 1> &acc,
-                                           int lane) {
+__device__ __forceinline__ void store_piece(const AggArgs &a, float *base, int64_t slot,
+                                            const Acc<OP, T, 1> &acc, int lane) {
     constexpr int NV = Chunk<T>::N;
-    const int64_t off = (int64_t)slot * a.F + (int64_t)lane * NV;
+    const int64_t off = slot * a.F + (int64_t)lane * NV;
+    if (OP == AGG_MAX) {
+        ulonglong2 *dst = reinterpret_cast<ulonglong2 *>(reinterpret_cast<unsigned long long *>(base) + off);
 #pragma unroll
-    for (int k = 0; k < NV; k += 4) {
-        if (OP == AGG_MAX) {
-            unsigned long long *dst = reinterpret_cast<unsigned long long *>(a.carry) + off + k;
-#pragma unroll
-            for (int z = 0; z < 4; ++z) {
-                const unsigned long long packed =
-                    ((unsigned long long)acc.key(0, k + z) << 32) |
-                    (unsigned long long)(0xFFFFFFFFu - (uint32_t)acc.idx[0][k + z]);
-                atomicMax(dst + z, packed);
-            }
-        } else {
-            atomicAdd(reinterpret_cast<float4 *>(a.carry + off + k),
-                      make_float4(acc.v[0][k], acc.v[0][k + 1], acc.v[0][k + 2], acc.v[0][k + 3]));
+        for (int k = 0; k < NV; k += 2) {
+            ulonglong2 w;
+            w.x = ((unsigned long long)acc.key(0, k) << 32) | (0xFFFFFFFFu - (uint32_t)acc.idx[0][k]);
+            w.y = ((unsigned long long)acc.key(0, k + 1) << 32) | (0xFFFFFFFFu - (uint32_t)acc.idx[0][k + 1]);
+            dst[k / 2] = w;
         }
+    } else {
+        float4 *dst = reinterpret_cast<float4 *>(base + off);
+#pragma unroll
+        for (int k = 0; k < NV; k += 4)
+            dst[k / 4] = make_float4(acc.v[0][k], acc.v[0][k + 1], acc.v[0][k + 2], acc.v[0][k + 3]);
     }
 }
+
+// Max: every piece of a heavy row is folded into one slot with 64-bit
+// reductions (the merge is exact and order-free); the warp does not wait.
+template <class T>
+__device__ __forceinline__ void fold_max_piece(const AggArgs &a, int64_t slot,
+                                               const Acc<AGG_MAX, T, 1> &acc, int lane) {
+    constexpr int NV = Chunk<T>::N;
+    unsigned long long *dst = reinterpret_cast<unsigned long long *>(a.carry) + slot * a.F + (int64_t)lane * NV;
+#pragma unroll
+    for (int k = 0; k < NV; ++k)
+        atomicMax(dst + k, ((unsigned long long)acc.key(0, k) << 32) | (0xFFFFFFFFu - (uint32_t)acc.idx[0][k]));
+}
+
+// One lane's share of a piece record, loaded ahead of merging.
+template <int OP, class T>
+struct PieceVal {
+    static constexpr int NV = Chunk<T>::N;
+    static constexpr int NW = OP == AGG_MAX ? NV / 2 : NV / 4;  // 16-byte words
+    uint4 w[NW];
+    __device__ __forceinline__ void load(const AggArgs &a, const float *base, int64_t slot, int lane,
+                                         bool bypass_l1) {
+        const int64_t off = slot * a.F + (int64_t)lane * NV;
+        const uint4 *src = OP == AGG_MAX
+                               ? reinterpret_cast<const uint4 *>(reinterpret_cast<const unsigned long long *>(base) + off)
+                               : reinterpret_cast<const uint4 *>(base + off);
+#pragma unroll
+        for (int i = 0; i < NW; ++i) w[i] = bypass_l1 ? ldcg16(src + i) : ldg16(src + i);
+    }
+    // clear the record just read (the workspace is left zero-filled)
+    __device__ __forceinline__ static void clear(const AggArgs &a, float *base, int64_t slot, int lane) {
+        const int64_t off = slot * a.F + (int64_t)lane * NV;
+        uint4 *dst = OP == AGG_MAX
+                         ? reinterpret_cast<uint4 *>(reinterpret_cast<unsigned long long *>(base) + off)
+                         : reinterpret_cast<uint4 *>(base + off);
+#pragma unroll
+        for (int i = 0; i < NW; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    // acc := acc (+) this, in that order
+    __device__ __forceinline__ void merge_into(Acc<OP, T, 1> &acc) const {
+#pragma unroll
+        for (int i = 0; i < NW; ++i) {
+            if (OP == AGG_MAX) {
+                const unsigned long long p0 = ((unsigned long long)w[i].y << 32) | w[i].x;
+                const unsigned long long p1 = ((unsigned long long)w[i].w << 32) | w[i].z;
+#pragma unroll
+                for (int z = 0; z < 2; ++z) {
+                    const int k = 2 * i + z;
+                    const unsigned long long p = z ? p1 : p0;
+                    const unsigned long long cur =
+                        ((unsigned long long)acc.key(0, k) << 32) | (0xFFFFFFFFu - (uint32_t)acc.idx[0][k]);
+                    if (p > cur) acc.set_packed(0, k, p);
+                }
+            } else {
+                acc.v[0][4 * i] += __uint_as_float(w[i].x);
+                acc.v[0][4 * i + 1] += __uint_as_float(w[i].y);
+                acc.v[0][4 * i + 2] += __uint_as_float(w[i].z);
+                acc.v[0][4 * i + 3] += __uint_as_float(w[i].w);
+            }
+        }
+    }
+};
 
 // WT = false: unit edge weights and row factor 1 (segment sum / mean / max);
 // WT = true: the SpMM's per-edge weights and row factors.
@@ -631,10 +696,13 @@ k_agg_span(AggArgs a) {
     // rank of the row holding b0 = row ends before b0
     const uint32_t wb0 = __ldg(a.win_flags + (b0 >> 5));
     const int32_t k0 = __ldg(a.win_rowbase + (b0 >> 5)) + __popc(wb0 & ((1u << (b0 & 31)) - 1u));
-    // a span that starts inside a row starts inside a heavy row
-    const bool head0 = b0 > 0 && !((__ldg(a.win_flags + ((b0 - 1) >> 5)) >> ((b0 - 1) & 31)) & 1u);
-    bool head = head0;
-    const int32_t head_slot = head0 ? __ldg(a.win_rowstart + (b0 >> 5)) / kSpanEdges : 0;
+    // a span that starts inside a row starts inside a heavy row; that row's
+    // piece here goes to slot 2w, a heavy row that starts here and runs on
+    // leaves its first piece in slot 2w+1 (max: every piece of a row goes to
+    // the tail slot of the span the row starts in)
+    bool head = b0 > 0 && !((__ldg(a.win_flags + ((b0 - 1) >> 5)) >> ((b0 - 1) & 31)) & 1u);
+    const int64_t max_head_slot =
+        (OP == AGG_MAX && head) ? 2 * (int64_t)(__ldg(a.win_rowstart + (b0 >> 5)) / kSpanEdges) + 1 : 0;
     // lane l holds the id (and row factor) of the row of rank k0 + kofs + l
     int32_t kofs = 0;
     int32_t rid = k0 + lane < a.n_rows ? __ldg(a.ne_rows + k0 + lane) : 0;
@@ -706,7 +774,11 @@ k_agg_span(AggArgs a) {
                 if ((gb >> u) & 1u) {
                     const int32_t e = cb + u0 + u;
                     if (head) {
-                        fold_piece<OP, T>(a, head_slot, acc, lane);
+                        if constexpr (OP == AGG_MAX) {
+                            fold_max_piece<T>(a, max_head_slot, acc, lane);
+                        } else {
+                            store_piece<OP, T>(a, a.carry, 2 * (int64_t)w, acc, lane);
+                        }
                         head = false;
                     } else {
                         if (k - kofs == 32) {
@@ -730,60 +802,104 @@ k_agg_span(AggArgs a) {
         c_nxt = en < b1 ? __ldg(a.colidx + en) : 0;
         if (weighted) w_cur = cb + 32 + lane < b1 ? edge_weight(a, cb + 32 + lane, c_cur) : 1.f;
     }
-    // a heavy row reaches past this span: leave its piece in the slot of the
-    // span it starts in (an earlier one if it never closed here)
-    if (!last_closed) fold_piece<OP, T>(a, head ? head_slot : w, acc, lane);
+    // a heavy row reaches past this span: leave its piece
+    if (!last_closed) {
+        if constexpr (OP == AGG_MAX) {
+            fold_max_piece<T>(a, head ? max_head_slot : 2 * (int64_t)w + 1, acc, lane);
+        } else {
+            store_piece<OP, T>(a, a.carry, 2 * (int64_t)w + (head ? 0 : 1), acc, lane);
+        }
+    }
 }
 
-// Finalise heavy rows (degree > S, every one of them cut by at least one
-// span boundary): a persistent grid of warps strides over the prepared list
-// of heavy rows; for each, the warp reads the row's slot (the span its first
-// edge falls in), clears it and stores the row.
+// Finalise heavy rows (degree > S).  Such a row's edges lie in spans
+// s0..s1 and it left one piece in each: the tail piece of span s0 (slot
+// 2*s0+1), then the head pieces of spans s0+1..s1 (slots 2*s), in edge order
+// (max: all folded into slot 2*s0+1, which is cleared again for the next
+// call's reductions; the sum pieces are plain scratch, written before read).
+// A persistent grid of warps strides over the prepared work items, each the
+// pieces [16c, 16c+16) of one row, and sums them in edge order.  A row with
+// one item is stored at once; otherwise each item leaves its chunk sum in the
+// slot of its first piece, and the last of the row's items to finish (a
+// ticket, no spinning) sums the chunk sums in order and stores the row -- so
+// every sum is independent of scheduling.
+__device__ __forceinline__ int64_t piece_slot(int32_t s0, int32_t p) {
+    return p == 0 ? 2 * (int64_t)s0 + 1 : 2 * ((int64_t)s0 + p);
+}
+
+constexpr int kFixBlocksPerSm = 4;
+#ifndef GNN_FIX_WORDS
+#define GNN_FIX_WORDS 4
+#endif
+
 template <int OP, class T>
-__global__ void __launch_bounds__(256) k_agg_span_fix(AggArgs a) {
-    constexpr int NV = Chunk<T>::N;
+__global__ void __launch_bounds__(256, kFixBlocksPerSm) k_agg_span_fix(AggArgs a) {
+    // records in flight per lane: GNN_FIX_WORDS 16-byte words
+    constexpr int PF = GNN_FIX_WORDS / PieceVal<OP, T>::NW > 0 ? GNN_FIX_WORDS / PieceVal<OP, T>::NW : 1;
+    const unsigned FULL = 0xffffffffu;
     const int lane = threadIdx.x & 31;
     const int32_t nw = (int32_t)((gridDim.x * blockDim.x) >> 5);
     int32_t q = (int32_t)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
-    // the list is prep data: read it before waiting for the span kernel
-    const int32_t n_heavy = __ldg(a.heavy + a.n_rows);
-    int32_t row = q < n_heavy ? __ldg(a.heavy + q) : 0;
-    int32_t rb = q < n_heavy ? __ldg(a.rowptr + row) : 0;
-    int32_t re = q < n_heavy ? __ldg(a.rowptr + row + 1) : 0;
-    // wait for the span kernel (its whole grid, memory included)
+    // the items are prep data: read them before waiting for the span kernel
+    const int32_t n_items = __ldg(a.items_count);
+    int4 it = q < n_items ? __ldg(a.items + q) : make_int4(0, 0, 0, 0);
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    for (; q < n_heavy; q += nw) {
-        const int32_t slot = rb / kSpanEdges;
+    for (; q < n_items; q += nw) {
+        const int32_t row = it.x, rb = it.y, re = it.z, cidx = it.w;
+        if (q + nw < n_items) it = __ldg(a.items + q + nw);
+        const int32_t s0 = rb / kSpanEdges;
+        const int32_t np = (re - 1) / kSpanEdges - s0 + 1;
+        const int32_t nch = (np + kFixChunk - 1) / kFixChunk;
+        const int32_t p_lo = cidx * kFixChunk, p_hi = min(np, p_lo + kFixChunk);
         Acc<OP, T, 1> acc;
-        const int64_t off = (int64_t)slot * a.F + (int64_t)lane * NV;
+        acc.reset();
+        if constexpr (OP == AGG_MAX) {
+            // all pieces were folded into the first piece's slot
+            if (cidx != 0) continue;
+            PieceVal<OP, T> pv;
+            pv.load(a, a.carry, piece_slot(s0, 0), lane, false);
+            pv.merge_into(acc);
+            PieceVal<OP, T>::clear(a, a.carry, piece_slot(s0, 0), lane);
+            store_row<OP, T, 1>(a, row, re - rb, acc, lane);
+            continue;
+        }
+        for (int32_t p0 = p_lo; p0 < p_hi; p0 += PF) {
+            PieceVal<OP, T> pv[PF];
 #pragma unroll
-        for (int k = 0; k < NV; k += 4) {
-            if (OP == AGG_MAX) {
-                unsigned long long *p = reinterpret_cast<unsigned long long *>(a.carry) + off + k;
-#pragma unroll
-                for (int z = 0; z < 4; ++z) {
-                    acc.set_packed(0, k + z, __ldcg(p + z));
-                    p[z] = 0ull;
-                }
-            } else {
-                float4 *p = reinterpret_cast<float4 *>(a.carry + off + k);
-                const float4 v = __ldcg(p);
-                acc.v[0][k] = v.x;
-                acc.v[0][k + 1] = v.y;
-                acc.v[0][k + 2] = v.z;
-                acc.v[0][k + 3] = v.w;
-                *p = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int u = 0; u < PF; ++u) {
+                const int32_t p = p0 + u;
+                if (p < p_hi) pv[u].load(a, a.carry, piece_slot(s0, p), lane, false);
             }
+#pragma unroll
+            for (int u = 0; u < PF; ++u)
+                if (p0 + u < p_hi) pv[u].merge_into(acc);
         }
-        const int32_t cur = row, deg = re - rb;
-        // next row's list entry and pointers while this one is stored
-        const int32_t qn = q + nw;
-        if (qn < n_heavy) {
-            row = __ldg(a.heavy + qn);
-            rb = __ldg(a.rowptr + row);
-            re = __ldg(a.rowptr + row + 1);
+        if (nch == 1) {
+            store_row<OP, T, 1>(a, row, re - rb, acc, lane);
+            continue;
         }
-        store_row<OP, T, 1>(a, cur, deg, acc, lane);
+        // the chunk sum replaces the chunk's first piece (read above by this warp)
+        const int32_t q0 = q - cidx;  // the row's first item: its ticket
+        store_piece<OP, T>(a, a.carry, piece_slot(s0, p_lo), acc, lane);
+        __threadfence();
+        __syncwarp();
+        int32_t t = 0;
+        if (lane == 0) t = atomicAdd(a.tickets + q0, 1);
+        t = __shfl_sync(FULL, t, 0);
+        if (t != nch - 1) continue;
+        __threadfence();
+        acc.reset();
+        for (int32_t c0 = 0; c0 < nch; c0 += PF) {
+            PieceVal<OP, T> pv[PF];
+#pragma unroll
+            for (int u = 0; u < PF; ++u)
+                if (c0 + u < nch) pv[u].load(a, a.carry, piece_slot(s0, (c0 + u) * kFixChunk), lane, true);
+#pragma unroll
+            for (int u = 0; u < PF; ++u)
+                if (c0 + u < nch) pv[u].merge_into(acc);
+        }
+        store_row<OP, T, 1>(a, row, re - rb, acc, lane);
+        if (lane == 0) a.tickets[q0] = 0;
     }
 }
 
@@ -913,13 +1029,36 @@ static int64_t n_workers_for(const gnn_csr *g, int32_t E) {
     return n > 0 ? n : 1;
 }
 
+// Workspace, both AUTO schedules (a call uses one of them; the regions are
+// disjoint so either may follow the other on the same workspace):
+//   run tickets [n_runs] int32 and run slots [n_runs, F]     zero on entry and exit
+//   item tickets [span_item_cap] int32                        zero on entry and exit
+//   span piece slots [2 * n_spans, F]                         sums: written before read;
+//                                                             max: zero on entry and exit
+// Slots are fp32, or 64-bit (key, ~id) words for max.
+struct AggWs {
+    int32_t *run_tickets, *item_tickets;
+    float *run_slots, *pieces;
+    size_t bytes;
+};
+
+static AggWs agg_ws_layout(const gnn_csr *g, int32_t op, int32_t F, void *base) {
+    const int64_t nr = n_workers_for(g, kRunEdges);
+    const int64_t ns = std::max<int64_t>(n_spans_of(g->nnz), 1);
+    const size_t wmul = op == GNN_OP_MAX ? 2 : 1;
+    Carver cv(base);
+    AggWs L;
+    L.run_tickets = cv.take<int32_t>((size_t)nr);
+    L.item_tickets = cv.take<int32_t>((size_t)span_item_cap(g->nnz));
+    L.run_slots = cv.take<float>((size_t)nr * F * wmul);
+    L.pieces = cv.take<float>((size_t)2 * ns * F * wmul);
+    L.bytes = cv.used;
+    return L;
+}
+
 size_t agg_workspace_bytes(const gnn_csr *g, int32_t op, int32_t x_dtype_unused, int32_t F) {
     (void)x_dtype_unused;
-    int64_t nw = n_workers_for(g, std::min(kRunEdges, kSpanEdges));
-    size_t word = op == GNN_OP_MAX ? sizeof(unsigned long long) : sizeof(float);
-    size_t b = round_up(word * (size_t)nw * (size_t)F, 256);
-    b += round_up(sizeof(int32_t) * (size_t)nw, 256);
-    return b;
+    return agg_ws_layout(g, op, F, nullptr).bytes;
 }
 
 template <int OP, class T>
@@ -961,9 +1100,9 @@ static cudaError_t launch_span(const AggArgs &a, cudaStream_t s) {
     note_launch();
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || a.n_spans <= 1) return e;
-    // heavy rows number at most nnz / (S + 1); a few blocks per SM stride over them
-    const int64_t max_heavy = a.nnz / (kSpanEdges + 1);
-    const int64_t fix_blocks = std::min<int64_t>((max_heavy * 32 + 255) / 256, (int64_t)sm_count() * 4);
+    // one resident wave of blocks strides over the work items
+    const int64_t fix_blocks = std::min<int64_t>((span_item_cap(a.nnz) * 32 + 255) / 256,
+                                                 (int64_t)sm_count() * kFixBlocksPerSm);
     if (fix_blocks <= 0) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)fix_blocks);
@@ -1041,16 +1180,17 @@ gnn_status run_aggregate(const gnn_csr *g, const void *prep, int32_t op, int32_t
     size_t need = agg_workspace_bytes(g, op, x_dtype, F);
     if (!ws || ws_bytes < need) return GNN_ERR_WORKSPACE;
     if (!aligned256(ws)) return GNN_ERR_INVALID_ARG;
-    Carver cv(ws);
-    const int64_t n_slots = n_workers_for(g, std::min(kRunEdges, kSpanEdges));
-    a.carry = cv.take<float>((size_t)n_slots * F * (op == GNN_OP_MAX ? 2 : 1));
-    a.tickets = cv.take<int32_t>((size_t)n_slots);
+    const AggWs L = agg_ws_layout(g, op, F, ws);
+    a.carry = L.run_slots;
+    a.tickets = L.run_tickets;
 
     if (prep && sh.V == 32) {
-        prep_span_tables(g, prep, &a.win_flags, &a.win_rowbase, &a.ne_rows, &a.win_rowstart,
-                         &a.sp_begin, &a.heavy);
+        prep_span_tables(g, prep, &a.win_flags, &a.win_rowbase, &a.ne_rows, &a.sp_begin, &a.items,
+                         &a.items_count, &a.win_rowstart);
         a.E = kSpanEdges;
-        a.n_spans = (int32_t)((g->nnz + kSpanEdges - 1) / kSpanEdges);
+        a.n_spans = (int32_t)n_spans_of(g->nnz);
+        a.carry = L.pieces;
+        a.tickets = L.item_tickets;
         const bool wt = a.values || a.col_mode != COL_ONE || a.row_mode != ROW_ONE;
         cudaError_t e;
         if (op == GNN_OP_MAX) e = bf ? launch_span<AGG_MAX, __nv_bfloat16, false>(a, s)

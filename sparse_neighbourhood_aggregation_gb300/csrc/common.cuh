@@ -38,6 +38,13 @@ constexpr int32_t kRunEdges = GNN_RUN_EDGES;
 #endif
 constexpr int32_t kSpanEdges = GNN_SPAN_EDGES;
 static_assert(kSpanEdges % 32 == 0, "spans are whole 32-edge windows");
+inline int64_t n_spans_of(int64_t nnz) { return (nnz + kSpanEdges - 1) / kSpanEdges; }
+// A row of degree > kSpanEdges is cut into one piece per span it touches;
+// its pieces are summed in chunks of kFixChunk, one work item per chunk.
+constexpr int32_t kFixChunk = 16;
+inline int64_t span_item_cap(int64_t nnz) {
+    return nnz / (kSpanEdges + 1) + 2 * n_spans_of(nnz) / kFixChunk + 1;
+}
 inline int64_t n_runs(int64_t nnz, int32_t E) {
     int64_t n = (nnz + E - 1) / E;
     return n > 0 ? n : 1;

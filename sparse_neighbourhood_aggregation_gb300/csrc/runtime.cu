@@ -163,13 +163,24 @@ __global__ void k_span_begin(const int32_t *__restrict__ rowptr, int64_t nnz, in
     }
 }
 
-// Rows of degree > S (the ones the edge-span kernel cuts), appended in any
-// order; heavy[n_rows] holds their count.
-__global__ void k_heavy_rows(const int32_t *__restrict__ rowptr, int32_t n_rows,
-                             int32_t *__restrict__ heavy) {
+// Work items of the heavy-row finalising kernel: a row of degree > S touches
+// spans s0..s1 and leaves one piece in each; its pieces are taken kFixChunk
+// at a time, item {row, rowptr[row], rowptr[row+1], chunk index}.  A row's
+// items are contiguous (one atomic reservation); rows come in any order.
+// items_count holds their number.
+__global__ void k_heavy_items(const int32_t *__restrict__ rowptr, int32_t n_rows, int64_t cap,
+                              int4 *__restrict__ items, int32_t *__restrict__ items_count,
+                              int32_t *err) {
     int32_t stride = gridDim.x * blockDim.x;
-    for (int32_t r = blockIdx.x * blockDim.x + threadIdx.x; r < n_rows; r += stride)
-        if (rowptr[r + 1] - rowptr[r] > kSpanEdges) heavy[atomicAdd(heavy + n_rows, 1)] = r;
+    for (int32_t r = blockIdx.x * blockDim.x + threadIdx.x; r < n_rows; r += stride) {
+        const int32_t rb = rowptr[r], re = rowptr[r + 1];
+        if (re - rb <= kSpanEdges) continue;
+        const int32_t np = (re - 1) / kSpanEdges - rb / kSpanEdges + 1;
+        const int32_t nch = (np + kFixChunk - 1) / kFixChunk;
+        const int32_t base = atomicAdd(items_count, nch);
+        if ((int64_t)base + nch > cap) { set_device_error(err, GNN_ERR_DEVICE_CHECK); continue; }
+        for (int32_t c = 0; c < nch; ++c) items[base + c] = make_int4(r, rb, re, c);
+    }
 }
 
 }  // namespace gnn
@@ -186,9 +197,10 @@ struct PrepLayout {
     int32_t *win_count;      // [n_win] popcounts (scan input)
     int32_t *win_rowbase;    // [n_win] rank among non-empty rows of the row holding edge 32*win
     int32_t *ne_rows;        // [n_rows] non-empty rows, ascending (first n_nonempty entries)
-    int32_t *win_rowstart;   // [n_win] first edge of the row holding edge 32*win
     int32_t *sp_begin;       // [n_spans + 1] first edge of each edge span
-    int32_t *heavy;          // [n_rows + 1] rows of degree > kSpanEdges, then their count
+    int32_t *win_rowstart;   // [n_win] first edge of the row holding edge 32*win
+    int4 *items;             // [span_item_cap(nnz)] heavy-row chunks for the finalising kernel
+    int32_t *items_count;    // [1]
     int32_t n_spans;
     void *scan_tmp;
     size_t scan_tmp_bytes;
@@ -208,10 +220,11 @@ PrepLayout prep_layout(const gnn_csr *g, void *base) {
     L.win_count = c.take<int32_t>((size_t)L.n_win);
     L.win_rowbase = c.take<int32_t>((size_t)L.n_win);
     L.ne_rows = c.take<int32_t>((size_t)g->n_rows);
-    L.win_rowstart = c.take<int32_t>((size_t)L.n_win);
-    L.n_spans = (int32_t)((g->nnz + kSpanEdges - 1) / kSpanEdges);
+    L.n_spans = (int32_t)n_spans_of(g->nnz);
     L.sp_begin = c.take<int32_t>((size_t)L.n_spans + 1);
-    L.heavy = c.take<int32_t>((size_t)g->n_rows + 1);
+    L.win_rowstart = c.take<int32_t>((size_t)L.n_win);
+    L.items = c.take<int4>((size_t)span_item_cap(g->nnz));
+    L.items_count = c.take<int32_t>(1);
     L.scan_tmp_bytes = 0;
     if (L.n_win > 0)
         cub::DeviceScan::ExclusiveSum(nullptr, L.scan_tmp_bytes, (const int32_t *)nullptr,
@@ -254,15 +267,16 @@ const int32_t *prep_run_table(const gnn_csr *g, const void *prep) {
 
 void prep_span_tables(const gnn_csr *g, const void *prep, const uint32_t **win_flags,
                       const int32_t **win_rowbase, const int32_t **ne_rows,
-                      const int32_t **win_rowstart, const int32_t **sp_begin,
-                      const int32_t **heavy) {
+                      const int32_t **sp_begin, const int4 **items,
+                      const int32_t **items_count, const int32_t **win_rowstart) {
     PrepLayout L = prep_layout(g, const_cast<void *>(prep));
+    *win_rowstart = L.win_rowstart;
     *sp_begin = L.sp_begin;
-    *heavy = L.heavy;
+    *items = L.items;
+    *items_count = L.items_count;
     *win_flags = L.win_flags;
     *win_rowbase = L.win_rowbase;
     *ne_rows = L.ne_rows;
-    *win_rowstart = L.win_rowstart;
 }
 
 gnn_status check_csr_args(const gnn_csr *g) {
@@ -334,13 +348,15 @@ gnn_status gnn_graph_prepare(const gnn_csr *g, void *prep, size_t prep_bytes, vo
                                            L.win_rowbase, L.ne_rows);
         k_win_rowstart<<<wb, 256, 0, s>>>(g->rowptr, g->n_rows, L.n_win, L.win_rowbase, L.ne_rows,
                                           L.win_rowstart);
+        note_launch();
         const int sb = (int)std::min<int64_t>((L.n_spans + 1 + 255) / 256, (int64_t)sms * 8);
         k_span_begin<<<sb, 256, 0, s>>>(g->rowptr, g->nnz, L.n_spans, L.win_flags, L.win_rowbase,
                                         L.ne_rows, g->n_rows, L.sp_begin);
-        e = cudaMemsetAsync(L.heavy + g->n_rows, 0, sizeof(int32_t), s);
+        e = cudaMemsetAsync(L.items_count, 0, sizeof(int32_t), s);
         if (e != cudaSuccess) return cuda_status(e);
-        k_heavy_rows<<<rb, 256, 0, s>>>(g->rowptr, g->n_rows, L.heavy);
-        note_launch(4);
+        k_heavy_items<<<rb, 256, 0, s>>>(g->rowptr, g->n_rows, span_item_cap(g->nnz), L.items,
+                                         L.items_count, err);
+        note_launch(3);
         GNN_LAUNCH_CHECK();
     }
     return GNN_OK;

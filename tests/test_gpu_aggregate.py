@@ -183,18 +183,25 @@ def test_config2_rmat17_sampled(gnn):
 
 
 def test_repeat_calls_reuse_the_workspace(gnn):
-    # max is bit-identical run to run; sums of heavy rows are folded with fp32
-    # atomics, so repeats agree to rounding; both show the workspace slots and
-    # tickets are left zeroed for the next call
+    # with the prepared graph, heavy-row pieces are summed in edge order, so
+    # repeats are bit-identical; max is exact in any order.  Both show that
+    # the workspace slots and tickets are left ready for the next call.
     w = synth.workload("c2_rmat17")
     g = gnn.graph_prepare(dev(w["rowptr"]), dev(w["colidx"]))
     Xd = dev(w["X"])
-    a = gnn.gnn_spmm(g, Xd).cpu().numpy()
-    b = gnn.gnn_spmm(g, Xd).cpu().numpy()
-    assert_rowwise_close(b, a, 1e-6, "spmm repeat")
+    a = gnn.gnn_spmm(g, Xd)
+    b = gnn.gnn_spmm(g, Xd)
+    assert torch.equal(a, b), "spmm repeat differs"
+    s1 = gnn.gnn_segment_reduce_sum(g, Xd)
+    s2 = gnn.gnn_segment_reduce_sum(g, Xd)
+    assert torch.equal(s1, s2), "sum repeat differs"
     m1, i1 = gnn.gnn_segment_reduce_max(g, Xd)
     m2, i2 = gnn.gnn_segment_reduce_max(g, Xd)
     assert torch.equal(m1, m2) and torch.equal(i1, i2)
+    # without the prepared graph pieces are folded by fp32 atomics: equal to rounding
+    g0 = gnn.Graph(dev(w["rowptr"]), dev(w["colidx"]), prepare=False)
+    c = gnn.gnn_segment_reduce_sum(g0, Xd).cpu().numpy()
+    assert_rowwise_close(c, s1.cpu().numpy(), 1e-6, "sum without prep")
 
 
 def test_validate_flags_bad_csr(gnn):
