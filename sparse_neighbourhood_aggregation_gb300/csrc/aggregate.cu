@@ -85,7 +85,8 @@ struct AggArgs {
     const int32_t *win_rowstart;   // prepared first edge of the row holding edge 32*win
     const int4 *items;             // prepared heavy-row chunks {row, begin, end, chunk}
     const int32_t *items_count;    // prepared number of items
-    int32_t n_spans;               // edge-span kernel: spans of kSpanEdges edges
+    int32_t n_spans;               // edge-span kernel: spans of 1 << span_shift edges
+    int32_t span_shift;
     int64_t nnz;
     int64_t n_workers;
     int32_t n_rows;
@@ -504,7 +505,7 @@ __global__ void __launch_bounds__(256, (CPL <= 4 ? GNN_AGG_MINB : 2)) k_agg_auto
 
 // Edge-span AUTO kernel for rows of 32 16-byte chunks (fp32 F = 128, bf16
 // F = 256), used when the prepared graph is given.  The prepared graph cuts
-// the edge list into spans of about S = kSpanEdges edges: a row of degree
+// the edge list into spans of about S = span_edges(nnz) edges: a row of degree
 // <= S belongs whole to the span it starts in (so a span reads fewer than 2S
 // edges), and a heavier row is cut at every multiple of S.  Its row-end bits
 // (one 32-bit word per 32 edges) say where rows close, its window ranks and
@@ -702,7 +703,7 @@ k_agg_span(AggArgs a) {
     // the tail slot of the span the row starts in)
     bool head = b0 > 0 && !((__ldg(a.win_flags + ((b0 - 1) >> 5)) >> ((b0 - 1) & 31)) & 1u);
     const int64_t max_head_slot =
-        (OP == AGG_MAX && head) ? 2 * (int64_t)(__ldg(a.win_rowstart + (b0 >> 5)) / kSpanEdges) + 1 : 0;
+        (OP == AGG_MAX && head) ? 2 * (int64_t)(__ldg(a.win_rowstart + (b0 >> 5)) >> a.span_shift) + 1 : 0;
     // lane l holds the id (and row factor) of the row of rank k0 + kofs + l
     int32_t kofs = 0;
     int32_t rid = k0 + lane < a.n_rows ? __ldg(a.ne_rows + k0 + lane) : 0;
@@ -847,8 +848,8 @@ __global__ void __launch_bounds__(256, kFixBlocksPerSm) k_agg_span_fix(AggArgs a
     for (; q < n_items; q += nw) {
         const int32_t row = it.x, rb = it.y, re = it.z, cidx = it.w;
         if (q + nw < n_items) it = __ldg(a.items + q + nw);
-        const int32_t s0 = rb / kSpanEdges;
-        const int32_t np = (re - 1) / kSpanEdges - s0 + 1;
+        const int32_t s0 = rb >> a.span_shift;
+        const int32_t np = ((re - 1) >> a.span_shift) - s0 + 1;
         const int32_t nch = (np + kFixChunk - 1) / kFixChunk;
         const int32_t p_lo = cidx * kFixChunk, p_hi = min(np, p_lo + kFixChunk);
         Acc<OP, T, 1> acc;
@@ -1187,7 +1188,8 @@ gnn_status run_aggregate(const gnn_csr *g, const void *prep, int32_t op, int32_t
     if (prep && sh.V == 32) {
         prep_span_tables(g, prep, &a.win_flags, &a.win_rowbase, &a.ne_rows, &a.sp_begin, &a.items,
                          &a.items_count, &a.win_rowstart);
-        a.E = kSpanEdges;
+        a.E = span_edges(g->nnz);
+        a.span_shift = span_shift(g->nnz);
         a.n_spans = (int32_t)n_spans_of(g->nnz);
         a.carry = L.pieces;
         a.tickets = L.item_tickets;

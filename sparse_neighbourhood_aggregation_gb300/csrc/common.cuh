@@ -31,20 +31,31 @@ inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 #define GNN_RUN_EDGES 64
 #endif
 constexpr int32_t kRunEdges = GNN_RUN_EDGES;
-// Edges per span of the edge-span aggregation kernel (a multiple of 32); the
-// prepared graph stores each span's first edge.
+// Edges per span of the edge-span aggregation kernel: a power of two >= 64
+// chosen from the graph's size, so that a graph has at least ~16 resident
+// waves of spans (longer spans amortise each warp's start-up and cut fewer
+// rows; shorter ones keep small graphs busy).  The prepared graph stores each
+// span's first edge.
 #ifndef GNN_SPAN_EDGES
-#define GNN_SPAN_EDGES 64
+#define GNN_SPAN_EDGES 0   // 0: by graph size; otherwise fixed
 #endif
-constexpr int32_t kSpanEdges = GNN_SPAN_EDGES;
-static_assert(kSpanEdges % 32 == 0, "spans are whole 32-edge windows");
-inline int64_t n_spans_of(int64_t nnz) { return (nnz + kSpanEdges - 1) / kSpanEdges; }
-// A row of degree > kSpanEdges is cut into one piece per span it touches;
+inline int32_t span_shift(int64_t nnz) {
+    if (GNN_SPAN_EDGES > 0) {
+        int32_t k = 5;
+        while ((1 << k) < GNN_SPAN_EDGES) ++k;
+        return k;
+    }
+    return nnz >= ((int64_t)1 << 24) ? 8 : nnz >= ((int64_t)1 << 23) ? 7 : 6;
+}
+inline int32_t span_edges(int64_t nnz) { return 1 << span_shift(nnz); }
+inline int64_t n_spans_of(int64_t nnz) { return (nnz + span_edges(nnz) - 1) / span_edges(nnz); }
+// A row of degree > span_edges is cut into one piece per span it touches;
 // its pieces are summed in chunks of kFixChunk, one work item per chunk.
 constexpr int32_t kFixChunk = 16;
 inline int64_t span_item_cap(int64_t nnz) {
-    return nnz / (kSpanEdges + 1) + 2 * n_spans_of(nnz) / kFixChunk + 1;
+    return nnz / (span_edges(nnz) + 1) + 2 * n_spans_of(nnz) / kFixChunk + 1;
 }
+
 inline int64_t n_runs(int64_t nnz, int32_t E) {
     int64_t n = (nnz + E - 1) / E;
     return n > 0 ? n : 1;

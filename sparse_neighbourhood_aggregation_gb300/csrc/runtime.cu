@@ -146,7 +146,7 @@ __global__ void k_win_rowstart(const int32_t *__restrict__ rowptr, int32_t n_row
 // sp_begin[w] = first edge of span w.  The nominal span is [w*S, (w+1)*S);
 // a row of degree <= S that crosses w*S belongs whole to span w-1, so span w
 // starts after it; a heavier row is cut at w*S.  sp_begin[n_spans] = nnz.
-__global__ void k_span_begin(const int32_t *__restrict__ rowptr, int64_t nnz, int32_t n_spans,
+__global__ void k_span_begin(const int32_t *__restrict__ rowptr, int64_t nnz, int32_t n_spans, int32_t es,
                              const uint32_t *__restrict__ flags,
                              const int32_t *__restrict__ win_rowbase,
                              const int32_t *__restrict__ ne_rows, int32_t n_rows,
@@ -154,12 +154,12 @@ __global__ void k_span_begin(const int32_t *__restrict__ rowptr, int64_t nnz, in
     int32_t stride = gridDim.x * blockDim.x;
     for (int32_t w = blockIdx.x * blockDim.x + threadIdx.x; w <= n_spans; w += stride) {
         if (w == n_spans) { out[w] = (int32_t)nnz; continue; }
-        const int32_t e = w * kSpanEdges;
+        const int32_t e = w << es;
         if (e == 0 || ((flags[(e - 1) >> 5] >> ((e - 1) & 31)) & 1u)) { out[w] = e; continue; }
         const int32_t k = win_rowbase[e >> 5];
         const int32_t r = (uint32_t)k < (uint32_t)n_rows ? ne_rows[k] : 0;
         const int32_t s = rowptr[r], t = rowptr[r + 1];
-        out[w] = (t - s > kSpanEdges) ? e : t;
+        out[w] = (t - s > (1 << es)) ? e : t;
     }
 }
 
@@ -168,14 +168,14 @@ __global__ void k_span_begin(const int32_t *__restrict__ rowptr, int64_t nnz, in
 // at a time, item {row, rowptr[row], rowptr[row+1], chunk index}.  A row's
 // items are contiguous (one atomic reservation); rows come in any order.
 // items_count holds their number.
-__global__ void k_heavy_items(const int32_t *__restrict__ rowptr, int32_t n_rows, int64_t cap,
+__global__ void k_heavy_items(const int32_t *__restrict__ rowptr, int32_t n_rows, int32_t es, int64_t cap,
                               int4 *__restrict__ items, int32_t *__restrict__ items_count,
                               int32_t *err) {
     int32_t stride = gridDim.x * blockDim.x;
     for (int32_t r = blockIdx.x * blockDim.x + threadIdx.x; r < n_rows; r += stride) {
         const int32_t rb = rowptr[r], re = rowptr[r + 1];
-        if (re - rb <= kSpanEdges) continue;
-        const int32_t np = (re - 1) / kSpanEdges - rb / kSpanEdges + 1;
+        if (re - rb <= (1 << es)) continue;
+        const int32_t np = ((re - 1) >> es) - (rb >> es) + 1;
         const int32_t nch = (np + kFixChunk - 1) / kFixChunk;
         const int32_t base = atomicAdd(items_count, nch);
         if ((int64_t)base + nch > cap) { set_device_error(err, GNN_ERR_DEVICE_CHECK); continue; }
@@ -350,11 +350,13 @@ gnn_status gnn_graph_prepare(const gnn_csr *g, void *prep, size_t prep_bytes, vo
                                           L.win_rowstart);
         note_launch();
         const int sb = (int)std::min<int64_t>((L.n_spans + 1 + 255) / 256, (int64_t)sms * 8);
-        k_span_begin<<<sb, 256, 0, s>>>(g->rowptr, g->nnz, L.n_spans, L.win_flags, L.win_rowbase,
+        k_span_begin<<<sb, 256, 0, s>>>(g->rowptr, g->nnz, L.n_spans, span_shift(g->nnz), L.win_flags,
+                                        L.win_rowbase,
                                         L.ne_rows, g->n_rows, L.sp_begin);
         e = cudaMemsetAsync(L.items_count, 0, sizeof(int32_t), s);
         if (e != cudaSuccess) return cuda_status(e);
-        k_heavy_items<<<rb, 256, 0, s>>>(g->rowptr, g->n_rows, span_item_cap(g->nnz), L.items,
+        k_heavy_items<<<rb, 256, 0, s>>>(g->rowptr, g->n_rows, span_shift(g->nnz), span_item_cap(g->nnz),
+                                         L.items,
                                          L.items_count, err);
         note_launch(3);
         GNN_LAUNCH_CHECK();

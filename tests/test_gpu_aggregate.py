@@ -182,6 +182,29 @@ def test_config2_rmat17_sampled(gnn):
     run_all(gnn, rp, ci, X, rows=rows)
 
 
+@pytest.mark.parametrize("graph", ["rmat19_ef20", "c3_rmat20"])
+def test_longer_spans_on_larger_graphs(gnn, graph):
+    """Graphs of 2^23..2^24 edges run 128-edge spans and larger ones 256-edge
+    spans; SpMM (all norms and mappings), sum, mean and max on sampled rows
+    (the heaviest, rows around span boundaries, random rows)."""
+    if graph == "rmat19_ef20":
+        rp, ci = synth.rmat(19, 20)
+        assert (1 << 23) <= len(ci) < (1 << 24)
+    else:
+        w = synth.workload("c3_rmat20_gatv2", features=False)
+        rp, ci = w["rowptr"], w["colidx"]
+        assert len(ci) >= (1 << 24)
+    n = len(rp) - 1
+    X = synth.normal_f32((n, 128), 1.0, 31)
+    deg = np.diff(rp)
+    rng = np.random.default_rng(7)
+    span = 128 if len(ci) < (1 << 24) else 256
+    bnd = np.searchsorted(rp, np.arange(span, len(ci), span * 1013), side="right") - 1
+    rows = np.unique(np.concatenate([np.argsort(-deg, kind="stable")[:8], bnd,
+                                     rng.choice(n, 150, replace=False), [0, n - 1]])).astype(np.int32)
+    run_all(gnn, rp, ci, X, rows=rows, norms=(0, 3))
+
+
 def test_repeat_calls_reuse_the_workspace(gnn):
     # with the prepared graph, heavy-row pieces are summed in edge order, so
     # repeats are bit-identical; max is exact in any order.  Both show that
