@@ -59,7 +59,14 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kAttnRunMul = 4;
 constexpr int kAttnE = kRunEdges * kAttnRunMul;
 constexpr int kAttnWarps = 4;  // warps per block
-constexpr int kGroup = 4;      // edges scored together
+// Edges scored together and resident 4-warp blocks per SM asked of the
+// compiler, per attention kind (measured on GB300: GATv2 at c3, 2 edges and
+// 6 blocks, 2.07 ms against 2.32 ms for 4 edges at the compiler's choice of
+// 127 registers; GT at c4, 4 edges and 5 blocks, 2.11 against 2.32 ms).
+// Lanes holding more than 8 channels (wide fp32 heads) keep 4-edge groups
+// and the compiler's register choice.
+__host__ __device__ constexpr int att_group(int kind, int nc) { return (kind == 0 && nc <= 8) ? 2 : 4; }
+__host__ __device__ constexpr int att_min_blocks(int kind, int nc) { return nc > 8 ? 1 : kind == 0 ? 6 : 5; }
 
 enum AttnKind { ATT_GATV2 = 0, ATT_GT = 1 };
 
@@ -395,8 +402,9 @@ __device__ __forceinline__ void consume(const AttnArgs &a, const Lane<KIND, T, C
         const unsigned char *stage = R.stages + (size_t)R.cs * a.U * a.rec;
         const int32_t n = min(a.U - R.u, end - e);
         int32_t g = 0;
-        for (; g + kGroup <= n; g += kGroup)
-            fold_edges<KIND, T, CPL, LPH, kGroup>(a, L, stage + (size_t)(R.u + g) * a.rec, dq, al, st);
+        constexpr int NG = att_group(KIND, CPL * Elt<T>::N);
+        for (; g + NG <= n; g += NG)
+            fold_edges<KIND, T, CPL, LPH, NG>(a, L, stage + (size_t)(R.u + g) * a.rec, dq, al, st);
         for (; g < n; ++g) fold_edges<KIND, T, CPL, LPH, 1>(a, L, stage + (size_t)(R.u + g) * a.rec, dq, al, st);
         e += n;
         R.u += n;
@@ -417,7 +425,7 @@ __device__ __forceinline__ void consume(const AttnArgs &a, const Lane<KIND, T, C
 }
 
 template <int KIND, class T, int CPL, int LPH>
-__global__ void __launch_bounds__(kAttnWarps * 32) k_attn(AttnArgs a) {
+__global__ void __launch_bounds__(kAttnWarps * 32, att_min_blocks(KIND, CPL * Elt<T>::N)) k_attn(AttnArgs a) {
     constexpr int NC = CPL * Elt<T>::N;
     extern __shared__ __align__(128) unsigned char smem[];
     const int warp = threadIdx.x >> 5;
