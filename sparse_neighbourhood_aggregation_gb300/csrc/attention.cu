@@ -150,13 +150,6 @@ struct Lane {
     __device__ __forceinline__ bool act() const { return LPH > 0 ? true : active; }
 };
 
-// 2^x by the hardware approximation (ex2.approx.ftz; 2^-inf = +0)
-__device__ __forceinline__ float exp2_approx(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
 template <class T, int CPL>
 __device__ __forceinline__ void unpack_row(const uint4 *v, float *f) {
 #pragma unroll

@@ -146,6 +146,13 @@ __device__ __forceinline__ float key_value(uint32_t k) {
 
 __device__ __forceinline__ int lane_id() { return threadIdx.x & 31; }
 
+// 2^x by the hardware approximation (ex2.approx.ftz; 2^-inf = +0)
+__device__ __forceinline__ float exp2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // Packed fp32 pairs (Blackwell f32x2 instructions): d += a * b and a + b on
 // two lanes of a 64-bit register pair.
 __device__ __forceinline__ uint64_t pk2(float x, float y) {

@@ -9,12 +9,14 @@
 // kernel and the two softmax states are merged).
 //
 // GB300 design.  One CTA (4 warps, one thread per row) per 128-row group and
-// head.  The group's listed column blocks are taken in chunks of up to 12
-// blocks (192 columns):
+// head.  The group's listed column blocks are taken in chunks of up to
+// kChunkBlocks blocks:
 //   1. the chunk's K rows and V rows (head h) are gathered into shared memory
 //      in the no-swizzle core-matrix layout of tcgen05 operands (8 rows x 16
-//      bytes per core matrix); V is written transposed so that both operands
-//      of the second product are K-major;
+//      bytes per core matrix), every load of the chunk issued before the
+//      first store; V is written transposed so that both operands of the
+//      second product are K-major; each thread fetches its row's tile-mask
+//      bits for the chunk alongside;
 //   2. one thread issues S = Q K^T (M = 128, N = 16 x blocks, K = head_dim)
 //      into TMEM;
 //   3. each thread reads its row of S (tcgen05.ld), masks it with the tile
@@ -45,9 +47,13 @@ size_t gt_workspace_bytes(const gnn_csr *g, int32_t heads, int32_t head_dim);
 namespace {
 
 constexpr int kRows = 128;          // rows per group (MMA M)
-constexpr int kChunkBlocks = 12;    // column blocks per chunk (192 columns)
-constexpr int kTmemCols = 256;      // S: [0, 192), O: [192, 192 + D)
-constexpr int kOCol = 192;
+// Column blocks per chunk: S takes 16 per block TMEM columns and O the next
+// D, within a power-of-two allocation.  128 columns per CTA let four CTAs
+// share an SM's 512; measured on GB300 (GT at c4, D = 32, tiles at fill >=
+// 0.2): 12 blocks 1.23 ms, 8 1.12, 6 0.85, 4 0.88.
+__host__ __device__ constexpr int chunk_blocks(int D) { return D == 32 ? 6 : 4; }
+__host__ __device__ constexpr int o_col(int D) { return chunk_blocks(D) * 16; }
+__host__ __device__ constexpr int tmem_cols_for(int n) { return n <= 32 ? 32 : n <= 64 ? 64 : n <= 128 ? 128 : 256; }
 constexpr float kLog2eT = 1.4426950408889634f;
 constexpr float kLn2T = 0.6931471805599453f;
 
@@ -67,6 +73,10 @@ __device__ __forceinline__ void st16s(void *p, uint4 v) { *reinterpret_cast<uint
 
 template <int D>
 __global__ void __launch_bounds__(kRows) k_gt_tiles(TileArgs t) {
+    constexpr int kChunkBlocks = chunk_blocks(D);
+    constexpr int kOCol = o_col(D);
+    constexpr int kTmemCols = tmem_cols_for(kOCol + D);
+    static_assert(kOCol + D <= 256, "S and O must fit one 256-column allocation");
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *base = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                             ~(uintptr_t)1023);
@@ -119,19 +129,54 @@ __global__ void __launch_bounds__(kRows) k_gt_tiles(TileArgs t) {
     for (int c0 = b0; c0 < b1 && ok; c0 += kChunkBlocks) {
         const int nbk = min(kChunkBlocks, b1 - c0);
         const int NC = nbk * 16;
-        // gather K (as rows) and V (transposed) of the chunk's columns
-        for (int idx = tid; idx < NC * (D / 8); idx += kRows) {
-            const int c = idx / (D / 8), k = idx % (D / 8);
-            const int32_t col = __ldg(t.blk_cols + (int64_t)c0 * 16 + c);
-            const uint4 kv = ldg16(t.K + (int64_t)col * HD + h * D + 8 * k);
-            st16s(sK + ((c / 8) * (D / 8) + k) * 128 + (c % 8) * 16, kv);
-            const uint4 vv = ldg16(t.V + (int64_t)col * HD + h * D + 8 * k);
-            const uint16_t *ve = reinterpret_cast<const uint16_t *>(&vv);
+        // this row's mask bits of the chunk's blocks (16 per block), fetched
+        // together ahead of the gather
+        uint32_t mk[(kChunkBlocks + 1) / 2];
+        {
+            unsigned long long mw[kChunkBlocks];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const int d = 8 * k + q;
-                *reinterpret_cast<uint16_t *>(sV + ((d / 8) * (NC / 8) + c / 8) * 128 + (d % 8) * 16 + (c % 8) * 2) =
-                    ve[q];
+            for (int b = 0; b < kChunkBlocks; ++b)
+                mw[b] = b < nbk ? __ldg(t.blk_mask + ((int64_t)(c0 + b) * 8 + w) * 4 + (r * 16) / 64) : 0ull;
+#pragma unroll
+            for (int b = 0; b < kChunkBlocks; b += 2) {
+                const uint32_t lo = (uint32_t)(mw[b] >> ((r * 16) % 64)) & 0xFFFFu;
+                const uint32_t hi = b + 1 < kChunkBlocks ? (uint32_t)(mw[b + 1] >> ((r * 16) % 64)) & 0xFFFFu : 0u;
+                mk[b / 2] = lo | (hi << 16);
+            }
+        }
+        // gather K (as rows) and V (transposed) of the chunk's columns: all
+        // column ids first, then all rows, then the shared-memory stores
+        constexpr int IT = NCMAX * (D / 8) / kRows;
+        static_assert(NCMAX * (D / 8) % kRows == 0, "the gather covers a chunk in whole rounds");
+        int32_t colv[IT];
+#pragma unroll
+        for (int i = 0; i < IT; ++i) {
+            const int idx = tid + i * kRows;
+            colv[i] = idx < NC * (D / 8) ? __ldg(t.blk_cols + (int64_t)c0 * 16 + idx / (D / 8)) : 0;
+        }
+        uint4 kvv[IT], vvv[IT];
+#pragma unroll
+        for (int i = 0; i < IT; ++i) {
+            const int idx = tid + i * kRows;
+            if (idx < NC * (D / 8)) {
+                const int k = idx % (D / 8);
+                kvv[i] = ldg16(t.K + (int64_t)colv[i] * HD + h * D + 8 * k);
+                vvv[i] = ldg16(t.V + (int64_t)colv[i] * HD + h * D + 8 * k);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < IT; ++i) {
+            const int idx = tid + i * kRows;
+            if (idx < NC * (D / 8)) {
+                const int c = idx / (D / 8), k = idx % (D / 8);
+                st16s(sK + ((c / 8) * (D / 8) + k) * 128 + (c % 8) * 16, kvv[i]);
+                const uint16_t *ve = reinterpret_cast<const uint16_t *>(&vvv[i]);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const int d = 8 * k + q;
+                    *reinterpret_cast<uint16_t *>(sV + ((d / 8) * (NC / 8) + c / 8) * 128 + (d % 8) * 16 +
+                                                  (c % 8) * 2) = ve[q];
+                }
             }
         }
         fence_proxy_async_smem();
@@ -155,41 +200,29 @@ __global__ void __launch_bounds__(kRows) k_gt_tiles(TileArgs t) {
         // pass 1: masked row maximum of this chunk (scores in base-2 units)
         const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
         float cm = -INFINITY;
-        for (int cc = 0; cc < NC; cc += 32) {
+#pragma unroll
+        for (int cc = 0; cc < NCMAX; cc += 32) {
+            if (cc >= NC) break;
             uint32_t v[32];
             tmem_ld32(lane_base + (uint32_t)cc, v);
-            const unsigned long long w0 = __ldg(t.blk_mask + ((int64_t)(c0 + cc / 16) * 8 + w) * 4 + (r * 16) / 64);
-            const uint32_t m0 = (uint32_t)(w0 >> ((r * 16) % 64)) & 0xFFFFu;
-            uint32_t m1 = 0;
-            if (cc + 16 < NC) {
-                const unsigned long long w1 =
-                    __ldg(t.blk_mask + ((int64_t)(c0 + cc / 16 + 1) * 8 + w) * 4 + (r * 16) / 64);
-                m1 = (uint32_t)(w1 >> ((r * 16) % 64)) & 0xFFFFu;
-            }
-            const uint32_t mk = m0 | (m1 << 16);
+            const uint32_t mkc = (cc + 16 < NC) ? mk[cc / 32] : (mk[cc / 32] & 0xFFFFu);
 #pragma unroll
             for (int q = 0; q < 32; ++q)
-                if ((mk >> q) & 1u) cm = fmaxf(cm, __uint_as_float(v[q]) * t.qscale);
+                if ((mkc >> q) & 1u) cm = fmaxf(cm, __uint_as_float(v[q]) * t.qscale);
         }
         const float mn = fmaxf(m, cm);
-        const float sc = (m == -INFINITY) ? 0.f : exp2f(m - mn);
+        const float sc = (m == -INFINITY) ? 0.f : exp2_approx(m - mn);
         l *= sc;
 #pragma unroll
         for (int d = 0; d < D; ++d) o[d] *= sc;
         m = mn;
         // pass 2: P = exp2(s - m) (0 where masked), into shared memory
-        for (int cc = 0; cc < NC; cc += 32) {
+#pragma unroll
+        for (int cc = 0; cc < NCMAX; cc += 32) {
+            if (cc >= NC) break;
             uint32_t v[32];
             tmem_ld32(lane_base + (uint32_t)cc, v);
-            const unsigned long long w0 = __ldg(t.blk_mask + ((int64_t)(c0 + cc / 16) * 8 + w) * 4 + (r * 16) / 64);
-            const uint32_t m0 = (uint32_t)(w0 >> ((r * 16) % 64)) & 0xFFFFu;
-            uint32_t m1 = 0;
-            if (cc + 16 < NC) {
-                const unsigned long long w1 =
-                    __ldg(t.blk_mask + ((int64_t)(c0 + cc / 16 + 1) * 8 + w) * 4 + (r * 16) / 64);
-                m1 = (uint32_t)(w1 >> ((r * 16) % 64)) & 0xFFFFu;
-            }
-            const uint32_t mk = m0 | (m1 << 16);
+            const uint32_t mkc = (cc + 16 < NC) ? mk[cc / 32] : (mk[cc / 32] & 0xFFFFu);
             const int nq = min(32, NC - cc);
 #pragma unroll
             for (int g8 = 0; g8 < 4; ++g8) {
@@ -198,8 +231,8 @@ __global__ void __launch_bounds__(kRows) k_gt_tiles(TileArgs t) {
 #pragma unroll
                 for (int q2 = 0; q2 < 4; ++q2) {
                     const int q = g8 * 8 + 2 * q2;
-                    const float p0 = ((mk >> q) & 1u) ? exp2f(__uint_as_float(v[q]) * t.qscale - m) : 0.f;
-                    const float p1 = ((mk >> (q + 1)) & 1u) ? exp2f(__uint_as_float(v[q + 1]) * t.qscale - m) : 0.f;
+                    const float p0 = ((mkc >> q) & 1u) ? exp2_approx(__uint_as_float(v[q]) * t.qscale - m) : 0.f;
+                    const float p1 = ((mkc >> (q + 1)) & 1u) ? exp2_approx(__uint_as_float(v[q + 1]) * t.qscale - m) : 0.f;
                     const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
                     // the sum uses the rounded weights, the ones the product uses
                     l += __low2float(b2) + __high2float(b2);
@@ -266,10 +299,18 @@ __global__ void __launch_bounds__(kRows) k_gt_tiles(TileArgs t) {
     }
 }
 
+// Dynamic shared memory per CTA: the operands, raised if needed so that no
+// more CTAs are resident on an SM than its 512 TMEM columns serve (an extra
+// one would only wait in tcgen05.alloc).
 template <int D>
 size_t tile_smem_bytes() {
-    return 1024 + (size_t)kRows * D * 2 + 2 * (size_t)kChunkBlocks * 16 * D * 2 + (size_t)kRows * kChunkBlocks * 16 * 2 +
-           64;
+    constexpr int kChunkBlocks = chunk_blocks(D);
+    constexpr int kOCol = o_col(D);
+    const size_t need = 1024 + (size_t)kRows * D * 2 + 2 * (size_t)kChunkBlocks * 16 * D * 2 +
+                        (size_t)kRows * kChunkBlocks * 16 * 2 + 64;
+    const size_t ctas = 512 / tmem_cols_for(kOCol + D);
+    const size_t floor = (size_t)228 * 1024 / (ctas + 1) - 1024 + 64;
+    return std::max(need, floor);
 }
 
 template <int D>
