@@ -83,8 +83,8 @@ __global__ void __launch_bounds__(kRows) k_gt_tiles(TileArgs t) {
     constexpr int NCMAX = kChunkBlocks * 16;
     unsigned char *sQ = base;                         // [16][D/8] core matrices
     unsigned char *sK = sQ + kRows * D * 2;           // [NC/8][D/8]
-    unsigned char *sV = sK + NCMAX * D * 2;           // [D/8][NC/8] (V transposed)
-    unsigned char *sP = sV + NCMAX * D * 2;           // [16][NC/8]
+    unsigned char *sV = sK + NCMAX * D * 2;           // [D/8][NC/8] (V transposed), padded rows
+    unsigned char *sP = sV + NCMAX * D * 2 + (D / 8) * 16;  // [16][NC/8]
     uint64_t *bar = reinterpret_cast<uint64_t *>(sP + kRows * NCMAX * 2);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 1);
 
@@ -144,6 +144,10 @@ __global__ void __launch_bounds__(kRows) k_gt_tiles(TileArgs t) {
                 mk[b / 2] = lo | (hi << 16);
             }
         }
+        // V^T rows of core matrices are (NC/8)*128 + 16 bytes apart: the
+        // 16-byte pad puts the four channel groups that a warp writes at once
+        // in different shared-memory banks
+        const int vstride = (NC / 8) * 128 + 16;
         // gather K (as rows) and V (transposed) of the chunk's columns: all
         // column ids first, then all rows, then the shared-memory stores
         constexpr int IT = NCMAX * (D / 8) / kRows;
@@ -174,7 +178,7 @@ __global__ void __launch_bounds__(kRows) k_gt_tiles(TileArgs t) {
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
                     const int d = 8 * k + q;
-                    *reinterpret_cast<uint16_t *>(sV + ((d / 8) * (NC / 8) + c / 8) * 128 + (d % 8) * 16 +
+                    *reinterpret_cast<uint16_t *>(sV + (d / 8) * vstride + (c / 8) * 128 + (d % 8) * 16 +
                                                   (c % 8) * 2) = ve[q];
                 }
             }
@@ -250,7 +254,7 @@ __global__ void __launch_bounds__(kRows) k_gt_tiles(TileArgs t) {
         if (tid == 0) {
             for (int ks = 0; ks < NC / 16; ++ks)
                 umma_bf16(tmem + kOCol, plain_desc(su32(sP) + ks * 256, 128, (NC / 8) * 128),
-                          plain_desc(su32(sV) + ks * 256, 128, (NC / 8) * 128), idesc_o, ks > 0);
+                          plain_desc(su32(sV) + ks * 256, 128, vstride), idesc_o, ks > 0);
             umma_commit(bar);
         }
         if (!__syncthreads_and(mbar_wait_bounded(bar, phase))) {
@@ -306,7 +310,7 @@ template <int D>
 size_t tile_smem_bytes() {
     constexpr int kChunkBlocks = chunk_blocks(D);
     constexpr int kOCol = o_col(D);
-    const size_t need = 1024 + (size_t)kRows * D * 2 + 2 * (size_t)kChunkBlocks * 16 * D * 2 +
+    const size_t need = 1024 + (size_t)kRows * D * 2 + 2 * (size_t)kChunkBlocks * 16 * D * 2 + (D / 8) * 16 +
                         (size_t)kRows * kChunkBlocks * 16 * 2 + 64;
     const size_t ctas = 512 / tmem_cols_for(kOCol + D);
     const size_t floor = (size_t)228 * 1024 / (ctas + 1) - 1024 + 64;
