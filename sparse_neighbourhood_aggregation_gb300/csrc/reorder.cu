@@ -103,14 +103,22 @@ __global__ void k_inv_from_perm(const int32_t *__restrict__ perm, int32_t *__res
     if (i < n) inv[perm[i]] = i;
 }
 
-// |S(i)|, S = A + A^T without self-loops: merge of the sorted row i of A and
-// row i of A^T, counting distinct ids other than i.
+// |S(i)|, S = A + A^T without self-loops: the distinct ids other than i in
+// the sorted row i of A and row i of A^T.  A thread merges the two lists of a
+// row whose lengths sum to at most kSymLight; longer rows are queued for
+// k_sym_degree_heavy (heavy[0..*n_heavy)).
+constexpr int32_t kSymLight = 1024;
+
 __global__ void k_sym_degree(const int32_t *__restrict__ rp, const int32_t *__restrict__ ci,
                              const int32_t *__restrict__ tp, const int32_t *__restrict__ tc, int32_t n,
-                             int32_t *__restrict__ sdeg) {
+                             int32_t *__restrict__ sdeg, int32_t *__restrict__ heavy, int32_t *n_heavy) {
     const int32_t i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n) return;
     int32_t a = rp[i], ae = rp[i + 1], b = tp[i], be = tp[i + 1];
+    if ((ae - a) + (be - b) > kSymLight) {
+        heavy[atomicAdd(n_heavy, 1)] = i;
+        return;
+    }
     int32_t cnt = 0;
     while (a < ae || b < be) {
         int32_t x;
@@ -120,6 +128,57 @@ __global__ void k_sym_degree(const int32_t *__restrict__ rp, const int32_t *__re
         cnt += (x != i);
     }
     sdeg[i] = cnt;
+}
+
+// first position in sorted v[lo, hi) holding a value >= x
+__device__ __forceinline__ int32_t lower_bound_i32(const int32_t *__restrict__ v, int32_t lo, int32_t hi,
+                                                   int32_t x) {
+    while (lo < hi) {
+        const int32_t mid = lo + ((hi - lo) >> 1);
+        if (v[mid] < x) lo = mid + 1; else hi = mid;
+    }
+    return lo;
+}
+
+// A block per queued row: |S(i)| = |P \ {i}| + |Q \ {i}| - |(P n Q) \ {i}|,
+// P the shorter of the two lists; each thread takes every blockDim-th
+// element of P and looks it up in Q by binary search.  Exact integer counts.
+__global__ void __launch_bounds__(256) k_sym_degree_heavy(const int32_t *__restrict__ rp,
+                                                          const int32_t *__restrict__ ci,
+                                                          const int32_t *__restrict__ tp,
+                                                          const int32_t *__restrict__ tc,
+                                                          const int32_t *__restrict__ heavy,
+                                                          const int32_t *n_heavy, int32_t *__restrict__ sdeg) {
+    __shared__ int32_t s_inter, s_self_p, s_self_q;
+    const int32_t nh = *n_heavy;
+    for (int32_t q = blockIdx.x; q < nh; q += gridDim.x) {
+        const int32_t i = heavy[q];
+        const int32_t *P = ci + rp[i], *Q = tc + tp[i];
+        int32_t np = rp[i + 1] - rp[i], nq = tp[i + 1] - tp[i];
+        if (np > nq) {
+            const int32_t *t = P; P = Q; Q = t;
+            const int32_t tn = np; np = nq; nq = tn;
+        }
+        if (threadIdx.x == 0) {
+            s_inter = 0;
+            s_self_p = 0;
+            const int32_t k = lower_bound_i32(Q, 0, nq, i);
+            s_self_q = (k < nq && Q[k] == i) ? 1 : 0;
+        }
+        __syncthreads();
+        int32_t inter = 0, self_p = 0;
+        for (int32_t k = threadIdx.x; k < np; k += blockDim.x) {
+            const int32_t x = P[k];
+            if (x == i) { self_p = 1; continue; }
+            const int32_t j = lower_bound_i32(Q, 0, nq, x);
+            inter += (j < nq && Q[j] == x) ? 1 : 0;
+        }
+        if (inter) atomicAdd(&s_inter, inter);
+        if (self_p) atomicAdd(&s_self_p, 1);
+        __syncthreads();
+        if (threadIdx.x == 0) sdeg[i] = (np - s_self_p) + (nq - s_self_q) - s_inter;
+        __syncthreads();
+    }
 }
 
 // connected components of A (direction ignored): hook roots to the smaller
@@ -313,7 +372,7 @@ struct ReorderWs {
     int32_t *tp, *tc, *rowid, *tkeys;  // A^T rowptr / colidx, edge row ids, sorted column keys
     int32_t *sdeg, *order_di, *rank, *parent, *cmin, *csize, *by_rank, *base;
     int32_t *pos, *ppos, *flag, *fill, *front, *cand, *seg;
-    int32_t *counters;                 // [0] changed, [1] frontier size, [2] candidate count
+    int32_t *counters;                 // [0] changed, [1] frontier size, [2] candidate count, [3] heavy rows
     void *temp;
     size_t temp_bytes;
     size_t bytes;
@@ -419,9 +478,14 @@ gnn_status rcm_order(const gnn_csr *g, ReorderWs &W, int32_t *perm, cudaStream_t
     GNN_CUDA_TRY(cub::DeviceScan::ExclusiveSum(W.temp, tb, W.dout, W.tp, n + 1, s));
     note_launch();
     // degrees in S and the (degree, id) ranks
-    k_sym_degree<<<blocks_for(n), 256, 0, s>>>(g->rowptr, g->colidx, W.tp, W.tc, n, W.sdeg);
+    // (cmin is free until the components pass: it holds the queued heavy rows)
+    GNN_CUDA_TRY(cudaMemsetAsync(W.counters + 3, 0, sizeof(int32_t), s));
+    k_sym_degree<<<blocks_for(n), 256, 0, s>>>(g->rowptr, g->colidx, W.tp, W.tc, n, W.sdeg, W.cmin,
+                                                W.counters + 3);
+    k_sym_degree_heavy<<<sm_count() * 4, 256, 0, s>>>(g->rowptr, g->colidx, W.tp, W.tc, W.cmin, W.counters + 3,
+                                                      W.sdeg);
     k_iota<<<blocks_for(n), 256, 0, s>>>(W.id[0], n);
-    note_launch(2);
+    note_launch(3);
     GNN_CUDA_TRY(cub::DeviceRadixSort::SortPairs(W.temp, tb, reinterpret_cast<const uint32_t *>(W.sdeg),
                                                  W.key32[1], W.id[0], W.order_di, n, 0, 32, s));
     note_launch();
