@@ -26,7 +26,9 @@
 //   4. one thread issues O_chunk = P V (M = 128, N = head_dim, K = columns);
 //      each thread adds its row of O_chunk to its output row in registers.
 // The residual edges run first on the CSR kernel, which writes (out, lse);
-// the tile state is then merged with it through the logsumexp.  MMA
+// the tile state is then merged with it through the logsumexp.  With no
+// residual edges the tile kernel writes every row itself (empty rows: 0 and
+// lse = -inf), so out is neither pre-written nor read back.  MMA
 // completion is tracked with an mbarrier; every wait is bounded.
 #include <algorithm>
 #include <mutex>
@@ -65,6 +67,7 @@ struct TileArgs {
     float *out;        // holds the residual result on entry
     float *lse;        // [n, heads]: the residual logsumexp on entry, the merged one on exit
     int32_t n_rows, heads, D;
+    int32_t has_residual;  // 0: no residual edges; out and lse are written here, not merged
     float qscale;      // scale * log2 e
     int32_t *err;
 };
@@ -91,10 +94,19 @@ __global__ void __launch_bounds__(kRows) k_gt_tiles(TileArgs t) {
     const int g = blockIdx.x, h = blockIdx.y;
     const int tid = threadIdx.x, warp = tid >> 5;
     const int b0 = __ldg(t.grp_blk_offset + g), b1 = __ldg(t.grp_blk_offset + g + 1);
-    if (b0 == b1) return;  // no tiles: the residual result stands
     const int64_t HD = (int64_t)t.heads * D;
     const int32_t row = g * kRows + tid;
     const bool valid = row < t.n_rows;
+    if (b0 == b1) {
+        // no tiles: the residual result stands, or (no residual) the rows are empty
+        if (!t.has_residual && valid) {
+            float *orow = t.out + (int64_t)row * HD + h * D;
+#pragma unroll
+            for (int d = 0; d < D; d += 4) *reinterpret_cast<float4 *>(orow + d) = make_float4(0.f, 0.f, 0.f, 0.f);
+            t.lse[(int64_t)row * t.heads + h] = -INFINITY;
+        }
+        return;
+    }
 
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
@@ -279,8 +291,17 @@ __global__ void __launch_bounds__(kRows) k_gt_tiles(TileArgs t) {
         // an MMA still in flight completes before TMEM is released
         mbar_wait_bounded(bar, phase);
     }
+    if (ok && valid && !t.has_residual) {
+        // no residual edges: this is the whole result
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        float *orow = t.out + (int64_t)row * HD + h * D;
+#pragma unroll
+        for (int d = 0; d < D; d += 4)
+            *reinterpret_cast<float4 *>(orow + d) = make_float4(o[d] * inv, o[d + 1] * inv, o[d + 2] * inv, o[d + 3] * inv);
+        t.lse[(int64_t)row * t.heads + h] = l > 0.f ? (m + log2f(l)) * kLn2T : -INFINITY;
+    }
     // merge with the residual CSR result (out, lse_res) through the logsumexp
-    if (ok && valid && l > 0.f) {
+    if (ok && valid && t.has_residual && l > 0.f) {
         const float lse_t = (m + log2f(l)) * kLn2T;
         const float lse_r = t.lse[(int64_t)row * t.heads + h];
         const float L = lse_r == -INFINITY ? lse_t : fmaxf(lse_r, lse_t) + log1pf(expf(-fabsf(lse_r - lse_t)));
@@ -353,11 +374,15 @@ gnn_status gt_attn_tiles(const gnn_csr *g, const gnn_blocksparse *bs, const void
     float *lse_ws = cv.take<float>((size_t)g->n_rows * heads);
     float *lse_res = lse ? lse : lse_ws;
     void *csr_ws = static_cast<char *>(ws) + cv.used;
-    // residual edges: fused CSR kernel, writing (out, lse_res)
-    gnn_csr res{g->n_rows, g->n_cols, bs->nnz_residual, bs->res_rowptr, bs->res_colidx, nullptr};
-    gnn_status st = gnn_gt_attn_fwd(&res, nullptr, nullptr, Q, K, V, GNN_BF16, heads, head_dim, scale, out, lse_res,
-                                    csr_ws, ws_bytes - cv.used, s);
-    if (st != GNN_OK) return st;
+    // residual edges: fused CSR kernel, writing (out, lse_res); with no
+    // residual edges (and some tiles) the tile kernel writes every row itself
+    const bool has_residual = bs->nnz_residual > 0 || bs->n_blocks == 0;
+    if (has_residual) {
+        gnn_csr res{g->n_rows, g->n_cols, bs->nnz_residual, bs->res_rowptr, bs->res_colidx, nullptr};
+        gnn_status st = gnn_gt_attn_fwd(&res, nullptr, nullptr, Q, K, V, GNN_BF16, heads, head_dim, scale, out,
+                                        lse_res, csr_ws, ws_bytes - cv.used, s);
+        if (st != GNN_OK) return st;
+    }
     if (bs->n_blocks == 0) return GNN_OK;
     TileArgs t{};
     t.grp_blk_offset = bs->grp_blk_offset;
@@ -372,6 +397,7 @@ gnn_status gt_attn_tiles(const gnn_csr *g, const gnn_blocksparse *bs, const void
     t.heads = heads;
     t.D = head_dim;
     t.qscale = scale * kLog2eT;
+    t.has_residual = has_residual ? 1 : 0;
     t.err = err;
     cudaError_t e = head_dim == 32 ? launch_tiles<32>(t, bs->n_groups, s) : launch_tiles<64>(t, bs->n_groups, s);
     note_launch();

@@ -215,6 +215,24 @@ def test_gt_tiles_ragged_group_and_dense_block(gnn):
         check_gt_tiles(gnn, rp, ci, Q, K, V, 8, 32, 1.0 / math.sqrt(32), thr)
 
 
+@pytest.mark.parametrize("D", [32, 64])
+def test_gt_tiles_empty_groups_and_rows_without_residual(gnn, D):
+    """Every edge in a tile (threshold 0), so the tile kernel writes all rows
+    itself: row groups 1 and 3 (rows 128..255, 384..511) have no edges at
+    all, and single rows inside tiled groups have none either; they must come
+    out as 0 with lse = -inf."""
+    n = 600
+    rng = np.random.default_rng(11)
+    empty = set(range(128, 256)) | set(range(384, 512)) | {5, 70, 300, 599}
+    edges = [(int(rng.integers(n)), d) for d in range(n) if d not in empty for _ in range(6)]
+    rp, ci = G.from_edges(n, edges, self_loops=False)
+    assert all(rp[r + 1] == rp[r] for r in empty)
+    heads = 256 // D
+    Q, K, V = (synth.normal_bf16((n, 256), 1.0, 95 + k) for k in range(3))
+    bs = check_gt_tiles(gnn, rp, ci, Q, K, V, heads, D, 1.0 / math.sqrt(D), 0.0)
+    assert bs.meta.nnz_residual == 0 and bs.meta.n_tiles_kept > 0
+
+
 def test_gt_tiles_config4_sampled(gnn):
     w = synth.workload("c4_clustered_gt")
     rp, ci = w["rowptr"], w["colidx"]
