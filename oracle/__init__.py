@@ -26,7 +26,7 @@ _lock = threading.Lock()
 _lib = None
 
 NORM_NONE, NORM_LEFT, NORM_RIGHT, NORM_BOTH = 0, 1, 2, 3
-OP_SUM, OP_MEAN, OP_MAX = 0, 1, 2
+OP_SUM, OP_MEAN, OP_MAX, OP_MIN = 0, 1, 2, 3
 
 _VP = ctypes.c_void_p
 
@@ -124,16 +124,17 @@ def spmm(rowptr, colidx, X, norm=NORM_BOTH, values=None, rows=None):
 
 
 def segment_reduce(op, rowptr, colidx, X, rows=None):
-    """op: OP_SUM / OP_MEAN / OP_MAX.  Returns Y (and argmax for OP_MAX)."""
+    """op: OP_SUM / OP_MEAN / OP_MAX / OP_MIN.  Returns Y (and the argmax or
+    argmin for OP_MAX / OP_MIN)."""
     rp, ci, n = _csr(rowptr, colidx)
     Xc, dt = _feat(X)
     F = Xc.shape[1]
     r, ns = _rows(rows, n)
     Y = np.empty((ns, F), np.float64)
-    am = np.empty((ns, F), np.int32) if op == OP_MAX else None
+    am = np.empty((ns, F), np.int32) if op in (OP_MAX, OP_MIN) else None
     _check(_load().orc_segment_reduce(op, n, _p(rp), _p(ci), _p(Xc), dt, F, _p(r), ns, _p(Y),
                                       _p(am)), "segment_reduce")
-    return (Y, am) if op == OP_MAX else Y
+    return (Y, am) if op in (OP_MAX, OP_MIN) else Y
 
 
 def gatv2(rowptr, colidx, H, W_l, a, heads, head_dim, slope=0.2, W_r=None, rows=None,

@@ -112,10 +112,14 @@ uint32_t orc_order_key(float v) {
 }
 
 /*
- * op 0 sum, 1 mean (= sum / d_in(i)), 2 max.
+ * op 0 sum, 1 mean (= sum / d_in(i)), 2 max, 3 min.
  * max: the neighbour value with the largest order key; among equal keys the
- * smallest source node id wins; argmax[s,f] = that source node id.  A row
- * with no edges gives 0 (and argmax -1).  Y is [n_sel, F].
+ * smallest source node id wins; argmax[s,f] = that source node id.
+ * min (IO-aware GNN layers, Appendix D.1: the min reduction with its argmin,
+ * values compared through the order-preserving key and ties resolved by the
+ * source index): the neighbour value with the smallest order key, the
+ * smallest source id among equal keys; argmin[s,f] = that id.
+ * A row with no edges gives 0 (and arg -1).  Y is [n_sel, F].
  */
 int orc_segment_reduce(int op, int32_t n_rows, const int32_t *rowptr,
                        const int32_t *colidx, const void *X, int dtype,
@@ -133,9 +137,10 @@ int orc_segment_reduce(int op, int32_t n_rows, const int32_t *rowptr,
             for (int64_t e = b; e < e_end; ++e) {
                 int32_t j = colidx[e];
                 double v = widen(X, dtype, (int64_t)j * F + f);
-                if (op == 2) {
+                if (op == 2 || op == 3) {
                     uint32_t k = orc_order_key((float)v);
-                    if (best_j < 0 || k > best_key || (k == best_key && j < best_j)) {
+                    int better = (op == 2) ? (k > best_key) : (k < best_key);
+                    if (best_j < 0 || better || (k == best_key && j < best_j)) {
                         best_key = k;
                         best_j = j;
                         best_v = v;
@@ -149,7 +154,7 @@ int orc_segment_reduce(int op, int32_t n_rows, const int32_t *rowptr,
             else if (op == 1) out = (e_end > b) ? acc / (double)(e_end - b) : 0.0;
             else out = (best_j >= 0) ? best_v : 0.0;
             Y[(int64_t)s * F + f] = out;
-            if (op == 2 && argmax) argmax[(int64_t)s * F + f] = best_j;
+            if ((op == 2 || op == 3) && argmax) argmax[(int64_t)s * F + f] = best_j;
         }
     }
     return ORC_OK;

@@ -165,6 +165,41 @@ def test_max_orders_negative_zero_below_positive_zero():
     assert am[2, 0] == 0
 
 
+def test_min_argmin_bruteforce_with_ties_and_signed_zero():
+    """min by plain comparison (value, then -0 before +0, then smallest id),
+    written without the order key."""
+    rng = np.random.default_rng(12)
+    for rp, ci in _tiny_graphs():
+        n = len(rp) - 1
+        A = G.dense_adjacency(rp, ci)
+        X = rng.integers(-3, 4, (n, 5)).astype(np.float32)
+        X[rng.random(X.shape) < 0.25] = -0.0
+        y, am = oracle.segment_reduce(oracle.OP_MIN, rp, ci, X)
+        for i in range(n):
+            nb = np.nonzero(A[i])[0]
+            for f in range(5):
+                if len(nb) == 0:
+                    assert y[i, f] == 0 and am[i, f] == -1
+                    continue
+                best = min(nb, key=lambda j: (float(X[j, f]), 0 if math.copysign(1, X[j, f]) < 0 else 1, j))
+                assert am[i, f] == best
+                assert y[i, f] == X[best, f] and math.copysign(1, y[i, f]) == math.copysign(1, X[best, f])
+
+
+def test_min_is_negated_max_of_negation():
+    """min(X) = -max(-X), argmin = argmax of -X: negation reverses the order
+    of every pair of values (-0 and +0 included) and keeps the ids."""
+    rng = np.random.default_rng(13)
+    rp, ci = G.random_graph(60, 0.1, 5)
+    X = rng.integers(-4, 5, (60, 6)).astype(np.float32)
+    X[rng.random(X.shape) < 0.2] = -0.0
+    y, am = oracle.segment_reduce(oracle.OP_MIN, rp, ci, X)
+    y2, am2 = oracle.segment_reduce(oracle.OP_MAX, rp, ci, -X)
+    empty = np.diff(rp) == 0
+    assert np.array_equal(am, am2)
+    assert np.array_equal(np.signbit(y[~empty]), np.signbit(-y2[~empty])) and np.array_equal(y, -y2)
+
+
 # ---------------------------------------------------------------- relabel invariance
 
 @pytest.mark.parametrize("op", ["spmm", "sum", "mean", "max"])
