@@ -208,8 +208,14 @@ def setup_c2(torch, gnn, w):
            "mapping": "auto (degree-aware edge runs)"}
     # ~4 x 8.3M edge-rows of oracle work (all rows): ~10 s on one core
     rows = np.arange(n, dtype=np.int32)
+    # segment min + argmin, the pages' own degree-aware reduction (timed
+    # apart: the configured step is SpMM, sum, mean, max)
+    ymin = torch.empty((n, F), dtype=torch.float32, device="cuda")
+    amin = torch.empty((n, F), dtype=torch.int32, device="cuda")
+    min_only = (lambda: gnn.gnn_segment_reduce_min(g, X, out=ymin, argmin=amin), M * F,
+                idx + xb + yb + n * F * 4)
     return Workload("c2_rmat17", layers, [X], list(outs.values()) + [am], cfg, "f32",
-                    oracle_step, (rows, M))
+                    oracle_step, (rows, M), extra={"min_only": min_only})
 
 
 def setup_c3(torch, gnn, w):
@@ -562,6 +568,22 @@ def main():
         ms_t = per[W.layers[0].name]
         bsx["tile_mma_tflops"] = bsx["tile_mma_flop"] / (ms_t * 1e-3) / 1e12
         extra["blocksparse"] = bsx
+    if "min_only" in W.extra:
+        fn, units_min, b_min = W.extra["min_only"]
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        fn()
+        for k, (e0, e1) in enumerate(evs):
+            flush.fill_(float(k))
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        mms = float(np.mean([e0.elapsed_time(e1) for e0, e1 in evs]))
+        extra["segment_min_argmin"] = {"ms": mms, "gedge_feat_s": units_min / (mms * 1e-3) / 1e9,
+                                       "bcomp_bytes": b_min, "hbm_gbs": b_min / (mms * 1e-3) / 1e9,
+                                       "frac_of_measured": b_min / (mms * 1e-3) / 1e9 / hbm,
+                                       "note": "timed apart, cold (L2 flushed before each call)"}
     if "proj_only" in W.extra:
         fn, b_proj = W.extra["proj_only"]
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))

@@ -122,7 +122,7 @@ gnn_status gnn_last_device_error(void *stream, int32_t *code);
 typedef enum {
     GNN_OP_SPMM = 0, GNN_OP_SUM = 1, GNN_OP_MEAN = 2, GNN_OP_MAX = 3,
     GNN_OP_GATV2 = 4, GNN_OP_GT = 5, GNN_OP_REORDER = 6, GNN_OP_APPLY_PERM = 7,
-    GNN_OP_BLOCKSPARSE = 8
+    GNN_OP_BLOCKSPARSE = 8, GNN_OP_MIN = 9
 } gnn_op;
 
 /* OR-ed into `op` of gnn_workspace_size: size the workspace for bf16 inputs
@@ -202,6 +202,17 @@ gnn_status gnn_segment_reduce_mean(const gnn_csr *g, const void *prep, const voi
  * Inputs must be finite.  Bit-exact. */
 gnn_status gnn_segment_reduce_max(const gnn_csr *g, const void *prep, const void *X,
                                   int32_t x_dtype, int32_t F, float *Y, int32_t *argmax,
+                                  void *ws, size_t ws_bytes, void *stream);
+
+/* Y[i,f] = min over j in N(i) of X[j,f], argmin[i,f] = that j: the min
+ * reduction with argmin of IO-aware GNN layers, Appendix D.1.  Values are
+ * compared through the order-preserving key (so -0 < +0), ties go to the
+ * smallest source id, and cut rows merge a packed (key, index) word, so the
+ * result is exact and deterministic.  Empty rows give 0 and argmin -1.
+ * argmin may be NULL.  Shapes and F as gnn_spmm; workspace
+ * gnn_workspace_size(GNN_OP_MIN, ...). */
+gnn_status gnn_segment_reduce_min(const gnn_csr *g, const void *prep, const void *X,
+                                  int32_t x_dtype, int32_t F, float *Y, int32_t *argmin,
                                   void *ws, size_t ws_bytes, void *stream);
 
 /* -------------------------------------------- step a3: dense projection */

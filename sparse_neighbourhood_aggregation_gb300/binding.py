@@ -21,7 +21,7 @@ GNN_F32, GNN_BF16 = 0, 1
 GNN_NORM_NONE, GNN_NORM_LEFT, GNN_NORM_RIGHT, GNN_NORM_BOTH = 0, 1, 2, 3
 GNN_MAP_AUTO, GNN_MAP_FEAT, GNN_MAP_NEIGH = 0, 1, 2
 (GNN_OP_SPMM, GNN_OP_SUM, GNN_OP_MEAN, GNN_OP_MAX, GNN_OP_GATV2, GNN_OP_GT, GNN_OP_REORDER,
- GNN_OP_APPLY_PERM, GNN_OP_BLOCKSPARSE) = range(9)
+ GNN_OP_APPLY_PERM, GNN_OP_BLOCKSPARSE, GNN_OP_MIN) = range(10)
 GNN_PERM_IDENTITY, GNN_PERM_RANDOM, GNN_PERM_DEGREE, GNN_PERM_RCM = 0, 1, 2, 3
 
 
@@ -62,6 +62,8 @@ _SIGS = {
     "gnn_segment_reduce_sum_noalloc": (ctypes.c_int, ["csr", "p", "p", "i32", "i32", "p", "p"]),
     "gnn_segment_reduce_mean": (ctypes.c_int, ["csr", "p", "p", "i32", "i32", "p", "p", "sz", "p"]),
     "gnn_segment_reduce_max": (ctypes.c_int, ["csr", "p", "p", "i32", "i32", "p", "p", "p", "sz",
+                                              "p"]),
+    "gnn_segment_reduce_min": (ctypes.c_int, ["csr", "p", "p", "i32", "i32", "p", "p", "p", "sz",
                                               "p"]),
     "gnn_projection": (ctypes.c_int, ["p", "i32", "i64", "i32", "p", "i32", "p", "p"]),
     "gnn_gatv2_fwd": (ctypes.c_int, ["csr", "p", "p", "i32", "i32", "p", "p", "p", "i32", "i32",
@@ -223,21 +225,32 @@ def gnn_segment_reduce_mean(g: Graph, X, out=None, stream=None):
     return _reduce("gnn_segment_reduce_mean", GNN_OP_MEAN, g, X, out, stream)
 
 
-def gnn_segment_reduce_max(g: Graph, X, want_argmax: bool = True, out=None, argmax=None,
-                           stream=None):
+def _reduce_ext(name, op, g: Graph, X, want_arg, out, arg, stream):
     _require_cuda(X)
     F = X.shape[1]
     Y = out if out is not None else torch.empty((g.n_rows, F), dtype=torch.float32,
                                                 device=X.device)
     am = None
-    if want_argmax:
-        am = argmax if argmax is not None else torch.empty((g.n_rows, F), dtype=torch.int32,
-                                                           device=X.device)
-    ws = g.workspace(GNN_OP_MAX, F)
-    _check("gnn_segment_reduce_max", lib().gnn_segment_reduce_max(
+    if want_arg:
+        am = arg if arg is not None else torch.empty((g.n_rows, F), dtype=torch.int32,
+                                                     device=X.device)
+    ws = g.workspace(op, F)
+    _check(name, getattr(lib(), name)(
         ctypes.byref(g.csr), _ptr(g.prep), X.data_ptr(), _dtype_code(X), F, Y.data_ptr(),
         _ptr(am), ws.data_ptr(), ws.numel(), _stream(stream)))
     return Y, am
+
+
+def gnn_segment_reduce_max(g: Graph, X, want_argmax: bool = True, out=None, argmax=None,
+                           stream=None):
+    return _reduce_ext("gnn_segment_reduce_max", GNN_OP_MAX, g, X, want_argmax, out, argmax,
+                       stream)
+
+
+def gnn_segment_reduce_min(g: Graph, X, want_argmin: bool = True, out=None, argmin=None,
+                           stream=None):
+    return _reduce_ext("gnn_segment_reduce_min", GNN_OP_MIN, g, X, want_argmin, out, argmin,
+                       stream)
 
 
 def launch_count() -> int:

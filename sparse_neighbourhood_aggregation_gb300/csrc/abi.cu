@@ -24,7 +24,8 @@ extern "C" size_t gnn_workspace_size(int32_t op, const gnn_csr *g, int32_t F, in
         case GNN_OP_SUM:
         case GNN_OP_MEAN:
         case GNN_OP_MAX:
-            return agg_workspace_bytes(g, op, GNN_F32, F);
+        case GNN_OP_MIN:
+            return agg_workspace_bytes(g, op & ~GNN_OP_FLAG_BF16, GNN_F32, F);
         case GNN_OP_GATV2:
             return gatv2_workspace_bytes(g, F, heads, head_dim, esize);
         case GNN_OP_GT:

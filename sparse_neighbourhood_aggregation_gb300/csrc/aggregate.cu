@@ -60,7 +60,12 @@ void prep_span_tables(const gnn_csr *g, const void *prep, const uint32_t **win_f
                       const int32_t **sp_begin, const int4 **items, const int32_t **items_count,
                       const int32_t **win_rowstart);
 
-enum AggOp { AGG_WSUM = 0, AGG_MEAN = 1, AGG_MAX = 2 };
+enum AggOp { AGG_WSUM = 0, AGG_MEAN = 1, AGG_MAX = 2, AGG_MIN = 3 };
+// max and min share one code path: min keeps the complement of the order
+// key, so the largest stored key is the smallest value, and every packed
+// (key << 32) | ~source_id merge by unsigned maximum serves both (ties to
+// the smaller id).
+__host__ __device__ constexpr bool is_ext(int op) { return op == AGG_MAX || op == AGG_MIN; }
 // per-edge weight source / per-row factor source
 enum ColMode { COL_ONE = 0, COL_RSQRT = 1, COL_RECIP = 2 };
 enum RowMode { ROW_ONE = 0, ROW_RSQRT = 1, ROW_RECIP = 2 };
@@ -100,15 +105,15 @@ struct AggArgs {
 template <int OP, class T, int CPL>
 struct Acc {
     static constexpr int NV = Chunk<T>::N;
-    static constexpr bool MX = OP == AGG_MAX;
+    static constexpr bool MX = is_ext(OP);
     float v[MX ? 1 : CPL][MX ? 1 : NV];      // sums
-    uint32_t km[MX ? CPL : 1][MX ? NV : 1];  // max: order_key of the maximum, 0 = nothing seen
-    int32_t idx[MX ? CPL : 1][MX ? NV : 1];  // max: its source id, -1 = nothing seen
+    uint32_t km[MX ? CPL : 1][MX ? NV : 1];  // max: order_key of the maximum (min: its complement), 0 = none
+    int32_t idx[MX ? CPL : 1][MX ? NV : 1];  // its source id, -1 = nothing seen
 
     // every finite value's key is > 0, so a key of 0 means "no edge yet"
     __device__ __forceinline__ uint32_t key(int c, int k) const { return km[c][k]; }
     __device__ __forceinline__ float max_value(int c, int k) const {
-        return km[c][k] ? key_value(km[c][k]) : 0.f;
+        return km[c][k] ? key_value(OP == AGG_MIN ? ~km[c][k] : km[c][k]) : 0.f;
     }
     __device__ __forceinline__ void reset() {
 #pragma unroll
@@ -127,7 +132,7 @@ struct Acc {
             if (MX) {
 #pragma unroll
                 for (int k = 0; k < NV; ++k) {
-                    const uint32_t kk = order_key(f[k]);
+                    const uint32_t kk = OP == AGG_MIN ? ~order_key(f[k]) : order_key(f[k]);
                     // edges arrive in ascending source id: strict > keeps the
                     // smallest id among equal keys
                     if (kk > km[c][k]) { km[c][k] = kk; idx[c][k] = j; }
@@ -182,7 +187,7 @@ __device__ __forceinline__ void store_row(const AggArgs &a, int32_t r, int32_t d
 #pragma unroll
         for (int k = 0; k < NV; k += 4)
             *reinterpret_cast<float4 *>(a.Y + base + k) = make_float4(o[k], o[k + 1], o[k + 2], o[k + 3]);
-        if (OP == AGG_MAX && a.argmax) {
+        if (is_ext(OP) && a.argmax) {
 #pragma unroll
             for (int k = 0; k < NV; k += 4)
                 *reinterpret_cast<int4 *>(a.argmax + base + k) =
@@ -213,7 +218,7 @@ __device__ __forceinline__ void store_row_f(const AggArgs &a, int32_t r, int32_t
 #pragma unroll
         for (int k = 0; k < NV; k += 4)
             *reinterpret_cast<float4 *>(a.Y + base + k) = make_float4(o[k], o[k + 1], o[k + 2], o[k + 3]);
-        if (OP == AGG_MAX && a.argmax) {
+        if (is_ext(OP) && a.argmax) {
 #pragma unroll
             for (int k = 0; k < NV; k += 4)
                 *reinterpret_cast<int4 *>(a.argmax + base + k) =
@@ -243,7 +248,7 @@ __device__ __forceinline__ void flush_partial(const AggArgs &a, int64_t w, int s
         const int64_t off = wa * F + (int64_t)(c * a.lpr + gl) * NV;
 #pragma unroll
         for (int k = 0; k < NV; k += 4) {
-            if (OP == AGG_MAX) {
+            if (is_ext(OP)) {
                 unsigned long long *dst = reinterpret_cast<unsigned long long *>(a.carry) + off + k;
 #pragma unroll
                 for (int z = 0; z < 4; ++z) {
@@ -270,7 +275,7 @@ __device__ __forceinline__ void flush_partial(const AggArgs &a, int64_t w, int s
         const int64_t off = wa * F + (int64_t)(c * a.lpr + gl) * NV;
 #pragma unroll
         for (int k = 0; k < NV; k += 4) {
-            if (OP == AGG_MAX) {
+            if (is_ext(OP)) {
                 unsigned long long *src = reinterpret_cast<unsigned long long *>(a.carry) + off + k;
 #pragma unroll
                 for (int z = 0; z < 4; ++z) {
@@ -574,7 +579,7 @@ __device__ __forceinline__ void write_empty_rows(const AggArgs &a, int32_t q, in
             m &= m - 1;
             float4 *y = reinterpret_cast<float4 *>(a.Y + (size_t)r * a.F);
             for (int32_t c = lane; c < n4; c += 32) y[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (OP == AGG_MAX && a.argmax) {
+            if (is_ext(OP) && a.argmax) {
                 int4 *am = reinterpret_cast<int4 *>(a.argmax + (size_t)r * a.F);
                 for (int32_t c = lane; c < n4; c += 32) am[c] = make_int4(-1, -1, -1, -1);
             }
@@ -591,7 +596,7 @@ __device__ __forceinline__ void store_piece(const AggArgs &a, float *base, int64
                                             const Acc<OP, T, 1> &acc, int lane) {
     constexpr int NV = Chunk<T>::N;
     const int64_t off = slot * a.F + (int64_t)lane * NV;
-    if (OP == AGG_MAX) {
+    if (is_ext(OP)) {
         ulonglong2 *dst = reinterpret_cast<ulonglong2 *>(reinterpret_cast<unsigned long long *>(base) + off);
 #pragma unroll
         for (int k = 0; k < NV; k += 2) {
@@ -610,9 +615,9 @@ __device__ __forceinline__ void store_piece(const AggArgs &a, float *base, int64
 
 // Max: every piece of a heavy row is folded into one slot with 64-bit
 // reductions (the merge is exact and order-free); the warp does not wait.
-template <class T>
+template <int OP, class T>
 __device__ __forceinline__ void fold_max_piece(const AggArgs &a, int64_t slot,
-                                               const Acc<AGG_MAX, T, 1> &acc, int lane) {
+                                               const Acc<OP, T, 1> &acc, int lane) {
     constexpr int NV = Chunk<T>::N;
     unsigned long long *dst = reinterpret_cast<unsigned long long *>(a.carry) + slot * a.F + (int64_t)lane * NV;
 #pragma unroll
@@ -624,12 +629,12 @@ __device__ __forceinline__ void fold_max_piece(const AggArgs &a, int64_t slot,
 template <int OP, class T>
 struct PieceVal {
     static constexpr int NV = Chunk<T>::N;
-    static constexpr int NW = OP == AGG_MAX ? NV / 2 : NV / 4;  // 16-byte words
+    static constexpr int NW = is_ext(OP) ? NV / 2 : NV / 4;  // 16-byte words
     uint4 w[NW];
     __device__ __forceinline__ void load(const AggArgs &a, const float *base, int64_t slot, int lane,
                                          bool bypass_l1) {
         const int64_t off = slot * a.F + (int64_t)lane * NV;
-        const uint4 *src = OP == AGG_MAX
+        const uint4 *src = is_ext(OP)
                                ? reinterpret_cast<const uint4 *>(reinterpret_cast<const unsigned long long *>(base) + off)
                                : reinterpret_cast<const uint4 *>(base + off);
 #pragma unroll
@@ -638,7 +643,7 @@ struct PieceVal {
     // clear the record just read (the workspace is left zero-filled)
     __device__ __forceinline__ static void clear(const AggArgs &a, float *base, int64_t slot, int lane) {
         const int64_t off = slot * a.F + (int64_t)lane * NV;
-        uint4 *dst = OP == AGG_MAX
+        uint4 *dst = is_ext(OP)
                          ? reinterpret_cast<uint4 *>(reinterpret_cast<unsigned long long *>(base) + off)
                          : reinterpret_cast<uint4 *>(base + off);
 #pragma unroll
@@ -648,7 +653,7 @@ struct PieceVal {
     __device__ __forceinline__ void merge_into(Acc<OP, T, 1> &acc) const {
 #pragma unroll
         for (int i = 0; i < NW; ++i) {
-            if (OP == AGG_MAX) {
+            if (is_ext(OP)) {
                 const unsigned long long p0 = ((unsigned long long)w[i].y << 32) | w[i].x;
                 const unsigned long long p1 = ((unsigned long long)w[i].w << 32) | w[i].z;
 #pragma unroll
@@ -672,7 +677,7 @@ struct PieceVal {
 // WT = false: unit edge weights and row factor 1 (segment sum / mean / max);
 // WT = true: the SpMM's per-edge weights and row factors.
 template <int OP, class T, bool WT>
-__global__ void __launch_bounds__(kSpanBlock, ((OP != AGG_MAX && sizeof(T) == 4) ? GNN_SPAN_MINB : GNN_SPAN_MINB - 1) * 256 / kSpanBlock)
+__global__ void __launch_bounds__(kSpanBlock, ((!is_ext(OP) && sizeof(T) == 4) ? GNN_SPAN_MINB : GNN_SPAN_MINB - 1) * 256 / kSpanBlock)
 k_agg_span(AggArgs a) {
     constexpr int U = GNN_SPAN_U;
     const unsigned FULL = 0xffffffffu;
@@ -703,7 +708,7 @@ k_agg_span(AggArgs a) {
     // the tail slot of the span the row starts in)
     bool head = b0 > 0 && !((__ldg(a.win_flags + ((b0 - 1) >> 5)) >> ((b0 - 1) & 31)) & 1u);
     const int64_t max_head_slot =
-        (OP == AGG_MAX && head) ? 2 * (int64_t)(__ldg(a.win_rowstart + (b0 >> 5)) >> a.span_shift) + 1 : 0;
+        (is_ext(OP) && head) ? 2 * (int64_t)(__ldg(a.win_rowstart + (b0 >> 5)) >> a.span_shift) + 1 : 0;
     // lane l holds the id (and row factor) of the row of rank k0 + kofs + l
     int32_t kofs = 0;
     int32_t rid = k0 + lane < a.n_rows ? __ldg(a.ne_rows + k0 + lane) : 0;
@@ -775,8 +780,8 @@ k_agg_span(AggArgs a) {
                 if ((gb >> u) & 1u) {
                     const int32_t e = cb + u0 + u;
                     if (head) {
-                        if constexpr (OP == AGG_MAX) {
-                            fold_max_piece<T>(a, max_head_slot, acc, lane);
+                        if constexpr (is_ext(OP)) {
+                            fold_max_piece<OP, T>(a, max_head_slot, acc, lane);
                         } else {
                             store_piece<OP, T>(a, a.carry, 2 * (int64_t)w, acc, lane);
                         }
@@ -805,8 +810,8 @@ k_agg_span(AggArgs a) {
     }
     // a heavy row reaches past this span: leave its piece
     if (!last_closed) {
-        if constexpr (OP == AGG_MAX) {
-            fold_max_piece<T>(a, head ? max_head_slot : 2 * (int64_t)w + 1, acc, lane);
+        if constexpr (is_ext(OP)) {
+            fold_max_piece<OP, T>(a, head ? max_head_slot : 2 * (int64_t)w + 1, acc, lane);
         } else {
             store_piece<OP, T>(a, a.carry, 2 * (int64_t)w + (head ? 0 : 1), acc, lane);
         }
@@ -854,7 +859,7 @@ __global__ void __launch_bounds__(256, kFixBlocksPerSm) k_agg_span_fix(AggArgs a
         const int32_t p_lo = cidx * kFixChunk, p_hi = min(np, p_lo + kFixChunk);
         Acc<OP, T, 1> acc;
         acc.reset();
-        if constexpr (OP == AGG_MAX) {
+        if constexpr (is_ext(OP)) {
             // all pieces were folded into the first piece's slot
             if (cidx != 0) continue;
             PieceVal<OP, T> pv;
@@ -1046,7 +1051,7 @@ struct AggWs {
 static AggWs agg_ws_layout(const gnn_csr *g, int32_t op, int32_t F, void *base) {
     const int64_t nr = n_workers_for(g, kRunEdges);
     const int64_t ns = std::max<int64_t>(n_spans_of(g->nnz), 1);
-    const size_t wmul = op == GNN_OP_MAX ? 2 : 1;
+    const size_t wmul = (op == GNN_OP_MAX || op == GNN_OP_MIN) ? 2 : 1;
     Carver cv(base);
     AggWs L;
     L.run_tickets = cv.take<int32_t>((size_t)nr);
@@ -1197,6 +1202,8 @@ gnn_status run_aggregate(const gnn_csr *g, const void *prep, int32_t op, int32_t
         cudaError_t e;
         if (op == GNN_OP_MAX) e = bf ? launch_span<AGG_MAX, __nv_bfloat16, false>(a, s)
                                      : launch_span<AGG_MAX, float, false>(a, s);
+        else if (op == GNN_OP_MIN) e = bf ? launch_span<AGG_MIN, __nv_bfloat16, false>(a, s)
+                                          : launch_span<AGG_MIN, float, false>(a, s);
         else if (op == GNN_OP_MEAN) e = bf ? launch_span<AGG_MEAN, __nv_bfloat16, false>(a, s)
                                            : launch_span<AGG_MEAN, float, false>(a, s);
         else if (wt) e = bf ? launch_span<AGG_WSUM, __nv_bfloat16, true>(a, s)
@@ -1211,6 +1218,9 @@ gnn_status run_aggregate(const gnn_csr *g, const void *prep, int32_t op, int32_t
     if (op == GNN_OP_MAX) {
         if (bf) launch_auto<AGG_MAX, __nv_bfloat16>(a, sh.cpl, s);
         else launch_auto<AGG_MAX, float>(a, sh.cpl, s);
+    } else if (op == GNN_OP_MIN) {
+        if (bf) launch_auto<AGG_MIN, __nv_bfloat16>(a, sh.cpl, s);
+        else launch_auto<AGG_MIN, float>(a, sh.cpl, s);
     } else if (op == GNN_OP_MEAN) {
         if (bf) launch_auto<AGG_MEAN, __nv_bfloat16>(a, sh.cpl, s);
         else launch_auto<AGG_MEAN, float>(a, sh.cpl, s);
@@ -1254,6 +1264,13 @@ gnn_status gnn_segment_reduce_max(const gnn_csr *g, const void *prep, const void
                                   int32_t x_dtype, int32_t F, float *Y, int32_t *argmax,
                                   void *ws, size_t ws_bytes, void *stream) {
     return run_aggregate(g, prep, GNN_OP_MAX, GNN_NORM_NONE, X, x_dtype, F, Y, argmax,
+                         GNN_MAP_AUTO, ws, ws_bytes, stream);
+}
+
+gnn_status gnn_segment_reduce_min(const gnn_csr *g, const void *prep, const void *X,
+                                  int32_t x_dtype, int32_t F, float *Y, int32_t *argmin,
+                                  void *ws, size_t ws_bytes, void *stream) {
+    return run_aggregate(g, prep, GNN_OP_MIN, GNN_NORM_NONE, X, x_dtype, F, Y, argmin,
                          GNN_MAP_AUTO, ws, ws_bytes, stream);
 }
 

@@ -34,9 +34,10 @@ def feats_to_dev(X):
 
 
 def check_exact_max(y, am, ref_y, ref_am):
+    """max or min: values bit for bit (signed zeros included), arg exactly"""
     ref32 = ref_y.astype(np.float32)
-    assert np.array_equal(y.view(np.uint32), ref32.view(np.uint32)), "max values differ"
-    assert np.array_equal(am, ref_am), "argmax differs"
+    assert np.array_equal(y.view(np.uint32), ref32.view(np.uint32)), "max/min values differ"
+    assert np.array_equal(am, ref_am), "argmax/argmin differs"
 
 
 def run_all(gnn, rp, ci, X, rows=None, tol=TOL_F32, mappings=(0, 1, 2), norms=(0, 1, 2, 3),
@@ -60,6 +61,9 @@ def run_all(gnn, rp, ci, X, rows=None, tol=TOL_F32, mappings=(0, 1, 2), norms=(0
     yx, am = gnn.gnn_segment_reduce_max(g, Xd)
     ry, ram = oracle.segment_reduce(oracle.OP_MAX, rp, ci, X, rows=rows)
     check_exact_max(yx.cpu().numpy()[sel], am.cpu().numpy()[sel], ry, ram)
+    yn, an = gnn.gnn_segment_reduce_min(g, Xd)
+    rn, ran = oracle.segment_reduce(oracle.OP_MIN, rp, ci, X, rows=rows)
+    check_exact_max(yn.cpu().numpy()[sel], an.cpu().numpy()[sel], rn, ran)
     return g
 
 
@@ -91,6 +95,18 @@ def test_ties_and_signed_zero_max_exact(gnn):
     yx, am = gnn.gnn_segment_reduce_max(g, dev(X))
     ry, ram = oracle.segment_reduce(oracle.OP_MAX, rp, ci, X)
     check_exact_max(yx.cpu().numpy(), am.cpu().numpy(), ry, ram)
+
+
+def test_min_ties_and_signed_zero_exact(gnn):
+    rng = np.random.default_rng(4)
+    for F in (32, 128):  # k_agg_auto and the edge-span kernel
+        rp, ci = _hub_graph(600, hubs=(5, 300), deg=550)
+        X = rng.integers(-3, 4, (600, F)).astype(np.float32)
+        X[rng.random(X.shape) < 0.2] = -0.0
+        g = gnn.graph_prepare(dev(rp), dev(ci))
+        yn, an = gnn.gnn_segment_reduce_min(g, dev(X))
+        rn, ran = oracle.segment_reduce(oracle.OP_MIN, rp, ci, X)
+        check_exact_max(yn.cpu().numpy(), an.cpu().numpy(), rn, ran)
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
@@ -162,6 +178,9 @@ def test_unprepared_graph(gnn):
     yx, am = gnn.gnn_segment_reduce_max(g, Xd)
     ry, ram = oracle.segment_reduce(oracle.OP_MAX, rp, ci, X)
     check_exact_max(yx.cpu().numpy(), am.cpu().numpy(), ry, ram)
+    yn, an = gnn.gnn_segment_reduce_min(g, Xd)
+    rn, ran = oracle.segment_reduce(oracle.OP_MIN, rp, ci, X)
+    check_exact_max(yn.cpu().numpy(), an.cpu().numpy(), rn, ran)
 
 
 def test_config1_er(gnn):
