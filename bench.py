@@ -14,6 +14,8 @@ kernel launched through the C ABI (include/gnn.h) by the Python binding:
   c4_clustered_gt: clustered graph 1024 x 256 nodes (p = 0.3, 1% rewired),
       Q, K, V bf16 [N, 8x32]; Graph Transformer attention, CSR path.
   c5_rmat22: R-MAT scale 22, X bf16 [N,256]; GCN SpMM.
+  c4_clustered_spmm: GCN SpMM on the c4 graph, X bf16 [N,256]; CSR edge
+    spans, or with --tiles the tensor-core SpMM over block-sparse tiles.
 
 Prints ONE JSON line (rank 0).  Metric: aggregation Gedge*feat/s = edges x
 features aggregated per second, summed over the step's layers (attention:
@@ -300,6 +302,57 @@ def setup_c4(torch, gnn, w, tiles=None):
                     rows, extra=extra)
 
 
+def setup_c4_spmm(torch, gnn, w, tiles=None):
+    """GCN SpMM (norm BOTH) on the clustered graph of the GT workload with X
+    bf16 [N, 256] N(0,1): the CSR edge-span kernel, or with tiles the
+    tensor-core SpMM over the block-sparse layout plus the residual CSR."""
+    g = gnn.graph_prepare(_dev(torch, w["rowptr"]), _dev(torch, w["colidx"]))
+    n = len(w["rowptr"]) - 1
+    M = len(w["colidx"])
+    F = 256
+    Xh = synth_mod().normal_bf16((n, F), 1.0, 44)
+    X = _dev(torch, Xh)
+    Y = torch.empty((n, F), dtype=torch.float32, device="cuda")
+    idx = 4 * (n + 1) + 4 * M
+    bcomp = idx + n * F * 2 + n * F * 4 + 8 * n
+    extra = {}
+    bs = None
+    if tiles is not None:
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        bs = gnn.gnn_blocksparse_build(g, tiles)
+        torch.cuda.synchronize()
+        m = bs.meta
+        extra["blocksparse"] = {"threshold": tiles, "build_ms": (time.perf_counter() - t0) * 1e3,
+                                "listed_blocks": m.n_blocks, "kept_tiles": m.n_tiles_kept,
+                                "tile_edges": m.nnz_tiles, "residual_edges": m.nnz_residual,
+                                # O += P X over every listed block's 16 columns
+                                "tile_mma_flop": 2.0 * 128 * 16 * F * m.n_blocks}
+        layers = [Layer("spmm_tiles", lambda ins: gnn.gnn_spmm_blocksparse(
+            g, ins[0], bs, norm=gnn.GNN_NORM_BOTH, out=Y), M * F, bcomp, "tensor")]
+    else:
+        layers = [Layer("spmm", lambda ins: gnn.gnn_spmm(g, ins[0], norm=gnn.GNN_NORM_BOTH,
+                                                         out=Y), M * F, bcomp)]
+
+    def oracle_step(rows):
+        import oracle
+        oracle.spmm(w["rowptr"], w["colidx"], Xh, norm=oracle.NORM_BOTH, rows=rows)
+
+    cfg = {"workload": "c4_clustered_spmm", "graph": "the GT workload's clustered graph: 1024 "
+           "clusters x 256 nodes, p=0.3, 1% of sources rewired, dedup + self-loops",
+           "nodes": n, "edges": M, "features": F, "x_dtype": "bf16",
+           "layers": ["gcn_spmm, CSR edge spans" if bs is None else
+                      f"gcn_spmm: tcgen05 16x16 tiles (fill >= {tiles}) + CSR residual"]}
+    rows = _sample_by_edges(w["rowptr"], 2000000)
+    return Workload("c4_clustered_spmm", layers, [X], [Y], cfg, "bf16", oracle_step, rows,
+                    extra=extra)
+
+
+def synth_mod():
+    import synth
+    return synth
+
+
 def setup_c5(torch, gnn, w, mapping="auto", ordering="original"):
     rp, ci = _dev(torch, w["rowptr"]), _dev(torch, w["colidx"])
     X = _dev(torch, w["X"])
@@ -341,6 +394,7 @@ def setup_c5(torch, gnn, w, mapping="auto", ordering="original"):
 
 
 SETUPS = {"c2_rmat17": setup_c2, "c3_rmat20_gatv2": setup_c3, "c4_clustered_gt": setup_c4,
+          "c4_clustered_spmm": setup_c4_spmm,
           "c5_rmat22": setup_c5}
 
 
@@ -358,7 +412,8 @@ def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    w = synth.workload(args.workload)
+    w = synth.workload("c4_clustered_gt", features=False) if args.workload == "c4_clustered_spmm" \
+        else synth.workload(args.workload)
     wl_meta = REF_META[args.workload](w)
     rows, ne, per_edge, fn = wl_meta
     for _ in range(args.warmup):
@@ -426,8 +481,20 @@ def _ref_c5(w):
     return rows, ne, w["X"].shape[1], fn
 
 
+def _ref_c4_spmm(w):
+    import oracle
+    import synth
+    rp, ci = w["rowptr"], w["colidx"]
+    X = synth.normal_bf16((len(rp) - 1, 256), 1.0, 44)
+    rows, ne = _sample_by_edges(rp, 400000)
+
+    def fn(r):
+        oracle.spmm(rp, ci, X, norm=oracle.NORM_BOTH, rows=r)
+    return rows, ne, 256, fn
+
+
 REF_META = {"c2_rmat17": _ref_c2, "c3_rmat20_gatv2": _ref_c3, "c4_clustered_gt": _ref_c4,
-            "c5_rmat22": _ref_c5}
+            "c5_rmat22": _ref_c5, "c4_clustered_spmm": _ref_c4_spmm}
 
 
 def time_layers(torch, W, steps, flush, stream):
@@ -516,11 +583,16 @@ def main():
         dist.init_process_group("nccl")
     gnn.lib()
 
-    w = synth.workload(args.workload)
+    if args.workload == "c4_clustered_spmm":
+        w = synth.workload("c4_clustered_gt", features=False)
+    else:
+        w = synth.workload(args.workload)
     if args.workload == "c5_rmat22":
         W = setup_c5(torch, gnn, w, args.mapping, args.ordering)
     elif args.workload == "c4_clustered_gt":
         W = setup_c4(torch, gnn, w, args.tiles)
+    elif args.workload == "c4_clustered_spmm":
+        W = setup_c4_spmm(torch, gnn, w, args.tiles)
     else:
         W = SETUPS[args.workload](torch, gnn, w)
     stream = torch.cuda.current_stream()
@@ -622,6 +694,9 @@ def main():
     if dom.bound == "alu":
         roofline["note"] = ("kernel is FP32-ALU heavy; frac is its compulsory-byte rate "
                             "against the HBM peak")
+    elif dom.bound == "tensor":
+        roofline["note"] = ("tensor-core tiles; frac is the compulsory-byte rate against the "
+                            "HBM peak, the tile MMA rate is in extra.blocksparse")
 
     e2e = None
     if not args.no_e2e:

@@ -122,7 +122,7 @@ gnn_status gnn_last_device_error(void *stream, int32_t *code);
 typedef enum {
     GNN_OP_SPMM = 0, GNN_OP_SUM = 1, GNN_OP_MEAN = 2, GNN_OP_MAX = 3,
     GNN_OP_GATV2 = 4, GNN_OP_GT = 5, GNN_OP_REORDER = 6, GNN_OP_APPLY_PERM = 7,
-    GNN_OP_BLOCKSPARSE = 8, GNN_OP_MIN = 9
+    GNN_OP_BLOCKSPARSE = 8, GNN_OP_MIN = 9, GNN_OP_SPMM_BLOCKSPARSE = 10
 } gnn_op;
 
 /* OR-ed into `op` of gnn_workspace_size: size the workspace for bf16 inputs
@@ -287,6 +287,20 @@ gnn_status gnn_blocksparse_build(const gnn_csr *g, gnn_blocksparse *bs, void *ou
                                  size_t out_bytes, void *ws, size_t ws_bytes, void *stream);
 
 /* ---------------------------- steps a5 + a7: Graph Transformer attention */
+
+/* GCN SpMM (as gnn_spmm, mapping aside) over a block-sparse layout from
+ * gnn_blocksparse_build: the kept 16x16 tiles on the tensor cores
+ * (tcgen05, bf16 operands, fp32 accumulation in TMEM), the residual edges on
+ * the CSR SpMM, the two results added (IO-aware GNN layers, Section 3.3 and
+ * Appendix D.3, the weighted block-sparse SpMM).  Each normalisation is a
+ * row factor times a column factor from the whole graph's degrees; inside a
+ * tile the column factor is rounded to bf16.  X bf16 [n_cols, F] with F a
+ * multiple of 64; Y fp32 [n_rows, F]; graphs with edge values are not
+ * supported (GNN_ERR_UNSUPPORTED).  prep required unless norm is NONE.
+ * Workspace gnn_workspace_size(GNN_OP_SPMM_BLOCKSPARSE, g, F, 0, 0). */
+gnn_status gnn_spmm_blocksparse(const gnn_csr *g, const void *prep, const gnn_blocksparse *bs,
+                                int32_t norm, const void *X, int32_t x_dtype, int32_t F, float *Y,
+                                void *ws, size_t ws_bytes, void *stream);
 
 /* Graph Transformer attention (IO-aware GNN layers, Section 2.2 (iii);
  * Appendix D.2 fused CSR forward; Appendix D.3 tensor-core attention):

@@ -21,7 +21,7 @@ GNN_F32, GNN_BF16 = 0, 1
 GNN_NORM_NONE, GNN_NORM_LEFT, GNN_NORM_RIGHT, GNN_NORM_BOTH = 0, 1, 2, 3
 GNN_MAP_AUTO, GNN_MAP_FEAT, GNN_MAP_NEIGH = 0, 1, 2
 (GNN_OP_SPMM, GNN_OP_SUM, GNN_OP_MEAN, GNN_OP_MAX, GNN_OP_GATV2, GNN_OP_GT, GNN_OP_REORDER,
- GNN_OP_APPLY_PERM, GNN_OP_BLOCKSPARSE, GNN_OP_MIN) = range(10)
+ GNN_OP_APPLY_PERM, GNN_OP_BLOCKSPARSE, GNN_OP_MIN, GNN_OP_SPMM_BLOCKSPARSE) = range(11)
 GNN_PERM_IDENTITY, GNN_PERM_RANDOM, GNN_PERM_DEGREE, GNN_PERM_RCM = 0, 1, 2, 3
 
 
@@ -72,6 +72,8 @@ _SIGS = {
     "gnn_blocksparse_build": (ctypes.c_int, ["csr", "bs", "p", "sz", "p", "sz", "p"]),
     "gnn_gt_attn_fwd": (ctypes.c_int, ["csr", "p", "bs", "p", "p", "p", "i32", "i32", "i32", "f32",
                                        "p", "p", "p", "sz", "p"]),
+    "gnn_spmm_blocksparse": (ctypes.c_int, ["csr", "p", "bs", "i32", "p", "i32", "i32", "p", "p",
+                                            "sz", "p"]),
     "gnn_reorder_perm": (ctypes.c_int, ["csr", "i32", "u64", "p", "p", "p", "sz", "p"]),
     "gnn_apply_perm": (ctypes.c_int, ["csr", "p", "p", "p", "p", "p", "i32", "i32", "p", "p", "sz",
                                       "p"]),
@@ -325,6 +327,21 @@ def gnn_gt_attn_fwd(g: Graph, Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor,
         _dtype_code(Q), heads, head_dim, float(scale), o.data_ptr(), _ptr(L), ws.data_ptr(),
         ws.numel(), _stream(stream)))
     return o, L
+
+
+def gnn_spmm_blocksparse(g: Graph, X: torch.Tensor, bs, norm: int = GNN_NORM_BOTH, out=None,
+                         stream=None):
+    """GCN SpMM over a BlockSparse from gnn_blocksparse_build: kept tiles on
+    the tensor cores, residual edges on the CSR kernel.  X bf16 [n_cols, F],
+    F a multiple of 64; returns Y fp32 [n_rows, F]."""
+    _require_cuda(X)
+    F = X.shape[1]
+    Y = out if out is not None else torch.empty((g.n_rows, F), dtype=torch.float32, device=X.device)
+    ws = g.workspace(GNN_OP_SPMM_BLOCKSPARSE, F, key=("bs", int(bs.meta.nnz_residual)))
+    _check("gnn_spmm_blocksparse", lib().gnn_spmm_blocksparse(
+        ctypes.byref(g.csr), _ptr(g.prep), ctypes.byref(bs.meta), int(norm), X.data_ptr(),
+        _dtype_code(X), F, Y.data_ptr(), ws.data_ptr(), ws.numel(), _stream(stream)))
+    return Y
 
 
 def gnn_reorder_perm(g: Graph, kind: int, seed: int = 7, stream=None):

@@ -10,6 +10,7 @@ size_t gt_tiles_workspace_bytes(const gnn_csr *g, int32_t heads, int32_t head_di
 size_t reorder_workspace_bytes(const gnn_csr *g);
 size_t apply_perm_workspace_bytes(const gnn_csr *g);
 size_t blocksparse_workspace_bytes(const gnn_csr *g);
+size_t tile_spmm_workspace_bytes(const gnn_csr *g, int32_t F);
 gnn_status check_csr_args(const gnn_csr *g);
 }  // namespace gnn
 
@@ -36,6 +37,8 @@ extern "C" size_t gnn_workspace_size(int32_t op, const gnn_csr *g, int32_t F, in
             return apply_perm_workspace_bytes(g);
         case GNN_OP_BLOCKSPARSE:
             return blocksparse_workspace_bytes(g);
+        case GNN_OP_SPMM_BLOCKSPARSE:
+            return tile_spmm_workspace_bytes(g, F);
         default:
             return 0;
     }
