@@ -52,6 +52,7 @@ def _load():
                                      i32, _VP, i32, _VP]
             lib.orc_segment_reduce.argtypes = [ctypes.c_int, i32, _VP, _VP, _VP, ctypes.c_int,
                                                i32, _VP, i32, _VP, _VP]
+            lib.orc_reduce_ext_backward.argtypes = [i32, i32, i32, _VP, _VP, _VP]
             lib.orc_gatv2.argtypes = [i32, _VP, _VP, _VP, ctypes.c_int, i32, _VP, _VP, _VP,
                                       i32, i32, dbl, _VP, i32, _VP, _VP, _VP]
             lib.orc_gt.argtypes = [i32, _VP, _VP, _VP, _VP, _VP, ctypes.c_int, i32, i32, dbl,
@@ -135,6 +136,18 @@ def segment_reduce(op, rowptr, colidx, X, rows=None):
     _check(_load().orc_segment_reduce(op, n, _p(rp), _p(ci), _p(Xc), dt, F, _p(r), ns, _p(Y),
                                       _p(am)), "segment_reduce")
     return (Y, am) if op in (OP_MAX, OP_MIN) else Y
+
+
+def reduce_ext_backward(arg, grad_out, n_cols):
+    """Gradient of the max / min reduction w.r.t. X from the stored arg
+    (argmax or argmin) and the output gradient: grad_X [n_cols, F], fp64."""
+    arg = np.ascontiguousarray(arg, np.int32)
+    go = np.ascontiguousarray(grad_out, np.float64)
+    n_rows, F = arg.shape
+    gx = np.empty((n_cols, F), np.float64)
+    _check(_load().orc_reduce_ext_backward(n_rows, n_cols, F, _p(arg), _p(go), _p(gx)),
+           "reduce_ext_backward")
+    return gx
 
 
 def gatv2(rowptr, colidx, H, W_l, a, heads, head_dim, slope=0.2, W_r=None, rows=None,

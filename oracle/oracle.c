@@ -160,6 +160,27 @@ int orc_segment_reduce(int op, int32_t n_rows, const int32_t *rowptr,
     return ORC_OK;
 }
 
+/*
+ * Backward of the max / min reduction (IO-aware GNN layers, Appendix D.1,
+ * the backward pass as a sparse scatter through the stored argmin): the
+ * gradient of out[v,f] flows only to the selected source, so
+ *   grad_X[j,f] = sum over v with arg[v,f] == j of grad_out[v,f]
+ * (arg -1, an empty row, contributes nothing).  arg and grad_out are
+ * [n_rows, F]; grad_X is [n_cols, F], fp64, overwritten.
+ */
+int orc_reduce_ext_backward(int32_t n_rows, int32_t n_cols, int32_t F, const int32_t *arg,
+                            const double *grad_out, double *grad_X) {
+    for (int64_t k = 0; k < (int64_t)n_cols * F; ++k) grad_X[k] = 0.0;
+    for (int32_t v = 0; v < n_rows; ++v)
+        for (int32_t f = 0; f < F; ++f) {
+            int32_t j = arg[(int64_t)v * F + f];
+            if (j < 0) continue;
+            if (j >= n_cols) return ORC_ERR;
+            grad_X[(int64_t)j * F + f] += grad_out[(int64_t)v * F + f];
+        }
+    return ORC_OK;
+}
+
 /* ------------------------------------------------------------------ */
 /* attention (IO-aware GNN layers, Section 2.2 (iii); Appendix D.2)    */
 /* ------------------------------------------------------------------ */
