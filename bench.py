@@ -216,8 +216,13 @@ def setup_c2(torch, gnn, w):
     amin = torch.empty((n, F), dtype=torch.int32, device="cuda")
     min_only = (lambda: gnn.gnn_segment_reduce_min(g, X, out=ymin, argmin=amin), M * F,
                 idx + xb + yb + n * F * 4)
+    # backward of max through its argmax (grad_out, argmax read; grad_X written)
+    gout = torch.randn((n, F), dtype=torch.float32, device="cuda")
+    gx = torch.empty((n, F), dtype=torch.float32, device="cuda")
+    bwd_only = (lambda: gnn.gnn_segment_reduce_ext_backward(am, gout, n, out=gx), n * F,
+                3 * n * F * 4)
     return Workload("c2_rmat17", layers, [X], list(outs.values()) + [am], cfg, "f32",
-                    oracle_step, (rows, M), extra={"min_only": min_only})
+                    oracle_step, (rows, M), extra={"min_only": min_only, "bwd_only": bwd_only})
 
 
 def setup_c3(torch, gnn, w):
@@ -656,6 +661,22 @@ def main():
                                        "bcomp_bytes": b_min, "hbm_gbs": b_min / (mms * 1e-3) / 1e9,
                                        "frac_of_measured": b_min / (mms * 1e-3) / 1e9 / hbm,
                                        "note": "timed apart, cold (L2 flushed before each call)"}
+    if "bwd_only" in W.extra:
+        fn, units_b, b_b = W.extra["bwd_only"]
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        fn()
+        for k, (e0, e1) in enumerate(evs):
+            flush.fill_(float(k))
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        bms = float(np.mean([e0.elapsed_time(e1) for e0, e1 in evs]))
+        extra["max_backward"] = {"ms": bms, "bcomp_bytes": b_b, "hbm_gbs": b_b / (bms * 1e-3) / 1e9,
+                                 "frac_of_measured": b_b / (bms * 1e-3) / 1e9 / hbm,
+                                 "note": "argmax scatter of grad_out into grad_X (zero-fill "
+                                         "included), timed apart, cold"}
     if "proj_only" in W.extra:
         fn, b_proj = W.extra["proj_only"]
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))

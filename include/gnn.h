@@ -215,6 +215,19 @@ gnn_status gnn_segment_reduce_min(const gnn_csr *g, const void *prep, const void
                                   int32_t x_dtype, int32_t F, float *Y, int32_t *argmin,
                                   void *ws, size_t ws_bytes, void *stream);
 
+/* Backward of gnn_segment_reduce_max / _min (IO-aware GNN layers, Appendix
+ * D.1: the gradient flows only along the stored argmin / argmax, a sparse
+ * scatter-add): grad_X[arg[v,f], f] += grad_out[v,f] for every v, f with
+ * arg[v,f] >= 0.  arg int32 and grad_out fp32 are [n_rows, F]; grad_X fp32
+ * [n_cols, F] is overwritten (zero-filled first).  F % 4 == 0 (else
+ * GNN_ERR_UNSUPPORTED), every pointer 16-byte aligned.  fp32 atomic adds:
+ * sums of several gradients into one entry round in arrival order.  An arg
+ * >= n_cols sets the device error word (GNN_ERR_DEVICE_CHECK) and is
+ * skipped.  No workspace.  Asynchronous. */
+gnn_status gnn_segment_reduce_ext_backward(const int32_t *arg, int32_t n_rows, int32_t F,
+                                           const float *grad_out, int32_t n_cols, float *grad_X,
+                                           void *stream);
+
 /* -------------------------------------------- step a3: dense projection */
 
 /* C = H W  (IO-aware GNN layers, Section 2.2 (i), the dense GEMM of

@@ -65,6 +65,7 @@ _SIGS = {
                                               "p"]),
     "gnn_segment_reduce_min": (ctypes.c_int, ["csr", "p", "p", "i32", "i32", "p", "p", "p", "sz",
                                               "p"]),
+    "gnn_segment_reduce_ext_backward": (ctypes.c_int, ["p", "i32", "i32", "p", "i32", "p", "p"]),
     "gnn_projection": (ctypes.c_int, ["p", "i32", "i64", "i32", "p", "i32", "p", "p"]),
     "gnn_gatv2_fwd": (ctypes.c_int, ["csr", "p", "p", "i32", "i32", "p", "p", "p", "i32", "i32",
                                      "f32", "p", "p", "p", "sz", "p"]),
@@ -177,6 +178,13 @@ def csr_validate(g: Graph, stream=None) -> int:
     _check("gnn_csr_validate", L.gnn_csr_validate(ctypes.byref(g.csr), _stream(stream)))
     code = ctypes.c_int32(0)
     _check("gnn_last_device_error", L.gnn_last_device_error(_stream(stream), ctypes.byref(code)))
+    return code.value
+
+
+def last_device_error(stream=None) -> int:
+    """Waits for the stream, returns and clears the device error word."""
+    code = ctypes.c_int32(0)
+    _check("gnn_last_device_error", lib().gnn_last_device_error(_stream(stream), ctypes.byref(code)))
     return code.value
 
 
@@ -327,6 +335,19 @@ def gnn_gt_attn_fwd(g: Graph, Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor,
         _dtype_code(Q), heads, head_dim, float(scale), o.data_ptr(), _ptr(L), ws.data_ptr(),
         ws.numel(), _stream(stream)))
     return o, L
+
+
+def gnn_segment_reduce_ext_backward(arg: torch.Tensor, grad_out: torch.Tensor, n_cols: int,
+                                    out=None, stream=None):
+    """Gradient w.r.t. X of gnn_segment_reduce_max / _min from their arg
+    output and the output gradient: grad_X fp32 [n_cols, F]."""
+    _require_cuda(arg, grad_out)
+    n_rows, F = arg.shape
+    gx = out if out is not None else torch.empty((n_cols, F), dtype=torch.float32,
+                                                 device=arg.device)
+    _check("gnn_segment_reduce_ext_backward", lib().gnn_segment_reduce_ext_backward(
+        arg.data_ptr(), n_rows, F, grad_out.data_ptr(), n_cols, gx.data_ptr(), _stream(stream)))
+    return gx
 
 
 def gnn_spmm_blocksparse(g: Graph, X: torch.Tensor, bs, norm: int = GNN_NORM_BOTH, out=None,

@@ -1012,6 +1012,30 @@ __global__ void __launch_bounds__(256) k_agg_neigh(AggArgs a) {
     }
 }
 
+// Backward of max / min (IO-aware GNN layers, Appendix D.1, the sparse
+// scatter through the stored argmin): grad_X[arg[v,f], f] += grad_out[v,f].
+// One thread per 4 consecutive (v, f) entries (F % 4 == 0): coalesced
+// 16-byte reads of arg and grad_out, fp32 atomic adds the thread does not
+// wait for.  An arg outside [-1, n_cols) sets the device error word and is
+// skipped.
+__global__ void k_ext_backward(const int4 *__restrict__ arg, const float4 *__restrict__ go, int64_t n4,
+                               int32_t F, int32_t n_cols, float *__restrict__ gx, int32_t *err) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride) {
+        const int4 a = __ldg(arg + i);
+        const float4 g = __ldg(go + i);
+        const int32_t f = (int32_t)((i * 4) % F);
+        const int32_t js[4] = {a.x, a.y, a.z, a.w};
+        const float gs[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            if (js[k] < 0) continue;
+            if (js[k] >= n_cols) { set_device_error(err, GNN_ERR_DEVICE_CHECK); continue; }
+            atomicAdd(gx + (int64_t)js[k] * F + f + k, gs[k]);
+        }
+    }
+}
+
 // ------------------------------------------------------------- host side
 
 struct AggShape {
@@ -1265,6 +1289,30 @@ gnn_status gnn_segment_reduce_max(const gnn_csr *g, const void *prep, const void
                                   void *ws, size_t ws_bytes, void *stream) {
     return run_aggregate(g, prep, GNN_OP_MAX, GNN_NORM_NONE, X, x_dtype, F, Y, argmax,
                          GNN_MAP_AUTO, ws, ws_bytes, stream);
+}
+
+gnn_status gnn_segment_reduce_ext_backward(const int32_t *arg, int32_t n_rows, int32_t F,
+                                           const float *grad_out, int32_t n_cols, float *grad_X,
+                                           void *stream) {
+    if (n_rows < 0 || n_cols < 0 || F <= 0 || F % 4) return F > 0 && F % 4 ? GNN_ERR_UNSUPPORTED : GNN_ERR_INVALID_ARG;
+    const int64_t n = (int64_t)n_rows * F;
+    if ((n > 0 && (!arg || !grad_out)) || (n_cols > 0 && !grad_X)) return GNN_ERR_INVALID_ARG;
+    if (!aligned16(arg) || !aligned16(grad_out) || !aligned16(grad_X)) return GNN_ERR_INVALID_ARG;
+    int32_t *err = device_error_word();
+    if (!err) return GNN_ERR_CUDA;
+    cudaStream_t s = as_stream(stream);
+    if (n_cols > 0) {
+        const cudaError_t e = cudaMemsetAsync(grad_X, 0, sizeof(float) * (size_t)n_cols * F, s);
+        if (e != cudaSuccess) return cuda_status(e);
+    }
+    if (n == 0) return GNN_OK;
+    const int64_t n4 = n / 4;
+    const int blocks = (int)std::min<int64_t>((n4 + 255) / 256, (int64_t)sm_count() * 16);
+    k_ext_backward<<<blocks, 256, 0, s>>>(reinterpret_cast<const int4 *>(arg), reinterpret_cast<const float4 *>(grad_out),
+                                          n4, F, n_cols, grad_X, err);
+    note_launch();
+    GNN_LAUNCH_CHECK();
+    return GNN_OK;
 }
 
 gnn_status gnn_segment_reduce_min(const gnn_csr *g, const void *prep, const void *X,

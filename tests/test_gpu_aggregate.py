@@ -183,6 +183,33 @@ def test_unprepared_graph(gnn):
     check_exact_max(yn.cpu().numpy(), an.cpu().numpy(), rn, ran)
 
 
+@pytest.mark.parametrize("op", ["max", "min"])
+def test_reduce_backward_config2(gnn, op):
+    """grad_X of max / min from the oracle's own arg (every row of R-MAT
+    scale 17, F = 128) and a random output gradient."""
+    w = synth.workload("c2_rmat17")
+    rp, ci, X = w["rowptr"], w["colidx"], w["X"]
+    code = oracle.OP_MAX if op == "max" else oracle.OP_MIN
+    _, arg = oracle.segment_reduce(code, rp, ci, X)
+    go = synth.normal_f32(arg.shape, 1.0, 51)
+    n = len(rp) - 1
+    gx = gnn.gnn_segment_reduce_ext_backward(dev(arg), dev(go), n).cpu().numpy()
+    assert_rowwise_close(gx, oracle.reduce_ext_backward(arg, go.astype(np.float64), n), TOL_F32,
+                         f"{op} backward")
+
+
+def test_reduce_backward_shared_sources_and_bad_index(gnn):
+    arg = np.array([[2, -1, 2, 0], [2, 0, -1, 0], [-1, 0, 1, 1]], np.int32)
+    go = np.arange(12, dtype=np.float32).reshape(3, 4) + 1
+    gx = gnn.gnn_segment_reduce_ext_backward(dev(arg), dev(go), 3).cpu().numpy()
+    assert np.array_equal(gx, oracle.reduce_ext_backward(arg, go.astype(np.float64), 3))
+    # an index past n_cols is caught by the kernel's bounds check and reported
+    gnn.gnn_segment_reduce_ext_backward(dev(np.array([[0, 0, 0, 9]], np.int32)),
+                                        dev(np.ones((1, 4), np.float32)), 3)
+    assert gnn.last_device_error() == gnn.GNN_ERR_DEVICE_CHECK
+    assert gnn.last_device_error() == 0
+
+
 def test_config1_er(gnn):
     w = synth.workload("c1_er1k")
     run_all(gnn, w["rowptr"], w["colidx"], w["X"])
