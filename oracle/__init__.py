@@ -53,6 +53,7 @@ def _load():
             lib.orc_segment_reduce.argtypes = [ctypes.c_int, i32, _VP, _VP, _VP, ctypes.c_int,
                                                i32, _VP, i32, _VP, _VP]
             lib.orc_reduce_ext_backward.argtypes = [i32, i32, i32, _VP, _VP, _VP]
+            lib.orc_csr_transpose.argtypes = [i32, i32, _VP, _VP, _VP, _VP, _VP, _VP]
             lib.orc_gatv2.argtypes = [i32, _VP, _VP, _VP, ctypes.c_int, i32, _VP, _VP, _VP,
                                       i32, i32, dbl, _VP, i32, _VP, _VP, _VP]
             lib.orc_gt.argtypes = [i32, _VP, _VP, _VP, _VP, _VP, ctypes.c_int, i32, i32, dbl,
@@ -136,6 +137,20 @@ def segment_reduce(op, rowptr, colidx, X, rows=None):
     _check(_load().orc_segment_reduce(op, n, _p(rp), _p(ci), _p(Xc), dt, F, _p(r), ns, _p(Y),
                                       _p(am)), "segment_reduce")
     return (Y, am) if op in (OP_MAX, OP_MIN) else Y
+
+
+def csr_transpose(rowptr, colidx, n_cols=None, values=None):
+    """CSR^T: (rowptr_t [n_cols+1], colidx_t [nnz], values_t or None)."""
+    rp, ci, n = _csr(rowptr, colidx)
+    nc = n if n_cols is None else int(n_cols)
+    m = len(ci)
+    rpt = np.empty(nc + 1, np.int32)
+    cit = np.empty(max(m, 1), np.int32)
+    vals = None if values is None else np.ascontiguousarray(values, np.float32)
+    vt = None if values is None else np.empty(max(m, 1), np.float32)
+    _check(_load().orc_csr_transpose(n, nc, _p(rp), _p(ci), _p(vals), _p(rpt), _p(cit), _p(vt)),
+           "csr_transpose")
+    return rpt, cit[:m], (None if vt is None else vt[:m])
 
 
 def reduce_ext_backward(arg, grad_out, n_cols):

@@ -161,6 +161,35 @@ int orc_segment_reduce(int op, int32_t n_rows, const int32_t *rowptr,
 }
 
 /*
+ * CSR^T (the transpose the backward kernels of IO-aware GNN layers,
+ * Appendix D.2, run over): row j of the result lists every i with j in
+ * N(i), in ascending i, with that edge's value.  rowptr_t [n_cols + 1],
+ * colidx_t and values_t (may be NULL) [nnz].
+ */
+int orc_csr_transpose(int32_t n_rows, int32_t n_cols, const int32_t *rowptr, const int32_t *colidx,
+                      const float *values, int32_t *rowptr_t, int32_t *colidx_t, float *values_t) {
+    for (int32_t j = 0; j <= n_cols; ++j) rowptr_t[j] = 0;
+    for (int32_t i = 0; i < n_rows; ++i)
+        for (int64_t e = rowptr[i]; e < rowptr[i + 1]; ++e) {
+            if (colidx[e] < 0 || colidx[e] >= n_cols) return ORC_ERR;
+            rowptr_t[colidx[e] + 1] += 1;
+        }
+    for (int32_t j = 0; j < n_cols; ++j) rowptr_t[j + 1] += rowptr_t[j];
+    /* fill row by row in ascending i: each transposed row comes out sorted */
+    int32_t *next = (int32_t *)malloc(sizeof(int32_t) * (size_t)(n_cols > 0 ? n_cols : 1));
+    if (!next) return ORC_ERR;
+    for (int32_t j = 0; j < n_cols; ++j) next[j] = rowptr_t[j];
+    for (int32_t i = 0; i < n_rows; ++i)
+        for (int64_t e = rowptr[i]; e < rowptr[i + 1]; ++e) {
+            int32_t k = next[colidx[e]]++;
+            colidx_t[k] = i;
+            if (values_t) values_t[k] = values ? values[e] : 1.0f;
+        }
+    free(next);
+    return ORC_OK;
+}
+
+/*
  * Backward of the max / min reduction (IO-aware GNN layers, Appendix D.1,
  * the backward pass as a sparse scatter through the stored argmin): the
  * gradient of out[v,f] flows only to the selected source, so

@@ -233,6 +233,46 @@ def test_reduce_backward_empty_rows_and_shared_sources():
     assert np.array_equal(gx, [[0.0, 7.0], [0.0, 0.0], [3.0, 0.0]])
 
 
+def test_csr_transpose_is_the_transposed_adjacency_and_an_involution():
+    for rp, ci in _tiny_graphs():
+        n = len(rp) - 1
+        rpt, cit, _ = oracle.csr_transpose(rp, ci)
+        assert np.array_equal(G.dense_adjacency(rpt, cit), G.dense_adjacency(rp, ci).T)
+        rp2, ci2, _ = oracle.csr_transpose(rpt, cit)
+        assert np.array_equal(rp2, rp) and np.array_equal(ci2, ci)
+    # rectangular, with values following their edges
+    rp = np.array([0, 2, 3], np.int32)
+    ci = np.array([1, 4, 0], np.int32)
+    vals = np.array([0.5, 2.0, 3.0], np.float32)
+    rpt, cit, vt = oracle.csr_transpose(rp, ci, n_cols=5, values=vals)
+    assert np.array_equal(rpt, [0, 1, 2, 2, 2, 3]) and np.array_equal(cit, [1, 0, 0])
+    assert np.array_equal(vt, [3.0, 0.5, 2.0])
+
+
+@pytest.mark.parametrize("norm,spmm_norm", [(oracle.NORM_BOTH, oracle.NORM_BOTH),
+                                            (oracle.NORM_NONE, oracle.NORM_NONE),
+                                            (oracle.NORM_LEFT, oracle.NORM_RIGHT)])
+def test_spmm_backward_is_spmm_on_the_transpose(norm, spmm_norm):
+    """d/dX of sum(G * spmm(A, X)) = (normalised A)^T G, built densely, equals
+    the SpMM on CSR^T: GCN with BOTH, sum with NONE, mean (LEFT) with RIGHT."""
+    rng = np.random.default_rng(41)
+    rp, ci = G.random_graph(30, 0.15, 8)
+    n = 30
+    A = G.dense_adjacency(rp, ci).astype(np.float64)
+    din, dout = A.sum(1), A.sum(0)
+    with np.errstate(divide="ignore"):
+        if norm == oracle.NORM_BOTH:
+            An = A * np.where(din > 0, din ** -0.5, 0)[:, None] * np.where(dout > 0, dout ** -0.5, 0)[None, :]
+        elif norm == oracle.NORM_LEFT:
+            An = A * np.where(din > 0, 1.0 / din, 0)[:, None]
+        else:
+            An = A
+    Gy = rng.standard_normal((n, 4))
+    rpt, cit, _ = oracle.csr_transpose(rp, ci)
+    got = oracle.spmm(rpt, cit, Gy.astype(np.float32), norm=spmm_norm)
+    assert np.allclose(got, An.T @ Gy.astype(np.float32).astype(np.float64), rtol=1e-12, atol=1e-12)
+
+
 # ---------------------------------------------------------------- relabel invariance
 
 @pytest.mark.parametrize("op", ["spmm", "sum", "mean", "max"])
