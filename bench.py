@@ -222,7 +222,8 @@ def setup_c2(torch, gnn, w):
     bwd_only = (lambda: gnn.gnn_segment_reduce_ext_backward(am, gout, n, out=gx), n * F,
                 3 * n * F * 4)
     return Workload("c2_rmat17", layers, [X], list(outs.values()) + [am], cfg, "f32",
-                    oracle_step, (rows, M), extra={"min_only": min_only, "bwd_only": bwd_only})
+                    oracle_step, (rows, M), extra={"min_only": min_only, "bwd_only": bwd_only,
+                                                  "transpose_only": lambda: gnn.gnn_csr_transpose(g)})
 
 
 def setup_c3(torch, gnn, w):
@@ -677,6 +678,20 @@ def main():
                                  "frac_of_measured": b_b / (bms * 1e-3) / 1e9 / hbm,
                                  "note": "argmax scatter of grad_out into grad_X (zero-fill "
                                          "included), timed apart, cold"}
+    if "transpose_only" in W.extra:
+        fn = W.extra["transpose_only"]
+        fn()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for k, (e0, e1) in enumerate(evs):
+            flush.fill_(float(k))
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        extra["csr_transpose"] = {"ms": float(np.mean([e0.elapsed_time(e1) for e0, e1 in evs])),
+                                  "note": "CSR^T build (count, stable radix sort, scan), timed "
+                                          "apart, cold; the SpMM backward is a SpMM on it"}
     if "proj_only" in W.extra:
         fn, b_proj = W.extra["proj_only"]
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))

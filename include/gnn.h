@@ -122,7 +122,7 @@ gnn_status gnn_last_device_error(void *stream, int32_t *code);
 typedef enum {
     GNN_OP_SPMM = 0, GNN_OP_SUM = 1, GNN_OP_MEAN = 2, GNN_OP_MAX = 3,
     GNN_OP_GATV2 = 4, GNN_OP_GT = 5, GNN_OP_REORDER = 6, GNN_OP_APPLY_PERM = 7,
-    GNN_OP_BLOCKSPARSE = 8, GNN_OP_MIN = 9, GNN_OP_SPMM_BLOCKSPARSE = 10
+    GNN_OP_BLOCKSPARSE = 8, GNN_OP_MIN = 9, GNN_OP_SPMM_BLOCKSPARSE = 10, GNN_OP_TRANSPOSE = 11
 } gnn_op;
 
 /* OR-ed into `op` of gnn_workspace_size: size the workspace for bf16 inputs
@@ -356,6 +356,18 @@ gnn_status gnn_apply_perm(const gnn_csr *g, const int32_t *perm, const int32_t *
                           int32_t *rowptr_out, int32_t *colidx_out, const void *X,
                           int32_t x_dtype, int32_t F, void *X_out, void *ws, size_t ws_bytes,
                           void *stream);
+
+/* CSR^T (the CSR-transpose build the backward passes need): the graph with
+ * every edge j -> i turned into i -> j, as a CSR by (former) source
+ * (IO-aware GNN layers, Appendix D.2, backward kernels over CSR^T).
+ * rowptr_t [n_cols + 1], colidx_t [nnz]: row j of the result lists the i
+ * with j in N(i), ascending; values_t [nnz] (may be NULL; requires
+ * g->values) carries each edge's value.  The backward of gnn_spmm is a
+ * gnn_spmm on the result: GCN (BOTH) as is (the transposed graph's prepared
+ * degrees swap roles), plain sum with NONE, mean with RIGHT.  Workspace
+ * gnn_workspace_size(GNN_OP_TRANSPOSE, g, 0, 0, 0).  Asynchronous. */
+gnn_status gnn_csr_transpose(const gnn_csr *g, int32_t *rowptr_t, int32_t *colidx_t, float *values_t,
+                             void *ws, size_t ws_bytes, void *stream);
 
 /* ------------------------------------------------------------ utilities */
 

@@ -21,7 +21,8 @@ GNN_F32, GNN_BF16 = 0, 1
 GNN_NORM_NONE, GNN_NORM_LEFT, GNN_NORM_RIGHT, GNN_NORM_BOTH = 0, 1, 2, 3
 GNN_MAP_AUTO, GNN_MAP_FEAT, GNN_MAP_NEIGH = 0, 1, 2
 (GNN_OP_SPMM, GNN_OP_SUM, GNN_OP_MEAN, GNN_OP_MAX, GNN_OP_GATV2, GNN_OP_GT, GNN_OP_REORDER,
- GNN_OP_APPLY_PERM, GNN_OP_BLOCKSPARSE, GNN_OP_MIN, GNN_OP_SPMM_BLOCKSPARSE) = range(11)
+ GNN_OP_APPLY_PERM, GNN_OP_BLOCKSPARSE, GNN_OP_MIN, GNN_OP_SPMM_BLOCKSPARSE,
+ GNN_OP_TRANSPOSE) = range(12)
 GNN_PERM_IDENTITY, GNN_PERM_RANDOM, GNN_PERM_DEGREE, GNN_PERM_RCM = 0, 1, 2, 3
 
 
@@ -66,6 +67,7 @@ _SIGS = {
     "gnn_segment_reduce_min": (ctypes.c_int, ["csr", "p", "p", "i32", "i32", "p", "p", "p", "sz",
                                               "p"]),
     "gnn_segment_reduce_ext_backward": (ctypes.c_int, ["p", "i32", "i32", "p", "i32", "p", "p"]),
+    "gnn_csr_transpose": (ctypes.c_int, ["csr", "p", "p", "p", "p", "sz", "p"]),
     "gnn_projection": (ctypes.c_int, ["p", "i32", "i64", "i32", "p", "i32", "p", "p"]),
     "gnn_gatv2_fwd": (ctypes.c_int, ["csr", "p", "p", "i32", "i32", "p", "p", "p", "i32", "i32",
                                      "f32", "p", "p", "p", "sz", "p"]),
@@ -348,6 +350,22 @@ def gnn_segment_reduce_ext_backward(arg: torch.Tensor, grad_out: torch.Tensor, n
     _check("gnn_segment_reduce_ext_backward", lib().gnn_segment_reduce_ext_backward(
         arg.data_ptr(), n_rows, F, grad_out.data_ptr(), n_cols, gx.data_ptr(), _stream(stream)))
     return gx
+
+
+def gnn_csr_transpose(g: Graph, stream=None):
+    """CSR^T of g: returns (rowptr_t [n_cols+1], colidx_t [nnz], values_t or
+    None) int32 / fp32 tensors; prepare the result with graph_prepare to run
+    the backward of gnn_spmm as a gnn_spmm on it."""
+    rp = torch.empty(g.csr.n_cols + 1, dtype=torch.int32, device=g.device)
+    ci = torch.empty(max(g.csr.nnz, 1), dtype=torch.int32, device=g.device)[:g.csr.nnz]
+    vals = None
+    if g.csr.values:
+        vals = torch.empty(max(g.csr.nnz, 1), dtype=torch.float32, device=g.device)[:g.csr.nnz]
+    ws = g.workspace(GNN_OP_TRANSPOSE)
+    _check("gnn_csr_transpose", lib().gnn_csr_transpose(
+        ctypes.byref(g.csr), rp.data_ptr(), ci.data_ptr() if g.csr.nnz else None, _ptr(vals),
+        ws.data_ptr(), ws.numel(), _stream(stream)))
+    return rp, ci, vals
 
 
 def gnn_spmm_blocksparse(g: Graph, X: torch.Tensor, bs, norm: int = GNN_NORM_BOTH, out=None,

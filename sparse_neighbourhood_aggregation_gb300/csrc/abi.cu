@@ -11,6 +11,7 @@ size_t reorder_workspace_bytes(const gnn_csr *g);
 size_t apply_perm_workspace_bytes(const gnn_csr *g);
 size_t blocksparse_workspace_bytes(const gnn_csr *g);
 size_t tile_spmm_workspace_bytes(const gnn_csr *g, int32_t F);
+size_t transpose_workspace_bytes(const gnn_csr *g);
 gnn_status check_csr_args(const gnn_csr *g);
 }  // namespace gnn
 
@@ -39,6 +40,8 @@ extern "C" size_t gnn_workspace_size(int32_t op, const gnn_csr *g, int32_t F, in
             return blocksparse_workspace_bytes(g);
         case GNN_OP_SPMM_BLOCKSPARSE:
             return tile_spmm_workspace_bytes(g, F);
+        case GNN_OP_TRANSPOSE:
+            return transpose_workspace_bytes(g);
         default:
             return 0;
     }

@@ -562,8 +562,66 @@ gnn_status rcm_order(const gnn_csr *g, ReorderWs &W, int32_t *perm, cudaStream_t
     return GNN_OK;
 }
 
+// CSR^T: per-column counts, the row id of every edge, and a stable sort of
+// (column, edge) pairs; the sorted edge ids give the transposed column ids
+// (source rows, ascending within a column) and carry the edge values.
+struct TransposeWs {
+    int32_t *cnt, *rowid, *keys_out, *eid[2];
+    void *temp;
+    size_t temp_bytes, bytes;
+};
+
+TransposeWs transpose_layout(const gnn_csr *g, void *base) {
+    Carver c(base);
+    TransposeWs W;
+    const int64_t m = std::max<int64_t>(g->nnz, 1);
+    W.cnt = c.take<int32_t>((size_t)g->n_cols + 1);
+    W.rowid = c.take<int32_t>((size_t)m);
+    W.keys_out = c.take<int32_t>((size_t)m);
+    W.eid[0] = c.take<int32_t>((size_t)m);
+    W.eid[1] = c.take<int32_t>((size_t)m);
+    size_t t = 0, x = 0;
+    cub::DeviceRadixSort::SortPairs(nullptr, x, (const int32_t *)nullptr, (int32_t *)nullptr,
+                                    (const int32_t *)nullptr, (int32_t *)nullptr, m);
+    t = std::max(t, x);
+    cub::DeviceScan::ExclusiveSum(nullptr, x, (const int32_t *)nullptr, (int32_t *)nullptr, g->n_cols + 1);
+    t = std::max(t, x);
+    W.temp_bytes = t;
+    W.temp = c.take<uint8_t>(t);
+    W.bytes = c.used;
+    return W;
+}
+
+// per-column edge counts; a column id outside [0, n_cols) sets the error word
+__global__ void k_count_cols_checked(const int32_t *__restrict__ colidx, int64_t nnz, int32_t n_cols,
+                                     int32_t *__restrict__ cnt, int32_t *err) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < nnz; e += stride) {
+        const int32_t j = colidx[e];
+        if ((uint32_t)j >= (uint32_t)n_cols) { set_device_error(err, GNN_ERR_DEVICE_CHECK); continue; }
+        atomicAdd(&cnt[j], 1);
+    }
+}
+
+__global__ void k_iota_i64(int32_t *__restrict__ v, int64_t n) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) v[i] = (int32_t)i;
+}
+
+__global__ void k_transpose_fill(const int32_t *__restrict__ eid, const int32_t *__restrict__ rowid,
+                                 const float *__restrict__ vals, int64_t m, int32_t *__restrict__ colidx_t,
+                                 float *__restrict__ vals_t) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < m; k += stride) {
+        const int32_t e = eid[k];
+        colidx_t[k] = rowid[e];
+        if (vals_t) vals_t[k] = vals[e];
+    }
+}
+
 }  // namespace
 
+size_t transpose_workspace_bytes(const gnn_csr *g) { return transpose_layout(g, nullptr).bytes; }
 size_t reorder_workspace_bytes(const gnn_csr *g) { return reorder_layout(g, nullptr).bytes; }
 size_t apply_perm_workspace_bytes(const gnn_csr *g) { return perm_layout(g, nullptr).bytes; }
 
@@ -666,6 +724,40 @@ gnn_status gnn_apply_perm(const gnn_csr *g, const int32_t *perm, const int32_t *
                                                                    static_cast<uint4 *>(X_out));
         note_launch();
     }
+    GNN_LAUNCH_CHECK();
+    return GNN_OK;
+}
+
+gnn_status gnn_csr_transpose(const gnn_csr *g, int32_t *rowptr_t, int32_t *colidx_t, float *values_t, void *ws,
+                             size_t ws_bytes, void *stream) {
+    gnn_status st = check_csr_args(g);
+    if (st != GNN_OK) return st;
+    if (!rowptr_t || (g->nnz > 0 && !colidx_t)) return GNN_ERR_INVALID_ARG;
+    if (values_t && !g->values) return GNN_ERR_INVALID_ARG;
+    TransposeWs W = transpose_layout(g, ws);
+    if (!ws || ws_bytes < W.bytes) return GNN_ERR_WORKSPACE;
+    if (!aligned256(ws)) return GNN_ERR_INVALID_ARG;
+    cudaStream_t s = as_stream(stream);
+    const int64_t m = g->nnz;
+    const int32_t nc = g->n_cols;
+    size_t tb = W.temp_bytes;
+    GNN_CUDA_TRY(cudaMemsetAsync(W.cnt, 0, sizeof(int32_t) * ((size_t)nc + 1), s));
+    if (m > 0) {
+        int32_t *err = device_error_word();
+        if (!err) return GNN_ERR_CUDA;
+        k_count_cols_checked<<<std::min(blocks_for(m), sm_count() * 8), 256, 0, s>>>(g->colidx, m, nc, W.cnt, err);
+        k_edge_rows<<<blocks_for((int64_t)g->n_rows * 32), 256, 0, s>>>(g->rowptr, g->n_rows, W.rowid);
+        k_iota_i64<<<std::min(blocks_for(m), sm_count() * 8), 256, 0, s>>>(W.eid[0], m);
+        note_launch(3);
+        GNN_CUDA_TRY(cub::DeviceRadixSort::SortPairs(W.temp, tb, g->colidx, W.keys_out, W.eid[0], W.eid[1], m, 0,
+                                                     bits_for(nc), s));
+        note_launch();
+        k_transpose_fill<<<std::min(blocks_for(m), sm_count() * 8), 256, 0, s>>>(W.eid[1], W.rowid, g->values, m,
+                                                                                 colidx_t, values_t);
+        note_launch();
+    }
+    GNN_CUDA_TRY(cub::DeviceScan::ExclusiveSum(W.temp, tb, W.cnt, rowptr_t, nc + 1, s));
+    note_launch();
     GNN_LAUNCH_CHECK();
     return GNN_OK;
 }
