@@ -54,6 +54,8 @@ def _load():
                                                i32, _VP, i32, _VP, _VP]
             lib.orc_reduce_ext_backward.argtypes = [i32, i32, i32, _VP, _VP, _VP]
             lib.orc_csr_transpose.argtypes = [i32, i32, _VP, _VP, _VP, _VP, _VP, _VP]
+            lib.orc_gt_backward.argtypes = [i32, _VP, _VP, _VP, _VP, _VP, ctypes.c_int, i32, i32, dbl,
+                                            _VP, _VP, _VP, _VP]
             lib.orc_gatv2.argtypes = [i32, _VP, _VP, _VP, ctypes.c_int, i32, _VP, _VP, _VP,
                                       i32, i32, dbl, _VP, i32, _VP, _VP, _VP]
             lib.orc_gt.argtypes = [i32, _VP, _VP, _VP, _VP, _VP, ctypes.c_int, i32, i32, dbl,
@@ -208,6 +210,20 @@ def gt(rowptr, colidx, Q, K, V, heads, head_dim, scale, rows=None, want_alpha=Fa
     _check(_load().orc_gt(n, _p(rp), _p(ci), _p(Qc), _p(Kc), _p(Vc), dt, heads, head_dim,
                           scale, _p(r), ns, _p(out), _p(lse), _p(alpha)), "gt")
     return (out, lse, alpha) if want_alpha else (out, lse)
+
+
+def gt_backward(rowptr, colidx, Q, K, V, heads, head_dim, scale, dO):
+    """Gradients (dQ, dK, dV) fp64 [n, heads*head_dim] of sum(dO * gt(...)[0])."""
+    rp, ci, n = _csr(rowptr, colidx)
+    Qc, dt = _feat(Q)
+    Kc, _ = _feat(K)
+    Vc, _ = _feat(V)
+    go = np.ascontiguousarray(dO, np.float64)
+    HD = heads * head_dim
+    dQ, dK, dV = (np.empty((n, HD), np.float64) for _ in range(3))
+    _check(_load().orc_gt_backward(n, _p(rp), _p(ci), _p(Qc), _p(Kc), _p(Vc), dt, heads, head_dim,
+                                   scale, _p(go), _p(dQ), _p(dK), _p(dV)), "gt_backward")
+    return dQ, dK, dV
 
 
 def blocksparse(rowptr, colidx, threshold):

@@ -350,6 +350,65 @@ int orc_gt(int32_t n_rows, const int32_t *rowptr, const int32_t *colidx,
     return ORC_OK;
 }
 
+/*
+ * Backward of the Graph Transformer attention (IO-aware GNN layers,
+ * Appendix D.2, the GT backward: Delta = <O, dO> per destination and head,
+ * then the score gradient from the recomputed weights).  For row i, head h,
+ * with s_ij = scale <q_i, k_j> over j in N(i), alpha = softmax_j(s), O_i =
+ * sum_j alpha_ij v_j and Delta_i = <O_i, dO_i>:
+ *   ds_ij  = alpha_ij (<dO_i, v_j> - Delta_i)
+ *   dQ_i  += scale ds_ij k_j,  dK_j += scale ds_ij q_i,  dV_j += alpha_ij dO_i.
+ * Q, K, V [n, heads*D] (dtype as orc_gt); dO, dQ, dK, dV fp64 [n, heads*D];
+ * the graph is square.  dQ, dK, dV are overwritten.
+ */
+int orc_gt_backward(int32_t n, const int32_t *rowptr, const int32_t *colidx, const void *Q,
+                    const void *K, const void *V, int dtype, int32_t heads, int32_t D, double scale,
+                    const double *dO, double *dQ, double *dK, double *dV) {
+    int32_t HD = heads * D;
+    for (int64_t k = 0; k < (int64_t)n * HD; ++k) dQ[k] = dK[k] = dV[k] = 0.0;
+    int64_t max_deg = 0;
+    for (int32_t i = 0; i < n; ++i)
+        if (rowptr[i + 1] - rowptr[i] > max_deg) max_deg = rowptr[i + 1] - rowptr[i];
+    double *e = malloc(sizeof(double) * (size_t)(max_deg > 0 ? max_deg : 1));
+    double *al = malloc(sizeof(double) * (size_t)(max_deg > 0 ? max_deg : 1));
+    double *o = malloc(sizeof(double) * (size_t)(D > 0 ? D : 1));
+    if (!e || !al || !o) { free(e); free(al); free(o); return ORC_ERR; }
+    for (int32_t i = 0; i < n; ++i) {
+        int64_t b = rowptr[i], deg = rowptr[i + 1] - b;
+        if (deg == 0) continue;
+        for (int32_t h = 0; h < heads; ++h) {
+            int64_t qo = (int64_t)i * HD + h * D;
+            for (int64_t k = 0; k < deg; ++k) {
+                int64_t ko = (int64_t)colidx[b + k] * HD + h * D;
+                double acc = 0.0;
+                for (int32_t d = 0; d < D; ++d) acc += widen(Q, dtype, qo + d) * widen(K, dtype, ko + d);
+                e[k] = scale * acc;
+            }
+            softmax_row(e, deg, al);
+            double delta = 0.0;
+            for (int32_t d = 0; d < D; ++d) {
+                o[d] = 0.0;
+                for (int64_t k = 0; k < deg; ++k)
+                    o[d] += al[k] * widen(V, dtype, (int64_t)colidx[b + k] * HD + h * D + d);
+                delta += o[d] * dO[qo + d];
+            }
+            for (int64_t k = 0; k < deg; ++k) {
+                int64_t ko = (int64_t)colidx[b + k] * HD + h * D;
+                double da = 0.0;
+                for (int32_t d = 0; d < D; ++d) da += dO[qo + d] * widen(V, dtype, ko + d);
+                double ds = al[k] * (da - delta);
+                for (int32_t d = 0; d < D; ++d) {
+                    dQ[qo + d] += scale * ds * widen(K, dtype, ko + d);
+                    dK[ko + d] += scale * ds * widen(Q, dtype, qo + d);
+                    dV[ko + d] += al[k] * dO[qo + d];
+                }
+            }
+        }
+    }
+    free(e); free(al); free(o);
+    return ORC_OK;
+}
+
 /* ------------------------------------------------------------------ */
 /* block-sparse tiles (IO-aware GNN layers, Appendix D.3, WSB format)  */
 /* ------------------------------------------------------------------ */

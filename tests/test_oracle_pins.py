@@ -273,6 +273,37 @@ def test_spmm_backward_is_spmm_on_the_transpose(norm, spmm_norm):
     assert np.allclose(got, An.T @ Gy.astype(np.float32).astype(np.float64), rtol=1e-12, atol=1e-12)
 
 
+def test_gt_backward_matches_finite_differences():
+    """dQ, dK, dV of sum(dO * GT(Q, K, V)) by central differences of the
+    forward oracle on a small graph (2 heads x 4)."""
+    rng = np.random.default_rng(51)
+    rp, ci = G.random_graph(9, 0.4, 9)
+    n, heads, D, scale = 9, 2, 4, 0.7
+    # fp32 inputs (the oracle's input type) and a step they represent exactly
+    Q, K, V = (rng.standard_normal((n, heads * D)).astype(np.float32) for _ in range(3))
+    dO = rng.standard_normal((n, heads * D))
+    dQ, dK, dV = oracle.gt_backward(rp, ci, Q, K, V, heads, D, scale, dO)
+
+    def loss(Qx, Kx, Vx):
+        out, _ = oracle.gt(rp, ci, Qx, Kx, Vx, heads, D, scale)
+        return float(np.sum(dO * out))
+
+    eps = 2.0 ** -10
+    for got, which in ((dQ, 0), (dK, 1), (dV, 2)):
+        num = np.zeros_like(got)
+        for idx in np.ndindex(*got.shape):
+            args_p = [Q.copy(), K.copy(), V.copy()]
+            args_m = [Q.copy(), K.copy(), V.copy()]
+            args_p[which][idx] += eps
+            args_m[which][idx] -= eps
+            num[idx] = (loss(*args_p) - loss(*args_m)) / (2 * eps)
+        assert np.allclose(got, num, rtol=1e-4, atol=1e-6), ("dQ", "dK", "dV")[which]
+    # every row's weights sum to 1, so dV summed over the sources is dO summed
+    # over the rows with edges
+    has = np.diff(rp) > 0
+    assert np.allclose(dV.sum(0), dO[has].sum(0), rtol=1e-12, atol=1e-12)
+
+
 # ---------------------------------------------------------------- relabel invariance
 
 @pytest.mark.parametrize("op", ["spmm", "sum", "mean", "max"])
