@@ -288,6 +288,16 @@ def setup_c4(torch, gnn, w, tiles=None):
                                 "tile_edges": m.nnz_tiles, "residual_edges": m.nnz_residual,
                                 # S = Q K^T and O = P V over every listed block's 16 columns
                                 "tile_mma_flop": 4.0 * 128 * D * 16 * m.n_blocks * heads}
+    if bs is None:
+        # backward of the CSR-path attention (transpose built once here)
+        rpt, cit, _ = gnn.gnn_csr_transpose(g)
+        gtr = gnn.Graph(rpt, cit, None, None, False)
+        dout = torch.randn((n, HD), dtype=torch.float32, device="cuda")
+        bwd_bytes = 3 * n * HD * 2 + 2 * n * HD * 4 + 3 * n * HD * 4 + 2 * (idx + 4 * M)
+        extra["timed"] = {"gt_backward": (
+            lambda: gnn.gnn_gt_attn_bwd(g, gtr, Q, K, V, heads, D, w["scale"], out, lse, dout),
+            bwd_bytes, "dQ over CSR, dK and dV over CSR^T (Delta fused into the dQ pass), from "
+                       "the forward's out and lse; timed apart, cold")}
     name = "gt_tiles" if bs is not None else "gt_csr"
     layers = [Layer(name, lambda ins: gnn.gnn_gt_attn_fwd(g, ins[0], ins[1], ins[2], heads, D,
                                                           w["scale"], bs=bs, out=out, lse=lse),
@@ -678,6 +688,19 @@ def main():
                                  "frac_of_measured": b_b / (bms * 1e-3) / 1e9 / hbm,
                                  "note": "argmax scatter of grad_out into grad_X (zero-fill "
                                          "included), timed apart, cold"}
+    for tname, (fn, tbytes, tnote) in W.extra.get("timed", {}).items():
+        fn()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for k, (e0, e1) in enumerate(evs):
+            flush.fill_(float(k))
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        tms = float(np.mean([e0.elapsed_time(e1) for e0, e1 in evs]))
+        extra[tname] = {"ms": tms, "bytes": tbytes, "hbm_gbs": tbytes / (tms * 1e-3) / 1e9,
+                        "frac_of_measured": tbytes / (tms * 1e-3) / 1e9 / hbm, "note": tnote}
     if "transpose_only" in W.extra:
         fn = W.extra["transpose_only"]
         fn()

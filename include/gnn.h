@@ -122,7 +122,8 @@ gnn_status gnn_last_device_error(void *stream, int32_t *code);
 typedef enum {
     GNN_OP_SPMM = 0, GNN_OP_SUM = 1, GNN_OP_MEAN = 2, GNN_OP_MAX = 3,
     GNN_OP_GATV2 = 4, GNN_OP_GT = 5, GNN_OP_REORDER = 6, GNN_OP_APPLY_PERM = 7,
-    GNN_OP_BLOCKSPARSE = 8, GNN_OP_MIN = 9, GNN_OP_SPMM_BLOCKSPARSE = 10, GNN_OP_TRANSPOSE = 11
+    GNN_OP_BLOCKSPARSE = 8, GNN_OP_MIN = 9, GNN_OP_SPMM_BLOCKSPARSE = 10, GNN_OP_TRANSPOSE = 11,
+    GNN_OP_GT_BACKWARD = 12
 } gnn_op;
 
 /* OR-ed into `op` of gnn_workspace_size: size the workspace for bf16 inputs
@@ -329,6 +330,22 @@ gnn_status gnn_gt_attn_fwd(const gnn_csr *g, const void *prep, const gnn_blocksp
                            const void *Q, const void *K, const void *V, int32_t dtype,
                            int32_t heads, int32_t head_dim, float scale, float *out,
                            float *lse, void *ws, size_t ws_bytes, void *stream);
+
+/* Backward of gnn_gt_attn_fwd on the CSR path (IO-aware GNN layers,
+ * Appendix D.2: Delta = <O, dO> per destination and head, then the weights
+ * recomputed from the stored logsumexp, dQ over the CSR and dK, dV over
+ * CSR^T, each gradient row owned by one warp: no atomics, deterministic).
+ * g square; gt its transpose from gnn_csr_transpose (rows = sources).
+ * Q, K, V bf16 [n, heads*head_dim] as in the forward; out, lse (natural
+ * log) from the forward; dout fp32 [n, heads*head_dim]; dQ, dK, dV fp32
+ * [n, heads*head_dim], overwritten.  heads*head_dim in {128, 256} and
+ * head_dim a power-of-two multiple of heads*head_dim/32 (else
+ * GNN_ERR_UNSUPPORTED).  Workspace gnn_workspace_size(GNN_OP_GT_BACKWARD,
+ * g, 0, heads, head_dim).  Asynchronous. */
+gnn_status gnn_gt_attn_bwd(const gnn_csr *g, const gnn_csr *gt, const void *Q, const void *K,
+                           const void *V, int32_t dtype, int32_t heads, int32_t head_dim, float scale,
+                           const float *out, const float *lse, const float *dout, float *dQ, float *dK,
+                           float *dV, void *ws, size_t ws_bytes, void *stream);
 
 /* --------------------------------------------------- step a8: reordering */
 

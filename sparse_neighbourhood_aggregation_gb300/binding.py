@@ -22,7 +22,7 @@ GNN_NORM_NONE, GNN_NORM_LEFT, GNN_NORM_RIGHT, GNN_NORM_BOTH = 0, 1, 2, 3
 GNN_MAP_AUTO, GNN_MAP_FEAT, GNN_MAP_NEIGH = 0, 1, 2
 (GNN_OP_SPMM, GNN_OP_SUM, GNN_OP_MEAN, GNN_OP_MAX, GNN_OP_GATV2, GNN_OP_GT, GNN_OP_REORDER,
  GNN_OP_APPLY_PERM, GNN_OP_BLOCKSPARSE, GNN_OP_MIN, GNN_OP_SPMM_BLOCKSPARSE,
- GNN_OP_TRANSPOSE) = range(12)
+ GNN_OP_TRANSPOSE, GNN_OP_GT_BACKWARD) = range(13)
 GNN_PERM_IDENTITY, GNN_PERM_RANDOM, GNN_PERM_DEGREE, GNN_PERM_RCM = 0, 1, 2, 3
 
 
@@ -68,6 +68,8 @@ _SIGS = {
                                               "p"]),
     "gnn_segment_reduce_ext_backward": (ctypes.c_int, ["p", "i32", "i32", "p", "i32", "p", "p"]),
     "gnn_csr_transpose": (ctypes.c_int, ["csr", "p", "p", "p", "p", "sz", "p"]),
+    "gnn_gt_attn_bwd": (ctypes.c_int, ["csr", "csr", "p", "p", "p", "i32", "i32", "i32", "f32", "p",
+                                       "p", "p", "p", "p", "p", "p", "sz", "p"]),
     "gnn_projection": (ctypes.c_int, ["p", "i32", "i64", "i32", "p", "i32", "p", "p"]),
     "gnn_gatv2_fwd": (ctypes.c_int, ["csr", "p", "p", "i32", "i32", "p", "p", "p", "i32", "i32",
                                      "f32", "p", "p", "p", "sz", "p"]),
@@ -366,6 +368,24 @@ def gnn_csr_transpose(g: Graph, stream=None):
         ctypes.byref(g.csr), rp.data_ptr(), ci.data_ptr() if g.csr.nnz else None, _ptr(vals),
         ws.data_ptr(), ws.numel(), _stream(stream)))
     return rp, ci, vals
+
+
+def gnn_gt_attn_bwd(g: Graph, gt: Graph, Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor,
+                    heads: int, head_dim: int, scale: float, out: torch.Tensor, lse: torch.Tensor,
+                    dout: torch.Tensor, stream=None):
+    """Backward of gnn_gt_attn_fwd (CSR path): returns (dQ, dK, dV) fp32.
+    gt: the transpose of g (Graph over gnn_csr_transpose's arrays)."""
+    _require_cuda(Q, K, V, out, lse, dout)
+    HD = heads * head_dim
+    dQ, dK, dV = (torch.empty((g.n_rows, HD), dtype=torch.float32, device=Q.device)
+                  for _ in range(3))
+    ws = g.workspace(GNN_OP_GT_BACKWARD, 0, heads, head_dim)
+    _check("gnn_gt_attn_bwd", lib().gnn_gt_attn_bwd(
+        ctypes.byref(g.csr), ctypes.byref(gt.csr), Q.data_ptr(), K.data_ptr(), V.data_ptr(),
+        _dtype_code(Q), heads, head_dim, float(scale), out.data_ptr(), lse.data_ptr(),
+        dout.data_ptr(), dQ.data_ptr(), dK.data_ptr(), dV.data_ptr(), ws.data_ptr(), ws.numel(),
+        _stream(stream)))
+    return dQ, dK, dV
 
 
 def gnn_spmm_blocksparse(g: Graph, X: torch.Tensor, bs, norm: int = GNN_NORM_BOTH, out=None,

@@ -12,6 +12,7 @@ size_t apply_perm_workspace_bytes(const gnn_csr *g);
 size_t blocksparse_workspace_bytes(const gnn_csr *g);
 size_t tile_spmm_workspace_bytes(const gnn_csr *g, int32_t F);
 size_t transpose_workspace_bytes(const gnn_csr *g);
+size_t gt_bwd_workspace_bytes(const gnn_csr *g, int32_t heads);
 gnn_status check_csr_args(const gnn_csr *g);
 }  // namespace gnn
 
@@ -42,6 +43,8 @@ extern "C" size_t gnn_workspace_size(int32_t op, const gnn_csr *g, int32_t F, in
             return tile_spmm_workspace_bytes(g, F);
         case GNN_OP_TRANSPOSE:
             return transpose_workspace_bytes(g);
+        case GNN_OP_GT_BACKWARD:
+            return gt_bwd_workspace_bytes(g, heads);
         default:
             return 0;
     }

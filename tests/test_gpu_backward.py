@@ -6,7 +6,7 @@ import pytest
 import oracle
 import synth
 from tests import graphs as G
-from tests.tolerance import TOL_F32, assert_rowwise_close
+from tests.tolerance import TOL_BF16, TOL_F32, assert_rowwise_close
 
 pytestmark = pytest.mark.gpu
 
@@ -77,3 +77,51 @@ def test_spmm_backward_on_the_transpose_config2(gnn, norm, bnorm):
                                      np.argsort(-np.diff(erp))[:8]])).astype(np.int32)
     ref = oracle.spmm(erp, eci, gy, norm=bnorm, rows=rows)
     assert_rowwise_close(got[rows], ref, TOL_F32, f"spmm backward norm={norm}")
+
+
+def _bf16(shape, seed):
+    return synth.normal_bf16(shape, 1.0, seed)
+
+
+def check_gt_backward(gnn, rp, ci, heads, D, seed=0):
+    n = len(rp) - 1
+    HD = heads * D
+    Q, K, V = (_bf16((n, HD), 70 + 3 * seed + k) for k in range(3))
+    dO = synth.normal_f32((n, HD), 1.0, 80 + seed)
+    scale = 1.0 / np.sqrt(D)
+    g = gnn.graph_prepare(dev(rp), dev(ci))
+    qd, kd, vd = (dev(x.view(np.int16)).view(torch.bfloat16) for x in (Q, K, V))
+    out, lse = gnn.gnn_gt_attn_fwd(g, qd, kd, vd, heads, D, scale)
+    rpt, cit, _ = gnn.gnn_csr_transpose(gnn.Graph(dev(rp), dev(ci), None, None, False))
+    gt = gnn.Graph(rpt, cit, None, None, False)
+    dQ, dK, dV = gnn.gnn_gt_attn_bwd(g, gt, qd, kd, vd, heads, D, scale, out, lse, dev(dO))
+    rQ, rK, rV = oracle.gt_backward(rp, ci, Q, K, V, heads, D, scale, dO)
+    for got, ref, name in ((dQ, rQ, "dQ"), (dK, rK, "dK"), (dV, rV, "dV")):
+        assert_rowwise_close(got.cpu().numpy(), ref, TOL_BF16, f"gt backward {name} {heads}x{D}")
+
+
+@pytest.mark.parametrize("heads,D", [(8, 32), (4, 64), (4, 32), (2, 64)])
+def test_gt_backward_small_graphs(gnn, heads, D):
+    rng = np.random.default_rng(heads * D)
+    n = 400
+    edges = [(int(rng.integers(n)), int(rng.integers(n))) for _ in range(6 * n)]
+    edges += [(int(s), 7) for s in rng.choice(n, 300, replace=False)]  # a hub destination
+    edges += [(3, int(d)) for d in rng.choice(n, 200, replace=False)]  # a hub source
+    rp, ci = G.from_edges(n, [(s, d) for s, d in edges if d not in (50, 51)], self_loops=False)
+    check_gt_backward(gnn, rp, ci, heads, D)
+
+
+def test_gt_backward_clustered(gnn):
+    rp, ci = synth.clustered(32, 128, 0.3, 0.02, 5)
+    check_gt_backward(gnn, rp, ci, 8, 32, seed=1)
+
+
+def test_gt_backward_rejects_unsupported_shapes(gnn):
+    rp, ci = G.random_graph(20, 0.2, 1)
+    g = gnn.graph_prepare(dev(rp), dev(ci))
+    gt = gnn.Graph(*gnn.gnn_csr_transpose(g)[:2], None, None, False)
+    x = torch.zeros((20, 96), dtype=torch.bfloat16, device="cuda")
+    f = torch.zeros((20, 96), dtype=torch.float32, device="cuda")
+    with pytest.raises(gnn.GnnError) as e:
+        gnn.gnn_gt_attn_bwd(g, gt, x, x, x, 3, 32, 0.2, f, torch.zeros((20, 3), device="cuda"), f)
+    assert e.value.code == gnn.GNN_ERR_UNSUPPORTED
