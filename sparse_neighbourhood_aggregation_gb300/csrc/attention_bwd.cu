@@ -22,7 +22,12 @@ gnn_status check_csr_args(const gnn_csr *g);
 
 namespace {
 
-constexpr int kBwdU = 4;  // edges whose rows are loaded together
+// Edges whose rows a warp loads together.  One edge at a time is the
+// fastest on a clustered 500K-node graph (8 heads x 32): 4.8 ms per
+// backward, against 6.0-7.5 ms with 2, 7.5 with 4 and 13.7 with 8, and
+// asking for more resident blocks made it slower still; the gathered rows
+// thrash L1 before they are reused, so fewer rows in flight win.
+constexpr int kBwdU = 1;
 
 struct GtBwdArgs {
     const int32_t *rowptr, *colidx;      // CSR (destination rows) or CSR^T (source rows)
