@@ -23,7 +23,7 @@ gnn_status check_csr_args(const gnn_csr *g);
 namespace {
 
 // Edges whose rows a warp loads together.  One edge at a time is the
-// fastest on a clustered 500K-node graph (8 heads x 32): 4.8 ms per
+// fastest on a clustered 262K-node graph (8 heads x 32): 4.8 ms per
 // backward, against 6.0-7.5 ms with 2, 7.5 with 4 and 13.7 with 8, and
 // asking for more resident blocks made it slower still; the gathered rows
 // thrash L1 before they are reused, so fewer rows in flight win.
