@@ -56,6 +56,8 @@ def _load():
             lib.orc_csr_transpose.argtypes = [i32, i32, _VP, _VP, _VP, _VP, _VP, _VP]
             lib.orc_gt_backward.argtypes = [i32, _VP, _VP, _VP, _VP, _VP, ctypes.c_int, i32, i32, dbl,
                                             _VP, _VP, _VP, _VP]
+            lib.orc_gatv2_backward.argtypes = [i32, _VP, _VP, _VP, _VP, ctypes.c_int, _VP, i32, i32,
+                                               dbl, _VP, _VP, _VP, _VP]
             lib.orc_gatv2.argtypes = [i32, _VP, _VP, _VP, ctypes.c_int, i32, _VP, _VP, _VP,
                                       i32, i32, dbl, _VP, i32, _VP, _VP, _VP]
             lib.orc_gt.argtypes = [i32, _VP, _VP, _VP, _VP, _VP, ctypes.c_int, i32, i32, dbl,
@@ -224,6 +226,26 @@ def gt_backward(rowptr, colidx, Q, K, V, heads, head_dim, scale, dO):
     _check(_load().orc_gt_backward(n, _p(rp), _p(ci), _p(Qc), _p(Kc), _p(Vc), dt, heads, head_dim,
                                    scale, _p(go), _p(dQ), _p(dK), _p(dV)), "gt_backward")
     return dQ, dK, dV
+
+
+def gatv2_backward(rowptr, colidx, Cl, Cr, a, heads, head_dim, dO, slope=0.2):
+    """Gradients (dl, dr fp64 [n, heads*head_dim], da fp64 [heads, head_dim])
+    of sum(dO * out) for the GATv2 attention over the per-node features
+    l = Cl (destination side) and r = Cr (source side); Cr=None: r = l."""
+    rp, ci, n = _csr(rowptr, colidx)
+    Lc, dt = _feat(Cl)
+    Rc, dt_r = _feat(Cl if Cr is None else Cr)
+    if dt_r != dt:
+        raise TypeError("Cl and Cr must have one dtype")
+    av = np.ascontiguousarray(a, np.float32)
+    go = np.ascontiguousarray(dO, np.float64)
+    HD = heads * head_dim
+    dl, dr = (np.empty((n, HD), np.float64) for _ in range(2))
+    da = np.empty((heads, head_dim), np.float64)
+    _check(_load().orc_gatv2_backward(n, _p(rp), _p(ci), _p(Lc), _p(Rc), dt, _p(av), heads,
+                                      head_dim, float(slope), _p(go), _p(dl), _p(dr), _p(da)),
+           "gatv2_backward")
+    return dl, dr, da
 
 
 def blocksparse(rowptr, colidx, threshold):

@@ -409,6 +409,75 @@ int orc_gt_backward(int32_t n, const int32_t *rowptr, const int32_t *colidx, con
     return ORC_OK;
 }
 
+/*
+ * Backward of the GATv2 attention with respect to its per-node features and
+ * the attention vector (IO-aware GNN layers, Appendix D.2, the GATv2
+ * backward: the weights are recomputed from the logits, the statistic
+ * G_i,h = sum_j alpha_ij <dO_i, r_j> is formed per destination and head, the
+ * left-feature and attention-vector gradients come from the destination
+ * rows and the right-feature gradient gathers over the incoming edges of
+ * each source).  For row i, head h, edge j in N(i), with x_ij = l_i + r_j
+ * (the head's D channels), sigma = LeakyReLU_slope, e_ij = <a_h, sigma(x_ij)>
+ * and alpha = softmax_j(e):
+ *   de_ij = alpha_ij (<dO_i, r_j> - G_i)
+ *   dl_i += de_ij a_h . sigma'(x_ij)
+ *   dr_j += alpha_ij dO_i + de_ij a_h . sigma'(x_ij)
+ *   da_h += de_ij sigma(x_ij)
+ * sigma'(x) = 1 for x > 0, else slope.  Cl, Cr [n, heads*D] (dtype as
+ * orc_gt; Cl == Cr for a shared projection); dO, dl, dr fp64 [n, heads*D];
+ * da fp64 [heads*D].  The graph is square.  Outputs are overwritten.
+ */
+int orc_gatv2_backward(int32_t n, const int32_t *rowptr, const int32_t *colidx, const void *Cl,
+                       const void *Cr, int dtype, const float *a, int32_t heads, int32_t D,
+                       double slope, const double *dO, double *dl, double *dr, double *da) {
+    int32_t HD = heads * D;
+    for (int64_t k = 0; k < (int64_t)n * HD; ++k) dl[k] = dr[k] = 0.0;
+    for (int32_t c = 0; c < HD; ++c) da[c] = 0.0;
+    int64_t max_deg = 0;
+    for (int32_t i = 0; i < n; ++i)
+        if (rowptr[i + 1] - rowptr[i] > max_deg) max_deg = rowptr[i + 1] - rowptr[i];
+    size_t md = (size_t)(max_deg > 0 ? max_deg : 1);
+    double *e = malloc(sizeof(double) * md);
+    double *al = malloc(sizeof(double) * md);
+    double *p = malloc(sizeof(double) * md);
+    if (!e || !al || !p) { free(e); free(al); free(p); return ORC_ERR; }
+    for (int32_t i = 0; i < n; ++i) {
+        int64_t b = rowptr[i], deg = rowptr[i + 1] - b;
+        if (deg == 0) continue;
+        for (int32_t h = 0; h < heads; ++h) {
+            int64_t io = (int64_t)i * HD + h * D;
+            /* logits, weights and <dO_i, r_j> */
+            for (int64_t k = 0; k < deg; ++k) {
+                int64_t jo = (int64_t)colidx[b + k] * HD + h * D;
+                double acc = 0.0, pr = 0.0;
+                for (int32_t d = 0; d < D; ++d) {
+                    double x = widen(Cl, dtype, io + d) + widen(Cr, dtype, jo + d);
+                    acc += (double)a[h * D + d] * (x > 0.0 ? x : slope * x);
+                    pr += dO[io + d] * widen(Cr, dtype, jo + d);
+                }
+                e[k] = acc;
+                p[k] = pr;
+            }
+            softmax_row(e, deg, al);
+            double G = 0.0;
+            for (int64_t k = 0; k < deg; ++k) G += al[k] * p[k];
+            for (int64_t k = 0; k < deg; ++k) {
+                int64_t jo = (int64_t)colidx[b + k] * HD + h * D;
+                double de = al[k] * (p[k] - G);
+                for (int32_t d = 0; d < D; ++d) {
+                    double x = widen(Cl, dtype, io + d) + widen(Cr, dtype, jo + d);
+                    double g = de * (double)a[h * D + d] * (x > 0.0 ? 1.0 : slope);
+                    dl[io + d] += g;
+                    dr[jo + d] += al[k] * dO[io + d] + g;
+                    da[h * D + d] += de * (x > 0.0 ? x : slope * x);
+                }
+            }
+        }
+    }
+    free(e); free(al); free(p);
+    return ORC_OK;
+}
+
 /* ------------------------------------------------------------------ */
 /* block-sparse tiles (IO-aware GNN layers, Appendix D.3, WSB format)  */
 /* ------------------------------------------------------------------ */

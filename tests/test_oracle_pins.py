@@ -304,6 +304,91 @@ def test_gt_backward_matches_finite_differences():
     assert np.allclose(dV.sum(0), dO[has].sum(0), rtol=1e-12, atol=1e-12)
 
 
+def _gatv2_grid_features(rng, n, HD):
+    """l and r on the grid k/8 + 1/32: every l_i + r_j sits at least 1/16
+    from LeakyReLU's kink, so a step of 2^-10 never crosses it."""
+    return tuple((rng.integers(-12, 13, (n, HD)) / 8 + 1 / 32).astype(np.float32)
+                 for _ in range(2))
+
+
+def test_gatv2_backward_matches_finite_differences():
+    """dl, dr, da of sum(dO * GATv2(l, r)) by central differences of the
+    forward oracle (2 heads x 4, separate left and right projections):
+    H = [l | r] with W_l = [I; 0], W_r = [0; I] makes the projected rows l
+    and r themselves."""
+    rng = np.random.default_rng(53)
+    rp, ci = G.random_graph(9, 0.4, 11)
+    n, heads, D, slope = 9, 2, 4, 0.2
+    HD = heads * D
+    l, r = _gatv2_grid_features(rng, n, HD)
+    a = rng.standard_normal((heads, D)).astype(np.float32)
+    dO = rng.standard_normal((n, HD))
+    dl, dr, da = oracle.gatv2_backward(rp, ci, l, r, a, heads, D, dO, slope)
+    eye, zero = np.eye(HD, dtype=np.float32), np.zeros((HD, HD), np.float32)
+    W_l, W_r = np.vstack([eye, zero]), np.vstack([zero, eye])
+
+    def loss(lx, rx, ax):
+        out, _ = oracle.gatv2(rp, ci, np.hstack([lx, rx]), W_l, ax, heads, D, slope, W_r=W_r)
+        return float(np.sum(dO * out))
+
+    eps = 2.0 ** -10
+    for got, which in ((dl, 0), (dr, 1), (da, 2)):
+        num = np.zeros_like(got)
+        for idx in np.ndindex(*got.shape):
+            args_p = [l.copy(), r.copy(), a.copy()]
+            args_m = [l.copy(), r.copy(), a.copy()]
+            args_p[which][idx] += eps
+            args_m[which][idx] -= eps
+            num[idx] = (loss(*args_p) - loss(*args_m)) / (2 * eps)
+        assert np.allclose(got, num, rtol=1e-4, atol=1e-6), ("dl", "dr", "da")[which]
+
+
+def test_gatv2_backward_shared_projection_is_dl_plus_dr():
+    """With one projection (r = l = C) the gradient of C is dl + dr: central
+    differences of the forward with H = C, W = I (1 head x 8, a hub row)."""
+    rng = np.random.default_rng(54)
+    n, heads, D, slope = 8, 1, 8, 0.2
+    rp, ci = G.from_edges(n, [(s, 0) for s in range(1, n)] + [(2, 5), (6, 3), (4, 7)])
+    C, _ = _gatv2_grid_features(rng, n, D)
+    a = rng.standard_normal((heads, D)).astype(np.float32)
+    dO = rng.standard_normal((n, D))
+    dl, dr, _ = oracle.gatv2_backward(rp, ci, C, None, a, heads, D, dO, slope)
+    eye = np.eye(D, dtype=np.float32)
+    eps = 2.0 ** -10
+    num = np.zeros((n, D))
+    for idx in np.ndindex(n, D):
+        cp, cm = C.copy(), C.copy()
+        cp[idx] += eps
+        cm[idx] -= eps
+        num[idx] = (np.sum(dO * oracle.gatv2(rp, ci, cp, eye, a, heads, D, slope)[0]) -
+                    np.sum(dO * oracle.gatv2(rp, ci, cm, eye, a, heads, D, slope)[0])) / (2 * eps)
+    assert np.allclose(dl + dr, num, rtol=1e-4, atol=1e-6)
+
+
+def test_gatv2_backward_special_cases():
+    """slope 1: LeakyReLU is the identity, the logit's l_i part is constant
+    over the row and cancels in the softmax, so dl = 0.  a = 0: uniform
+    weights, dl = 0, da is still defined and dr_j = sum over the rows i that
+    list j of dO_i / deg(i)."""
+    rng = np.random.default_rng(55)
+    rp, ci = G.random_graph(30, 0.2, 12)
+    n, heads, D = 30, 2, 4
+    HD = heads * D
+    l, r = (rng.standard_normal((n, HD)).astype(np.float32) for _ in range(2))
+    a = rng.standard_normal((heads, D)).astype(np.float32)
+    dO = rng.standard_normal((n, HD))
+    dl, _, _ = oracle.gatv2_backward(rp, ci, l, r, a, heads, D, dO, 1.0)
+    assert np.max(np.abs(dl)) < 1e-12
+    dl0, dr0, _ = oracle.gatv2_backward(rp, ci, l, r, np.zeros_like(a), heads, D, dO, 0.2)
+    assert np.max(np.abs(dl0)) == 0.0
+    want = np.zeros((n, HD))
+    for i in range(n):
+        deg = rp[i + 1] - rp[i]
+        for j in ci[rp[i]:rp[i + 1]]:
+            want[j] += dO[i] / deg
+    assert np.allclose(dr0, want, rtol=1e-12, atol=1e-13)
+
+
 # ---------------------------------------------------------------- relabel invariance
 
 @pytest.mark.parametrize("op", ["spmm", "sum", "mean", "max"])
