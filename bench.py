@@ -254,13 +254,26 @@ def setup_c3(torch, gnn, w):
         oracle.gatv2(w["rowptr"], w["colidx"], w["H"], w["W"], w["a"], heads, D, w["slope"],
                      rows=rows)
 
+    # backward of the attention (AL over CSR, R over CSR^T, attention-vector
+    # reduction) from the timed forward's out and lse; C = H W as the forward
+    # scored it; compulsory bytes: C read by each kernel, dO by each, O once,
+    # dl and dr written, lse and G read twice / written once, both index sets
+    rpt, cit, _ = gnn.gnn_csr_transpose(g)
+    gtr = gnn.Graph(rpt, cit, None, None, False)
+    dout = torch.randn((n, HD), dtype=torch.float32, device="cuda")
+    gnn.gnn_projection(H, W, out=C)
+    b_bwd = 2 * n * HD * 2 + 2 * n * HD * 4 + n * HD * 4 + 2 * n * HD * 4 + 4 * n * heads * 4 + 2 * idx
+    timed = {"gatv2_backward": (
+        lambda: gnn.gnn_gatv2_attn_bwd(g, gtr, C, None, a, heads, D, out, lse, dout, w["slope"]),
+        b_bwd, "dl and da over CSR, dr over CSR^T, from the forward's out and lse (one projection: "
+               "dC = dl + dr); timed apart, cold")}
     cfg = {"workload": "c3_rmat20_gatv2", "graph": "R-MAT scale 20, edge factor 16, dedup + "
            "self-loops", "nodes": n, "edges": M, "heads": heads, "head_dim": D, "f_in": 256,
            "dtype": "bf16 H, W and C; fp32 softmax and accumulation; fp32 out",
            "layers": ["tcgen05 projection + fused GATv2 (score, online softmax, aggregate)"]}
     rows = _sample_by_edges(w["rowptr"], 40000)
     return Workload("c3_rmat20_gatv2", layers, [H], [out, lse], cfg, "bf16", oracle_step, rows,
-                    extra={"proj_only": (proj_only, b_proj), "b_attn": b_attn,
+                    extra={"proj_only": (proj_only, b_proj), "b_attn": b_attn, "timed": timed,
                            "unfused": (g, H, W, a, heads, D, w["slope"])})
 
 

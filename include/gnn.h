@@ -123,7 +123,7 @@ typedef enum {
     GNN_OP_SPMM = 0, GNN_OP_SUM = 1, GNN_OP_MEAN = 2, GNN_OP_MAX = 3,
     GNN_OP_GATV2 = 4, GNN_OP_GT = 5, GNN_OP_REORDER = 6, GNN_OP_APPLY_PERM = 7,
     GNN_OP_BLOCKSPARSE = 8, GNN_OP_MIN = 9, GNN_OP_SPMM_BLOCKSPARSE = 10, GNN_OP_TRANSPOSE = 11,
-    GNN_OP_GT_BACKWARD = 12
+    GNN_OP_GT_BACKWARD = 12, GNN_OP_GATV2_BACKWARD = 13
 } gnn_op;
 
 /* OR-ed into `op` of gnn_workspace_size: size the workspace for bf16 inputs
@@ -346,6 +346,37 @@ gnn_status gnn_gt_attn_bwd(const gnn_csr *g, const gnn_csr *gt, const void *Q, c
                            const void *V, int32_t dtype, int32_t heads, int32_t head_dim, float scale,
                            const float *out, const float *lse, const float *dout, float *dQ, float *dK,
                            float *dV, void *ws, size_t ws_bytes, void *stream);
+
+/* Backward of the GATv2 attention with respect to its per-node features and
+ * its attention vector (IO-aware GNN layers, Appendix D.2, the GATv2
+ * backward: an AL kernel over the CSR for the left features and the
+ * attention vector, with G_i = sum_j alpha_ij <dO_i, r_j>, an R kernel over
+ * CSR^T for the right features, and a reduction of the attention-vector
+ * gradient over the nodes).  With x_ij = l_i + r_j per head, sigma =
+ * LeakyReLU(neg_slope), e_ij = <a_h, sigma(x_ij)> and alpha_ij =
+ * exp(e_ij - lse_i):
+ *   de_ij = alpha_ij (<dO_i, r_j> - G_i)
+ *   dl_i = sum_j de_ij a_h . sigma'(x_ij),  da_h = sum_ij de_ij sigma(x_ij),
+ *   dr_j = sum_i alpha_ij dO_i + de_ij a_h . sigma'(x_ij).
+ * G_i is computed as <out_i, dout_i> (equal, since out_i = sum_j alpha_ij
+ * r_j).  Cl (l, destination side) and Cr (r, source side) are the projected
+ * features [n, heads*head_dim] the forward scored, fp32 or bf16 (dtype);
+ * with one projection (W_r = W_l) pass the same C for both, and its
+ * gradient is dl + dr.  The gradient through the projection itself (dW =
+ * H^T dC, dH = dC W^T) is a dense GEMM left to the caller.  a fp32
+ * [heads, head_dim]; out, lse from gnn_gatv2_fwd; dout fp32; dl, dr fp32
+ * [n, heads*head_dim] and da fp32 [heads*head_dim], overwritten.  g square,
+ * gt its transpose (gnn_csr_transpose).  heads*head_dim in {32, 64, 128,
+ * 256} with head_dim a power-of-two multiple of heads*head_dim/32 (else
+ * GNN_ERR_UNSUPPORTED).  Rows are worked in runs of 256 edges with heavy
+ * rows cut and their pieces summed in edge order: deterministic.  Workspace
+ * gnn_workspace_size(GNN_OP_GATV2_BACKWARD, g, 0, heads, head_dim), any
+ * contents (the call clears what it needs).  Asynchronous. */
+gnn_status gnn_gatv2_attn_bwd(const gnn_csr *g, const gnn_csr *gt, const void *Cl, const void *Cr,
+                              int32_t dtype, const float *a, int32_t heads, int32_t head_dim,
+                              float neg_slope, const float *out, const float *lse,
+                              const float *dout, float *dl, float *dr, float *da, void *ws,
+                              size_t ws_bytes, void *stream);
 
 /* --------------------------------------------------- step a8: reordering */
 

@@ -22,7 +22,7 @@ GNN_NORM_NONE, GNN_NORM_LEFT, GNN_NORM_RIGHT, GNN_NORM_BOTH = 0, 1, 2, 3
 GNN_MAP_AUTO, GNN_MAP_FEAT, GNN_MAP_NEIGH = 0, 1, 2
 (GNN_OP_SPMM, GNN_OP_SUM, GNN_OP_MEAN, GNN_OP_MAX, GNN_OP_GATV2, GNN_OP_GT, GNN_OP_REORDER,
  GNN_OP_APPLY_PERM, GNN_OP_BLOCKSPARSE, GNN_OP_MIN, GNN_OP_SPMM_BLOCKSPARSE,
- GNN_OP_TRANSPOSE, GNN_OP_GT_BACKWARD) = range(13)
+ GNN_OP_TRANSPOSE, GNN_OP_GT_BACKWARD, GNN_OP_GATV2_BACKWARD) = range(14)
 GNN_PERM_IDENTITY, GNN_PERM_RANDOM, GNN_PERM_DEGREE, GNN_PERM_RCM = 0, 1, 2, 3
 
 
@@ -70,6 +70,8 @@ _SIGS = {
     "gnn_csr_transpose": (ctypes.c_int, ["csr", "p", "p", "p", "p", "sz", "p"]),
     "gnn_gt_attn_bwd": (ctypes.c_int, ["csr", "csr", "p", "p", "p", "i32", "i32", "i32", "f32", "p",
                                        "p", "p", "p", "p", "p", "p", "sz", "p"]),
+    "gnn_gatv2_attn_bwd": (ctypes.c_int, ["csr", "csr", "p", "p", "i32", "p", "i32", "i32", "f32",
+                                          "p", "p", "p", "p", "p", "p", "p", "sz", "p"]),
     "gnn_projection": (ctypes.c_int, ["p", "i32", "i64", "i32", "p", "i32", "p", "p"]),
     "gnn_gatv2_fwd": (ctypes.c_int, ["csr", "p", "p", "i32", "i32", "p", "p", "p", "i32", "i32",
                                      "f32", "p", "p", "p", "sz", "p"]),
@@ -386,6 +388,29 @@ def gnn_gt_attn_bwd(g: Graph, gt: Graph, Q: torch.Tensor, K: torch.Tensor, V: to
         dout.data_ptr(), dQ.data_ptr(), dK.data_ptr(), dV.data_ptr(), ws.data_ptr(), ws.numel(),
         _stream(stream)))
     return dQ, dK, dV
+
+
+def gnn_gatv2_attn_bwd(g: Graph, gt: Graph, Cl: torch.Tensor, Cr, a: torch.Tensor, heads: int,
+                       head_dim: int, out: torch.Tensor, lse: torch.Tensor, dout: torch.Tensor,
+                       neg_slope: float = 0.2, stream=None):
+    """Backward of the GATv2 attention over the projected features: returns
+    (dl, dr fp32 [n, heads*head_dim], da fp32 [heads, head_dim]).  Cl: the
+    destination-side features l; Cr: the source-side features r (None: one
+    projection, r = l, whose gradient is dl + dr).  gt: the transpose of g."""
+    Cr = Cl if Cr is None else Cr
+    _require_cuda(Cl, Cr, a, out, lse, dout)
+    if a.dtype != torch.float32 or Cr.dtype != Cl.dtype:
+        raise TypeError("a must be fp32 and Cl, Cr of one dtype")
+    HD = heads * head_dim
+    dl, dr = (torch.empty((g.n_rows, HD), dtype=torch.float32, device=Cl.device) for _ in range(2))
+    da = torch.empty((heads, head_dim), dtype=torch.float32, device=Cl.device)
+    ws = g.workspace(GNN_OP_GATV2_BACKWARD, 0, heads, head_dim)
+    _check("gnn_gatv2_attn_bwd", lib().gnn_gatv2_attn_bwd(
+        ctypes.byref(g.csr), ctypes.byref(gt.csr), Cl.data_ptr(), Cr.data_ptr(), _dtype_code(Cl),
+        a.data_ptr(), heads, head_dim, float(neg_slope), out.data_ptr(), lse.data_ptr(),
+        dout.data_ptr(), dl.data_ptr(), dr.data_ptr(), da.data_ptr(), ws.data_ptr(), ws.numel(),
+        _stream(stream)))
+    return dl, dr, da
 
 
 def gnn_spmm_blocksparse(g: Graph, X: torch.Tensor, bs, norm: int = GNN_NORM_BOTH, out=None,

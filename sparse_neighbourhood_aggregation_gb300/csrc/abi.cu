@@ -13,6 +13,7 @@ size_t blocksparse_workspace_bytes(const gnn_csr *g);
 size_t tile_spmm_workspace_bytes(const gnn_csr *g, int32_t F);
 size_t transpose_workspace_bytes(const gnn_csr *g);
 size_t gt_bwd_workspace_bytes(const gnn_csr *g, int32_t heads);
+size_t gatv2_bwd_workspace_bytes(const gnn_csr *g, int32_t heads, int32_t head_dim);
 gnn_status check_csr_args(const gnn_csr *g);
 }  // namespace gnn
 
@@ -45,6 +46,8 @@ extern "C" size_t gnn_workspace_size(int32_t op, const gnn_csr *g, int32_t F, in
             return transpose_workspace_bytes(g);
         case GNN_OP_GT_BACKWARD:
             return gt_bwd_workspace_bytes(g, heads);
+        case GNN_OP_GATV2_BACKWARD:
+            return gatv2_bwd_workspace_bytes(g, heads, head_dim);
         default:
             return 0;
     }

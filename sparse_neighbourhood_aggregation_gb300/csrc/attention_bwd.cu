@@ -12,6 +12,29 @@
 // sums are deterministic.  Lane l holds channels [l*NC, (l+1)*NC) of the
 // HD = 32 NC channels; the D / NC lanes of a head reduce its dot products
 // with shuffles.  The edge loop loads the rows of U edges before using any.
+//
+// Backward of the fused GATv2 attention (same appendix, the GATv2 backward:
+// an AL kernel for the left features and the attention vector, which also
+// forms G_i = sum_j alpha_ij <dO_i, r_j>, and an R kernel over CSR^T for the
+// right features; the attention-vector gradient is reduced over nodes at the
+// end).  With x_ij = l_i + r_j per head, sigma = LeakyReLU(slope), e_ij =
+// <a_h, sigma(x_ij)> and alpha_ij = exp(e_ij - L_i):
+//   de_ij = alpha_ij (<dO_i, r_j> - G_i)
+//   dl_i  = sum_j de_ij a_h . sigma'(x_ij)              (k_gatv2_bwd<AL>)
+//   da_h  = sum_ij de_ij sigma(x_ij)                     (AL, then k_gatv2_bwd_da)
+//   dr_j  = sum_i alpha_ij dO_i + de_ij a_h . sigma'(x_ij)  (k_gatv2_bwd<R>)
+// G_i is formed as <O_i, dO_i>, the same number since O_i = sum_j alpha_ij
+// r_j, so no pass over the row is spent on it before the gradients.
+// Schedule: power-law graphs have rows of tens of thousands of edges, so a
+// warp per row would leave one warp with a hub's whole list.  A warp is a
+// worker over a run of kGatE consecutive edges instead (the forward's
+// schedule): it owns the rows whose first edge lies in its run, processes a
+// light row whole, and cuts a heavy row (degree > kGatE) at run boundaries.
+// Every piece of a heavy row leaves its partial gradient row in a slot; the
+// last piece to finish (ticket counter, no waiting) sums the slots in edge
+// order, so the result does not depend on which warp ran first.  The
+// attention-vector gradient is kept per warp in registers, summed per block,
+// and the block partials are summed in a fixed order by k_gatv2_bwd_da.
 #include <algorithm>
 
 #include "common.cuh"
@@ -194,6 +217,352 @@ __global__ void __launch_bounds__(256) k_gt_bwd_kv(GtBwdArgs a) {
     st_f32<NC>(a.dB + ro, dv);
 }
 
+// ---------------------------------------------------------------- GATv2
+
+constexpr int64_t kGatE = 256;     // edges per worker run
+constexpr int kGatWarps = 8;       // warps per block
+constexpr int kDaBlocks = 128;     // blocks of the attention-vector reduction
+
+enum GatSide { GAT_AL = 0, GAT_R = 1 };
+
+struct GatBwdArgs {
+    const int32_t *rowptr, *colidx;  // AL: CSR (destination rows); R: CSR^T (source rows)
+    const int32_t *run_rows;         // [n_runs + 1]: first row whose first edge is in run w
+    const void *Cl, *Cr;             // l and r features [n, HD] (fp32 or bf16)
+    const float *a;                  // [HD]
+    const float *O, *lse, *dO;       // forward output, logsumexp [n, heads], grad of O
+    float *G;                        // [n, heads]: AL writes, R reads
+    float *grad;                     // AL: dl; R: dr  [n, HD]
+    float *slots;                    // [2 n_runs, HD] partial rows of heavy-row pieces
+    int32_t *tickets;                // [n_runs], zero between calls
+    float *da_part;                  // AL: [gridDim, HD] per-block attention-vector sums
+    int64_t nnz, n_runs;
+    int32_t n, heads, D, HD;
+    float slope;
+};
+
+// NC channels of a feature row, widened to fp32
+template <typename T, int NC>
+__device__ __forceinline__ void ld_row(const void *base, int64_t off, float *f) {
+    if constexpr (sizeof(T) == 4) {
+        const float *p = static_cast<const float *>(base) + off;
+        if constexpr (NC == 1) {
+            f[0] = __ldg(p);
+        } else if constexpr (NC == 2) {
+            const float2 v = __ldg(reinterpret_cast<const float2 *>(p));
+            f[0] = v.x; f[1] = v.y;
+        } else {
+#pragma unroll
+            for (int c = 0; c < NC; c += 4) {
+                const float4 v = __ldg(reinterpret_cast<const float4 *>(p + c));
+                f[c] = v.x; f[c + 1] = v.y; f[c + 2] = v.z; f[c + 3] = v.w;
+            }
+        }
+    } else {
+        const __nv_bfloat16 *p = static_cast<const __nv_bfloat16 *>(base) + off;
+        if constexpr (NC == 1) {
+            f[0] = bf16lo(__ldg(reinterpret_cast<const unsigned short *>(p)));
+        } else if constexpr (NC == 2) {
+            const uint32_t v = __ldg(reinterpret_cast<const unsigned int *>(p));
+            f[0] = bf16lo(v); f[1] = bf16hi(v);
+        } else {
+            ld_bf16<NC>(p, f);
+        }
+    }
+}
+
+template <int NC>
+__device__ __forceinline__ void st_row(float *p, const float *f) {
+    if constexpr (NC == 1) {
+        *p = f[0];
+    } else if constexpr (NC == 2) {
+        *reinterpret_cast<float2 *>(p) = make_float2(f[0], f[1]);
+    } else {
+        st_f32<NC>(p, f);
+    }
+}
+
+template <int NC>
+__device__ __forceinline__ void st_row_cg(float *p, const float *f) {
+#pragma unroll
+    for (int c = 0; c < NC; ++c) __stcg(p + c, f[c]);
+}
+
+// Destination-side (AL) or source-side (R) data of the row a warp works on.
+template <int SIDE, int NC>
+struct GatRow {
+    float own[NC];   // AL: l_i; R: r_j
+    float g[NC];     // AL: dO_i
+    float L, G;      // AL: logsumexp and G of (i, head)
+};
+
+template <int SIDE, typename T, int NC>
+__device__ __forceinline__ void gat_load_row(const GatBwdArgs &p, int32_t r, int lane, int hd, int lph,
+                                             bool nonempty, GatRow<SIDE, NC> &R) {
+    const int64_t ro = (int64_t)r * p.HD + lane * NC;
+    if constexpr (SIDE == GAT_AL) {
+        ld_row<T, NC>(p.Cl, ro, R.own);
+        float o[NC];
+        ld_row<float, NC>(p.O, ro, o);
+        ld_row<float, NC>(p.dO, ro, R.g);
+        float s = 0.f;
+#pragma unroll
+        for (int c = 0; c < NC; ++c) s = fmaf(o[c], R.g[c], s);
+        R.G = head_sum(s, lph);
+        R.L = nonempty ? __ldg(p.lse + (int64_t)r * p.heads + hd) : 0.f;
+    } else {
+        ld_row<T, NC>(p.Cr, ro, R.own);
+    }
+}
+
+// Gradient contributions of the edges [eb, ee) of one row into acc (dl_i or
+// dr_j) and, on the AL side, ga (attention vector).
+template <int SIDE, typename T, int NC>
+__device__ __forceinline__ void gat_edges(const GatBwdArgs &p, const GatRow<SIDE, NC> &R, const float *av,
+                                          int lane, int hd, int lph, int32_t eb, int32_t ee, float *acc,
+                                          float *ga) {
+    for (int32_t cb = eb; cb < ee; cb += 32) {
+        const int32_t cn = cb + lane < ee ? __ldg(p.colidx + cb + lane) : 0;
+        const int m = min(32, ee - cb);
+        for (int u = 0; u < m; ++u) {
+            const int32_t k = __shfl_sync(0xffffffffu, cn, u);
+            const int64_t ko = (int64_t)k * p.HD + lane * NC;
+            float x[NC], rr[NC], gg[NC];
+            float L, G;
+            if constexpr (SIDE == GAT_AL) {
+                ld_row<T, NC>(p.Cr, ko, rr);     // r_j of neighbour j
+#pragma unroll
+                for (int c = 0; c < NC; ++c) { x[c] = R.own[c] + rr[c]; gg[c] = R.g[c]; }
+                L = R.L;
+                G = R.G;
+            } else {
+                float lk[NC];
+                ld_row<T, NC>(p.Cl, ko, lk);     // l_i of destination i
+                ld_row<float, NC>(p.dO, ko, gg);
+                L = __ldg(p.lse + (int64_t)k * p.heads + hd);
+                G = __ldg(p.G + (int64_t)k * p.heads + hd);
+#pragma unroll
+                for (int c = 0; c < NC; ++c) { rr[c] = R.own[c]; x[c] = lk[c] + rr[c]; }
+            }
+            float e = 0.f, pr = 0.f;
+#pragma unroll
+            for (int c = 0; c < NC; ++c) {
+                e = fmaf(av[c], x[c] > 0.f ? x[c] : p.slope * x[c], e);
+                pr = fmaf(gg[c], rr[c], pr);
+            }
+            e = head_sum(e, lph);
+            pr = head_sum(pr, lph);
+            const float al = __expf(e - L);
+            const float de = al * (pr - G);
+#pragma unroll
+            for (int c = 0; c < NC; ++c) {
+                const float d1 = x[c] > 0.f ? 1.f : p.slope;
+                if constexpr (SIDE == GAT_AL) {
+                    acc[c] = fmaf(de * d1, av[c], acc[c]);
+                    ga[c] = fmaf(de, d1 * x[c], ga[c]);
+                } else {
+                    acc[c] = fmaf(al, gg[c], fmaf(de * d1, av[c], acc[c]));
+                }
+            }
+        }
+    }
+}
+
+// A piece of heavy row r leaves acc in its slot; the last of the row's
+// pieces to arrive sums them in edge order and writes the gradient row.
+template <int NC>
+__device__ __forceinline__ void gat_flush_piece(const GatBwdArgs &p, int64_t w, int32_t r, int lane,
+                                                const float *acc) {
+    const int32_t rb = __ldg(p.rowptr + r), re = __ldg(p.rowptr + r + 1);
+    const int64_t wa = rb / kGatE, wb = ((int64_t)re - 1) / kGatE;
+    st_row_cg<NC>(p.slots + (2 * w + (w == wa ? 1 : 0)) * p.HD + lane * NC, acc);
+    __threadfence();
+    __syncwarp();
+    int t = 0;
+    if (lane == 0) t = atomicAdd(p.tickets + wa, 1);
+    t = __shfl_sync(0xffffffffu, t, 0);
+    if (t != (int)(wb - wa)) return;
+    __threadfence();
+    float sum[NC];
+#pragma unroll
+    for (int c = 0; c < NC; ++c) sum[c] = 0.f;
+    for (int64_t k = wa; k <= wb; ++k) {
+        const float *sk = p.slots + (2 * k + (k == wa ? 1 : 0)) * p.HD + lane * NC;
+#pragma unroll
+        for (int c = 0; c < NC; ++c) sum[c] += __ldcg(sk + c);
+    }
+    st_row<NC>(p.grad + (int64_t)r * p.HD + lane * NC, sum);
+    __syncwarp();
+    if (lane == 0) p.tickets[wa] = 0;
+}
+
+template <int SIDE, typename T, int NC>
+__global__ void __launch_bounds__(kGatWarps * 32) k_gatv2_bwd(GatBwdArgs p) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t w = (int64_t)blockIdx.x * kGatWarps + warp;
+    const int lph = p.D / NC;
+    const int hd = (lane * NC) / p.D;
+    float av[NC], ga[NC];
+    ld_row<float, NC>(p.a, lane * NC, av);
+#pragma unroll
+    for (int c = 0; c < NC; ++c) ga[c] = 0.f;
+    if (w < p.n_runs) {
+        const int64_t e0 = w * kGatE, e1 = min(e0 + kGatE, p.nnz);
+        const int32_t lo = __ldg(p.run_rows + w), lo_end = __ldg(p.run_rows + w + 1);
+        // a heavy row that started in an earlier run and reaches into this one
+        if (lo > 0 && e0 < p.nnz) {
+            const int32_t lo_beg = __ldg(p.rowptr + lo);
+            if (lo_beg > e0 && lo_beg - __ldg(p.rowptr + lo - 1) > kGatE) {
+                GatRow<SIDE, NC> R;
+                gat_load_row<SIDE, T, NC>(p, lo - 1, lane, hd, lph, true, R);
+                float acc[NC];
+#pragma unroll
+                for (int c = 0; c < NC; ++c) acc[c] = 0.f;
+                gat_edges<SIDE, T, NC>(p, R, av, lane, hd, lph, (int32_t)e0, (int32_t)min((int64_t)lo_beg, e1),
+                                       acc, ga);
+                gat_flush_piece<NC>(p, w, lo - 1, lane, acc);
+            }
+        }
+        // owned rows, bounds read 32 at a time
+        for (int32_t rbase = lo; rbase < lo_end; rbase += 32) {
+            const int32_t rr = rbase + lane;
+            int32_t my_b = 0, my_e = 0;
+            if (rr < lo_end) {
+                my_b = __ldg(p.rowptr + rr);
+                my_e = __ldg(p.rowptr + rr + 1);
+            }
+            const int cnt = min(32, lo_end - rbase);
+            for (int k = 0; k < cnt; ++k) {
+                const int32_t r = rbase + k;
+                const int32_t rb = __shfl_sync(0xffffffffu, my_b, k), re = __shfl_sync(0xffffffffu, my_e, k);
+                GatRow<SIDE, NC> R;
+                gat_load_row<SIDE, T, NC>(p, r, lane, hd, lph, re > rb, R);
+                if constexpr (SIDE == GAT_AL) {
+                    if (lane % lph == 0) p.G[(int64_t)r * p.heads + hd] = R.G;
+                }
+                float acc[NC];
+#pragma unroll
+                for (int c = 0; c < NC; ++c) acc[c] = 0.f;
+                if (re - rb > kGatE) {  // heavy: its first piece (the last owned row)
+                    gat_edges<SIDE, T, NC>(p, R, av, lane, hd, lph, rb, (int32_t)e1, acc, ga);
+                    gat_flush_piece<NC>(p, w, r, lane, acc);
+                } else {
+                    gat_edges<SIDE, T, NC>(p, R, av, lane, hd, lph, rb, re, acc, ga);
+                    st_row<NC>(p.grad + (int64_t)r * p.HD + lane * NC, acc);
+                }
+            }
+        }
+    }
+    if constexpr (SIDE == GAT_AL) {
+        // per-block sum of the warps' attention-vector gradients, in warp order
+        __shared__ float sga[kGatWarps][256];
+#pragma unroll
+        for (int c = 0; c < NC; ++c) sga[warp][lane * NC + c] = ga[c];
+        __syncthreads();
+        for (int c = threadIdx.x; c < p.HD; c += blockDim.x) {
+            float t = 0.f;
+#pragma unroll
+            for (int k = 0; k < kGatWarps; ++k) t += sga[k][c];
+            p.da_part[(int64_t)blockIdx.x * p.HD + c] = t;
+        }
+    }
+}
+
+// run_rows[w] = first row r with rowptr[r] >= w * kGatE, for the runs of the
+// CSR (run_rows) and of CSR^T (run_rows_t); run_rows[n_runs] = n.  Thread r
+// (0 <= r <= n) covers the runs whose start lies in (rowptr[r-1], rowptr[r]];
+// r = n takes the runs that start inside the last row (no row begins there).
+// Also clears the tickets (thread r < n_runs) and the reduction ticket.
+__global__ void k_gatv2_bwd_runs(const int32_t *__restrict__ rowptr, const int32_t *__restrict__ rowptr_t,
+                                 int32_t n, int64_t n_runs, int32_t *__restrict__ run_rows,
+                                 int32_t *__restrict__ run_rows_t, int32_t *__restrict__ tickets,
+                                 int32_t *__restrict__ da_ticket) {
+    const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (r < n_runs) tickets[r] = 0;
+    if (r == 0) *da_ticket = 0;
+    if (r > n) return;
+    if (r == n) {
+        run_rows[n_runs] = n;
+        run_rows_t[n_runs] = n;
+    }
+    const int32_t *rps[2] = {rowptr, rowptr_t};
+    int32_t *outs[2] = {run_rows, run_rows_t};
+    for (int k = 0; k < 2; ++k) {
+        const int64_t hi = rps[k][r];
+        const int64_t lo = r > 0 ? (int64_t)rps[k][r - 1] + 1 : 0;
+        for (int64_t w = (lo + kGatE - 1) / kGatE; w * kGatE <= hi && w < n_runs; ++w) outs[k][w] = (int32_t)r;
+    }
+}
+
+// da[c] = sum over the AL blocks of da_part[b, c]: block q sums a fixed
+// slice of the partial rows, the last block to finish sums the slices in
+// order.
+__global__ void __launch_bounds__(256) k_gatv2_bwd_da(const float *__restrict__ part, int64_t n_part, int32_t HD,
+                                                      float *__restrict__ part2, int32_t *__restrict__ ticket,
+                                                      float *__restrict__ da) {
+    const int c = threadIdx.x;
+    const int64_t r0 = (int64_t)blockIdx.x * n_part / gridDim.x;
+    const int64_t r1 = (int64_t)(blockIdx.x + 1) * n_part / gridDim.x;
+    if (c < HD) {
+        float s = 0.f;
+        for (int64_t r = r0; r < r1; ++r) s += __ldg(part + r * HD + c);
+        __stcg(part2 + (int64_t)blockIdx.x * HD + c, s);
+    }
+    __threadfence();
+    __syncthreads();
+    __shared__ int last;
+    if (threadIdx.x == 0) last = atomicAdd(ticket, 1) == (int)gridDim.x - 1;
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    if (c < HD) {
+        float t = 0.f;
+        for (int q = 0; q < (int)gridDim.x; ++q) t += __ldcg(part2 + (int64_t)q * HD + c);
+        da[c] = t;
+    }
+    if (threadIdx.x == 0) *ticket = 0;
+}
+
+struct GatBwdWs {
+    float *G, *slots, *da_part, *da_part2;
+    int32_t *run_rows, *run_rows_t, *tickets, *da_ticket;
+    size_t bytes;
+};
+
+GatBwdWs gat_bwd_layout(const gnn_csr *g, int32_t heads, int32_t HD, void *base) {
+    const int64_t nr = n_runs(g->nnz, (int32_t)kGatE);
+    const int64_t blocks = (nr + kGatWarps - 1) / kGatWarps;
+    GatBwdWs W{};
+    char *b = static_cast<char *>(base);
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        char *q = b ? b + o : nullptr;
+        o = round_up(o + bytes, 256);
+        return q;
+    };
+    W.G = reinterpret_cast<float *>(take(sizeof(float) * (size_t)std::max<int64_t>((int64_t)g->n_rows * heads, 1)));
+    W.slots = reinterpret_cast<float *>(take(sizeof(float) * (size_t)(2 * nr) * HD));
+    W.da_part = reinterpret_cast<float *>(take(sizeof(float) * (size_t)blocks * HD));
+    W.da_part2 = reinterpret_cast<float *>(take(sizeof(float) * (size_t)kDaBlocks * HD));
+    W.run_rows = reinterpret_cast<int32_t *>(take(sizeof(int32_t) * (size_t)(nr + 1)));
+    W.run_rows_t = reinterpret_cast<int32_t *>(take(sizeof(int32_t) * (size_t)(nr + 1)));
+    W.tickets = reinterpret_cast<int32_t *>(take(sizeof(int32_t) * (size_t)nr));
+    W.da_ticket = reinterpret_cast<int32_t *>(take(sizeof(int32_t)));
+    W.bytes = o;
+    return W;
+}
+
+template <typename T, int NC>
+void launch_gatv2_bwd(const GatBwdArgs &al, const GatBwdArgs &r, const GatBwdWs &W, float *da, cudaStream_t s) {
+    const int blocks = (int)((al.n_runs + kGatWarps - 1) / kGatWarps);
+    const int64_t nt = std::max<int64_t>((int64_t)al.n + 1, al.n_runs);
+    k_gatv2_bwd_runs<<<(unsigned)((nt + 255) / 256), 256, 0, s>>>(al.rowptr, r.rowptr, al.n, al.n_runs, W.run_rows,
+                                                                   W.run_rows_t, W.tickets, W.da_ticket);
+    k_gatv2_bwd<GAT_AL, T, NC><<<blocks, kGatWarps * 32, 0, s>>>(al);
+    k_gatv2_bwd<GAT_R, T, NC><<<blocks, kGatWarps * 32, 0, s>>>(r);
+    k_gatv2_bwd_da<<<kDaBlocks, 256, 0, s>>>(W.da_part, blocks, al.HD, W.da_part2, W.da_ticket, da);
+}
+
 template <int NC>
 void launch_gt_bwd(GtBwdArgs q, GtBwdArgs kv, cudaStream_t s) {
     const int blocks = (int)(((int64_t)q.n * 32 + 255) / 256);
@@ -205,6 +574,11 @@ void launch_gt_bwd(GtBwdArgs q, GtBwdArgs kv, cudaStream_t s) {
 
 size_t gt_bwd_workspace_bytes(const gnn_csr *g, int32_t heads) {
     return round_up(sizeof(float) * (size_t)std::max<int64_t>((int64_t)g->n_rows * heads, 1), 256);
+}
+
+size_t gatv2_bwd_workspace_bytes(const gnn_csr *g, int32_t heads, int32_t head_dim) {
+    if (heads <= 0 || head_dim <= 0) return 0;
+    return gat_bwd_layout(g, heads, heads * head_dim, nullptr).bytes;
 }
 
 }  // namespace gnn
@@ -260,6 +634,76 @@ extern "C" gnn_status gnn_gt_attn_bwd(const gnn_csr *g, const gnn_csr *gt, const
     if (NC == 4) launch_gt_bwd<4>(q, kv, s);
     else launch_gt_bwd<8>(q, kv, s);
     note_launch(2);
+    GNN_LAUNCH_CHECK();
+    return GNN_OK;
+}
+
+extern "C" gnn_status gnn_gatv2_attn_bwd(const gnn_csr *g, const gnn_csr *gt, const void *Cl, const void *Cr,
+                                        int32_t dtype, const float *a, int32_t heads, int32_t head_dim,
+                                        float neg_slope, const float *out, const float *lse, const float *dout,
+                                        float *dl, float *dr, float *da, void *ws, size_t ws_bytes,
+                                        void *stream) {
+    gnn_status st = check_csr_args(g);
+    if (st != GNN_OK) return st;
+    st = check_csr_args(gt);
+    if (st != GNN_OK) return st;
+    if (g->n_rows != g->n_cols || gt->n_rows != g->n_cols || gt->n_cols != g->n_rows || gt->nnz != g->nnz)
+        return GNN_ERR_INVALID_ARG;
+    if (dtype != GNN_F32 && dtype != GNN_BF16) return GNN_ERR_UNSUPPORTED;
+    if (heads <= 0 || head_dim <= 0) return GNN_ERR_INVALID_ARG;
+    const int32_t HD = heads * head_dim;
+    if (HD != 32 && HD != 64 && HD != 128 && HD != 256) return GNN_ERR_UNSUPPORTED;
+    const int NC = HD / 32;
+    const int lph = head_dim / NC;
+    if (head_dim % NC || lph < 1 || (lph & (lph - 1))) return GNN_ERR_UNSUPPORTED;
+    if (!Cl || !Cr || !a || !out || !lse || !dout || !dl || !dr || !da) return GNN_ERR_INVALID_ARG;
+    if (!aligned16(Cl) || !aligned16(Cr) || !aligned16(a) || !aligned16(out) || !aligned16(dout) ||
+        !aligned16(dl) || !aligned16(dr))
+        return GNN_ERR_INVALID_ARG;
+    if (!ws || ws_bytes < gatv2_bwd_workspace_bytes(g, heads, head_dim)) return GNN_ERR_WORKSPACE;
+    if (g->n_rows == 0) {
+        cudaStream_t s = as_stream(stream);
+        if (cudaMemsetAsync(da, 0, sizeof(float) * (size_t)HD, s) != cudaSuccess) return GNN_ERR_CUDA;
+        return GNN_OK;
+    }
+    const GatBwdWs W = gat_bwd_layout(g, heads, HD, ws);
+    GatBwdArgs al{};
+    al.rowptr = g->rowptr;
+    al.colidx = g->colidx;
+    al.run_rows = W.run_rows;
+    al.Cl = Cl;
+    al.Cr = Cr;
+    al.a = a;
+    al.O = out;
+    al.lse = lse;
+    al.dO = dout;
+    al.G = W.G;
+    al.grad = dl;
+    al.slots = W.slots;
+    al.tickets = W.tickets;
+    al.da_part = W.da_part;
+    al.nnz = g->nnz;
+    al.n_runs = n_runs(g->nnz, (int32_t)kGatE);
+    al.n = g->n_rows;
+    al.heads = heads;
+    al.D = head_dim;
+    al.HD = HD;
+    al.slope = neg_slope;
+    GatBwdArgs r = al;
+    r.rowptr = gt->rowptr;
+    r.colidx = gt->colidx;
+    r.run_rows = W.run_rows_t;
+    r.grad = dr;
+    r.da_part = nullptr;
+    cudaStream_t s = as_stream(stream);
+    const bool bf = dtype == GNN_BF16;
+    switch (NC) {
+        case 1: bf ? launch_gatv2_bwd<__nv_bfloat16, 1>(al, r, W, da, s) : launch_gatv2_bwd<float, 1>(al, r, W, da, s); break;
+        case 2: bf ? launch_gatv2_bwd<__nv_bfloat16, 2>(al, r, W, da, s) : launch_gatv2_bwd<float, 2>(al, r, W, da, s); break;
+        case 4: bf ? launch_gatv2_bwd<__nv_bfloat16, 4>(al, r, W, da, s) : launch_gatv2_bwd<float, 4>(al, r, W, da, s); break;
+        default: bf ? launch_gatv2_bwd<__nv_bfloat16, 8>(al, r, W, da, s) : launch_gatv2_bwd<float, 8>(al, r, W, da, s); break;
+    }
+    note_launch(4);
     GNN_LAUNCH_CHECK();
     return GNN_OK;
 }

@@ -9,6 +9,13 @@ row-wise form.
 Tolerances (row-wise relative): fp32 sum, mean, SpMM and attention 1e-4;
 bf16-input paths with fp32 accumulation 2e-2; max/argmax, indexing,
 permutation and build outputs bit-exact.
+
+Gradients whose terms cancel (the attention backward: the score gradients
+of a row sum to zero) are compared per element against the magnitude of
+the terms they sum, the scale a floating-point sum's error is bounded by:
+    |g - r| <= tol * S,   S = sum over the terms of |term|
+(assert_terms_close).  A row whose terms cancel can be far smaller than
+its terms, so its row-wise relative error says nothing about the kernel.
 """
 import numpy as np
 
@@ -58,3 +65,22 @@ def assert_lse_close(got, ref, tol, what="lse"):
         i = np.unravel_index(int(np.argmax(d)), d.shape)
         raise AssertionError(f"{what}: {i} got {got[i]} ref {ref[i]}")
     return float(np.max(d, initial=0.0))
+
+
+def assert_terms_close(got, ref, scale, tol, what=""):
+    """|got - ref| <= tol * scale element by element, scale the summed
+    magnitude of each element's terms (an element without terms must match
+    to 1e-12)."""
+    got = np.asarray(got, np.float64).reshape(-1)
+    ref = np.asarray(ref, np.float64).reshape(-1)
+    scale = np.asarray(scale, np.float64).reshape(-1)
+    if not (got.shape == ref.shape == scale.shape):
+        raise AssertionError(f"{what}: shapes {got.shape} {ref.shape} {scale.shape}")
+    diff = np.abs(got - ref)
+    diff = np.where(np.isnan(diff), np.inf, diff)
+    ratio = diff / (tol * scale + 1e-12)
+    if ratio.size and np.max(ratio) > 1.0:
+        k = int(np.argmax(ratio))
+        raise AssertionError(f"{what}: element {k} error {diff[k]:.3e} > {tol:g} x terms "
+                             f"{scale[k]:.3e} ({int(np.sum(ratio > 1))} elements)")
+    return float(np.max(diff / np.maximum(scale, 1e-300), initial=0.0))
