@@ -367,8 +367,8 @@ gnn_status gnn_gt_attn_bwd(const gnn_csr *g, const gnn_csr *gt, const void *Q, c
  * [heads, head_dim]; out, lse from gnn_gatv2_fwd; dout fp32; dl, dr fp32
  * [n, heads*head_dim] and da fp32 [heads*head_dim], overwritten.  g square,
  * gt its transpose (gnn_csr_transpose).  heads*head_dim in {32, 64, 128,
- * 256} with head_dim a power-of-two multiple of heads*head_dim/32 (else
- * GNN_ERR_UNSUPPORTED).  Rows are worked in runs of 256 edges with heavy
+ * 256}; with c = heads*head_dim/32 channels per lane, head_dim must be a
+ * power-of-two multiple of c (else GNN_ERR_UNSUPPORTED).  Rows are worked in runs of 256 edges with heavy
  * rows cut and their pieces summed in edge order: deterministic.  Workspace
  * gnn_workspace_size(GNN_OP_GATV2_BACKWARD, g, 0, heads, head_dim), any
  * contents (the call clears what it needs).  Asynchronous. */

@@ -297,9 +297,9 @@ struct GatRow {
 };
 
 template <int SIDE, typename T, int NC>
-__device__ __forceinline__ void gat_load_row(const GatBwdArgs &p, int32_t r, int lane, int hd, int lph,
+__device__ __forceinline__ void gat_load_row(const GatBwdArgs &p, int32_t r, int ch, int hd, int lph,
                                              bool nonempty, GatRow<SIDE, NC> &R) {
-    const int64_t ro = (int64_t)r * p.HD + lane * NC;
+    const int64_t ro = (int64_t)r * p.HD + ch;
     if constexpr (SIDE == GAT_AL) {
         ld_row<T, NC>(p.Cl, ro, R.own);
         float o[NC];
@@ -315,54 +315,126 @@ __device__ __forceinline__ void gat_load_row(const GatBwdArgs &p, int32_t r, int
     }
 }
 
+// NC channels of a feature row as loaded (fp32, or bf16 words kept packed
+// until use, so a load issued for the next edge is not waited on now).
+template <typename T, int NC>
+struct Raw {
+    float f[NC];
+    __device__ __forceinline__ void load(const void *base, int64_t off) {
+        ld_row<float, NC>(base, off, f);
+    }
+    __device__ __forceinline__ void unpack(float *o) const {
+#pragma unroll
+        for (int c = 0; c < NC; ++c) o[c] = f[c];
+    }
+};
+
+template <int NC>
+struct Raw<__nv_bfloat16, NC> {
+    uint32_t w[(NC + 1) / 2];
+    __device__ __forceinline__ void load(const void *base, int64_t off) {
+        const __nv_bfloat16 *p = static_cast<const __nv_bfloat16 *>(base) + off;
+        if constexpr (NC == 1) {
+            w[0] = __ldg(reinterpret_cast<const unsigned short *>(p));
+        } else if constexpr (NC == 2) {
+            w[0] = __ldg(reinterpret_cast<const unsigned int *>(p));
+        } else if constexpr (NC == 4) {
+            const uint2 v = __ldg(reinterpret_cast<const uint2 *>(p));
+            w[0] = v.x; w[1] = v.y;
+        } else {
+#pragma unroll
+            for (int c = 0; c < NC / 8; ++c) {
+                const uint4 v = ldg16(p + 8 * c);
+                w[4 * c] = v.x; w[4 * c + 1] = v.y; w[4 * c + 2] = v.z; w[4 * c + 3] = v.w;
+            }
+        }
+    }
+    __device__ __forceinline__ void unpack(float *o) const {
+        if constexpr (NC == 1) {
+            o[0] = bf16lo(w[0]);
+        } else {
+#pragma unroll
+            for (int c = 0; c < NC / 2; ++c) { o[2 * c] = bf16lo(w[c]); o[2 * c + 1] = bf16hi(w[c]); }
+        }
+    }
+};
+
+// What one edge gathers: AL the neighbour's r_j; R the destination's l_i,
+// dO_i, logsumexp and G.
+template <int SIDE, typename T, int NC>
+struct EdgeData {
+    Raw<T, NC> v;
+    Raw<float, NC> g;
+    float L, G;
+    __device__ __forceinline__ void load(const GatBwdArgs &p, int32_t k, int ch, int hd) {
+        const int64_t ko = (int64_t)k * p.HD + ch;
+        if constexpr (SIDE == GAT_AL) {
+            v.load(p.Cr, ko);
+        } else {
+            v.load(p.Cl, ko);
+            g.load(p.dO, ko);
+            L = __ldg(p.lse + (int64_t)k * p.heads + hd);
+            G = __ldg(p.G + (int64_t)k * p.heads + hd);
+        }
+    }
+};
+
 // Gradient contributions of the edges [eb, ee) of one row into acc (dl_i or
-// dr_j) and, on the AL side, ga (attention vector).
+// dr_j) and, on the AL side, ga (attention vector).  The gathers run one
+// edge ahead of the arithmetic.
 template <int SIDE, typename T, int NC>
 __device__ __forceinline__ void gat_edges(const GatBwdArgs &p, const GatRow<SIDE, NC> &R, const float *av,
-                                          int lane, int hd, int lph, int32_t eb, int32_t ee, float *acc,
-                                          float *ga) {
-    for (int32_t cb = eb; cb < ee; cb += 32) {
-        const int32_t cn = cb + lane < ee ? __ldg(p.colidx + cb + lane) : 0;
-        const int m = min(32, ee - cb);
-        for (int u = 0; u < m; ++u) {
-            const int32_t k = __shfl_sync(0xffffffffu, cn, u);
-            const int64_t ko = (int64_t)k * p.HD + lane * NC;
-            float x[NC], rr[NC], gg[NC];
-            float L, G;
+                                          int lane, int ch, int hd, int lph, int32_t eb, int32_t ee,
+                                          float *acc, float *ga) {
+    if (eb >= ee) return;
+    int32_t base = eb;
+    int32_t cn = base + lane < ee ? __ldg(p.colidx + base + lane) : 0;
+    EdgeData<SIDE, T, NC> nxt;
+    nxt.load(p, __shfl_sync(0xffffffffu, cn, 0), ch, hd);
+    for (int32_t e = eb; e < ee; ++e) {
+        const EdgeData<SIDE, T, NC> cur = nxt;
+        if (e + 1 < ee) {
+            if (e + 1 - base == 32) {
+                base = e + 1;
+                cn = base + lane < ee ? __ldg(p.colidx + base + lane) : 0;
+            }
+            nxt.load(p, __shfl_sync(0xffffffffu, cn, e + 1 - base), ch, hd);
+        }
+        float x[NC], rr[NC], gg[NC];
+        float L, G;
+        if constexpr (SIDE == GAT_AL) {
+            cur.v.unpack(rr);                    // r_j of neighbour j
+#pragma unroll
+            for (int c = 0; c < NC; ++c) { x[c] = R.own[c] + rr[c]; gg[c] = R.g[c]; }
+            L = R.L;
+            G = R.G;
+        } else {
+            float lk[NC];
+            cur.v.unpack(lk);                    // l_i of destination i
+            cur.g.unpack(gg);                    // dO_i
+            L = cur.L;
+            G = cur.G;
+#pragma unroll
+            for (int c = 0; c < NC; ++c) { rr[c] = R.own[c]; x[c] = lk[c] + rr[c]; }
+        }
+        float ev = 0.f, pr = 0.f;
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+            ev = fmaf(av[c], x[c] > 0.f ? x[c] : p.slope * x[c], ev);
+            pr = fmaf(gg[c], rr[c], pr);
+        }
+        ev = head_sum(ev, lph);
+        pr = head_sum(pr, lph);
+        const float al = __expf(ev - L);
+        const float de = al * (pr - G);
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+            const float d1 = x[c] > 0.f ? 1.f : p.slope;
             if constexpr (SIDE == GAT_AL) {
-                ld_row<T, NC>(p.Cr, ko, rr);     // r_j of neighbour j
-#pragma unroll
-                for (int c = 0; c < NC; ++c) { x[c] = R.own[c] + rr[c]; gg[c] = R.g[c]; }
-                L = R.L;
-                G = R.G;
+                acc[c] = fmaf(de * d1, av[c], acc[c]);
+                ga[c] = fmaf(de, d1 * x[c], ga[c]);
             } else {
-                float lk[NC];
-                ld_row<T, NC>(p.Cl, ko, lk);     // l_i of destination i
-                ld_row<float, NC>(p.dO, ko, gg);
-                L = __ldg(p.lse + (int64_t)k * p.heads + hd);
-                G = __ldg(p.G + (int64_t)k * p.heads + hd);
-#pragma unroll
-                for (int c = 0; c < NC; ++c) { rr[c] = R.own[c]; x[c] = lk[c] + rr[c]; }
-            }
-            float e = 0.f, pr = 0.f;
-#pragma unroll
-            for (int c = 0; c < NC; ++c) {
-                e = fmaf(av[c], x[c] > 0.f ? x[c] : p.slope * x[c], e);
-                pr = fmaf(gg[c], rr[c], pr);
-            }
-            e = head_sum(e, lph);
-            pr = head_sum(pr, lph);
-            const float al = __expf(e - L);
-            const float de = al * (pr - G);
-#pragma unroll
-            for (int c = 0; c < NC; ++c) {
-                const float d1 = x[c] > 0.f ? 1.f : p.slope;
-                if constexpr (SIDE == GAT_AL) {
-                    acc[c] = fmaf(de * d1, av[c], acc[c]);
-                    ga[c] = fmaf(de, d1 * x[c], ga[c]);
-                } else {
-                    acc[c] = fmaf(al, gg[c], fmaf(de * d1, av[c], acc[c]));
-                }
+                acc[c] = fmaf(al, gg[c], fmaf(de * d1, av[c], acc[c]));
             }
         }
     }
@@ -371,15 +443,16 @@ __device__ __forceinline__ void gat_edges(const GatBwdArgs &p, const GatRow<SIDE
 // A piece of heavy row r leaves acc in its slot; the last of the row's
 // pieces to arrive sums them in edge order and writes the gradient row.
 template <int NC>
-__device__ __forceinline__ void gat_flush_piece(const GatBwdArgs &p, int64_t w, int32_t r, int lane,
+__device__ __forceinline__ void gat_flush_piece(const GatBwdArgs &p, int64_t w, int32_t r, int lane, int ch,
                                                 const float *acc) {
     const int32_t rb = __ldg(p.rowptr + r), re = __ldg(p.rowptr + r + 1);
     const int64_t wa = rb / kGatE, wb = ((int64_t)re - 1) / kGatE;
-    st_row_cg<NC>(p.slots + (2 * w + (w == wa ? 1 : 0)) * p.HD + lane * NC, acc);
+    int32_t *ticket = p.tickets + blockIdx.y * p.n_runs + wa;  // one ticket set per channel group
+    st_row_cg<NC>(p.slots + (2 * w + (w == wa ? 1 : 0)) * p.HD + ch, acc);
     __threadfence();
     __syncwarp();
     int t = 0;
-    if (lane == 0) t = atomicAdd(p.tickets + wa, 1);
+    if (lane == 0) t = atomicAdd(ticket, 1);
     t = __shfl_sync(0xffffffffu, t, 0);
     if (t != (int)(wb - wa)) return;
     __threadfence();
@@ -387,23 +460,29 @@ __device__ __forceinline__ void gat_flush_piece(const GatBwdArgs &p, int64_t w, 
 #pragma unroll
     for (int c = 0; c < NC; ++c) sum[c] = 0.f;
     for (int64_t k = wa; k <= wb; ++k) {
-        const float *sk = p.slots + (2 * k + (k == wa ? 1 : 0)) * p.HD + lane * NC;
+        const float *sk = p.slots + (2 * k + (k == wa ? 1 : 0)) * p.HD + ch;
 #pragma unroll
         for (int c = 0; c < NC; ++c) sum[c] += __ldcg(sk + c);
     }
-    st_row<NC>(p.grad + (int64_t)r * p.HD + lane * NC, sum);
+    st_row<NC>(p.grad + (int64_t)r * p.HD + ch, sum);
     __syncwarp();
-    if (lane == 0) p.tickets[wa] = 0;
+    if (lane == 0) *ticket = 0;
 }
 
+// Three resident blocks per SM (80 registers a thread): 9.3 ms for the
+// whole backward on R-MAT scale 20 (4 heads x 64, bf16) against 11.4 ms at
+// the compiler's 94 registers; the edge loop waits on gathers, so resident
+// warps matter more than the few values spilled.
+constexpr int kGatMinBlocks = 3;
 template <int SIDE, typename T, int NC>
-__global__ void __launch_bounds__(kGatWarps * 32) k_gatv2_bwd(GatBwdArgs p) {
+__global__ void __launch_bounds__(kGatWarps * 32, kGatMinBlocks) k_gatv2_bwd(GatBwdArgs p) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t w = (int64_t)blockIdx.x * kGatWarps + warp;
     const int lph = p.D / NC;
-    const int hd = (lane * NC) / p.D;
+    const int ch = (int)blockIdx.y * 32 * NC + lane * NC;  // this lane's first channel
+    const int hd = ch / p.D;
     float av[NC], ga[NC];
-    ld_row<float, NC>(p.a, lane * NC, av);
+    ld_row<float, NC>(p.a, ch, av);
 #pragma unroll
     for (int c = 0; c < NC; ++c) ga[c] = 0.f;
     if (w < p.n_runs) {
@@ -414,13 +493,13 @@ __global__ void __launch_bounds__(kGatWarps * 32) k_gatv2_bwd(GatBwdArgs p) {
             const int32_t lo_beg = __ldg(p.rowptr + lo);
             if (lo_beg > e0 && lo_beg - __ldg(p.rowptr + lo - 1) > kGatE) {
                 GatRow<SIDE, NC> R;
-                gat_load_row<SIDE, T, NC>(p, lo - 1, lane, hd, lph, true, R);
+                gat_load_row<SIDE, T, NC>(p, lo - 1, ch, hd, lph, true, R);
                 float acc[NC];
 #pragma unroll
                 for (int c = 0; c < NC; ++c) acc[c] = 0.f;
-                gat_edges<SIDE, T, NC>(p, R, av, lane, hd, lph, (int32_t)e0, (int32_t)min((int64_t)lo_beg, e1),
-                                       acc, ga);
-                gat_flush_piece<NC>(p, w, lo - 1, lane, acc);
+                gat_edges<SIDE, T, NC>(p, R, av, lane, ch, hd, lph, (int32_t)e0,
+                                       (int32_t)min((int64_t)lo_beg, e1), acc, ga);
+                gat_flush_piece<NC>(p, w, lo - 1, lane, ch, acc);
             }
         }
         // owned rows, bounds read 32 at a time
@@ -436,7 +515,7 @@ __global__ void __launch_bounds__(kGatWarps * 32) k_gatv2_bwd(GatBwdArgs p) {
                 const int32_t r = rbase + k;
                 const int32_t rb = __shfl_sync(0xffffffffu, my_b, k), re = __shfl_sync(0xffffffffu, my_e, k);
                 GatRow<SIDE, NC> R;
-                gat_load_row<SIDE, T, NC>(p, r, lane, hd, lph, re > rb, R);
+                gat_load_row<SIDE, T, NC>(p, r, ch, hd, lph, re > rb, R);
                 if constexpr (SIDE == GAT_AL) {
                     if (lane % lph == 0) p.G[(int64_t)r * p.heads + hd] = R.G;
                 }
@@ -444,26 +523,27 @@ __global__ void __launch_bounds__(kGatWarps * 32) k_gatv2_bwd(GatBwdArgs p) {
 #pragma unroll
                 for (int c = 0; c < NC; ++c) acc[c] = 0.f;
                 if (re - rb > kGatE) {  // heavy: its first piece (the last owned row)
-                    gat_edges<SIDE, T, NC>(p, R, av, lane, hd, lph, rb, (int32_t)e1, acc, ga);
-                    gat_flush_piece<NC>(p, w, r, lane, acc);
+                    gat_edges<SIDE, T, NC>(p, R, av, lane, ch, hd, lph, rb, (int32_t)e1, acc, ga);
+                    gat_flush_piece<NC>(p, w, r, lane, ch, acc);
                 } else {
-                    gat_edges<SIDE, T, NC>(p, R, av, lane, hd, lph, rb, re, acc, ga);
-                    st_row<NC>(p.grad + (int64_t)r * p.HD + lane * NC, acc);
+                    gat_edges<SIDE, T, NC>(p, R, av, lane, ch, hd, lph, rb, re, acc, ga);
+                    st_row<NC>(p.grad + (int64_t)r * p.HD + ch, acc);
                 }
             }
         }
     }
     if constexpr (SIDE == GAT_AL) {
-        // per-block sum of the warps' attention-vector gradients, in warp order
-        __shared__ float sga[kGatWarps][256];
+        // per-block sum of the warps' attention-vector gradients over this
+        // block's channel group, in warp order
+        __shared__ float sga[kGatWarps][32 * NC];
 #pragma unroll
         for (int c = 0; c < NC; ++c) sga[warp][lane * NC + c] = ga[c];
         __syncthreads();
-        for (int c = threadIdx.x; c < p.HD; c += blockDim.x) {
+        for (int c = threadIdx.x; c < 32 * NC; c += blockDim.x) {
             float t = 0.f;
 #pragma unroll
             for (int k = 0; k < kGatWarps; ++k) t += sga[k][c];
-            p.da_part[(int64_t)blockIdx.x * p.HD + c] = t;
+            p.da_part[(int64_t)blockIdx.x * p.HD + blockIdx.y * 32 * NC + c] = t;
         }
     }
 }
@@ -472,13 +552,13 @@ __global__ void __launch_bounds__(kGatWarps * 32) k_gatv2_bwd(GatBwdArgs p) {
 // CSR (run_rows) and of CSR^T (run_rows_t); run_rows[n_runs] = n.  Thread r
 // (0 <= r <= n) covers the runs whose start lies in (rowptr[r-1], rowptr[r]];
 // r = n takes the runs that start inside the last row (no row begins there).
-// Also clears the tickets (thread r < n_runs) and the reduction ticket.
+// Also clears the tickets (every channel group's) and the reduction ticket.
 __global__ void k_gatv2_bwd_runs(const int32_t *__restrict__ rowptr, const int32_t *__restrict__ rowptr_t,
                                  int32_t n, int64_t n_runs, int32_t *__restrict__ run_rows,
                                  int32_t *__restrict__ run_rows_t, int32_t *__restrict__ tickets,
-                                 int32_t *__restrict__ da_ticket) {
+                                 int64_t n_tickets, int32_t *__restrict__ da_ticket) {
     const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (r < n_runs) tickets[r] = 0;
+    for (int64_t t = r; t < n_tickets; t += (int64_t)gridDim.x * blockDim.x) tickets[t] = 0;
     if (r == 0) *da_ticket = 0;
     if (r > n) return;
     if (r == n) {
@@ -529,6 +609,15 @@ struct GatBwdWs {
     size_t bytes;
 };
 
+// Channels per lane: a warp covers 32 NC channels, one channel group (grid
+// y).  Rows of up to 256 channels are one group: splitting a 256-channel row
+// over two warps of 4 channels a lane was slower on R-MAT scale 20 (4 heads
+// x 64: 11.6 ms at the best occupancy against 9.3 ms), since every edge then
+// costs each warp its index, score reductions and exponential again.
+constexpr int kGatMaxNC = 8;
+inline int gat_nc(int32_t HD) { return std::min(HD / 32, kGatMaxNC); }
+inline int gat_groups(int32_t HD) { return HD / (32 * gat_nc(HD)); }
+
 GatBwdWs gat_bwd_layout(const gnn_csr *g, int32_t heads, int32_t HD, void *base) {
     const int64_t nr = n_runs(g->nnz, (int32_t)kGatE);
     const int64_t blocks = (nr + kGatWarps - 1) / kGatWarps;
@@ -546,7 +635,7 @@ GatBwdWs gat_bwd_layout(const gnn_csr *g, int32_t heads, int32_t HD, void *base)
     W.da_part2 = reinterpret_cast<float *>(take(sizeof(float) * (size_t)kDaBlocks * HD));
     W.run_rows = reinterpret_cast<int32_t *>(take(sizeof(int32_t) * (size_t)(nr + 1)));
     W.run_rows_t = reinterpret_cast<int32_t *>(take(sizeof(int32_t) * (size_t)(nr + 1)));
-    W.tickets = reinterpret_cast<int32_t *>(take(sizeof(int32_t) * (size_t)nr));
+    W.tickets = reinterpret_cast<int32_t *>(take(sizeof(int32_t) * (size_t)nr * gat_groups(HD)));
     W.da_ticket = reinterpret_cast<int32_t *>(take(sizeof(int32_t)));
     W.bytes = o;
     return W;
@@ -555,11 +644,13 @@ GatBwdWs gat_bwd_layout(const gnn_csr *g, int32_t heads, int32_t HD, void *base)
 template <typename T, int NC>
 void launch_gatv2_bwd(const GatBwdArgs &al, const GatBwdArgs &r, const GatBwdWs &W, float *da, cudaStream_t s) {
     const int blocks = (int)((al.n_runs + kGatWarps - 1) / kGatWarps);
-    const int64_t nt = std::max<int64_t>((int64_t)al.n + 1, al.n_runs);
+    const dim3 grid(blocks, gat_groups(al.HD));
+    const int64_t nt = (int64_t)al.n + 1;
     k_gatv2_bwd_runs<<<(unsigned)((nt + 255) / 256), 256, 0, s>>>(al.rowptr, r.rowptr, al.n, al.n_runs, W.run_rows,
-                                                                   W.run_rows_t, W.tickets, W.da_ticket);
-    k_gatv2_bwd<GAT_AL, T, NC><<<blocks, kGatWarps * 32, 0, s>>>(al);
-    k_gatv2_bwd<GAT_R, T, NC><<<blocks, kGatWarps * 32, 0, s>>>(r);
+                                                                   W.run_rows_t, W.tickets,
+                                                                   al.n_runs * gat_groups(al.HD), W.da_ticket);
+    k_gatv2_bwd<GAT_AL, T, NC><<<grid, kGatWarps * 32, 0, s>>>(al);
+    k_gatv2_bwd<GAT_R, T, NC><<<grid, kGatWarps * 32, 0, s>>>(r);
     k_gatv2_bwd_da<<<kDaBlocks, 256, 0, s>>>(W.da_part, blocks, al.HD, W.da_part2, W.da_ticket, da);
 }
 
@@ -653,9 +744,10 @@ extern "C" gnn_status gnn_gatv2_attn_bwd(const gnn_csr *g, const gnn_csr *gt, co
     if (heads <= 0 || head_dim <= 0) return GNN_ERR_INVALID_ARG;
     const int32_t HD = heads * head_dim;
     if (HD != 32 && HD != 64 && HD != 128 && HD != 256) return GNN_ERR_UNSUPPORTED;
-    const int NC = HD / 32;
+    const int NC = gat_nc(HD);
     const int lph = head_dim / NC;
-    if (head_dim % NC || lph < 1 || (lph & (lph - 1))) return GNN_ERR_UNSUPPORTED;
+    // a head lies within one warp's channel group, on a power of two of lanes
+    if (head_dim % NC || (32 * NC) % head_dim || (lph & (lph - 1))) return GNN_ERR_UNSUPPORTED;
     if (!Cl || !Cr || !a || !out || !lse || !dout || !dl || !dr || !da) return GNN_ERR_INVALID_ARG;
     if (!aligned16(Cl) || !aligned16(Cr) || !aligned16(a) || !aligned16(out) || !aligned16(dout) ||
         !aligned16(dl) || !aligned16(dr))
