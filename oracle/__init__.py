@@ -56,6 +56,7 @@ def _load():
             lib.orc_csr_transpose.argtypes = [i32, i32, _VP, _VP, _VP, _VP, _VP, _VP]
             lib.orc_gt_backward.argtypes = [i32, _VP, _VP, _VP, _VP, _VP, ctypes.c_int, i32, i32, dbl,
                                             _VP, _VP, _VP, _VP]
+            lib.orc_degree_stats.argtypes = [i32, _VP, _VP]
             lib.orc_gatv2_backward.argtypes = [i32, _VP, _VP, _VP, _VP, ctypes.c_int, _VP, i32, i32,
                                                dbl, _VP, _VP, _VP, _VP]
             lib.orc_gatv2.argtypes = [i32, _VP, _VP, _VP, ctypes.c_int, i32, _VP, _VP, _VP,
@@ -226,6 +227,14 @@ def gt_backward(rowptr, colidx, Q, K, V, heads, head_dim, scale, dO):
     _check(_load().orc_gt_backward(n, _p(rp), _p(ci), _p(Qc), _p(Kc), _p(Vc), dt, heads, head_dim,
                                    scale, _p(go), _p(dQ), _p(dK), _p(dV)), "gt_backward")
     return dQ, dK, dV
+
+
+def degree_stats(rowptr):
+    """(mean, std, skewness, max) of the row lengths, population moments."""
+    rp = np.ascontiguousarray(rowptr, np.int32)
+    out = np.empty(4, np.float64)
+    _check(_load().orc_degree_stats(len(rp) - 1, _p(rp), _p(out)), "degree_stats")
+    return tuple(float(x) for x in out)
 
 
 def gatv2_backward(rowptr, colidx, Cl, Cr, a, heads, head_dim, dO, slope=0.2):

@@ -54,6 +54,36 @@ int orc_degrees(int32_t n_rows, int32_t n_cols, const int32_t *rowptr,
     return ORC_OK;
 }
 
+/* Degree statistics of the row lengths d_i = rowptr[i+1] - rowptr[i] (the
+ * in-degrees), the graph statistics an adaptive choice of backend reads
+ * (IO-aware GNN layers, Section 5, degree skew; Appendix B.1, Table 5's
+ * skewness): out = {mean, standard deviation, skewness, max}, population
+ * moments from two passes: mean = sum d / n, m_k = sum (d - mean)^k / n,
+ * std = sqrt(m_2), skewness = m_3 / m_2^(3/2) (0 when m_2 = 0). */
+int orc_degree_stats(int32_t n, const int32_t *rowptr, double *out) {
+    out[0] = out[1] = out[2] = out[3] = 0.0;
+    if (n <= 0) return ORC_OK;
+    double sum = 0.0, mx = 0.0;
+    for (int32_t i = 0; i < n; ++i) {
+        double d = (double)(rowptr[i + 1] - rowptr[i]);
+        sum += d;
+        if (d > mx) mx = d;
+    }
+    double mean = sum / n, m2 = 0.0, m3 = 0.0;
+    for (int32_t i = 0; i < n; ++i) {
+        double c = (double)(rowptr[i + 1] - rowptr[i]) - mean;
+        m2 += c * c;
+        m3 += c * c * c;
+    }
+    m2 /= n;
+    m3 /= n;
+    out[0] = mean;
+    out[1] = sqrt(m2);
+    out[2] = m2 > 0.0 ? m3 / (m2 * sqrt(m2)) : 0.0;
+    out[3] = mx;
+    return ORC_OK;
+}
+
 /* ------------------------------------------------------------------ */
 /* SpMM  (IO-aware GNN layers, Section 2.2 (i); Appendix D.4)          */
 /* ------------------------------------------------------------------ */

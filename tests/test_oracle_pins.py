@@ -8,6 +8,7 @@ import numpy as np
 import pytest
 
 import oracle
+import synth
 from tests import graphs as G
 
 GOLD = os.path.join(os.path.dirname(__file__), "golden")
@@ -387,6 +388,45 @@ def test_gatv2_backward_special_cases():
         for j in ci[rp[i]:rp[i + 1]]:
             want[j] += dO[i] / deg
     assert np.allclose(dr0, want, rtol=1e-12, atol=1e-13)
+
+
+# ---------------------------------------------------------------- degree statistics
+
+def _rowptr_of(deg):
+    rp = np.zeros(len(deg) + 1, np.int32)
+    rp[1:] = np.cumsum(deg)
+    return rp
+
+
+def test_degree_stats_regular_graph():
+    """Every row of length 7: mean 7, no spread, skewness 0 by convention."""
+    assert oracle.degree_stats(_rowptr_of([7] * 50)) == (7.0, 0.0, 0.0, 7.0)
+
+
+def test_degree_stats_two_point_closed_form():
+    """One row of length k, n - 1 rows of length 1: a two-point law with
+    p = 1/n, whose skewness is (1 - 2p) / sqrt(p (1 - p)) and standard
+    deviation (k - 1) sqrt(p (1 - p))."""
+    n, k = 40, 301
+    mean, std, skew, mx = oracle.degree_stats(_rowptr_of([k] + [1] * (n - 1)))
+    p = 1.0 / n
+    assert mx == k
+    assert mean == pytest.approx(1 + (k - 1) * p, rel=1e-15)
+    assert std == pytest.approx((k - 1) * np.sqrt(p * (1 - p)), rel=1e-13)
+    assert skew == pytest.approx((1 - 2 * p) / np.sqrt(p * (1 - p)), rel=1e-13)
+
+
+def test_degree_stats_matches_scipy():
+    """Power-law row lengths (R-MAT scale 12): scipy's biased sample
+    skewness and numpy's population deviation."""
+    stats = pytest.importorskip("scipy.stats")
+    rp, _ = synth.rmat(12, 16)
+    d = np.diff(rp).astype(np.float64)
+    mean, std, skew, mx = oracle.degree_stats(rp)
+    assert mean == pytest.approx(d.mean(), rel=1e-14)
+    assert std == pytest.approx(d.std(), rel=1e-12)
+    assert skew == pytest.approx(stats.skew(d, bias=True), rel=1e-10)
+    assert mx == d.max()
 
 
 # ---------------------------------------------------------------- relabel invariance
