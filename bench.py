@@ -173,6 +173,22 @@ def _sample_by_edges(rp, target_edges, seed=0):
     return rows, int(np.sum(rp[rows + 1] - rp[rows]))
 
 
+def selector_report(torch, gnn, g, op, dtype, F=0, heads=0, head_dim=0):
+    """Graph statistics measured on the GPU (degree moments, local density)
+    and the backend the rule picks for op; the statistics pass is timed on
+    the host clock around the synchronous call (prep, not in a step)."""
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    st = gnn.gnn_graph_stats_compute(g)
+    ms = (time.perf_counter() - t0) * 1e3
+    backend, thr = gnn.gnn_select_backend(st, op, dtype, F, heads, head_dim)
+    return {"stats_ms": ms, "max_degree": st.max_degree, "mean_degree": st.mean_degree,
+            "degree_std": st.degree_std, "degree_skewness": st.degree_skewness,
+            "listed_blocks": st.n_blocks, "edges_per_block": st.edges_per_block,
+            "backend": "tiles" if backend == gnn.GNN_BACKEND_TILES else "csr",
+            "fill_threshold": thr if backend == gnn.GNN_BACKEND_TILES else None}
+
+
 def setup_c2(torch, gnn, w):
     g = gnn.graph_prepare(_dev(torch, w["rowptr"]), _dev(torch, w["colidx"]))
     X = _dev(torch, w["X"])
@@ -223,7 +239,9 @@ def setup_c2(torch, gnn, w):
                 3 * n * F * 4)
     return Workload("c2_rmat17", layers, [X], list(outs.values()) + [am], cfg, "f32",
                     oracle_step, (rows, M), extra={"min_only": min_only, "bwd_only": bwd_only,
-                                                  "transpose_only": lambda: gnn.gnn_csr_transpose(g)})
+                                                  "transpose_only": lambda: gnn.gnn_csr_transpose(g),
+                                                  "selector": selector_report(
+                                                      torch, gnn, g, gnn.GNN_OP_SPMM, gnn.GNN_F32, F)})
 
 
 def setup_c3(torch, gnn, w):
@@ -327,6 +345,7 @@ def setup_c4(torch, gnn, w, tiles=None):
            "layers": ["fused GT attention, CSR path" if bs is None else
                       f"GT attention: tcgen05 16x16 tiles (fill >= {tiles}) + CSR residual"]}
     rows = _sample_by_edges(w["rowptr"], 400000)
+    extra["selector"] = selector_report(torch, gnn, g, gnn.GNN_OP_GT, gnn.GNN_BF16, 0, heads, D)
     return Workload("c4_clustered_gt", layers, [Q, K, V], [out, lse], cfg, "bf16", oracle_step,
                     rows, extra=extra)
 
@@ -662,6 +681,8 @@ def main():
                           "bcomp_bytes": L.bcomp, "hbm_gbs": gbs, "frac_of_measured": gbs / hbm,
                           "frac_of_8tbs": gbs / NORTH_STAR_HBM_GBS, "bound": L.bound}
     extra = {}
+    if "selector" in W.extra:
+        extra["selector"] = W.extra["selector"]
     if "reorder_prep" in W.extra:
         extra["reorder_prep"] = W.extra["reorder_prep"]
     if "blocksparse" in W.extra:

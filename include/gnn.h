@@ -123,7 +123,7 @@ typedef enum {
     GNN_OP_SPMM = 0, GNN_OP_SUM = 1, GNN_OP_MEAN = 2, GNN_OP_MAX = 3,
     GNN_OP_GATV2 = 4, GNN_OP_GT = 5, GNN_OP_REORDER = 6, GNN_OP_APPLY_PERM = 7,
     GNN_OP_BLOCKSPARSE = 8, GNN_OP_MIN = 9, GNN_OP_SPMM_BLOCKSPARSE = 10, GNN_OP_TRANSPOSE = 11,
-    GNN_OP_GT_BACKWARD = 12, GNN_OP_GATV2_BACKWARD = 13
+    GNN_OP_GT_BACKWARD = 12, GNN_OP_GATV2_BACKWARD = 13, GNN_OP_GRAPH_STATS = 14
 } gnn_op;
 
 /* OR-ed into `op` of gnn_workspace_size: size the workspace for bf16 inputs
@@ -377,6 +377,44 @@ gnn_status gnn_gatv2_attn_bwd(const gnn_csr *g, const gnn_csr *gt, const void *C
                               float neg_slope, const float *out, const float *lse,
                               const float *dout, float *dl, float *dr, float *da, void *ws,
                               size_t ws_bytes, void *stream);
+
+/* ------------------------------------------- adaptive choice of backend */
+
+/* Graph statistics an adaptive runtime chooses backends from (IO-aware GNN
+ * layers, Section 5: degree skew, local density, feature size; Appendix
+ * B.1, Table 5's degree skewness).  Degrees are row lengths (in-degrees);
+ * moments are population moments: skewness = m3 / m2^(3/2), 0 when m2 = 0.
+ * n_blocks: 128 x 16 column blocks holding at least one edge (the
+ * block-sparse plan at fill 0); edges_per_block = nnz / n_blocks, the local
+ * density the tensor-core tiles depend on. */
+typedef struct {
+    int32_t n_rows;
+    int64_t nnz;
+    int32_t max_degree;
+    double mean_degree, degree_std, degree_skewness;
+    int64_t n_blocks;
+    double edges_per_block;
+} gnn_graph_stats;
+
+typedef enum { GNN_BACKEND_CSR = 0, GNN_BACKEND_TILES = 1 } gnn_backend;
+
+/* Measures *out on the GPU (one pass over rowptr, then the block-sparse
+ * plan).  Synchronous: returns with *out filled.  Deterministic.  Workspace
+ * gnn_workspace_size(GNN_OP_GRAPH_STATS, g, 0, 0, 0). */
+gnn_status gnn_graph_stats_compute(const gnn_csr *g, gnn_graph_stats *out, void *ws,
+                                   size_t ws_bytes, void *stream);
+
+/* Host rule, no GPU work: the backend for op (GNN_OP_SPMM or GNN_OP_GT;
+ * every other op has only the CSR kernels) on a graph with statistics *s,
+ * features of `dtype` and width F (SpMM) or heads x head_dim (GT).  Tiles
+ * need bf16, F % 64 == 0 (SpMM) or head_dim in {32, 64} (GT), and pay off
+ * above a local density measured on GB300: 158 edges per listed block for
+ * SpMM, 129 for GT (the tile rate in blocks/s against the CSR rate in
+ * edges/s; both scale with the feature width alike).  *fill_threshold (may
+ * be NULL) receives the threshold to build the tiles with: 0 (every edge in
+ * a tile), the fastest setting measured.  Returns a gnn_backend. */
+int32_t gnn_select_backend(const gnn_graph_stats *s, int32_t op, int32_t dtype, int32_t F,
+                           int32_t heads, int32_t head_dim, float *fill_threshold);
 
 /* --------------------------------------------------- step a8: reordering */
 

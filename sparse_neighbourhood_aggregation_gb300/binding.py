@@ -22,7 +22,8 @@ GNN_NORM_NONE, GNN_NORM_LEFT, GNN_NORM_RIGHT, GNN_NORM_BOTH = 0, 1, 2, 3
 GNN_MAP_AUTO, GNN_MAP_FEAT, GNN_MAP_NEIGH = 0, 1, 2
 (GNN_OP_SPMM, GNN_OP_SUM, GNN_OP_MEAN, GNN_OP_MAX, GNN_OP_GATV2, GNN_OP_GT, GNN_OP_REORDER,
  GNN_OP_APPLY_PERM, GNN_OP_BLOCKSPARSE, GNN_OP_MIN, GNN_OP_SPMM_BLOCKSPARSE,
- GNN_OP_TRANSPOSE, GNN_OP_GT_BACKWARD, GNN_OP_GATV2_BACKWARD) = range(14)
+ GNN_OP_TRANSPOSE, GNN_OP_GT_BACKWARD, GNN_OP_GATV2_BACKWARD, GNN_OP_GRAPH_STATS) = range(15)
+GNN_BACKEND_CSR, GNN_BACKEND_TILES = 0, 1
 GNN_PERM_IDENTITY, GNN_PERM_RANDOM, GNN_PERM_DEGREE, GNN_PERM_RCM = 0, 1, 2, 3
 
 
@@ -47,6 +48,13 @@ class gnn_blocksparse(ctypes.Structure):
                 ("grp_blk_offset", ctypes.c_void_p), ("blk_cols", ctypes.c_void_p),
                 ("blk_mask", ctypes.c_void_p), ("res_rowptr", ctypes.c_void_p),
                 ("res_colidx", ctypes.c_void_p)]
+
+
+class gnn_graph_stats(ctypes.Structure):
+    _fields_ = [("n_rows", ctypes.c_int32), ("nnz", ctypes.c_int64), ("max_degree", ctypes.c_int32),
+                ("mean_degree", ctypes.c_double), ("degree_std", ctypes.c_double),
+                ("degree_skewness", ctypes.c_double), ("n_blocks", ctypes.c_int64),
+                ("edges_per_block", ctypes.c_double)]
 
 
 _lib = None
@@ -84,12 +92,15 @@ _SIGS = {
     "gnn_reorder_perm": (ctypes.c_int, ["csr", "i32", "u64", "p", "p", "p", "sz", "p"]),
     "gnn_apply_perm": (ctypes.c_int, ["csr", "p", "p", "p", "p", "p", "i32", "i32", "p", "p", "sz",
                                       "p"]),
+    "gnn_graph_stats_compute": (ctypes.c_int, ["csr", "st", "p", "sz", "p"]),
+    "gnn_select_backend": (ctypes.c_int32, ["st", "i32", "i32", "i32", "i32", "i32", "p"]),
     "gnn_status_string": (ctypes.c_char_p, ["i32"]),
     "gnn_launch_count": (ctypes.c_uint64, []),
     "gnn_version": (ctypes.c_char_p, []),
 }
 
 _CT = {"csr": ctypes.POINTER(gnn_csr), "bs": ctypes.POINTER(gnn_blocksparse),
+       "st": ctypes.POINTER(gnn_graph_stats),
        "p": ctypes.c_void_p, "sz": ctypes.c_size_t, "i32": ctypes.c_int32,
        "i64": ctypes.c_int64, "u64": ctypes.c_uint64, "f32": ctypes.c_float}
 
@@ -411,6 +422,26 @@ def gnn_gatv2_attn_bwd(g: Graph, gt: Graph, Cl: torch.Tensor, Cr, a: torch.Tenso
         dout.data_ptr(), dl.data_ptr(), dr.data_ptr(), da.data_ptr(), ws.data_ptr(), ws.numel(),
         _stream(stream)))
     return dl, dr, da
+
+
+def gnn_graph_stats_compute(g: Graph, stream=None) -> gnn_graph_stats:
+    """Degree moments and local density of g, measured on the GPU
+    (synchronous); returns the filled gnn_graph_stats."""
+    st = gnn_graph_stats()
+    ws = g.workspace(GNN_OP_GRAPH_STATS)
+    _check("gnn_graph_stats_compute", lib().gnn_graph_stats_compute(
+        ctypes.byref(g.csr), ctypes.byref(st), ws.data_ptr(), ws.numel(), _stream(stream)))
+    return st
+
+
+def gnn_select_backend(stats: gnn_graph_stats, op: int, dtype: int, F: int = 0, heads: int = 0,
+                       head_dim: int = 0):
+    """Host rule: (GNN_BACKEND_CSR or GNN_BACKEND_TILES, fill threshold for
+    the tile build) for op GNN_OP_SPMM or GNN_OP_GT.  No GPU work."""
+    thr = ctypes.c_float(0.0)
+    b = lib().gnn_select_backend(ctypes.byref(stats), int(op), int(dtype), int(F), int(heads),
+                                 int(head_dim), ctypes.byref(thr))
+    return int(b), float(thr.value)
 
 
 def gnn_spmm_blocksparse(g: Graph, X: torch.Tensor, bs, norm: int = GNN_NORM_BOTH, out=None,

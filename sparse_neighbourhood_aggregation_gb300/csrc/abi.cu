@@ -14,6 +14,7 @@ size_t tile_spmm_workspace_bytes(const gnn_csr *g, int32_t F);
 size_t transpose_workspace_bytes(const gnn_csr *g);
 size_t gt_bwd_workspace_bytes(const gnn_csr *g, int32_t heads);
 size_t gatv2_bwd_workspace_bytes(const gnn_csr *g, int32_t heads, int32_t head_dim);
+size_t graph_stats_workspace_bytes(const gnn_csr *g);
 gnn_status check_csr_args(const gnn_csr *g);
 }  // namespace gnn
 
@@ -48,6 +49,8 @@ extern "C" size_t gnn_workspace_size(int32_t op, const gnn_csr *g, int32_t F, in
             return gt_bwd_workspace_bytes(g, heads);
         case GNN_OP_GATV2_BACKWARD:
             return gatv2_bwd_workspace_bytes(g, heads, head_dim);
+        case GNN_OP_GRAPH_STATS:
+            return graph_stats_workspace_bytes(g);
         default:
             return 0;
     }

@@ -56,3 +56,36 @@ def test_host_side_calls(lib):
     # unsupported widths: F=12 fp32 is three 16-byte chunks
     assert lib.gnn_spmm(ctypes.byref(csr), None, 0, 16, 0, 12, 16, 0, None, 0, None) == \
         b.GNN_ERR_UNSUPPORTED
+
+
+def test_select_backend_rule(lib):
+    """The backend rule is host code: no GPU.  Local density at or above the
+    measured break-even (158 edges a block for SpMM, 129 for GT) picks the
+    tiles when the inputs qualify; everything else runs on CSR."""
+    import oracle
+    import synth
+    from sparse_neighbourhood_aggregation_gb300 import binding as b
+
+    def stats(epb, nnz=1000):
+        return b.gnn_graph_stats(n_rows=100, nnz=nnz, max_degree=10, mean_degree=10.0,
+                                 degree_std=1.0, degree_skewness=0.0, n_blocks=max(1, int(nnz / epb)),
+                                 edges_per_block=epb)
+
+    sp, gt = b.GNN_OP_SPMM, b.GNN_OP_GT
+    assert b.gnn_select_backend(stats(439.0), sp, b.GNN_BF16, 256) == (b.GNN_BACKEND_TILES, 0.0)
+    assert b.gnn_select_backend(stats(158.0), sp, b.GNN_BF16, 64)[0] == b.GNN_BACKEND_TILES
+    assert b.gnn_select_backend(stats(157.9), sp, b.GNN_BF16, 64)[0] == b.GNN_BACKEND_CSR
+    assert b.gnn_select_backend(stats(439.0), sp, b.GNN_F32, 256)[0] == b.GNN_BACKEND_CSR
+    assert b.gnn_select_backend(stats(439.0), sp, b.GNN_BF16, 96)[0] == b.GNN_BACKEND_CSR
+    assert b.gnn_select_backend(stats(130.0), gt, b.GNN_BF16, 0, 8, 32)[0] == b.GNN_BACKEND_TILES
+    assert b.gnn_select_backend(stats(128.0), gt, b.GNN_BF16, 0, 8, 32)[0] == b.GNN_BACKEND_CSR
+    assert b.gnn_select_backend(stats(439.0), gt, b.GNN_BF16, 0, 2, 128)[0] == b.GNN_BACKEND_CSR
+    assert b.gnn_select_backend(stats(439.0), b.GNN_OP_MAX, b.GNN_BF16, 256)[0] == b.GNN_BACKEND_CSR
+    assert b.gnn_select_backend(stats(439.0, nnz=0), sp, b.GNN_BF16, 256)[0] == b.GNN_BACKEND_CSR
+    # on densities the oracle measures: a clustered graph qualifies, R-MAT does not
+    for (rp, ci), want in ((synth.clustered(8, 128, 0.3, 0.01, 3), b.GNN_BACKEND_TILES),
+                           (synth.rmat(12, 16), b.GNN_BACKEND_CSR)):
+        nb = oracle.blocksparse(rp, ci, 0.0)["n_blocks"]
+        s = stats(len(ci) / nb, nnz=len(ci))
+        assert b.gnn_select_backend(s, sp, b.GNN_BF16, 256)[0] == want
+        assert b.gnn_select_backend(s, gt, b.GNN_BF16, 0, 8, 32)[0] == want
