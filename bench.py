@@ -448,6 +448,23 @@ SETUPS = {"c2_rmat17": setup_c2, "c3_rmat20_gatv2": setup_c3, "c4_clustered_gt":
 
 # ---------------------------------------------------------------- main
 
+def max_over_ranks(torch, ms, world):
+    """The slowest rank's time (all_reduce MAX over the process group, on its
+    backend's device): the job is done when every rank is."""
+    if world <= 1:
+        return ms
+    dev = "cuda" if torch.distributed.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world, units_per_rank, steps, total_ms):
+    """Whole-job throughput in G units/s: each rank processed units_per_rank
+    a step for `steps` steps, and the job took the slowest rank's total_ms."""
+    return world * units_per_rank * steps / (total_ms * 1e-3) / 1e9
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -664,14 +681,10 @@ def main():
     step_ms, per = time_layers(torch, W, args.steps, flush, stream)
     launches = gnn.launch_count() - launches0
     clk = clocks.stop()
-    total_ms = float(np.sum(step_ms))
-    if world > 1:
-        t = torch.tensor([total_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(torch, float(np.sum(step_ms)), world)
     ms = total_ms / args.steps
     units = sum(L.units for L in W.layers)
-    value = world * units * args.steps / (total_ms * 1e-3) / 1e9
+    value = job_rate(world, units, args.steps, total_ms)
 
     hbm, bf16_tf, peak_kind = measured_peaks()
     layers = {}
@@ -808,8 +821,8 @@ def main():
                 oh.copy_(od, non_blocking=True)
             b.record(stream)
         torch.cuda.synchronize()
-        e2e_ms = float(np.mean([a.elapsed_time(b) for a, b in e2e_ev]))
-        e2e = {"value": world * units / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
+        e2e_ms = max_over_ranks(torch, float(np.mean([a.elapsed_time(b) for a, b in e2e_ev])), world)
+        e2e = {"value": job_rate(world, units, 1, e2e_ms), "unit": UNIT,
                "h2d_bytes_per_step": sum(x.numel() * x.element_size() for x in ins_h),
                "d2h_bytes_per_step": sum(o.numel() * o.element_size() for o in outs_h),
                "ms_per_step": e2e_ms}
