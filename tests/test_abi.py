@@ -89,3 +89,41 @@ def test_select_backend_rule(lib):
         s = stats(len(ci) / nb, nnz=len(ci))
         assert b.gnn_select_backend(s, sp, b.GNN_BF16, 256)[0] == want
         assert b.gnn_select_backend(s, gt, b.GNN_BF16, 0, 8, 32)[0] == want
+
+
+def test_backward_and_statistics_host_validation(lib):
+    """The GATv2 backward and the statistics call reject bad arguments and
+    short workspaces on the host, before any CUDA call."""
+    from sparse_neighbourhood_aggregation_gb300 import binding as b
+    sq = b.gnn_csr(1000, 1000, 5000, 16, 16, None)
+    rect = b.gnn_csr(1000, 900, 5000, 16, 16, None)
+    other = b.gnn_csr(1000, 1000, 4000, 16, 16, None)
+    P = 4096  # a 16-byte aligned stand-in for a device pointer (never dereferenced)
+
+    def bwd(g, gt, dtype=b.GNN_BF16, heads=4, D=64, a=P, dl=P, ws=P, ws_bytes=1 << 40):
+        return lib.gnn_gatv2_attn_bwd(None if g is None else ctypes.byref(g), ctypes.byref(gt), P, P,
+                                      dtype, a, heads, D, 0.2, P, P, P, dl, P, P, ws, ws_bytes, None)
+
+    assert bwd(None, sq) == b.GNN_ERR_INVALID_ARG
+    assert bwd(rect, sq) == b.GNN_ERR_INVALID_ARG          # not square
+    assert bwd(sq, other) == b.GNN_ERR_INVALID_ARG         # transpose of another graph
+    assert bwd(sq, sq, dtype=7) == b.GNN_ERR_UNSUPPORTED
+    assert bwd(sq, sq, heads=3, D=32) == b.GNN_ERR_UNSUPPORTED   # 96 channels
+    assert bwd(sq, sq, heads=64, D=4) == b.GNN_ERR_UNSUPPORTED   # 8 channels a lane, heads of 4
+    assert bwd(sq, sq, a=None) == b.GNN_ERR_INVALID_ARG
+    assert bwd(sq, sq, dl=P + 4) == b.GNN_ERR_INVALID_ARG        # dl not 16-byte aligned
+    assert bwd(sq, sq, ws_bytes=0) == b.GNN_ERR_WORKSPACE
+    need = lib.gnn_workspace_size(b.GNN_OP_GATV2_BACKWARD, ctypes.byref(sq), 0, 4, 64)
+    assert need > lib.gnn_workspace_size(b.GNN_OP_GATV2_BACKWARD, ctypes.byref(sq), 0, 1, 32) > 0
+    assert bwd(sq, sq, ws_bytes=need - 1) == b.GNN_ERR_WORKSPACE
+
+    st = b.gnn_graph_stats()
+    assert lib.gnn_graph_stats_compute(None, ctypes.byref(st), P, 1 << 40, None) == b.GNN_ERR_INVALID_ARG
+    assert lib.gnn_graph_stats_compute(ctypes.byref(sq), None, P, 1 << 40, None) == b.GNN_ERR_INVALID_ARG
+    assert lib.gnn_graph_stats_compute(ctypes.byref(sq), ctypes.byref(st), P, 0, None) == \
+        b.GNN_ERR_WORKSPACE
+    assert lib.gnn_workspace_size(b.GNN_OP_GRAPH_STATS, ctypes.byref(sq), 0, 0, 0) > 0
+    empty = b.gnn_csr(0, 0, 0, 16, None, None)
+    assert lib.gnn_graph_stats_compute(ctypes.byref(empty), ctypes.byref(st), None, 0, None) == b.GNN_OK
+    assert (st.n_rows, st.nnz, st.n_blocks, st.edges_per_block) == (0, 0, 0, 0.0)
+    assert lib.gnn_select_backend(None, b.GNN_OP_SPMM, b.GNN_BF16, 256, 0, 0, None) == b.GNN_BACKEND_CSR
