@@ -234,8 +234,8 @@ struct GatBwdArgs {
     float *G;                        // [n, heads]: AL writes, R reads
     float *grad;                     // AL: dl; R: dr  [n, HD]
     float *slots;                    // [2 n_runs, HD] partial rows of heavy-row pieces
-    int32_t *tickets;                // [n_runs], zero between calls
-    float *da_part;                  // AL: [gridDim, HD] per-block attention-vector sums
+    int32_t *tickets;                // [channel groups, n_runs], cleared at the start of a call
+    float *da_part;                  // AL: [gridDim.x, HD] per-block attention-vector sums
     int64_t nnz, n_runs;
     int32_t n, heads, D, HD;
     float slope;
