@@ -52,7 +52,7 @@ NCU_TRAFFIC = {("c2_rmat17", "spmm"): (89.525248 + 43.183872 + 13.461760) * 1e6,
                ("c2_rmat17", "sum"): (88.022784 + 39.964928 + 13.320960) * 1e6,
                ("c2_rmat17", "mean"): (87.809280 + 39.904256 + 13.320448) * 1e6,
                ("c2_rmat17", "max"): (102.362112 + 82.384384 + 5.767424 + 0.000256) * 1e6}
-NORTH_STAR_HBM_GBS = 8000.0
+NOMINAL_HBM_GBS = 8000.0
 METRIC = "aggregation Gedge*feat/s"
 UNIT = "Gedge*feat/s"
 
@@ -692,7 +692,7 @@ def main():
         gbs = L.bcomp / (per[L.name] * 1e-3) / 1e9
         layers[L.name] = {"ms": per[L.name], "gedge_feat_s": L.units / (per[L.name] * 1e-3) / 1e9,
                           "bcomp_bytes": L.bcomp, "hbm_gbs": gbs, "frac_of_measured": gbs / hbm,
-                          "frac_of_8tbs": gbs / NORTH_STAR_HBM_GBS, "bound": L.bound}
+                          "frac_of_8tbs": gbs / NOMINAL_HBM_GBS, "bound": L.bound}
     extra = {}
     if "selector" in W.extra:
         extra["selector"] = W.extra["selector"]
@@ -794,7 +794,7 @@ def main():
     achieved = dom.bcomp / (per[dom.name] * 1e-3) / 1e9
     roofline = {"bound": "hbm", "kernel": dom.name, "achieved": achieved, "peak": hbm,
                 "unit": "GB/s", "frac": achieved / hbm, "peak_kind": peak_kind,
-                "frac_of_8tbs": achieved / NORTH_STAR_HBM_GBS,
+                "frac_of_8tbs": achieved / NOMINAL_HBM_GBS,
                 "traffic": NCU_TRAFFIC.get((W.name, dom.name)),
                 "bcomp_bytes": dom.bcomp}
     if dom.bound == "alu":
