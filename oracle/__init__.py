@@ -64,6 +64,8 @@ def _load():
             lib.orc_gt.argtypes = [i32, _VP, _VP, _VP, _VP, _VP, ctypes.c_int, i32, i32, dbl,
                                    _VP, i32, _VP, _VP, _VP]
             lib.orc_blocksparse.argtypes = [i32, _VP, _VP, flt, _VP, _VP, _VP, _VP, _VP, _VP]
+            lib.orc_blocksparse_packed.argtypes = [i32, _VP, _VP, flt, ctypes.c_int, _VP, _VP, _VP,
+                                                   _VP, _VP, _VP]
             lib.orc_order_key.restype = ctypes.c_uint32
             lib.orc_order_key.argtypes = [flt]
             lib.orc_splitmix64.restype = ctypes.c_uint64
@@ -257,14 +259,20 @@ def gatv2_backward(rowptr, colidx, Cl, Cr, a, heads, head_dim, dO, slope=0.2):
     return dl, dr, da
 
 
-def blocksparse(rowptr, colidx, threshold):
+PACK_ID, PACK_COUNT = 0, 1
+
+
+def blocksparse(rowptr, colidx, threshold, packing=PACK_ID):
     """Returns dict(grp_blk_offset, blk_cols [B,16], blk_mask [B,8,4] uint64,
-    res_rowptr, res_colidx, n_tiles_kept, nnz_tiles)."""
+    res_rowptr, res_colidx, n_tiles_kept, nnz_tiles).  packing: PACK_ID
+    (columns by ascending id) or PACK_COUNT (by descending edge count in the
+    group, ties by id)."""
     rp, ci, n = _csr(rowptr, colidx)
     lib = _load()
     counts = np.zeros(4, np.int64)
-    _check(lib.orc_blocksparse(n, _p(rp), _p(ci), float(threshold), _p(counts), None, None,
-                               None, None, None), "blocksparse(count)")
+    _check(lib.orc_blocksparse_packed(n, _p(rp), _p(ci), float(threshold), int(packing),
+                                      _p(counts), None, None, None, None, None),
+           "blocksparse(count)")
     nb, nk, nt, nr = (int(x) for x in counts)
     n_groups = (n + 127) // 128
     off = np.empty(n_groups + 1, np.int32)
@@ -272,8 +280,9 @@ def blocksparse(rowptr, colidx, threshold):
     mask = np.empty((nb, 8, 4), np.uint64)
     rrp = np.empty(n + 1, np.int32)
     rci = np.empty(max(nr, 1), np.int32)
-    _check(lib.orc_blocksparse(n, _p(rp), _p(ci), float(threshold), _p(counts), _p(off),
-                               _p(cols), _p(mask), _p(rrp), _p(rci)), "blocksparse")
+    _check(lib.orc_blocksparse_packed(n, _p(rp), _p(ci), float(threshold), int(packing),
+                                      _p(counts), _p(off), _p(cols), _p(mask), _p(rrp), _p(rci)),
+           "blocksparse")
     return dict(grp_blk_offset=off, blk_cols=cols, blk_mask=mask, res_rowptr=rrp,
                 res_colidx=rci[:nr], n_blocks=nb, n_tiles_kept=nk, nnz_tiles=nt,
                 nnz_residual=nr)

@@ -517,6 +517,25 @@ static int cmp_i32(const void *a, const void *b) {
     return (x > y) - (x < y);
 }
 
+typedef struct { int64_t cnt; int32_t id; int32_t k; } orc_colcount;
+
+/* descending count, then ascending column id */
+static int cmp_colcount(const void *a, const void *b) {
+    const orc_colcount *x = a, *y = b;
+    if (x->cnt != y->cnt) return x->cnt > y->cnt ? -1 : 1;
+    return (x->id > y->id) - (x->id < y->id);
+}
+
+/* index of column j in the sorted unique list U[0..nu) (j is present) */
+static int64_t find_col(const int32_t *U, int64_t nu, int32_t j) {
+    int64_t lo = 0, hi = nu - 1;
+    while (lo < hi) {
+        int64_t mid = (lo + hi) / 2;
+        if (U[mid] < j) lo = mid + 1; else hi = mid;
+    }
+    return lo;
+}
+
 /*
  * Rows are cut into windows of 16 and groups of 8 windows (128 rows).  For a
  * group g, U_g = the sorted unique source columns of its rows; column block
@@ -533,11 +552,18 @@ static int cmp_i32(const void *a, const void *b) {
  * Output arrays may be NULL (count only).  grp_blk_offset [n_groups+1],
  * blk_cols [n_blocks*16], blk_mask [n_blocks*8*4], res_rowptr [n_rows+1],
  * res_colidx [nnz_residual].
+ *
+ * packing 0 orders U_g by ascending column id, the plain reading of the
+ * pages' "sorted" columns.  packing 1 orders it by descending count of the
+ * column's edges into the group's rows, ties by ascending id, so the
+ * columns that carry most edges share the first blocks and their tiles
+ * fill up (the fill-raising packing the threshold rule benefits from); the
+ * set of columns, and so the number of blocks at threshold 0, is the same.
  */
-int orc_blocksparse(int32_t n_rows, const int32_t *rowptr, const int32_t *colidx,
-                    float threshold, int64_t *counts, int32_t *grp_blk_offset,
-                    int32_t *blk_cols, uint64_t *blk_mask, int32_t *res_rowptr,
-                    int32_t *res_colidx) {
+int orc_blocksparse_packed(int32_t n_rows, const int32_t *rowptr, const int32_t *colidx,
+                           float threshold, int packing, int64_t *counts,
+                           int32_t *grp_blk_offset, int32_t *blk_cols, uint64_t *blk_mask,
+                           int32_t *res_rowptr, int32_t *res_colidx) {
     int32_t n_groups = (n_rows + 127) / 128;
     int64_t n_blocks = 0, n_kept = 0, nnz_tiles = 0, nnz_res = 0;
     int64_t max_ge = 0;
@@ -546,12 +572,19 @@ int orc_blocksparse(int32_t n_rows, const int32_t *rowptr, const int32_t *colidx
         int64_t ge = rowptr[r1] - rowptr[r0];
         if (ge > max_ge) max_ge = ge;
     }
-    int32_t *U = malloc(sizeof(int32_t) * (size_t)(max_ge > 0 ? max_ge : 1));
+    size_t mg = (size_t)(max_ge > 0 ? max_ge : 1);
+    int32_t *U = malloc(sizeof(int32_t) * mg);
+    int32_t *P = malloc(sizeof(int32_t) * mg);      /* packed order of U */
+    int64_t *rank = malloc(sizeof(int64_t) * mg);   /* position in P of U[k] */
+    orc_colcount *cc = malloc(sizeof(orc_colcount) * mg);
     /* per group: masks[block][window][4] */
     int64_t max_blocks = (max_ge + 15) / 16;
     uint64_t *masks = malloc(sizeof(uint64_t) * (size_t)(max_blocks > 0 ? max_blocks : 1) * 32);
     uint8_t *kept = malloc((size_t)(max_blocks > 0 ? max_blocks : 1) * 8);
-    if (!U || !masks || !kept) { free(U); free(masks); free(kept); return ORC_ERR; }
+    if (!U || !P || !rank || !cc || !masks || !kept) {
+        free(U); free(P); free(rank); free(cc); free(masks); free(kept);
+        return ORC_ERR;
+    }
     if (res_rowptr) res_rowptr[0] = 0;
     if (grp_blk_offset) grp_blk_offset[0] = 0;
     for (int32_t g = 0; g < n_groups; ++g) {
@@ -562,19 +595,20 @@ int orc_blocksparse(int32_t n_rows, const int32_t *rowptr, const int32_t *colidx
         int64_t nu = 0;
         for (int64_t k = 0; k < ge; ++k)
             if (nu == 0 || U[nu - 1] != U[k]) U[nu++] = U[k];
+        /* the packed order P of the columns and the position of each */
+        for (int64_t k = 0; k < nu; ++k) { cc[k].cnt = 0; cc[k].id = U[k]; cc[k].k = (int32_t)k; }
+        if (packing == 1) {
+            for (int64_t e = rowptr[r0]; e < rowptr[r1]; ++e) cc[find_col(U, nu, colidx[e])].cnt++;
+            qsort(cc, (size_t)nu, sizeof(orc_colcount), cmp_colcount);
+        }
+        for (int64_t q = 0; q < nu; ++q) { P[q] = cc[q].id; rank[cc[q].k] = q; }
         int64_t nb = (nu + 15) / 16;
         memset(masks, 0, sizeof(uint64_t) * (size_t)nb * 32);
         /* place every edge of the group */
         for (int32_t i = r0; i < r1; ++i) {
             int32_t w = (i - r0) / 16, r = (i - r0) % 16;
             for (int64_t e = rowptr[i]; e < rowptr[i + 1]; ++e) {
-                int32_t j = colidx[e];
-                /* position of j in U (binary search) */
-                int64_t lo = 0, hi = nu - 1;
-                while (lo < hi) {
-                    int64_t mid = (lo + hi) / 2;
-                    if (U[mid] < j) lo = mid + 1; else hi = mid;
-                }
+                int64_t lo = rank[find_col(U, nu, colidx[e])];
                 int64_t b = lo / 16, c = lo % 16, bit = r * 16 + c;
                 masks[(b * 8 + w) * 4 + bit / 64] |= 1ull << (bit % 64);
             }
@@ -591,7 +625,7 @@ int orc_blocksparse(int32_t n_rows, const int32_t *rowptr, const int32_t *colidx
             if (any) {
                 if (blk_cols)
                     for (int c = 0; c < 16; ++c)
-                        blk_cols[n_blocks * 16 + c] = (16 * b + c < nu) ? U[16 * b + c] : 0;
+                        blk_cols[n_blocks * 16 + c] = (16 * b + c < nu) ? P[16 * b + c] : 0;
                 if (blk_mask)
                     for (int32_t w = 0; w < 8; ++w)
                         for (int q = 0; q < 4; ++q)
@@ -606,11 +640,7 @@ int orc_blocksparse(int32_t n_rows, const int32_t *rowptr, const int32_t *colidx
             int32_t w = (i - r0) / 16;
             for (int64_t e = rowptr[i]; e < rowptr[i + 1]; ++e) {
                 int32_t j = colidx[e];
-                int64_t lo = 0, hi = nu - 1;
-                while (lo < hi) {
-                    int64_t mid = (lo + hi) / 2;
-                    if (U[mid] < j) lo = mid + 1; else hi = mid;
-                }
+                int64_t lo = rank[find_col(U, nu, j)];
                 if (!kept[(lo / 16) * 8 + w]) {
                     if (res_colidx) res_colidx[nnz_res] = j;
                     nnz_res++;
@@ -623,8 +653,17 @@ int orc_blocksparse(int32_t n_rows, const int32_t *rowptr, const int32_t *colidx
     counts[1] = n_kept;
     counts[2] = nnz_tiles;
     counts[3] = nnz_res;
-    free(U); free(masks); free(kept);
+    free(U); free(P); free(rank); free(cc); free(masks); free(kept);
     return ORC_OK;
+}
+
+/* The layout with columns in ascending id order (packing 0). */
+int orc_blocksparse(int32_t n_rows, const int32_t *rowptr, const int32_t *colidx,
+                    float threshold, int64_t *counts, int32_t *grp_blk_offset,
+                    int32_t *blk_cols, uint64_t *blk_mask, int32_t *res_rowptr,
+                    int32_t *res_colidx) {
+    return orc_blocksparse_packed(n_rows, rowptr, colidx, threshold, 0, counts, grp_blk_offset,
+                                  blk_cols, blk_mask, res_rowptr, res_colidx);
 }
 
 /* ------------------------------------------------------------------ */
