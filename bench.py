@@ -219,7 +219,10 @@ def setup_c2(torch, gnn, w):
         oracle.segment_reduce(oracle.OP_MEAN, rp, ci, Xh, rows=rows)
         oracle.segment_reduce(oracle.OP_MAX, rp, ci, Xh, rows=rows)
 
-    cfg = {"workload": "c2_rmat17", "graph": "R-MAT scale 17, edge factor 16, "
+    # rows narrower than 32 16-byte chunks (e.g. F = 32 fp32) run on the
+    # sub-warp workers of the generic kernel: its own workload name
+    name = "c2_rmat17" if F == 128 else f"c2_rmat17_f{F}"
+    cfg = {"workload": name, "graph": "R-MAT scale 17, edge factor 16, "
            "a,b,c,d=.57,.19,.19,.05, dedup + self-loops", "nodes": n, "edges": M, "features": F,
            "x_dtype": "fp32", "layers": ["gcn_spmm", "segment_sum", "segment_mean",
                                          "segment_max+argmax"],
@@ -237,7 +240,7 @@ def setup_c2(torch, gnn, w):
     gx = torch.empty((n, F), dtype=torch.float32, device="cuda")
     bwd_only = (lambda: gnn.gnn_segment_reduce_ext_backward(am, gout, n, out=gx), n * F,
                 3 * n * F * 4)
-    return Workload("c2_rmat17", layers, [X], list(outs.values()) + [am], cfg, "f32",
+    return Workload(name, layers, [X], list(outs.values()) + [am], cfg, "f32",
                     oracle_step, (rows, M), extra={"min_only": min_only, "bwd_only": bwd_only,
                                                   "transpose_only": lambda: gnn.gnn_csr_transpose(g),
                                                   "selector": selector_report(
@@ -472,13 +475,20 @@ def dist_env():
     return rank, world, local
 
 
+def with_feature_width(synth, w, args):
+    """c2 with --features F: X regenerated as N(0, 1) fp32 [N, F] (same seed)."""
+    if args.features and args.workload == "c2_rmat17":
+        w["X"] = synth.normal_f32((len(w["rowptr"]) - 1, args.features), 1.0, synth.SEED_X)
+    return w
+
+
 def run_reference(args):
     import synth
     rank, world, _ = dist_env()
     if rank != 0:
         return
     w = synth.workload("c4_clustered_gt", features=False) if args.workload == "c4_clustered_spmm" \
-        else synth.workload(args.workload)
+        else with_feature_width(synth, synth.workload(args.workload), args)
     wl_meta = REF_META[args.workload](w)
     rows, ne, per_edge, fn = wl_meta
     for _ in range(args.warmup):
@@ -488,12 +498,15 @@ def run_reference(args):
         fn(rows)
     dt = (time.perf_counter() - t) / args.steps
     v = ne * per_edge / dt / 1e9
-    sample = f"{len(rows)} destination rows ({ne} edges) of {args.workload} per step"
+    wname = args.workload
+    if args.features and args.workload == "c2_rmat17" and args.features != 128:
+        wname = f"c2_rmat17_f{args.features}"
+    sample = f"{len(rows)} destination rows ({ne} edges) of {wname} per step"
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload, "sample": sample},
+            "config": {"workload": wname, "sample": sample},
             "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -620,6 +633,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="c2_rmat17", choices=sorted(SETUPS))
+    ap.add_argument("--features", type=int, default=None,
+                    help="c2_rmat17 only: feature width F (fp32, a multiple of 4; default 128)")
     ap.add_argument("--mapping", default="auto", choices=["auto", "feat", "neigh"],
                     help="SpMM kernel mapping (c5_rmat22)")
     ap.add_argument("--ordering", default="original",
@@ -651,7 +666,7 @@ def main():
     if args.workload == "c4_clustered_spmm":
         w = synth.workload("c4_clustered_gt", features=False)
     else:
-        w = synth.workload(args.workload)
+        w = with_feature_width(synth, synth.workload(args.workload), args)
     if args.workload == "c5_rmat22":
         W = setup_c5(torch, gnn, w, args.mapping, args.ordering)
     elif args.workload == "c4_clustered_gt":

@@ -120,6 +120,21 @@ def test_heavy_rows_split_across_workers(gnn, dtype):
     run_all(gnn, rp, ci, X, tol=tol)
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_heavy_rows_on_sub_warp_workers(gnn, dtype):
+    """Rows of 8 chunks (F = 32 fp32, F = 64 bf16) run on 8-lane workers, four
+    to a warp, each over its own run of edges (the slice-coalescing mapping
+    for small F); hub rows of degree 2500 are cut across ~40 runs and their
+    pieces merged."""
+    rp, ci = _hub_graph(seed=5)
+    n = len(rp) - 1
+    if dtype == "f32":
+        X, tol = synth.normal_f32((n, 32), 1.0, 13), TOL_F32
+    else:
+        X, tol = synth.normal_bf16((n, 64), 1.0, 13), TOL_BF16
+    run_all(gnn, rp, ci, X, tol=tol)
+
+
 def test_edge_values_and_wide_features(gnn):
     rp, ci = _hub_graph(1500, hubs=(3,), deg=1400, seed=4)
     n = len(rp) - 1
