@@ -132,7 +132,7 @@ def test_heavy_rows_on_sub_warp_workers(gnn, dtype):
         X, tol = synth.normal_f32((n, 32), 1.0, 13), TOL_F32
     else:
         X, tol = synth.normal_bf16((n, 64), 1.0, 13), TOL_BF16
-    run_all(gnn, rp, ci, X, tol=tol)
+    run_all(gnn, rp, ci, X, tol=tol, mappings=(0,))
 
 
 def test_edge_values_and_wide_features(gnn):
