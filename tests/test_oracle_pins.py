@@ -429,6 +429,27 @@ def test_degree_stats_matches_scipy():
     assert mx == d.max()
 
 
+def test_backward_and_statistics_degenerate_graphs():
+    """No edges: every gradient is zero (no weight, no score).  A single
+    self-loop row: its weight is 1, so the score gradient vanishes and dr of
+    the node is dO.  No nodes: statistics are zero."""
+    rng = np.random.default_rng(56)
+    n, heads, D = 6, 2, 4
+    HD = heads * D
+    rp, ci = G.from_edges(n, [], self_loops=False)
+    l, r = (rng.standard_normal((n, HD)).astype(np.float32) for _ in range(2))
+    a = rng.standard_normal((heads, D)).astype(np.float32)
+    dO = rng.standard_normal((n, HD))
+    for out in oracle.gatv2_backward(rp, ci, l, r, a, heads, D, dO):
+        assert not np.any(out)
+    for out in oracle.gt_backward(rp, ci, l, r, r, heads, D, 0.5, dO):
+        assert not np.any(out)
+    rp1, ci1 = G.from_edges(n, [], self_loops=True)
+    dl, dr, da = oracle.gatv2_backward(rp1, ci1, l, r, a, heads, D, dO)
+    assert not np.any(dl) and not np.any(da) and np.array_equal(dr, dO)
+    assert oracle.degree_stats(np.zeros(1, np.int32)) == (0.0, 0.0, 0.0, 0.0)
+
+
 # ---------------------------------------------------------------- relabel invariance
 
 @pytest.mark.parametrize("op", ["spmm", "sum", "mean", "max"])
