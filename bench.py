@@ -1,29 +1,40 @@
 #!/usr/bin/env python3
 """Benchmark of the CSR neighbourhood-aggregation hot path on GB300.
 
-A "step" is one pass of a workload's layers over one synthetic input, every
-kernel launched through the C ABI (include/gnn.h) by the Python binding:
+Every kernel is launched through the C ABI (include/gnn.h) by the Python
+binding.  With no --workload the run measures, in one process and one JSON
+line:
 
-  c2_rmat17 (default): R-MAT scale 17 (131,072 nodes, edge factor 16,
-      a,b,c,d = .57,.19,.19,.05, duplicates removed, self-loops added),
-      X fp32 N(0,1) [N,128]; GCN SpMM (symmetric normalisation), segment
-      sum, mean and max (+argmax), degree-aware edge-run mapping.
-  c3_rmat20_gatv2: R-MAT scale 20, H bf16 [N,256], W bf16 [256,256],
-      4 heads x 64; one fused GATv2 forward (tcgen05 projection + fused
-      score / online softmax / aggregate).
-  c4_clustered_gt: clustered graph 1024 x 256 nodes (p = 0.3, 1% rewired),
-      Q, K, V bf16 [N, 8x32]; Graph Transformer attention, CSR path.
-  c5_rmat22: R-MAT scale 22, X bf16 [N,256]; GCN SpMM.
-  c4_clustered_spmm: GCN SpMM on the c4 graph, X bf16 [N,256]; CSR edge
-    spans, or with --tiles the tensor-core SpMM over block-sparse tiles.
+  headline step, c5_rmat22: GCN SpMM (symmetric normalisation) on R-MAT
+      scale 22 (4,194,304 nodes, edge factor 16, a,b,c,d = .57,.19,.19,.05,
+      duplicates removed, self-loops added), X bf16 N(0,1) [N,256], fp32
+      accumulation and output, original vertex ids, AUTO (edge-span)
+      mapping -- the largest power-law graph of the workloads;
+  families, each on its own graph and timed the same way:
+    c2_rmat17: R-MAT scale 17, X fp32 N(0,1) [N,128]: SpMM, segment sum,
+        mean and max (+argmax);
+    c3_rmat20_gatv2: R-MAT scale 20, H bf16 [N,256], W bf16 [256,256],
+        4 heads x 64: the fused GATv2 layer (tcgen05 projection + fused
+        score / online softmax / aggregate), the projection alone, and the
+        attention by difference;
+    c4_clustered_gt: clustered graph 1024 x 256 nodes (p = 0.3, 1% rewired),
+        Q, K, V bf16 [N, 8x32]: Graph Transformer attention on the backend
+        the adaptive selector picks (and the CSR path beside it).
 
-Prints ONE JSON line (rank 0).  Metric: aggregation Gedge*feat/s = edges x
-features aggregated per second, summed over the step's layers (attention:
-edges x heads x head_dim).  Timing: CUDA events on the launching stream;
-an L2 flush (a 512 MB write) precedes every timed step outside the events;
-max over ranks.  The roofline object describes the step's dominant kernel:
-achieved = its compulsory bytes (indices read once, every feature row read
-once, every output written once) / its mean event-timed duration.
+--workload NAME runs one workload alone (c2_rmat17, c3_rmat20_gatv2,
+c4_clustered_gt, c4_clustered_spmm, c5_rmat22; --mapping / --ordering for
+the c5 study, --tiles for the c4 tile paths, --features for c2).
+
+Metric: aggregation Gedge*feat/s = edges x features aggregated per second
+(attention: edges x heads x head_dim).  Timing: CUDA events on the
+launching stream around every layer, an L2 flush (a 512 MB write, outside
+the events) before EVERY timed layer ("cold"); median, min and mean over the
+K steps; "warm" = the same layer K times back to back with no flush (the
+second-pass cache mode).  Max over ranks.  The roofline object describes
+the headline step's dominant kernel: achieved = its compulsory bytes
+(indices read once, every feature row read once, every output written
+once) / its mean event-timed duration; traffic = the DRAM bytes of an ncu
+capture recorded for the same kernel sources, else null.
 
 --impl reference times the CPU oracle (plain single-threaded C, fp64) on a
 bounded sample of destination rows of the same workload.
@@ -31,8 +42,10 @@ bounded sample of destination rows of the same workload.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
+import platform
 import subprocess
 import sys
 import threading
@@ -44,17 +57,62 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 FALLBACK_HBM_GBS = 6800.0
-# DRAM bytes (read + write) per c2 layer (edge-span kernel + heavy-row
-# finalising kernel), from the committed ncu capture
-# profiles/k_agg_span_c2_rmat17.md (same kernel build); set to None when the
-# kernels change.
-NCU_TRAFFIC = {("c2_rmat17", "spmm"): (89.525248 + 43.183872 + 13.461760) * 1e6,
-               ("c2_rmat17", "sum"): (88.022784 + 39.964928 + 13.320960) * 1e6,
-               ("c2_rmat17", "mean"): (87.809280 + 39.904256 + 13.320448) * 1e6,
-               ("c2_rmat17", "max"): (102.362112 + 82.384384 + 5.767424 + 0.000256) * 1e6}
 NOMINAL_HBM_GBS = 8000.0
 METRIC = "aggregation Gedge*feat/s"
 UNIT = "Gedge*feat/s"
+HEADLINE = "c5_rmat22"
+FAMILIES = ("c2_rmat17", "c3_rmat20_gatv2", "c4_clustered_gt")
+CSRC = os.path.join(ROOT, "sparse_neighbourhood_aggregation_gb300", "csrc")
+# kernel sources whose ncu DRAM counters a recorded traffic figure covers
+TRAFFIC_SOURCES = {"spmm": ("aggregate.cu", "common.cuh", "runtime.cu"),
+                   "sum": ("aggregate.cu", "common.cuh", "runtime.cu"),
+                   "mean": ("aggregate.cu", "common.cuh", "runtime.cu"),
+                   "max": ("aggregate.cu", "common.cuh", "runtime.cu")}
+TRAFFIC_TABLE = os.path.join(ROOT, "profiles", "dram_traffic.md")
+
+
+def sources_sha16(files) -> str:
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, layer: str):
+    """DRAM bytes (read + write) per launch of `layer` on `workload` from the
+    recorded ncu table, or None when no capture exists or the kernel sources
+    changed since it was taken (their hash differs)."""
+    files = TRAFFIC_SOURCES.get(layer)
+    if not files or not os.path.exists(TRAFFIC_TABLE):
+        return None, None
+    sha = sources_sha16(files)
+    with open(TRAFFIC_TABLE) as f:
+        for ln in f:
+            cells = [c.strip() for c in ln.strip().strip("|").split("|")]
+            if len(cells) >= 4 and cells[0] == workload and cells[1] == layer:
+                try:
+                    val = float(cells[2])
+                except ValueError:
+                    continue
+                if cells[3] == sha:
+                    return val, sha
+                return None, sha
+    return None, sha
+
+
+def host_cpu():
+    """CPU model and logical core count of this host (for the CPU baseline)."""
+    model = platform.processor() or platform.machine()
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.startswith("Model name:"):
+                model = ln.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    return model, os.cpu_count()
 
 
 def measured_peaks():
@@ -146,14 +204,10 @@ class Workload:
         self.sample_rows = sample_rows
         self.extra = extra or {}
 
-    def step(self, ins=None, events=None):
+    def step(self, ins=None):
         ins = self.inputs if ins is None else ins
         for L in self.layers:
-            if events is not None:
-                events[L.name][0].record()
             L.fn(ins)
-            if events is not None:
-                events[L.name][1].record()
 
 
 def _dev(torch, a):
@@ -233,16 +287,21 @@ def setup_c2(torch, gnn, w):
     # apart: the configured step is SpMM, sum, mean, max)
     ymin = torch.empty((n, F), dtype=torch.float32, device="cuda")
     amin = torch.empty((n, F), dtype=torch.int32, device="cuda")
-    min_only = (lambda: gnn.gnn_segment_reduce_min(g, X, out=ymin, argmin=amin), M * F,
-                idx + xb + yb + n * F * 4)
     # backward of max through its argmax (grad_out, argmax read; grad_X written)
     gout = torch.randn((n, F), dtype=torch.float32, device="cuda")
     gx = torch.empty((n, F), dtype=torch.float32, device="cuda")
-    bwd_only = (lambda: gnn.gnn_segment_reduce_ext_backward(am, gout, n, out=gx), n * F,
-                3 * n * F * 4)
+    timed = {
+        "segment_min_argmin": (lambda: gnn.gnn_segment_reduce_min(g, X, out=ymin, argmin=amin),
+                               idx + xb + yb + n * F * 4, "timed apart, cold", M * F),
+        "max_backward": (lambda: gnn.gnn_segment_reduce_ext_backward(am, gout, n, out=gx),
+                         3 * n * F * 4, "argmax scatter of grad_out into grad_X (zero-fill "
+                                        "included), timed apart, cold"),
+        "csr_transpose": (lambda: gnn.gnn_csr_transpose(g), 0,
+                          "CSR^T build (count, stable radix sort, scan), timed apart, cold; the "
+                          "SpMM backward is a SpMM on it"),
+    }
     return Workload(name, layers, [X], list(outs.values()) + [am], cfg, "f32",
-                    oracle_step, (rows, M), extra={"min_only": min_only, "bwd_only": bwd_only,
-                                                  "transpose_only": lambda: gnn.gnn_csr_transpose(g),
+                    oracle_step, (rows, M), extra={"timed": timed,
                                                   "selector": selector_report(
                                                       torch, gnn, g, gnn.GNN_OP_SPMM, gnn.GNN_F32, F)})
 
@@ -298,7 +357,11 @@ def setup_c3(torch, gnn, w):
                            "unfused": (g, H, W, a, heads, D, w["slope"])})
 
 
-def setup_c4(torch, gnn, w, tiles=None):
+def setup_c4(torch, gnn, w, tiles=None, packing=0):
+    """GT attention on the clustered graph.  tiles = None: the CSR path;
+    a number: the tile path at that fill threshold; "auto": the backend and
+    threshold the adaptive selector picks, timed first, with the other path
+    timed beside it."""
     g = gnn.graph_prepare(_dev(torch, w["rowptr"]), _dev(torch, w["colidx"]))
     Q, K, V = (_dev(torch, w[k]) for k in ("Q", "K", "V"))
     n = Q.shape[0]
@@ -309,21 +372,37 @@ def setup_c4(torch, gnn, w, tiles=None):
     lse = torch.empty((n, heads), dtype=torch.float32, device="cuda")
     idx = 4 * (n + 1) + 4 * M
     bcomp = idx + 3 * n * HD * 2 + n * HD * 4 + n * heads * 4
-    extra = {}
+    extra = {"selector": selector_report(torch, gnn, g, gnn.GNN_OP_GT, gnn.GNN_BF16, 0, heads, D)}
+    sel = extra["selector"]
+    both = tiles == "auto"
+    if both:
+        tiles = sel["fill_threshold"] if sel["backend"] == "tiles" else None
     bs = None
     if tiles is not None:
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        bs = gnn.gnn_blocksparse_build(g, tiles)
+        bs = gnn.gnn_blocksparse_build(g, tiles, packing=packing)
         torch.cuda.synchronize()
         m = bs.meta
-        extra["blocksparse"] = {"threshold": tiles, "build_ms": (time.perf_counter() - t0) * 1e3,
+        extra["blocksparse"] = {"threshold": tiles, "packing": ["id", "count"][packing],
+                                "build_ms": (time.perf_counter() - t0) * 1e3,
                                 "listed_blocks": m.n_blocks, "kept_tiles": m.n_tiles_kept,
                                 "tile_edges": m.nnz_tiles, "residual_edges": m.nnz_residual,
                                 # S = Q K^T and O = P V over every listed block's 16 columns
                                 "tile_mma_flop": 4.0 * 128 * D * 16 * m.n_blocks * heads}
-    if bs is None:
-        # backward of the CSR-path attention (transpose built once here)
+
+    def gt_layer(use_bs):
+        nm = "gt_tiles" if use_bs is not None else "gt_csr"
+        return Layer(nm, lambda ins: gnn.gnn_gt_attn_fwd(g, ins[0], ins[1], ins[2], heads, D,
+                                                         w["scale"], bs=use_bs, out=out, lse=lse),
+                     M * HD, bcomp, "alu" if use_bs is None else "tensor")
+
+    layers = [gt_layer(bs)]
+    if both and bs is not None:
+        layers.append(gt_layer(None))
+    if bs is None or both:
+        # backward of the attention (transpose built once here), from the
+        # forward's out and lse, which every path leaves identical
         rpt, cit, _ = gnn.gnn_csr_transpose(g)
         gtr = gnn.Graph(rpt, cit, None, None, False)
         dout = torch.randn((n, HD), dtype=torch.float32, device="cuda")
@@ -332,28 +411,26 @@ def setup_c4(torch, gnn, w, tiles=None):
             lambda: gnn.gnn_gt_attn_bwd(g, gtr, Q, K, V, heads, D, w["scale"], out, lse, dout),
             bwd_bytes, "dQ over CSR, dK and dV over CSR^T (Delta fused into the dQ pass), from "
                        "the forward's out and lse; timed apart, cold")}
-    name = "gt_tiles" if bs is not None else "gt_csr"
-    layers = [Layer(name, lambda ins: gnn.gnn_gt_attn_fwd(g, ins[0], ins[1], ins[2], heads, D,
-                                                          w["scale"], bs=bs, out=out, lse=lse),
-                    M * HD, bcomp, "alu" if bs is None else "tensor")]
 
     def oracle_step(rows):
         import oracle
         oracle.gt(w["rowptr"], w["colidx"], w["Q"], w["K"], w["V"], heads, D, w["scale"],
                   rows=rows)
 
+    desc = ("fused GT attention, CSR path" if bs is None else
+            f"GT attention: tcgen05 16x16 tiles (fill >= {tiles}) + CSR residual")
     cfg = {"workload": "c4_clustered_gt", "graph": "1024 clusters x 256 nodes, p=0.3, 1% of "
            "sources rewired, dedup + self-loops", "nodes": n, "edges": M, "heads": heads,
            "head_dim": D, "dtype": "bf16 Q, K, V; fp32 softmax and accumulation; fp32 out",
-           "layers": ["fused GT attention, CSR path" if bs is None else
-                      f"GT attention: tcgen05 16x16 tiles (fill >= {tiles}) + CSR residual"]}
+           "layers": [desc] + (["fused GT attention, CSR path (beside the selected one)"]
+                               if len(layers) > 1 else [])}
     rows = _sample_by_edges(w["rowptr"], 400000)
-    extra["selector"] = selector_report(torch, gnn, g, gnn.GNN_OP_GT, gnn.GNN_BF16, 0, heads, D)
+    # with "auto" the selected layer comes first and the other is timed beside it
     return Workload("c4_clustered_gt", layers, [Q, K, V], [out, lse], cfg, "bf16", oracle_step,
                     rows, extra=extra)
 
 
-def setup_c4_spmm(torch, gnn, w, tiles=None):
+def setup_c4_spmm(torch, gnn, w, tiles=None, packing=0):
     """GCN SpMM (norm BOTH) on the clustered graph of the GT workload with X
     bf16 [N, 256] N(0,1): the CSR edge-span kernel, or with tiles the
     tensor-core SpMM over the block-sparse layout plus the residual CSR."""
@@ -371,10 +448,11 @@ def setup_c4_spmm(torch, gnn, w, tiles=None):
     if tiles is not None:
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        bs = gnn.gnn_blocksparse_build(g, tiles)
+        bs = gnn.gnn_blocksparse_build(g, tiles, packing=packing)
         torch.cuda.synchronize()
         m = bs.meta
-        extra["blocksparse"] = {"threshold": tiles, "build_ms": (time.perf_counter() - t0) * 1e3,
+        extra["blocksparse"] = {"threshold": tiles, "packing": ["id", "count"][packing],
+                                "build_ms": (time.perf_counter() - t0) * 1e3,
                                 "listed_blocks": m.n_blocks, "kept_tiles": m.n_tiles_kept,
                                 "tile_edges": m.nnz_tiles, "residual_edges": m.nnz_residual,
                                 # O += P X over every listed block's 16 columns
@@ -439,7 +517,8 @@ def setup_c5(torch, gnn, w, mapping="auto", ordering="original"):
     cfg = {"workload": "c5_rmat22", "graph": "R-MAT scale 22, edge factor 16, dedup + "
            "self-loops", "nodes": n, "edges": M, "features": F, "x_dtype": "bf16",
            "ordering": ordering, "mapping": mapping, "layers": ["gcn_spmm"]}
-    rows = _sample_by_edges(w["rowptr"], 2000000)
+    # ~16M edges x 256 features of single-core oracle work (~10 s)
+    rows = _sample_by_edges(w["rowptr"], 16000000)
     return Workload("c5_rmat22", layers, [X], [Y], cfg, "bf16", oracle_step, rows,
                     extra={"reorder_prep": prep} if prep else None)
 
@@ -508,6 +587,7 @@ def run_reference(args):
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": wname, "sample": sample},
             "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "cpu_model": host_cpu()[0], "nproc": host_cpu()[1],
                              "sample": sample},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -552,7 +632,7 @@ def _ref_c4(w):
 
 def _ref_c5(w):
     import oracle
-    rows, ne = _sample_by_edges(w["rowptr"], 500000)
+    rows, ne = _sample_by_edges(w["rowptr"], 1000000)
 
     def fn(r):
         oracle.spmm(w["rowptr"], w["colidx"], w["X"], norm=oracle.NORM_BOTH, rows=r)
@@ -575,21 +655,111 @@ REF_META = {"c2_rmat17": _ref_c2, "c3_rmat20_gatv2": _ref_c3, "c4_clustered_gt":
             "c5_rmat22": _ref_c5, "c4_clustered_spmm": _ref_c4_spmm}
 
 
-def time_layers(torch, W, steps, flush, stream):
-    names = [L.name for L in W.layers]
-    ev = [{k: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for k in names} for _ in range(steps)]
-    st = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(steps)]
-    for k in range(steps):
+def _ev(torch):
+    return torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+
+def time_cold(torch, fn, steps, flush, stream):
+    """fn() K times, each after an L2 flush (outside the events); per-call ms."""
+    evs = [_ev(torch) for _ in range(steps)]
+    for k, (e0, e1) in enumerate(evs):
         flush.fill_(float(k))
-        st[k][0].record(stream)
-        W.step(events=ev[k])
-        st[k][1].record(stream)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
     torch.cuda.synchronize()
-    step_ms = [a.elapsed_time(b) for a, b in st]
-    per = {k: float(np.mean([e[k][0].elapsed_time(e[k][1]) for e in ev])) for k in names}
+    return [e0.elapsed_time(e1) for e0, e1 in evs]
+
+
+def time_warm(torch, fn, steps, stream):
+    """fn() K times back to back (the caches keep what the last call left)."""
+    fn()
+    evs = [_ev(torch) for _ in range(steps)]
+    for e0, e1 in evs:
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return [e0.elapsed_time(e1) for e0, e1 in evs]
+
+
+def summary(ms):
+    return {"ms_median": float(np.median(ms)), "ms_min": float(np.min(ms)),
+            "ms_mean": float(np.mean(ms))}
+
+
+def time_layers(torch, W, steps, flush, stream):
+    """K steps of W; an L2 flush precedes every layer of every step, outside
+    the events.  Returns (per-step ms = sum of its layers, per-layer ms lists)."""
+    names = [L.name for L in W.layers]
+    ev = [{k: _ev(torch) for k in names} for _ in range(steps)]
+    for k in range(steps):
+        for L in W.layers:
+            flush.fill_(float(k))
+            ev[k][L.name][0].record(stream)
+            L.fn(W.inputs)
+            ev[k][L.name][1].record(stream)
+    torch.cuda.synchronize()
+    per = {nm: [e[nm][0].elapsed_time(e[nm][1]) for e in ev] for nm in names}
+    step_ms = [sum(per[nm][k] for nm in names) for k in range(steps)]
     return step_ms, per
+
+
+def layer_report(torch, W, L, cold_ms, warm_ms, hbm):
+    """One layer's numbers: cold median / min / mean, warm median, its rate
+    and its compulsory-byte fraction of the HBM peak (from the cold mean)."""
+    c = summary(cold_ms)
+    t = c["ms_mean"]
+    gbs = L.bcomp / (t * 1e-3) / 1e9
+    r = {"ms": t, **c, "warm_ms_median": float(np.median(warm_ms)),
+         "gedge_feat_s": L.units / (t * 1e-3) / 1e9, "bcomp_bytes": L.bcomp, "hbm_gbs": gbs,
+         "frac": gbs / hbm, "frac_of_8tbs": gbs / NOMINAL_HBM_GBS, "bound": L.bound}
+    tr, _ = recorded_traffic(W.name, L.name)
+    if tr is not None:
+        r["dram_bytes_ncu"] = tr
+        r["dram_over_bcomp"] = tr / L.bcomp
+    return r
+
+
+def timed_extras(torch, W, steps, flush, stream, hbm, layers):
+    """The workload's side measurements, each cold (flush before every call)."""
+    extra = {}
+    if "selector" in W.extra:
+        extra["selector"] = W.extra["selector"]
+    if "reorder_prep" in W.extra:
+        extra["reorder_prep"] = W.extra["reorder_prep"]
+    if "blocksparse" in W.extra:
+        bsx = dict(W.extra["blocksparse"])
+        bsx["tile_mma_tflops"] = bsx["tile_mma_flop"] / (layers[W.layers[0].name]["ms"] * 1e-3) / 1e12
+        extra["blocksparse"] = bsx
+    for tname, spec in W.extra.get("timed", {}).items():
+        fn, tbytes, tnote = spec[:3]
+        tunits = spec[3] if len(spec) > 3 else None
+        fn()
+        c = summary(time_cold(torch, fn, steps, flush, stream))
+        t = c["ms_mean"]
+        e = {"ms": t, **c, "note": tnote}
+        if tbytes:
+            e.update(bytes=tbytes, hbm_gbs=tbytes / (t * 1e-3) / 1e9,
+                     frac=tbytes / (t * 1e-3) / 1e9 / hbm)
+        if tunits:
+            e["gedge_feat_s"] = tunits / (t * 1e-3) / 1e9
+        extra[tname] = e
+    if "proj_only" in W.extra:
+        fn, b_proj = W.extra["proj_only"]
+        c = summary(time_cold(torch, fn, steps, flush, stream))
+        pms = c["ms_median"]
+        gat = layers["gatv2_fwd"]["ms_median"]
+        extra["projection_alone"] = {"ms": pms, **c, "bytes": b_proj,
+                                     "hbm_gbs": b_proj / (pms * 1e-3) / 1e9,
+                                     "frac": b_proj / (pms * 1e-3) / 1e9 / hbm,
+                                     "tflops": 2 * W.inputs[0].shape[0] * 256 * 256 / (pms * 1e-3) / 1e12}
+        att_ms = max(gat - pms, 1e-6)
+        extra["attention_by_difference"] = {
+            "ms": att_ms, "note": "layer median minus projection median", "bytes": W.extra["b_attn"],
+            "hbm_gbs": W.extra["b_attn"] / (att_ms * 1e-3) / 1e9,
+            "frac": W.extra["b_attn"] / (att_ms * 1e-3) / 1e9 / hbm}
+    return extra
 
 
 def unfused_gatv2_peak(torch, gnn, args_tuple):
@@ -626,13 +796,73 @@ def unfused_gatv2_peak(torch, gnn, args_tuple):
     return t0.elapsed_time(t1), peak
 
 
+def load_workload(synth, name, args):
+    if name == "c4_clustered_spmm":
+        return synth.workload("c4_clustered_gt", features=False)
+    return with_feature_width(synth, synth.workload(name), args)
+
+
+def setup_workload(torch, gnn, w, name, args, family=False):
+    if name == "c5_rmat22":
+        return setup_c5(torch, gnn, w, args.mapping, args.ordering)
+    pk = {"id": 0, "count": 1}[args.packing]
+    if name == "c4_clustered_gt":
+        return setup_c4(torch, gnn, w, "auto" if family else args.tiles, 0 if family else pk)
+    if name == "c4_clustered_spmm":
+        return setup_c4_spmm(torch, gnn, w, args.tiles, pk)
+    return SETUPS[name](torch, gnn, w)
+
+
+def measure(torch, gnn, W, args, flush, stream, hbm, base_bytes):
+    """Warm-up, then K cold steps (flush before every layer) and K warm calls
+    per layer.  Returns (per-step ms, {layer: report}, launches in the cold
+    steps, peak device memory of the warm-up above base_bytes, the memory
+    held before the workload was set up)."""
+    torch.cuda.reset_peak_memory_stats()
+    for _ in range(args.warmup):
+        W.step()
+    torch.cuda.synchronize()
+    peak_mem = torch.cuda.max_memory_allocated() - base_bytes
+    launches0 = gnn.launch_count()
+    step_ms, per = time_layers(torch, W, args.steps, flush, stream)
+    launches = gnn.launch_count() - launches0
+    layers = {}
+    for L in W.layers:
+        warm = time_warm(torch, lambda: L.fn(W.inputs), args.steps, stream)
+        layers[L.name] = layer_report(torch, W, L, per[L.name], warm, hbm)
+    return step_ms, layers, launches, peak_mem
+
+
+def run_family(torch, gnn, synth, name, args, flush, stream, hbm):
+    """One family of the default run, on its own graph: its layers cold and
+    warm, its side measurements, then its device memory is released."""
+    base = torch.cuda.memory_allocated()
+    w = load_workload(synth, name, args)
+    W = setup_workload(torch, gnn, w, name, args, family=True)
+    _, layers, _, peak_mem = measure(torch, gnn, W, args, flush, stream, hbm, base)
+    rep = {"config": W.config, "layers": layers, "peak_memory_bytes": peak_mem}
+    rep.update(timed_extras(torch, W, args.steps, flush, stream, hbm, layers))
+    if name == "c3_rmat20_gatv2" and not args.no_comparator:
+        ums, upeak = unfused_gatv2_peak(torch, gnn, W.extra["unfused"])
+        rep["unfused_torch_comparator"] = {"ms": ums, "peak_bytes_above_inputs": upeak,
+                                           "fused_peak_bytes": peak_mem,
+                                           "peak_memory_ratio": upeak / max(peak_mem, 1),
+                                           "speedup": ums / layers["gatv2_fwd"]["ms_median"]}
+    del W, w
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return rep
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="c2_rmat17", choices=sorted(SETUPS))
+    ap.add_argument("--workload", default=None, choices=sorted(SETUPS),
+                    help="run one workload alone (default: the c5_rmat22 SpMM step plus the "
+                         "c2, c3 and c4 families)")
     ap.add_argument("--features", type=int, default=None,
                     help="c2_rmat17 only: feature width F (fp32, a multiple of 4; default 128)")
     ap.add_argument("--mapping", default="auto", choices=["auto", "feat", "neigh"],
@@ -641,7 +871,12 @@ def main():
                     choices=["original", "random", "degree", "rcm"],
                     help="vertex ordering applied before timing (c5_rmat22; prep timed apart)")
     ap.add_argument("--tiles", type=float, default=None,
-                    help="c4_clustered_gt: tensor-core tile path at this fill threshold")
+                    help="c4 workloads: tensor-core tile path at this fill threshold")
+    ap.add_argument("--packing", default="id", choices=["id", "count"],
+                    help="c4 tile paths: column order inside a row group (id, or descending "
+                         "edge count)")
+    ap.add_argument("--no-families", action="store_true",
+                    help="default run: the headline step only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-comparator", action="store_true",
@@ -649,6 +884,9 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    suite = args.workload is None
+    if suite:
+        args.workload = HEADLINE
     if args.impl == "reference":
         return run_reference(args)
 
@@ -662,27 +900,13 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl")
     gnn.lib()
+    hbm, bf16_tf, peak_kind = measured_peaks()
 
-    if args.workload == "c4_clustered_spmm":
-        w = synth.workload("c4_clustered_gt", features=False)
-    else:
-        w = with_feature_width(synth, synth.workload(args.workload), args)
-    if args.workload == "c5_rmat22":
-        W = setup_c5(torch, gnn, w, args.mapping, args.ordering)
-    elif args.workload == "c4_clustered_gt":
-        W = setup_c4(torch, gnn, w, args.tiles)
-    elif args.workload == "c4_clustered_spmm":
-        W = setup_c4_spmm(torch, gnn, w, args.tiles)
-    else:
-        W = SETUPS[args.workload](torch, gnn, w)
     stream = torch.cuda.current_stream()
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
-
-    torch.cuda.reset_peak_memory_stats()
-    for _ in range(args.warmup):
-        W.step()
-    torch.cuda.synchronize()
-    peak_mem = torch.cuda.max_memory_allocated() - flush.numel() * 4
+    base = torch.cuda.memory_allocated()
+    w = load_workload(synth, args.workload, args)
+    W = setup_workload(torch, gnn, w, args.workload, args)
 
     def barrier():
         if world > 1:
@@ -692,126 +916,28 @@ def main():
     clocks = ClockSampler(local)
     barrier()
     clocks.start()
-    launches0 = gnn.launch_count()
-    step_ms, per = time_layers(torch, W, args.steps, flush, stream)
-    launches = gnn.launch_count() - launches0
-    clk = clocks.stop()
+    step_ms, layers, launches, peak_mem = measure(torch, gnn, W, args, flush, stream, hbm, base)
+    barrier()
     total_ms = max_over_ranks(torch, float(np.sum(step_ms)), world)
     ms = total_ms / args.steps
     units = sum(L.units for L in W.layers)
     value = job_rate(world, units, args.steps, total_ms)
+    extra = timed_extras(torch, W, args.steps, flush, stream, hbm, layers)
+    if args.workload == "c3_rmat20_gatv2" and not args.no_comparator:
+        ums, upeak = unfused_gatv2_peak(torch, gnn, W.extra["unfused"])
+        extra["unfused_torch_comparator"] = {"ms": ums, "peak_bytes_above_inputs": upeak,
+                                             "fused_peak_bytes": peak_mem,
+                                             "peak_memory_ratio": upeak / max(peak_mem, 1),
+                                             "speedup": ums / layers["gatv2_fwd"]["ms_median"]}
 
-    hbm, bf16_tf, peak_kind = measured_peaks()
-    layers = {}
-    for L in W.layers:
-        gbs = L.bcomp / (per[L.name] * 1e-3) / 1e9
-        layers[L.name] = {"ms": per[L.name], "gedge_feat_s": L.units / (per[L.name] * 1e-3) / 1e9,
-                          "bcomp_bytes": L.bcomp, "hbm_gbs": gbs, "frac_of_measured": gbs / hbm,
-                          "frac_of_8tbs": gbs / NOMINAL_HBM_GBS, "bound": L.bound}
-    extra = {}
-    if "selector" in W.extra:
-        extra["selector"] = W.extra["selector"]
-    if "reorder_prep" in W.extra:
-        extra["reorder_prep"] = W.extra["reorder_prep"]
-    if "blocksparse" in W.extra:
-        bsx = dict(W.extra["blocksparse"])
-        ms_t = per[W.layers[0].name]
-        bsx["tile_mma_tflops"] = bsx["tile_mma_flop"] / (ms_t * 1e-3) / 1e12
-        extra["blocksparse"] = bsx
-    if "min_only" in W.extra:
-        fn, units_min, b_min = W.extra["min_only"]
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
-        fn()
-        for k, (e0, e1) in enumerate(evs):
-            flush.fill_(float(k))
-            e0.record(stream)
-            fn()
-            e1.record(stream)
-        torch.cuda.synchronize()
-        mms = float(np.mean([e0.elapsed_time(e1) for e0, e1 in evs]))
-        extra["segment_min_argmin"] = {"ms": mms, "gedge_feat_s": units_min / (mms * 1e-3) / 1e9,
-                                       "bcomp_bytes": b_min, "hbm_gbs": b_min / (mms * 1e-3) / 1e9,
-                                       "frac_of_measured": b_min / (mms * 1e-3) / 1e9 / hbm,
-                                       "note": "timed apart, cold (L2 flushed before each call)"}
-    if "bwd_only" in W.extra:
-        fn, units_b, b_b = W.extra["bwd_only"]
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
-        fn()
-        for k, (e0, e1) in enumerate(evs):
-            flush.fill_(float(k))
-            e0.record(stream)
-            fn()
-            e1.record(stream)
-        torch.cuda.synchronize()
-        bms = float(np.mean([e0.elapsed_time(e1) for e0, e1 in evs]))
-        extra["max_backward"] = {"ms": bms, "bcomp_bytes": b_b, "hbm_gbs": b_b / (bms * 1e-3) / 1e9,
-                                 "frac_of_measured": b_b / (bms * 1e-3) / 1e9 / hbm,
-                                 "note": "argmax scatter of grad_out into grad_X (zero-fill "
-                                         "included), timed apart, cold"}
-    for tname, (fn, tbytes, tnote) in W.extra.get("timed", {}).items():
-        fn()
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
-        for k, (e0, e1) in enumerate(evs):
-            flush.fill_(float(k))
-            e0.record(stream)
-            fn()
-            e1.record(stream)
-        torch.cuda.synchronize()
-        tms = float(np.mean([e0.elapsed_time(e1) for e0, e1 in evs]))
-        extra[tname] = {"ms": tms, "bytes": tbytes, "hbm_gbs": tbytes / (tms * 1e-3) / 1e9,
-                        "frac_of_measured": tbytes / (tms * 1e-3) / 1e9 / hbm, "note": tnote}
-    if "transpose_only" in W.extra:
-        fn = W.extra["transpose_only"]
-        fn()
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
-        for k, (e0, e1) in enumerate(evs):
-            flush.fill_(float(k))
-            e0.record(stream)
-            fn()
-            e1.record(stream)
-        torch.cuda.synchronize()
-        extra["csr_transpose"] = {"ms": float(np.mean([e0.elapsed_time(e1) for e0, e1 in evs])),
-                                  "note": "CSR^T build (count, stable radix sort, scan), timed "
-                                          "apart, cold; the SpMM backward is a SpMM on it"}
-    if "proj_only" in W.extra:
-        fn, b_proj = W.extra["proj_only"]
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
-        for k, (e0, e1) in enumerate(evs):
-            flush.fill_(float(k))
-            e0.record(stream)
-            fn()
-            e1.record(stream)
-        torch.cuda.synchronize()
-        pms = float(np.mean([e0.elapsed_time(e1) for e0, e1 in evs]))
-        gat = layers["gatv2_fwd"]["ms"]
-        extra["projection_alone"] = {"ms": pms, "bytes": b_proj,
-                                     "hbm_gbs": b_proj / (pms * 1e-3) / 1e9,
-                                     "frac_of_measured": b_proj / (pms * 1e-3) / 1e9 / hbm,
-                                     "tflops": 2 * W.inputs[0].shape[0] * 256 * 256 / (pms * 1e-3) / 1e12}
-        att_ms = max(gat - pms, 1e-6)
-        extra["attention_by_difference"] = {
-            "ms": att_ms, "bytes": W.extra["b_attn"],
-            "hbm_gbs": W.extra["b_attn"] / (att_ms * 1e-3) / 1e9,
-            "frac_of_measured": W.extra["b_attn"] / (att_ms * 1e-3) / 1e9 / hbm}
-        if not args.no_comparator:
-            ums, upeak = unfused_gatv2_peak(torch, gnn, W.extra["unfused"])
-            extra["unfused_torch_comparator"] = {"ms": ums, "peak_bytes_above_inputs": upeak,
-                                                 "fused_peak_bytes": peak_mem,
-                                                 "peak_memory_ratio": upeak / max(peak_mem, 1),
-                                                 "speedup": ums / gat}
-
-    dom = max(W.layers, key=lambda L: per[L.name])
-    achieved = dom.bcomp / (per[dom.name] * 1e-3) / 1e9
-    roofline = {"bound": "hbm", "kernel": dom.name, "achieved": achieved, "peak": hbm,
-                "unit": "GB/s", "frac": achieved / hbm, "peak_kind": peak_kind,
-                "frac_of_8tbs": achieved / NOMINAL_HBM_GBS,
-                "traffic": NCU_TRAFFIC.get((W.name, dom.name)),
-                "bcomp_bytes": dom.bcomp}
+    dom = max(W.layers, key=lambda L: layers[L.name]["ms"])
+    d = layers[dom.name]
+    traffic, sha = recorded_traffic(W.name, dom.name)
+    roofline = {"bound": "hbm", "kernel": dom.name, "achieved": d["hbm_gbs"], "peak": hbm,
+                "unit": "GB/s", "frac": d["hbm_gbs"] / hbm, "peak_kind": peak_kind,
+                "frac_of_8tbs": d["hbm_gbs"] / NOMINAL_HBM_GBS, "traffic": traffic,
+                "traffic_sources_sha16": sha, "bcomp_bytes": dom.bcomp,
+                "duration": "mean of the K cold launches (CUDA events, launching stream)"}
     if dom.bound == "alu":
         roofline["note"] = ("kernel is FP32-ALU heavy; frac is its compulsory-byte rate "
                             "against the HBM peak")
@@ -824,32 +950,42 @@ def main():
         ins_h = [x.cpu().pin_memory() for x in W.inputs]
         outs_h = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in W.outputs]
         ins_d = [torch.empty_like(x) for x in W.inputs]
-        e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                  for _ in range(max(3, args.steps // 4))]
-        for k, (a, b) in enumerate(e2e_ev):
+        e2e_ev = [_ev(torch) for _ in range(max(3, args.steps // 4))]
+        for k, (e0, e1) in enumerate(e2e_ev):
             flush.fill_(float(k))
-            a.record(stream)
+            e0.record(stream)
             for xd, xh in zip(ins_d, ins_h):
                 xd.copy_(xh, non_blocking=True)
             W.step(ins=ins_d)
             for oh, od in zip(outs_h, W.outputs):
                 oh.copy_(od, non_blocking=True)
-            b.record(stream)
+            e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(torch, float(np.mean([a.elapsed_time(b) for a, b in e2e_ev])), world)
         e2e = {"value": job_rate(world, units, 1, e2e_ms), "unit": UNIT,
                "h2d_bytes_per_step": sum(x.numel() * x.element_size() for x in ins_h),
                "d2h_bytes_per_step": sum(o.numel() * o.element_size() for o in outs_h),
                "ms_per_step": e2e_ms}
+        del ins_h, outs_h, ins_d
+
+    families = {}
+    if suite and not args.no_families:
+        oracle_w, oracle_W = w, W
+        for name in FAMILIES:
+            families[name] = run_family(torch, gnn, synth, name, args, flush, stream, hbm)
+        w, W = oracle_w, oracle_W
+    clk = clocks.stop()
 
     cfg = dict(W.config)
-    cfg["l2"] = "512 MB flush write before every timed step"
+    cfg["l2"] = "512 MB flush write before every timed layer (cold); warm = back to back"
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": W.dtype, "data": "synthetic",
             "config": cfg, "roofline": roofline, "layers": layers, "e2e": e2e,
             "gpu_launches": int(launches), "clocks": clk,
             "peak_memory_bytes": peak_mem}
+    if families:
+        line["families"] = families
     if extra:
         line["extra"] = extra
 
@@ -859,8 +995,9 @@ def main():
         W.oracle_step(rows)
         dt = time.perf_counter() - t
         per_edge = units / max(len(w["colidx"]), 1)
+        model, ncpu = host_cpu()
         line["cpu_baseline"] = {"value": ne * per_edge / dt / 1e9, "unit": UNIT, "cores": 1,
-                                "kind": "oracle",
+                                "kind": "oracle", "cpu_model": model, "nproc": ncpu,
                                 "sample": f"{len(rows)} destination rows ({ne} edges) of "
                                           f"{args.workload}, one step, {dt:.2f} s"}
     if rank == 0:

@@ -178,11 +178,16 @@ gnn_status gnn_segment_reduce_sum(const gnn_csr *g, const void *prep, const void
  * (roughly nnz / 64 * (12 F + 12) bytes; about 340 thousand edges at
  * F = 128 fp32); larger problems are rejected with GNN_ERR_WORKSPACE before
  * any launch.  Other arguments, validation and errors are as for
- * gnn_segment_reduce_sum.
+ * gnn_segment_reduce_sum, and are checked first, in the same order and with
+ * the same codes: a call rejected on the host touches neither the array nor
+ * the stream.  n_rows == 0 returns GNN_OK with nothing launched.
  *
  * The first call on a device, with that device current, looks up the
- * array's device address (cudaGetSymbolAddress) and caches it; make that
- * first call before any stream capture.  Each call clears the part of the
+ * array's device address (cudaGetSymbolAddress) and caches it per device
+ * ordinal; make that first call before any stream capture.  The cached
+ * address does not survive cudaDeviceReset: do not call this entry point on
+ * a device after resetting it in the same process.  X, Y and `stream` must
+ * belong to the current device.  Each call clears the part of the
  * array it uses (cudaMemsetAsync on `stream`) before its kernel runs.  All
  * calls on a device share the one array, which keeps the last call's
  * contents: calls that may overlap on the GPU (different streams without
@@ -277,6 +282,7 @@ typedef struct {
     int64_t nnz_tiles;       /* edges inside kept tiles */
     int64_t nnz_residual;    /* edges in the residual CSR */
     float fill_threshold;
+    int32_t packing;         /* gnn_packing the plan was made with */
     /* device pointers into the caller's buffer */
     int32_t *grp_blk_offset; /* [n_groups+1] */
     int32_t *blk_cols;       /* [n_blocks*16] */
@@ -285,12 +291,28 @@ typedef struct {
     int32_t *res_colidx;     /* [nnz_residual] */
 } gnn_blocksparse;
 
+/* Order of a group's columns before they are cut into 16-column blocks.
+ * GNN_PACK_ID: ascending source id (the pages' "sorted" columns).
+ * GNN_PACK_COUNT: descending number of the group's edges from that source,
+ * ties by ascending id, which gathers the busiest columns into the first
+ * blocks and raises their tiles' fill (IO-aware GNN layers, Appendix D.3,
+ * columns packed into tensor-core blocks).  Everything else in the layout is
+ * as above, with U_g taken in the packed order. */
+typedef enum { GNN_PACK_ID = 0, GNN_PACK_COUNT = 1 } gnn_packing;
+
 /* Synchronous planning pass: fills the counts of *bs (host struct; pointers
  * left NULL) and *out_bytes, the size of the buffer gnn_blocksparse_build
- * needs.  fill_threshold in [0, 1]. */
+ * needs.  fill_threshold in [0, 1].  Columns in id order (GNN_PACK_ID). */
 gnn_status gnn_blocksparse_plan(const gnn_csr *g, float fill_threshold, void *ws,
                                 size_t ws_bytes, gnn_blocksparse *bs, size_t *out_bytes,
                                 void *stream);
+
+/* As gnn_blocksparse_plan, with the column packing chosen (gnn_packing; any
+ * other value is GNN_ERR_INVALID_ARG).  The plan records it in bs->packing,
+ * which gnn_blocksparse_build follows.  Same workspace. */
+gnn_status gnn_blocksparse_plan_packed(const gnn_csr *g, float fill_threshold, int32_t packing,
+                                       void *ws, size_t ws_bytes, gnn_blocksparse *bs,
+                                       size_t *out_bytes, void *stream);
 
 /* Build the layout planned by gnn_blocksparse_plan into `out` (device,
  * out_bytes, 256-byte aligned); sets the device pointers of *bs (host struct).

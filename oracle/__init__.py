@@ -61,6 +61,8 @@ def _load():
                                                dbl, _VP, _VP, _VP, _VP]
             lib.orc_gatv2.argtypes = [i32, _VP, _VP, _VP, ctypes.c_int, i32, _VP, _VP, _VP,
                                       i32, i32, dbl, _VP, i32, _VP, _VP, _VP]
+            lib.orc_gatv2_ex.argtypes = [i32, _VP, _VP, _VP, ctypes.c_int, i32, _VP, _VP, _VP,
+                                         i32, i32, dbl, _VP, i32, ctypes.c_int, _VP, _VP, _VP]
             lib.orc_gt.argtypes = [i32, _VP, _VP, _VP, _VP, _VP, ctypes.c_int, i32, i32, dbl,
                                    _VP, i32, _VP, _VP, _VP]
             lib.orc_blocksparse.argtypes = [i32, _VP, _VP, flt, _VP, _VP, _VP, _VP, _VP, _VP]
@@ -74,7 +76,8 @@ def _load():
             lib.orc_perm_degree.argtypes = [i32, _VP, _VP, _VP]
             lib.orc_perm_rcm.argtypes = [i32, _VP, _VP, _VP]
             lib.orc_apply_perm.argtypes = [i32, _VP, _VP, _VP, _VP, _VP]
-            for f in ("orc_degrees", "orc_spmm", "orc_segment_reduce", "orc_gatv2", "orc_gt",
+            for f in ("orc_degrees", "orc_spmm", "orc_segment_reduce", "orc_gatv2",
+                      "orc_gatv2_ex", "orc_gt",
                       "orc_blocksparse", "orc_perm_random", "orc_perm_degree", "orc_perm_rcm",
                       "orc_apply_perm"):
                 getattr(lib, f).restype = ctypes.c_int
@@ -173,7 +176,10 @@ def reduce_ext_backward(arg, grad_out, n_cols):
 
 
 def gatv2(rowptr, colidx, H, W_l, a, heads, head_dim, slope=0.2, W_r=None, rows=None,
-          want_alpha=False):
+          want_alpha=False, round_c=False):
+    """GATv2 forward (IO-aware GNN layers, Section 2.2 (iii), App. D.2).
+    round_c: diagnostic mode, the projected features rounded to bf16 before
+    the attention (as the bf16 path stores them)."""
     rp, ci, n = _csr(rowptr, colidx)
     Hc, dt = _feat(H)
     Wl, dtw = _feat(W_l)
@@ -190,9 +196,9 @@ def gatv2(rowptr, colidx, H, W_l, a, heads, head_dim, slope=0.2, W_r=None, rows=
         sel = np.arange(n) if r is None else r
         ne = int(np.sum(rp[sel + 1] - rp[sel]))
         alpha = np.empty((ne, heads), np.float64)
-    _check(_load().orc_gatv2(n, _p(rp), _p(ci), _p(Hc), dt, Hc.shape[1], _p(Wl), _p(Wr),
-                             _p(ac), heads, head_dim, slope, _p(r), ns, _p(out), _p(lse),
-                             _p(alpha)), "gatv2")
+    _check(_load().orc_gatv2_ex(n, _p(rp), _p(ci), _p(Hc), dt, Hc.shape[1], _p(Wl), _p(Wr),
+                                _p(ac), heads, head_dim, slope, _p(r), ns, int(bool(round_c)),
+                                _p(out), _p(lse), _p(alpha)), "gatv2")
     return (out, lse, alpha) if want_alpha else (out, lse)
 
 

@@ -276,11 +276,47 @@ static void project_row(const void *H, int dtype, int32_t F_in, const void *W,
  * Head h owns columns [h*D, (h+1)*D).  out [n_sel, heads*D], lse [n_sel,
  * heads]; alpha (optional) [edges of the selected rows in order, heads].
  */
+/* x rounded to the nearest fp32 and then to the nearest bf16 (ties to
+ * even on the fp32 bits), returned widened: the storage rounding of the
+ * projected features in the bf16 path (IO-aware GNN layers, Section 2.2
+ * (iii): attention logits computed on projected features). */
+static double round_bf16(double x) {
+    float f = (float)x;
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    u = (u + 0x7FFFu + ((u >> 16) & 1u)) & 0xFFFF0000u;
+    memcpy(&f, &u, 4);
+    return (double)f;
+}
+
+static void round_bf16_all(double *v, int64_t n) {
+    for (int64_t k = 0; k < n; ++k) v[k] = round_bf16(v[k]);
+}
+
+int orc_gatv2_ex(int32_t n_rows, const int32_t *rowptr, const int32_t *colidx,
+                 const void *H, int dtype, int32_t F_in, const void *W_l,
+                 const void *W_r, const float *a, int32_t heads, int32_t D,
+                 double slope, const int32_t *rows, int32_t n_sel, int round_c,
+                 double *out, double *lse, double *alpha);
+
 int orc_gatv2(int32_t n_rows, const int32_t *rowptr, const int32_t *colidx,
               const void *H, int dtype, int32_t F_in, const void *W_l,
               const void *W_r, const float *a, int32_t heads, int32_t D,
               double slope, const int32_t *rows, int32_t n_sel, double *out,
               double *lse, double *alpha) {
+    return orc_gatv2_ex(n_rows, rowptr, colidx, H, dtype, F_in, W_l, W_r, a, heads, D, slope,
+                        rows, n_sel, 0, out, lse, alpha);
+}
+
+/* As orc_gatv2; round_c != 0 is the diagnostic mode: every projected
+ * feature l_i and r_j is rounded to bf16 before the attention, as the bf16
+ * path stores them, so what remains between a kernel and this result is the
+ * kernel's own arithmetic. */
+int orc_gatv2_ex(int32_t n_rows, const int32_t *rowptr, const int32_t *colidx,
+                 const void *H, int dtype, int32_t F_in, const void *W_l,
+                 const void *W_r, const float *a, int32_t heads, int32_t D,
+                 double slope, const int32_t *rows, int32_t n_sel, int round_c,
+                 double *out, double *lse, double *alpha) {
     (void)n_rows;
     int32_t HD = heads * D;
     if (!W_r) W_r = W_l;
@@ -302,6 +338,10 @@ int orc_gatv2(int32_t n_rows, const int32_t *rowptr, const int32_t *colidx,
         project_row(H, dtype, F_in, W_l, HD, i, l);
         for (int64_t k = 0; k < deg; ++k)
             project_row(H, dtype, F_in, W_r, HD, colidx[b + k], R + k * HD);
+        if (round_c) {
+            round_bf16_all(l, HD);
+            round_bf16_all(R, deg * HD);
+        }
         for (int32_t h = 0; h < heads; ++h) {
             for (int64_t k = 0; k < deg; ++k) {
                 double acc = 0.0;

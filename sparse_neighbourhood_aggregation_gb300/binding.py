@@ -25,6 +25,7 @@ GNN_MAP_AUTO, GNN_MAP_FEAT, GNN_MAP_NEIGH = 0, 1, 2
  GNN_OP_TRANSPOSE, GNN_OP_GT_BACKWARD, GNN_OP_GATV2_BACKWARD, GNN_OP_GRAPH_STATS) = range(15)
 GNN_BACKEND_CSR, GNN_BACKEND_TILES = 0, 1
 GNN_PERM_IDENTITY, GNN_PERM_RANDOM, GNN_PERM_DEGREE, GNN_PERM_RCM = 0, 1, 2, 3
+GNN_PACK_ID, GNN_PACK_COUNT = 0, 1
 
 
 class GnnError(RuntimeError):
@@ -44,7 +45,7 @@ class gnn_blocksparse(ctypes.Structure):
     _fields_ = [("n_rows", ctypes.c_int32), ("n_groups", ctypes.c_int32),
                 ("n_blocks", ctypes.c_int64), ("n_tiles_kept", ctypes.c_int64),
                 ("nnz_tiles", ctypes.c_int64), ("nnz_residual", ctypes.c_int64),
-                ("fill_threshold", ctypes.c_float),
+                ("fill_threshold", ctypes.c_float), ("packing", ctypes.c_int32),
                 ("grp_blk_offset", ctypes.c_void_p), ("blk_cols", ctypes.c_void_p),
                 ("blk_mask", ctypes.c_void_p), ("res_rowptr", ctypes.c_void_p),
                 ("res_colidx", ctypes.c_void_p)]
@@ -84,6 +85,7 @@ _SIGS = {
     "gnn_gatv2_fwd": (ctypes.c_int, ["csr", "p", "p", "i32", "i32", "p", "p", "p", "i32", "i32",
                                      "f32", "p", "p", "p", "sz", "p"]),
     "gnn_blocksparse_plan": (ctypes.c_int, ["csr", "f32", "p", "sz", "bs", "p", "p"]),
+    "gnn_blocksparse_plan_packed": (ctypes.c_int, ["csr", "f32", "i32", "p", "sz", "bs", "p", "p"]),
     "gnn_blocksparse_build": (ctypes.c_int, ["csr", "bs", "p", "sz", "p", "sz", "p"]),
     "gnn_gt_attn_fwd": (ctypes.c_int, ["csr", "p", "bs", "p", "p", "p", "i32", "i32", "i32", "f32",
                                        "p", "p", "p", "sz", "p"]),
@@ -152,6 +154,14 @@ def _require_cuda(*ts):
             raise ValueError("tensors must be contiguous CUDA tensors")
 
 
+def _check_out(t: torch.Tensor, shape, dtype, device):
+    """A caller-given output must match what the kernel writes."""
+    if (tuple(t.shape) != tuple(shape) or t.dtype != dtype or t.device != device
+            or not t.is_contiguous()):
+        raise ValueError(f"out must be a contiguous {dtype} tensor of shape {tuple(shape)} on "
+                         f"{device}; got {t.dtype} {tuple(t.shape)} on {t.device}")
+
+
 class Graph:
     """A CSR graph by destination on the GPU plus its prepared buffer (step
     a0) and cached, zero-initialised workspaces."""
@@ -209,6 +219,8 @@ def gnn_spmm(g: Graph, X: torch.Tensor, norm: int = GNN_NORM_BOTH, mapping: int 
              out=None, stream=None):
     _require_cuda(X)
     F = X.shape[1]
+    if out is not None:
+        _check_out(out, (g.n_rows, F), torch.float32, X.device)
     Y = out if out is not None else torch.empty((g.n_rows, F), dtype=torch.float32,
                                                 device=X.device)
     ws = g.workspace(GNN_OP_SPMM, F)
@@ -221,6 +233,8 @@ def gnn_spmm(g: Graph, X: torch.Tensor, norm: int = GNN_NORM_BOTH, mapping: int 
 def _reduce(name, op, g, X, out, stream):
     _require_cuda(X)
     F = X.shape[1]
+    if out is not None:
+        _check_out(out, (g.n_rows, F), torch.float32, X.device)
     Y = out if out is not None else torch.empty((g.n_rows, F), dtype=torch.float32,
                                                 device=X.device)
     ws = g.workspace(op, F)
@@ -240,11 +254,15 @@ def gnn_segment_reduce_sum_noalloc(g: Graph, X, out=None, stream=None):
     allocated here unless `out` is given)."""
     _require_cuda(X)
     F = X.shape[1]
-    Y = out if out is not None else torch.empty((g.n_rows, F), dtype=torch.float32,
-                                                device=X.device)
-    _check("gnn_segment_reduce_sum_noalloc", lib().gnn_segment_reduce_sum_noalloc(
-        ctypes.byref(g.csr), _ptr(g.prep), X.data_ptr(), _dtype_code(X), F, Y.data_ptr(),
-        _stream(stream)))
+    if out is not None:
+        _check_out(out, (g.n_rows, F), torch.float32, X.device)
+    # the library finds its array on the current device: make it X's
+    with torch.cuda.device(X.device):
+        Y = out if out is not None else torch.empty((g.n_rows, F), dtype=torch.float32,
+                                                    device=X.device)
+        _check("gnn_segment_reduce_sum_noalloc", lib().gnn_segment_reduce_sum_noalloc(
+            ctypes.byref(g.csr), _ptr(g.prep), X.data_ptr(), _dtype_code(X), F, Y.data_ptr(),
+            _stream(stream)))
     return Y
 
 
@@ -255,6 +273,10 @@ def gnn_segment_reduce_mean(g: Graph, X, out=None, stream=None):
 def _reduce_ext(name, op, g: Graph, X, want_arg, out, arg, stream):
     _require_cuda(X)
     F = X.shape[1]
+    if out is not None:
+        _check_out(out, (g.n_rows, F), torch.float32, X.device)
+    if arg is not None:
+        _check_out(arg, (g.n_rows, F), torch.int32, X.device)
     Y = out if out is not None else torch.empty((g.n_rows, F), dtype=torch.float32,
                                                 device=X.device)
     am = None
@@ -512,15 +534,18 @@ class BlockSparse:
                 "res_colidx": self._view(m.res_colidx, m.nnz_residual, torch.int32)}
 
 
-def gnn_blocksparse_build(g: Graph, fill_threshold: float, stream=None) -> BlockSparse:
-    """Plan and build the 16x16 block-sparse tile layout of g (synchronous)."""
+def gnn_blocksparse_build(g: Graph, fill_threshold: float, packing: int = 0,
+                          stream=None) -> BlockSparse:
+    """Plan and build the 16x16 block-sparse tile layout of g (synchronous).
+    packing: GNN_PACK_ID (columns by id) or GNN_PACK_COUNT (by descending
+    edge count in the group)."""
     ws = g.workspace(GNN_OP_BLOCKSPARSE)
     meta = gnn_blocksparse()
     nbytes = ctypes.c_size_t(0)
     L = lib()
-    _check("gnn_blocksparse_plan", L.gnn_blocksparse_plan(
-        ctypes.byref(g.csr), float(fill_threshold), ws.data_ptr(), ws.numel(), ctypes.byref(meta),
-        ctypes.byref(nbytes), _stream(stream)))
+    _check("gnn_blocksparse_plan_packed", L.gnn_blocksparse_plan_packed(
+        ctypes.byref(g.csr), float(fill_threshold), int(packing), ws.data_ptr(), ws.numel(),
+        ctypes.byref(meta), ctypes.byref(nbytes), _stream(stream)))
     buf = torch.empty(max(nbytes.value, 256), dtype=torch.uint8, device=g.device)
     _check("gnn_blocksparse_build", L.gnn_blocksparse_build(
         ctypes.byref(g.csr), ctypes.byref(meta), buf.data_ptr(), buf.numel(), ws.data_ptr(),

@@ -1149,9 +1149,11 @@ static cudaError_t launch_span(const AggArgs &a, cudaStream_t s) {
     return e;
 }
 
-gnn_status run_aggregate(const gnn_csr *g, const void *prep, int32_t op, int32_t norm,
-                         const void *X, int32_t x_dtype, int32_t F, float *Y, int32_t *argmax,
-                         int32_t mapping, void *ws, size_t ws_bytes, void *stream) {
+// Host checks shared by every aggregation entry point, in the order the
+// header documents; nothing is launched before they pass.
+gnn_status check_agg_args(const gnn_csr *g, const void *prep, int32_t norm, const void *X,
+                          int32_t x_dtype, int32_t F, const float *Y, const int32_t *argmax,
+                          int32_t mapping) {
     gnn_status st = check_csr_args(g);
     if (st != GNN_OK) return st;
     if (!Y || (!X && g->n_cols > 0)) return GNN_ERR_INVALID_ARG;
@@ -1162,6 +1164,16 @@ gnn_status run_aggregate(const gnn_csr *g, const void *prep, int32_t op, int32_t
     AggShape sh;
     if (!agg_shape(x_dtype, F, &sh)) return GNN_ERR_UNSUPPORTED;
     if (norm != GNN_NORM_NONE && !prep) return GNN_ERR_INVALID_ARG;
+    return GNN_OK;
+}
+
+gnn_status run_aggregate(const gnn_csr *g, const void *prep, int32_t op, int32_t norm,
+                         const void *X, int32_t x_dtype, int32_t F, float *Y, int32_t *argmax,
+                         int32_t mapping, void *ws, size_t ws_bytes, void *stream) {
+    gnn_status st = check_agg_args(g, prep, norm, X, x_dtype, F, Y, argmax, mapping);
+    if (st != GNN_OK) return st;
+    AggShape sh;
+    agg_shape(x_dtype, F, &sh);
     if (g->n_rows == 0) return GNN_OK;
 
     AggArgs a{};

@@ -21,6 +21,12 @@
 //     scan in ascending (group, block) order;
 //  4. the residual CSR is one exclusive scan over the per-edge flags "tile not
 //     kept" (edges stay in CSR order, so columns stay ascending).
+// Count-sorted packing (packing GNN_PACK_COUNT) orders each group's columns
+// by descending number of edges in the group, ties by ascending id, before
+// cutting them into blocks: the run length of each (group, source) key in the
+// sorted key list is its count, and one more radix sort of (group, 255 -
+// count, source) keys gives the packed order; every edge then maps its
+// id-sorted position to its packed position.
 // Planning runs the same pass without writing the output and reads the
 // counts back (synchronous).
 #include <cub/device/device_radix_sort.cuh>
@@ -72,11 +78,46 @@ __global__ void k_bs_unique(const uint64_t *__restrict__ key, int64_t m, int32_t
     }
 }
 
+// U[u] = source of the u-th unique key; first (may be null) = position of
+// its first occurrence in the sorted keys, and first[n_unique] = m
 __global__ void k_bs_ulist(const uint64_t *__restrict__ key, const int32_t *__restrict__ uflag,
-                           const int32_t *__restrict__ upos, int64_t m, int32_t *__restrict__ U) {
+                           const int32_t *__restrict__ upos, int64_t m, int32_t *__restrict__ U,
+                           int32_t *__restrict__ first) {
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < m; k += stride)
-        if (uflag[k]) U[upos[k]] = (int32_t)(uint32_t)key[k];
+    for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < m; k += stride) {
+        if (uflag[k]) {
+            U[upos[k]] = (int32_t)(uint32_t)key[k];
+            if (first) first[upos[k]] = (int32_t)k;
+        }
+        if (first && k == m - 1) first[upos[k] + uflag[k]] = (int32_t)m;
+    }
+}
+
+// packing keys of the unique (group, source) pairs: (group, 255 - count,
+// source), whose ascending order is the group's columns by descending edge
+// count, ties by ascending id (a count is at most the group's 128 rows)
+__global__ void k_bs_pack_keys(const uint64_t *__restrict__ key, const int32_t *__restrict__ first,
+                               int64_t nuniq, uint64_t *__restrict__ pk, int32_t *__restrict__ pv) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < nuniq; u += stride) {
+        const uint64_t k = key[first[u]];
+        const uint64_t cnt = (uint64_t)(first[u + 1] - first[u]);
+        pk[u] = ((k >> 32) << 40) | ((255ull - cnt) << 32) | (k & 0xffffffffull);
+        pv[u] = (int32_t)u;
+    }
+}
+
+// rank[u] = packed position of unique u (in the same group-major numbering);
+// P[q] = the source at packed position q (P may alias pv: thread q reads
+// pv[q] before it writes P[q])
+__global__ void k_bs_pack_rank(const uint64_t *__restrict__ pk, const int32_t *pv, int64_t nuniq,
+                               int32_t *__restrict__ rank, int32_t *P) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < nuniq; q += stride) {
+        const int32_t u = pv[q];
+        rank[u] = (int32_t)q;
+        P[q] = (int32_t)(uint32_t)pk[q];
+    }
 }
 
 __global__ void k_bs_nblk(const int32_t *__restrict__ nu, int32_t ng, int32_t *__restrict__ nblk) {
@@ -89,7 +130,8 @@ __global__ void k_bs_nblk(const int32_t *__restrict__ nu, int32_t ng, int32_t *_
 __global__ void k_bs_place(const int32_t *__restrict__ rowid, const int32_t *__restrict__ colidx, int64_t m,
                            const int32_t *__restrict__ U, const int32_t *__restrict__ uoff,
                            const int32_t *__restrict__ nu, const int32_t *__restrict__ boff,
-                           unsigned long long *__restrict__ mask, int32_t *__restrict__ tile_of) {
+                           const int32_t *__restrict__ rank, unsigned long long *__restrict__ mask,
+                           int32_t *__restrict__ tile_of) {
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < m; e += stride) {
         const int32_t i = rowid[e], j = colidx[e], g = i / kGroupRows;
@@ -99,6 +141,8 @@ __global__ void k_bs_place(const int32_t *__restrict__ rowid, const int32_t *__r
             const int32_t mid = (lo + hi) >> 1;
             if (u[mid] < j) lo = mid + 1; else hi = mid;
         }
+        // packed position (count-sorted packing); the id order otherwise
+        if (rank) lo = rank[uoff[g] + lo] - uoff[g];
         const int32_t b = lo / 16, c = lo % 16, w = (i % kGroupRows) / 16, r = i % 16;
         const int32_t bit = r * 16 + c;
         const int64_t t = ((int64_t)boff[g] + b) * 8 + w;
@@ -136,7 +180,7 @@ __global__ void k_bs_block_group(const int32_t *__restrict__ boff, int32_t ng, i
 __global__ void k_bs_emit(const int32_t *__restrict__ listed, const int32_t *__restrict__ lpos, int64_t nb,
                           const int32_t *__restrict__ bgrp, const int32_t *__restrict__ boff,
                           const int32_t *__restrict__ uoff, const int32_t *__restrict__ nu,
-                          const int32_t *__restrict__ U, const unsigned long long *__restrict__ mask,
+                          const int32_t *__restrict__ cols_of, const unsigned long long *__restrict__ mask,
                           const uint8_t *__restrict__ kept, int32_t *__restrict__ blk_cols,
                           unsigned long long *__restrict__ blk_mask) {
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -146,7 +190,7 @@ __global__ void k_bs_emit(const int32_t *__restrict__ listed, const int32_t *__r
         const int32_t g = bgrp[bk], b = (int32_t)(bk - boff[g]);
         for (int c = 0; c < 16; ++c) {
             const int32_t p = 16 * b + c;
-            blk_cols[o * 16 + c] = p < nu[g] ? U[uoff[g] + p] : 0;
+            blk_cols[o * 16 + c] = p < nu[g] ? cols_of[uoff[g] + p] : 0;
         }
         for (int w = 0; w < 8; ++w)
             for (int q = 0; q < 4; ++q)
@@ -223,6 +267,9 @@ BsWs bs_layout(const gnn_csr *g, void *base) {
     size_t t = 0, x = 0;
     cub::DeviceRadixSort::SortKeys(nullptr, x, (const uint64_t *)nullptr, (uint64_t *)nullptr, m);
     t = std::max(t, x);
+    cub::DeviceRadixSort::SortPairs(nullptr, x, (const uint64_t *)nullptr, (uint64_t *)nullptr,
+                                    (const int32_t *)nullptr, (int32_t *)nullptr, m);
+    t = std::max(t, x);
     cub::DeviceScan::ExclusiveSum(nullptr, x, (const int32_t *)nullptr, (int32_t *)nullptr,
                                   std::max<int64_t>(m + 1, W.max_blocks + 1));
     t = std::max(t, x);
@@ -261,8 +308,16 @@ BsOut bs_out_layout(int32_t n_rows, int64_t n_blocks, int64_t nnz_res, void *bas
 // nnz_tiles, nnz_residual}.  The layout is written only if out != nullptr,
 // and then only if the counts equal `expect` (the plan the caller sized
 // `out` with); otherwise GNN_ERR_INVALID_ARG and nothing is written.
-gnn_status bs_pass(const gnn_csr *g, float thr, BsWs &W, const BsOut *out, const int64_t *expect,
-                   int64_t *counts, cudaStream_t s) {
+gnn_status bs_pass(const gnn_csr *g, float thr, int32_t packing, BsWs &W, const BsOut *out,
+                   const int64_t *expect, int64_t *counts, cudaStream_t s) {
+    // count-sorted packing reuses scratch that is free at that point: the
+    // unsorted keys and the unique flags / positions (read only by k_bs_ulist)
+    // hold the packing keys and values, and the residual flags / positions
+    // (written only after k_bs_place) hold the first occurrences and ranks
+    const bool pack = packing == GNN_PACK_COUNT;
+    int32_t *first = pack ? W.rflag : nullptr;
+    int32_t *rank = pack ? W.rpos : nullptr;
+    int32_t *packed_cols = pack ? W.upos : nullptr;
     const int32_t n = g->n_rows;
     const int64_t m = g->nnz;
     const int32_t ng = (n + kGroupRows - 1) / kGroupRows;
@@ -278,8 +333,24 @@ gnn_status bs_pass(const gnn_csr *g, float thr, BsWs &W, const BsOut *out, const
         k_bs_unique<<<gs, 256, 0, s>>>(W.key[1], m, W.uflag, W.nu);
         note_launch(2);
         GNN_TRY(cub::DeviceScan::ExclusiveSum(W.temp, tb, W.uflag, W.upos, m, s));
-        k_bs_ulist<<<gs, 256, 0, s>>>(W.key[1], W.uflag, W.upos, m, W.U);
+        k_bs_ulist<<<gs, 256, 0, s>>>(W.key[1], W.uflag, W.upos, m, W.U, first);
         note_launch(2);
+        if (pack) {
+            int32_t last_pos = 0, last_flag = 0;
+            GNN_TRY(cudaMemcpyAsync(&last_pos, W.upos + m - 1, sizeof(int32_t), cudaMemcpyDeviceToHost, s));
+            GNN_TRY(cudaMemcpyAsync(&last_flag, W.uflag + m - 1, sizeof(int32_t), cudaMemcpyDeviceToHost, s));
+            GNN_TRY(cudaStreamSynchronize(s));
+            const int64_t nuniq = (int64_t)last_pos + last_flag;
+            const int gu = std::min(nblocks(nuniq), sm_count() * 8);
+            k_bs_pack_keys<<<gu, 256, 0, s>>>(W.key[1], first, nuniq, W.key[0], W.uflag);
+            note_launch();
+            // sorted packing keys into key[1] (the sorted edge keys are no
+            // longer needed), their unique ids into upos
+            GNN_TRY(cub::DeviceRadixSort::SortPairs(W.temp, tb, W.key[0], W.key[1], W.uflag, W.upos, nuniq,
+                                                    0, 40 + bits_of(ng), s));
+            k_bs_pack_rank<<<gu, 256, 0, s>>>(W.key[1], W.upos, nuniq, rank, packed_cols);
+            note_launch(2);
+        }
     }
     GNN_TRY(cub::DeviceScan::ExclusiveSum(W.temp, tb, W.nu, W.uoff, ng + 1, s));
     k_bs_nblk<<<nblocks(ng + 1), 256, 0, s>>>(W.nu, ng, W.nblk);
@@ -294,7 +365,8 @@ gnn_status bs_pass(const gnn_csr *g, float thr, BsWs &W, const BsOut *out, const
     GNN_TRY(cudaMemsetAsync(W.mask, 0, sizeof(unsigned long long) * (size_t)nt * 4, s));
     GNN_TRY(cudaMemsetAsync(W.listed, 0, sizeof(int32_t) * ((size_t)total_blocks + 1), s));
     if (m > 0) {
-        k_bs_place<<<gs, 256, 0, s>>>(W.rowid, g->colidx, m, W.U, W.uoff, W.nu, W.boff, W.mask, W.tile_of);
+        k_bs_place<<<gs, 256, 0, s>>>(W.rowid, g->colidx, m, W.U, W.uoff, W.nu, W.boff, rank, W.mask,
+                                      W.tile_of);
         note_launch();
     }
     if (nt > 0) {
@@ -329,7 +401,8 @@ gnn_status bs_pass(const gnn_csr *g, float thr, BsWs &W, const BsOut *out, const
     note_launch();
     if (total_blocks > 0) {
         k_bs_emit<<<std::min(nblocks(total_blocks), sm_count() * 8), 256, 0, s>>>(
-            W.listed, W.lpos, total_blocks, W.bgrp, W.boff, W.uoff, W.nu, W.U, W.mask, W.kept, out->blk_cols,
+            W.listed, W.lpos, total_blocks, W.bgrp, W.boff, W.uoff, W.nu, pack ? packed_cols : W.U, W.mask,
+            W.kept, out->blk_cols,
             reinterpret_cast<unsigned long long *>(out->blk_mask));
         note_launch();
     }
@@ -354,19 +427,22 @@ using namespace gnn;
 
 extern "C" {
 
-gnn_status gnn_blocksparse_plan(const gnn_csr *g, float fill_threshold, void *ws, size_t ws_bytes,
-                                gnn_blocksparse *bs, size_t *out_bytes, void *stream) {
+gnn_status gnn_blocksparse_plan_packed(const gnn_csr *g, float fill_threshold, int32_t packing, void *ws,
+                                       size_t ws_bytes, gnn_blocksparse *bs, size_t *out_bytes,
+                                       void *stream) {
     gnn_status st = check_csr_args(g);
     if (st != GNN_OK) return st;
     if (!bs || !out_bytes) return GNN_ERR_INVALID_ARG;
     if (!(fill_threshold >= 0.f && fill_threshold <= 1.f)) return GNN_ERR_INVALID_ARG;
+    if (packing != GNN_PACK_ID && packing != GNN_PACK_COUNT) return GNN_ERR_INVALID_ARG;
     BsWs W = bs_layout(g, ws);
     if (!ws || ws_bytes < W.bytes) return GNN_ERR_WORKSPACE;
     if (!aligned256(ws)) return GNN_ERR_INVALID_ARG;
     int64_t c[4] = {0, 0, 0, 0};
-    st = bs_pass(g, fill_threshold, W, nullptr, nullptr, c, as_stream(stream));
+    st = bs_pass(g, fill_threshold, packing, W, nullptr, nullptr, c, as_stream(stream));
     if (st != GNN_OK) return st;
     *bs = gnn_blocksparse{};
+    bs->packing = packing;
     bs->n_rows = g->n_rows;
     bs->n_groups = (g->n_rows + kGroupRows - 1) / kGroupRows;
     bs->n_blocks = c[0];
@@ -378,11 +454,17 @@ gnn_status gnn_blocksparse_plan(const gnn_csr *g, float fill_threshold, void *ws
     return GNN_OK;
 }
 
+gnn_status gnn_blocksparse_plan(const gnn_csr *g, float fill_threshold, void *ws, size_t ws_bytes,
+                                gnn_blocksparse *bs, size_t *out_bytes, void *stream) {
+    return gnn_blocksparse_plan_packed(g, fill_threshold, GNN_PACK_ID, ws, ws_bytes, bs, out_bytes, stream);
+}
+
 gnn_status gnn_blocksparse_build(const gnn_csr *g, gnn_blocksparse *bs, void *out, size_t out_bytes, void *ws,
                                  size_t ws_bytes, void *stream) {
     gnn_status st = check_csr_args(g);
     if (st != GNN_OK) return st;
     if (!bs || !out || bs->n_rows != g->n_rows) return GNN_ERR_INVALID_ARG;
+    if (bs->packing != GNN_PACK_ID && bs->packing != GNN_PACK_COUNT) return GNN_ERR_INVALID_ARG;
     if (!aligned256(out) || !aligned256(ws)) return GNN_ERR_INVALID_ARG;
     BsOut o = bs_out_layout(g->n_rows, bs->n_blocks, bs->nnz_residual, out);
     if (out_bytes < o.bytes) return GNN_ERR_WORKSPACE;
@@ -390,7 +472,7 @@ gnn_status gnn_blocksparse_build(const gnn_csr *g, gnn_blocksparse *bs, void *ou
     if (!ws || ws_bytes < W.bytes) return GNN_ERR_WORKSPACE;
     int64_t c[4];
     const int64_t expect[4] = {bs->n_blocks, bs->n_tiles_kept, bs->nnz_tiles, bs->nnz_residual};
-    st = bs_pass(g, bs->fill_threshold, W, &o, expect, c, as_stream(stream));
+    st = bs_pass(g, bs->fill_threshold, bs->packing, W, &o, expect, c, as_stream(stream));
     if (st != GNN_OK) return st;
     bs->grp_blk_offset = o.grp_blk_offset;
     bs->blk_cols = o.blk_cols;

@@ -6,7 +6,9 @@
 #include "common.cuh"
 
 namespace gnn {
-gnn_status check_csr_args(const gnn_csr *g);
+gnn_status check_agg_args(const gnn_csr *g, const void *prep, int32_t norm, const void *X,
+                          int32_t x_dtype, int32_t F, const float *Y, const int32_t *argmax,
+                          int32_t mapping);
 }
 
 namespace {
@@ -20,7 +22,9 @@ __device__ __align__(256) unsigned char g_noalloc_scratch[GNN_NOALLOC_SCRATCH_BY
 constexpr int kMaxDevices = 64;
 
 // Device address of g_noalloc_scratch on the current device, looked up on
-// the first call per device and cached; nullptr if the lookup fails.
+// the first call per device and cached; nullptr if the lookup fails.  The
+// cache is keyed by device ordinal, so it does not survive cudaDeviceReset
+// (the module, and with it the array, may be reloaded elsewhere).
 void *noalloc_scratch_address() {
     static void *addr[kMaxDevices] = {nullptr};
     static std::mutex mu;
@@ -40,7 +44,12 @@ void *noalloc_scratch_address() {
 extern "C" gnn_status gnn_segment_reduce_sum_noalloc(const gnn_csr *g, const void *prep,
                                                      const void *X, int32_t x_dtype, int32_t F,
                                                      float *Y, void *stream) {
-    if (gnn::check_csr_args(g) != GNN_OK) return GNN_ERR_INVALID_ARG;
+    // the checks of gnn_segment_reduce_sum, with the same codes, before the
+    // scratch is touched: a rejected call launches nothing
+    const gnn_status st = gnn::check_agg_args(g, prep, GNN_NORM_NONE, X, x_dtype, F, Y, nullptr,
+                                              GNN_MAP_AUTO);
+    if (st != GNN_OK) return st;
+    if (g->n_rows == 0) return GNN_OK;
     const size_t need = gnn_workspace_size(GNN_OP_SUM, g, F, 0, 0);
     if (need > GNN_NOALLOC_SCRATCH_BYTES) return GNN_ERR_WORKSPACE;
     void *ws = noalloc_scratch_address();

@@ -26,10 +26,11 @@ def dev(a):
     return torch.from_numpy(np.ascontiguousarray(a)).cuda()
 
 
-def check(gnn, rp, ci, thr):
+def check(gnn, rp, ci, thr, packing=0):
     g = gnn.Graph(dev(rp), dev(ci), prepare=False)
-    bs = gnn.gnn_blocksparse_build(g, thr)
-    ref = oracle.blocksparse(rp, ci, thr)
+    bs = gnn.gnn_blocksparse_build(g, thr, packing=packing)
+    assert bs.meta.packing == packing
+    ref = oracle.blocksparse(rp, ci, thr, packing=packing)
     m = bs.meta
     assert (m.n_blocks, m.n_tiles_kept, m.nnz_tiles, m.nnz_residual) == \
         (ref["n_blocks"], ref["n_tiles_kept"], ref["nnz_tiles"], ref["nnz_residual"]), thr
@@ -55,11 +56,38 @@ def clustered_small(n_clusters=6, size=256, p=0.3, seed=2):
     return G.from_edges(n_clusters * size, edges)
 
 
+@pytest.mark.parametrize("packing", [0, 1])
 @pytest.mark.parametrize("thr", [0.0, 0.02, 0.1, 0.3, 0.5, 1.0])
-def test_blocksparse_small_graphs(gnn, thr):
+def test_blocksparse_small_graphs(gnn, thr, packing):
     for rp, ci in (G.random_graph(40, 0.1, 1), G.from_edges(300, [(a, b) for a in range(60) for b in range(60)]),
                    G.star(150), G.from_edges(10, [], self_loops=False), clustered_small()):
-        check(gnn, rp, ci, thr)
+        check(gnn, rp, ci, thr, packing)
+
+
+def test_blocksparse_count_packing_config4(gnn):
+    """Count-sorted packing (columns by descending edge count in the group,
+    ties by id) on the clustered graph, bit for bit, at the fills where it
+    changes which tiles are kept."""
+    w = synth.workload("c4_clustered_gt", features=False)
+    kept = {}
+    for thr in (0.0, 0.3, 0.4, 0.5):
+        bs = check(gnn, w["rowptr"], w["colidx"], thr, packing=1)
+        assert bs.meta.nnz_tiles + bs.meta.nnz_residual == len(w["colidx"])
+        kept[thr] = bs.meta.n_tiles_kept
+    assert kept[0.0] >= kept[0.3] >= kept[0.4] >= kept[0.5]
+
+
+def test_blocksparse_rejects_unknown_packing(gnn):
+    import ctypes
+    rp, ci = G.random_graph(40, 0.1, 1)
+    g = gnn.Graph(dev(rp), dev(ci), prepare=False)
+    ws = g.workspace(gnn.GNN_OP_BLOCKSPARSE)
+    meta = gnn.binding.gnn_blocksparse()
+    nbytes = ctypes.c_size_t(0)
+    rc = gnn.lib().gnn_blocksparse_plan_packed(ctypes.byref(g.csr), 0.0, 2, ws.data_ptr(),
+                                               ws.numel(), ctypes.byref(meta),
+                                               ctypes.byref(nbytes), None)
+    assert rc == gnn.GNN_ERR_INVALID_ARG
 
 
 def test_blocksparse_config4_both_thresholds(gnn):

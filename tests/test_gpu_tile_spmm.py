@@ -30,9 +30,9 @@ def dev(a):
     return torch.from_numpy(a).cuda()
 
 
-def check(gnn, rp, ci, X, thr, norms=(0, 1, 2, 3), rows=None):
+def check(gnn, rp, ci, X, thr, norms=(0, 1, 2, 3), rows=None, packing=0):
     g = gnn.graph_prepare(dev(rp), dev(ci))
-    bs = gnn.gnn_blocksparse_build(g, thr)
+    bs = gnn.gnn_blocksparse_build(g, thr, packing=packing)
     Xd = dev(X)
     sel = slice(None) if rows is None else rows
     for norm in norms:
@@ -89,6 +89,17 @@ def test_config4_graph_sampled(gnn):
                                      [0, 127, 128, n - 1]])).astype(np.int32)
     for thr in (0.0, 0.2):
         check(gnn, rp, ci, X, thr, norms=(0, 3), rows=rows)
+    # columns in count-sorted order
+    for thr in (0.0, 0.3):
+        check(gnn, rp, ci, X, thr, norms=(3,), rows=rows, packing=1)
+
+
+@pytest.mark.parametrize("thr", [0.0, 0.3, 0.4])
+def test_count_packing_clustered(gnn, thr):
+    rp, ci = synth.clustered(6, 96, 0.3, 0.05, 4)
+    n = len(rp) - 1
+    X = synth.normal_bf16((n, 128), 1.0, 45)
+    check(gnn, rp, ci, X, thr, packing=1)
 
 
 def test_rejects_unsupported_inputs(gnn):

@@ -844,3 +844,36 @@ def test_apply_perm_matches_plain_relabel_and_commutes_with_spmm():
     X = rng.standard_normal((70, 3)).astype(np.float32)
     np.testing.assert_allclose(oracle.spmm(rpo, cio, X[p]), oracle.spmm(rp, ci, X)[p], rtol=1e-12,
                                atol=1e-14)
+
+
+def _bf16_rne_of_f32(x64):
+    """fp64 -> nearest fp32 -> nearest bf16 (ties to even), as bit patterns."""
+    u = np.asarray(x64, np.float64).astype(np.float32).view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
+    return (u >> 16).astype(np.uint16)
+
+
+def test_gatv2_rounded_projection_mode_equals_exact_mode_on_rounded_features():
+    """The diagnostic mode (projected features rounded to bf16 before the
+    attention, as the bf16 path stores them) equals the exact mode run on
+    features rounded here independently and projected by an identity W."""
+    rp, ci = G.random_graph(48, 0.15, 8)
+    n = len(rp) - 1
+    heads, D, F_in = 2, 16, 24
+    H = synth.normal_f32((n, F_in), 1.0, 31)
+    W = synth.normal_f32((F_in, heads * D), 1.0 / F_in, 32)
+    a = synth.normal_f32((heads, D), 1.0 / D, 33)
+    # the projection in the oracle's order (k ascending; fp32 products are
+    # exact in fp64), so both sides round the very same doubles
+    C = np.zeros((n, heads * D), np.float64)
+    for k in range(F_in):
+        C += H[:, k, None].astype(np.float64) * W[None, k, :].astype(np.float64)
+    Cb = _bf16_rne_of_f32(C)
+    I = np.zeros((heads * D, heads * D), np.uint16)
+    I[np.arange(heads * D), np.arange(heads * D)] = 0x3F80  # bf16 1.0
+    ro, rl = oracle.gatv2(rp, ci, H, W, a, heads, D, 0.2, round_c=True)
+    eo, el = oracle.gatv2(rp, ci, Cb, I, a, heads, D, 0.2)
+    assert np.array_equal(ro, eo) and np.array_equal(rl, el)
+    # and it is a different result from the unrounded one
+    uo, _ = oracle.gatv2(rp, ci, H, W, a, heads, D, 0.2)
+    assert not np.array_equal(uo, ro)

@@ -83,3 +83,38 @@ def test_noalloc_rejects_problems_beyond_the_fixed_scratch(gnn):
     rc = b.lib().gnn_segment_reduce_sum_noalloc(ctypes.byref(csr), None, 256, b.GNN_F32, 128,
                                                 256, None)
     assert rc == b.GNN_ERR_WORKSPACE
+
+
+def test_noalloc_rejections_match_the_workspace_entry_point(gnn):
+    """A call refused on the host returns gnn_segment_reduce_sum's code and
+    launches nothing, so the shared array and the stream are untouched: a
+    valid call right after it still matches the workspace entry point."""
+    rp, ci = _hub_graph(2000, (3, 1500), 1800, 7)
+    n = len(rp) - 1
+    X = _dev(synth.normal_f32((n, 128), 1.0, 23))
+    g = gnn.graph_prepare(_dev(rp), _dev(ci))
+    L = gnn.lib()
+    ws = g.workspace(gnn.GNN_OP_SUM, 128)
+    Y = torch.zeros((n, 128), device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    prep = g.prep.data_ptr()
+    cases = [
+        # F = 6 is not a whole number of 16-byte fp32 chunks
+        dict(F=6, Y=Y.data_ptr(), dt=gnn.GNN_F32),
+        # no output buffer
+        dict(F=128, Y=None, dt=gnn.GNN_F32),
+        # an unknown dtype code
+        dict(F=128, Y=Y.data_ptr(), dt=7),
+        # a negative width
+        dict(F=-128, Y=Y.data_ptr(), dt=gnn.GNN_F32),
+    ]
+    for c in cases:
+        ref_rc = L.gnn_segment_reduce_sum(ctypes.byref(g.csr), prep, X.data_ptr(), c["dt"],
+                                          c["F"], c["Y"], ws.data_ptr(), ws.numel(), stream)
+        rc = L.gnn_segment_reduce_sum_noalloc(ctypes.byref(g.csr), prep, X.data_ptr(), c["dt"],
+                                              c["F"], c["Y"], stream)
+        assert ref_rc != gnn.GNN_OK, c
+        assert rc == ref_rc, (c, rc, ref_rc)
+    ref = gnn.gnn_segment_reduce_sum(g, X).cpu().numpy()
+    got = gnn.gnn_segment_reduce_sum_noalloc(g, X).cpu().numpy()
+    assert_rowwise_close(got, ref, TOL_F32, "noalloc sum after refused calls")
