@@ -519,8 +519,10 @@ def setup_c5(torch, gnn, w, mapping="auto", ordering="original"):
            "ordering": ordering, "mapping": mapping, "layers": ["gcn_spmm"]}
     # ~16M edges x 256 features of single-core oracle work (~10 s)
     rows = _sample_by_edges(w["rowptr"], 16000000)
-    return Workload("c5_rmat22", layers, [X], [Y], cfg, "bf16", oracle_step, rows,
-                    extra={"reorder_prep": prep} if prep else None)
+    extra = {"graph": g}
+    if prep:
+        extra["reorder_prep"] = prep
+    return Workload("c5_rmat22", layers, [X], [Y], cfg, "bf16", oracle_step, rows, extra=extra)
 
 
 SETUPS = {"c2_rmat17": setup_c2, "c3_rmat20_gatv2": setup_c3, "c4_clustered_gt": setup_c4,
@@ -854,6 +856,41 @@ def run_family(torch, gnn, synth, name, args, flush, stream, hbm):
     return rep
 
 
+def run_study(torch, gnn, synth, args, flush, stream, hbm):
+    """The ordering x mapping study of IO-aware GNN layers, Section 4.1 /
+    App. E.1, on R-MAT scale 22: GCN SpMM under the AUTO (edge spans),
+    feature-parallel and neighbour-parallel mappings after each vertex
+    ordering; s = t_original / t_reordered per mapping, and
+    delta_s = s_neighbour - s_feature per ordering.  Each cell is the cold
+    median over K calls."""
+    w = synth.workload("c5_rmat22")
+    cells, prep = {}, {}
+    for ordering in ("original", "random", "degree", "rcm"):
+        W = setup_c5(torch, gnn, w, "auto", ordering)
+        L = W.layers[0]
+        prep[ordering] = W.extra.get("reorder_prep", {})
+        g, X, Y = W.extra["graph"], W.inputs[0], W.outputs[0]
+        for mname, mp in (("auto", gnn.GNN_MAP_AUTO), ("feat", gnn.GNN_MAP_FEAT),
+                          ("neigh", gnn.GNN_MAP_NEIGH)):
+            fn = (lambda mp=mp: gnn.gnn_spmm(g, X, norm=gnn.GNN_NORM_BOTH, mapping=mp, out=Y))
+            for _ in range(args.warmup):
+                fn()
+            c = summary(time_cold(torch, fn, args.steps, flush, stream))
+            gbs = L.bcomp / (c["ms_median"] * 1e-3) / 1e9
+            cells[f"{ordering}/{mname}"] = {**c, "gedge_feat_s": L.units / (c["ms_median"] * 1e-3) / 1e9,
+                                           "frac": gbs / hbm}
+        del W, g, X, Y
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    t = {k: v["ms_median"] for k, v in cells.items()}
+    s = {f"{o}/{m}": t[f"original/{m}"] / t[f"{o}/{m}"]
+         for o in ("random", "degree", "rcm") for m in ("auto", "feat", "neigh")}
+    ds = {o: s[f"{o}/neigh"] - s[f"{o}/feat"] for o in ("random", "degree", "rcm")}
+    return {"study": "c5_rmat22 orderings x mappings (GCN SpMM, bf16 X [N,256], fp32 out)",
+            "cells": cells, "s": s, "delta_s_neigh_minus_feat": ds, "reorder_prep_ms": prep,
+            "steps": args.steps, "l2": "512 MB flush before every timed call (cold)"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -875,6 +912,9 @@ def main():
     ap.add_argument("--packing", default="id", choices=["id", "count"],
                     help="c4 tile paths: column order inside a row group (id, or descending "
                          "edge count)")
+    ap.add_argument("--study", default=None, choices=["orderings"],
+                    help="orderings: the R-MAT scale 22 SpMM under every vertex ordering and "
+                         "kernel mapping (one JSON line; no headline step)")
     ap.add_argument("--no-families", action="store_true",
                     help="default run: the headline step only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -901,6 +941,16 @@ def main():
         dist.init_process_group("nccl")
     gnn.lib()
     hbm, bf16_tf, peak_kind = measured_peaks()
+    if args.study:
+        stream = torch.cuda.current_stream()
+        flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+        clocks = ClockSampler(local)
+        clocks.start()
+        rep = run_study(torch, gnn, synth, args, flush, stream, hbm)
+        rep["clocks"] = clocks.stop()
+        if rank == 0:
+            print(json.dumps(rep), flush=True)
+        return
 
     stream = torch.cuda.current_stream()
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")

@@ -166,6 +166,46 @@ __device__ __forceinline__ float edge_weight(const AggArgs &a, int64_t e, int32_
     return w;
 }
 
+// Output rows are written once and never read by the kernel: streaming
+// stores (st.global.cs, evict-first) keep them from displacing gathered
+// feature rows in L2.
+#ifndef GNN_Y_STREAM
+#define GNN_Y_STREAM 1
+#endif
+// Column ids are read once: streaming loads (ld.global.cs).
+#ifndef GNN_IDX_STREAM
+#define GNN_IDX_STREAM 1
+#endif
+
+// Source rows with d_out >= GNN_L1_HOT are gathered with L1 evict_last and
+// the others with L1 no_allocate (edge-span kernel), so the few rows that
+// most edges gather stay in the SM's L1; 0 = plain loads.
+#ifndef GNN_L1_HOT
+#define GNN_L1_HOT 0
+#endif
+
+__device__ __forceinline__ void st_out4(float *p, float4 v) {
+#if GNN_Y_STREAM
+    __stcs(reinterpret_cast<float4 *>(p), v);
+#else
+    *reinterpret_cast<float4 *>(p) = v;
+#endif
+}
+__device__ __forceinline__ void st_out4i(int32_t *p, int4 v) {
+#if GNN_Y_STREAM
+    __stcs(reinterpret_cast<int4 *>(p), v);
+#else
+    *reinterpret_cast<int4 *>(p) = v;
+#endif
+}
+__device__ __forceinline__ int32_t ld_col(const int32_t *p) {
+#if GNN_IDX_STREAM
+    return __ldcs(p);
+#else
+    return __ldg(p);
+#endif
+}
+
 // Store a finished row (fp32 features; the lane owns chunks c*lpr + gl).
 template <int OP, class T, int CPL>
 __device__ __forceinline__ void store_row(const AggArgs &a, int32_t r, int32_t deg,
@@ -185,13 +225,12 @@ __device__ __forceinline__ void store_row(const AggArgs &a, int32_t r, int32_t d
             else o[k] = acc.max_value(c, k);
         }
 #pragma unroll
-        for (int k = 0; k < NV; k += 4)
-            *reinterpret_cast<float4 *>(a.Y + base + k) = make_float4(o[k], o[k + 1], o[k + 2], o[k + 3]);
+        for (int k = 0; k < NV; k += 4) st_out4(a.Y + base + k, make_float4(o[k], o[k + 1], o[k + 2], o[k + 3]));
         if (is_ext(OP) && a.argmax) {
 #pragma unroll
             for (int k = 0; k < NV; k += 4)
-                *reinterpret_cast<int4 *>(a.argmax + base + k) =
-                    make_int4(acc.idx[c][k], acc.idx[c][k + 1], acc.idx[c][k + 2], acc.idx[c][k + 3]);
+                st_out4i(a.argmax + base + k,
+                         make_int4(acc.idx[c][k], acc.idx[c][k + 1], acc.idx[c][k + 2], acc.idx[c][k + 3]));
         }
     }
 }
@@ -216,13 +255,12 @@ __device__ __forceinline__ void store_row_f(const AggArgs &a, int32_t r, int32_t
             else o[k] = acc.max_value(c, k);
         }
 #pragma unroll
-        for (int k = 0; k < NV; k += 4)
-            *reinterpret_cast<float4 *>(a.Y + base + k) = make_float4(o[k], o[k + 1], o[k + 2], o[k + 3]);
+        for (int k = 0; k < NV; k += 4) st_out4(a.Y + base + k, make_float4(o[k], o[k + 1], o[k + 2], o[k + 3]));
         if (is_ext(OP) && a.argmax) {
 #pragma unroll
             for (int k = 0; k < NV; k += 4)
-                *reinterpret_cast<int4 *>(a.argmax + base + k) =
-                    make_int4(acc.idx[c][k], acc.idx[c][k + 1], acc.idx[c][k + 2], acc.idx[c][k + 3]);
+                st_out4i(a.argmax + base + k,
+                         make_int4(acc.idx[c][k], acc.idx[c][k + 1], acc.idx[c][k + 2], acc.idx[c][k + 3]));
         }
     }
 }
@@ -697,8 +735,8 @@ k_agg_span(AggArgs a) {
     const bool rsq = WT && a.row_mode == ROW_RSQRT;
 
     // first window's column ids (the next window's are fetched one ahead)
-    int32_t c_cur = b0 + lane < b1 ? __ldg(a.colidx + b0 + lane) : 0;
-    int32_t c_nxt = b0 + 32 + lane < b1 ? __ldg(a.colidx + b0 + 32 + lane) : 0;
+    int32_t c_cur = b0 + lane < b1 ? ld_col(a.colidx + b0 + lane) : 0;
+    int32_t c_nxt = b0 + 32 + lane < b1 ? ld_col(a.colidx + b0 + 32 + lane) : 0;
     // rank of the row holding b0 = row ends before b0
     const uint32_t wb0 = __ldg(a.win_flags + (b0 >> 5));
     const int32_t k0 = __ldg(a.win_rowbase + (b0 >> 5)) + __popc(wb0 & ((1u << (b0 & 31)) - 1u));
@@ -714,6 +752,9 @@ k_agg_span(AggArgs a) {
     int32_t rid = k0 + lane < a.n_rows ? __ldg(a.ne_rows + k0 + lane) : 0;
     float w_cur = (weighted && b0 + lane < b1) ? edge_weight(a, b0 + lane, c_cur) : 1.f;
     float rf = rsq ? __ldg(a.dinv_in + rid) : 1.f;
+#if GNN_L1_HOT > 0
+    uint32_t hotm = __ballot_sync(FULL, b0 + lane < b1 && __ldg(a.d_out + c_cur) >= GNN_L1_HOT);
+#endif
 
     Acc<OP, T, 1> acc;
     acc.reset();
@@ -733,7 +774,13 @@ k_agg_span(AggArgs a) {
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 jv[u] = __shfl_sync(FULL, c_cur, (u0 + u) & 31);
+#if GNN_L1_HOT > 0
+                if (u0 + u < n)
+                    xv[u] = ((hotm >> ((u0 + u) & 31)) & 1u) ? ldg16_l1_last(a.X + (size_t)jv[u] * 32 + lane)
+                                                               : ldg16_l1_noalloc(a.X + (size_t)jv[u] * 32 + lane);
+#else
                 if (u0 + u < n) xv[u] = ldg16(a.X + (size_t)jv[u] * 32 + lane);
+#endif
             }
             const uint32_t gb = (bits >> u0) & ((1u << U) - 1u);
             if (gb == 0 && u0 + U <= n) {
@@ -805,8 +852,11 @@ k_agg_span(AggArgs a) {
         // advance the column window
         c_cur = c_nxt;
         const int32_t en = cb + 64 + lane;
-        c_nxt = en < b1 ? __ldg(a.colidx + en) : 0;
+        c_nxt = en < b1 ? ld_col(a.colidx + en) : 0;
         if (weighted) w_cur = cb + 32 + lane < b1 ? edge_weight(a, cb + 32 + lane, c_cur) : 1.f;
+#if GNN_L1_HOT > 0
+        hotm = __ballot_sync(FULL, cb + 32 + lane < b1 && __ldg(a.d_out + c_cur) >= GNN_L1_HOT);
+#endif
     }
     // a heavy row reaches past this span: leave its piece
     if (!last_closed) {
@@ -816,6 +866,111 @@ k_agg_span(AggArgs a) {
             store_piece<OP, T>(a, a.carry, 2 * (int64_t)w + (head ? 0 : 1), acc, lane);
         }
     }
+}
+
+// Lean variant of k_agg_span for the sum-like ops (SpMM, sum, mean): the
+// same spans, row-end bits, row ranks and piece slots, but one loop over
+// groups of U edges with the row closes tested edge by edge, instead of
+// separate close-free, whole-row and head-piece paths.  Fewer values stay
+// live across the loop, so more warps fit on an SM; the kernel is bound by
+// the feature rows in flight per SM (warps x U).
+// rows in flight per lane, and resident 64-thread blocks per SM asked of the
+// compiler (U = 8 at 12 blocks fits 80 registers without spills: 24 warps x
+// 8 rows in flight per SM, against 28 x 4 for k_agg_span)
+#ifndef GNN_LEAN_U
+#define GNN_LEAN_U 4
+#endif
+#ifndef GNN_LEAN_MINB
+#define GNN_LEAN_MINB 16
+#endif
+#ifndef GNN_SPAN_LEAN
+#define GNN_SPAN_LEAN 1
+#endif
+template <int OP, class T, bool WT>
+__global__ void __launch_bounds__(kSpanBlock, GNN_LEAN_MINB * 64 / kSpanBlock) k_agg_span_lean(AggArgs a) {
+    static_assert(!is_ext(OP), "sum-like ops only");
+    constexpr int U = GNN_LEAN_U;
+    static_assert(32 % U == 0, "groups tile a 32-edge window");
+    const unsigned FULL = 0xffffffffu;
+    asm volatile("griddepcontrol.launch_dependents;");
+    const int lane = threadIdx.x & 31;
+    const int32_t w = (int32_t)(((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+    if (w >= a.n_spans) {
+        if (w - a.n_spans < (a.n_rows + kEmptyRowsPerWarp - 1) / kEmptyRowsPerWarp)
+            write_empty_rows<OP>(a, w - a.n_spans, lane);
+        return;
+    }
+    const int32_t b0 = __ldg(a.sp_begin + w), b1 = __ldg(a.sp_begin + w + 1);
+    if (b0 >= b1) return;
+    const int32_t n_win = (int32_t)((a.nnz + 31) >> 5);
+    const bool weighted = WT && (a.values || a.col_mode != COL_ONE);
+    const bool rsq = WT && a.row_mode == ROW_RSQRT;
+
+    int32_t c_cur = b0 + lane < b1 ? ld_col(a.colidx + b0 + lane) : 0;
+    int32_t c_nxt = b0 + 32 + lane < b1 ? ld_col(a.colidx + b0 + 32 + lane) : 0;
+    // rank of the row holding b0; a span that starts inside a row starts
+    // inside a heavy row, whose piece here goes to slot 2w
+    const uint32_t wb0 = __ldg(a.win_flags + (b0 >> 5));
+    const int32_t k0 = __ldg(a.win_rowbase + (b0 >> 5)) + __popc(wb0 & ((1u << (b0 & 31)) - 1u));
+    bool head = b0 > 0 && !((__ldg(a.win_flags + ((b0 - 1) >> 5)) >> ((b0 - 1) & 31)) & 1u);
+    int32_t kofs = 0;  // lane l holds the id (and row factor) of the row of rank k0 + kofs + l
+    int32_t rid = k0 + lane < a.n_rows ? __ldg(a.ne_rows + k0 + lane) : 0;
+    float w_cur = (weighted && b0 + lane < b1) ? edge_weight(a, b0 + lane, c_cur) : 1.f;
+    float rf = rsq ? __ldg(a.dinv_in + rid) : 1.f;
+    const uint4 *__restrict__ Xl = a.X + lane;
+
+    Acc<OP, T, 1> acc;
+    acc.reset();
+    int32_t k = 0;    // rows closed so far in this span
+    int32_t rs = b0;  // first edge of the open row
+    uint32_t last_closed = 1u;
+#pragma unroll 1
+    for (int32_t cb = b0; cb < b1; cb += 32) {
+        const int n = min(32, b1 - cb);
+        const uint32_t bits_all = end_bits(a.win_flags, n_win, cb);
+        last_closed = (bits_all >> (n - 1)) & 1u;
+#pragma unroll 1
+        for (int u0 = 0; u0 < n; u0 += U) {
+            uint4 xv[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int32_t j = __shfl_sync(FULL, c_cur, (u0 + u) & 31);
+                if (u0 + u < n) xv[u] = ldg16(Xl + (size_t)j * 32);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (u0 + u >= n) break;
+                const float ww = weighted ? __shfl_sync(FULL, w_cur, (u0 + u) & 31) : 1.f;
+                acc.add(&xv[u], ww, 0);
+                if ((bits_all >> (u0 + u)) & 1u) {
+                    const int32_t e = cb + u0 + u;
+                    if (head) {
+                        store_piece<OP, T>(a, a.carry, 2 * (int64_t)w, acc, lane);
+                        head = false;
+                    } else {
+                        if (k - kofs == 32) {
+                            kofs += 32;
+                            rid = k0 + kofs + lane < a.n_rows ? __ldg(a.ne_rows + k0 + kofs + lane) : 0;
+                            if (rsq) rf = __ldg(a.dinv_in + rid);
+                        }
+                        const int32_t r = __shfl_sync(FULL, rid, k - kofs);
+                        const float f = rsq ? __shfl_sync(FULL, rf, k - kofs) : 1.f;
+                        store_row_f<OP, T, 1>(a, r, e - rs + 1, f, acc, lane);
+                    }
+                    acc.reset();
+                    ++k;
+                    rs = e + 1;
+                }
+            }
+        }
+        // advance the column window
+        c_cur = c_nxt;
+        const int32_t en = cb + 64 + lane;
+        c_nxt = en < b1 ? ld_col(a.colidx + en) : 0;
+        if (weighted) w_cur = cb + 32 + lane < b1 ? edge_weight(a, cb + 32 + lane, c_cur) : 1.f;
+    }
+    // a heavy row reaches past this span: leave its piece
+    if (!last_closed) store_piece<OP, T>(a, a.carry, 2 * (int64_t)w + (head ? 0 : 1), acc, lane);
 }
 
 // Finalise heavy rows (degree > S).  Such a row's edges lie in spans
@@ -1126,7 +1281,14 @@ template <int OP, class T, bool WT>
 static cudaError_t launch_span(const AggArgs &a, cudaStream_t s) {
     const int64_t warps =
         (int64_t)a.n_spans + ((int64_t)a.n_rows + kEmptyRowsPerWarp - 1) / kEmptyRowsPerWarp;
-    k_agg_span<OP, T, WT><<<(int)((warps * 32 + kSpanBlock - 1) / kSpanBlock), kSpanBlock, 0, s>>>(a);
+    const int span_blocks = (int)((warps * 32 + kSpanBlock - 1) / kSpanBlock);
+    // bf16 rows: the lean kernel fits 32 warps per SM where k_agg_span's 72
+    // registers fit 28 (R-MAT scale 22 SpMM 4.89 against 5.49 ms); fp32 rows
+    // keep k_agg_span, which already fits 32 (scale 17: 0.136 against 0.146)
+    if (GNN_SPAN_LEAN && !is_ext(OP) && sizeof(T) == 2)
+        k_agg_span_lean<(is_ext(OP) ? AGG_WSUM : OP), T, WT><<<span_blocks, kSpanBlock, 0, s>>>(a);
+    else
+        k_agg_span<OP, T, WT><<<span_blocks, kSpanBlock, 0, s>>>(a);
     note_launch();
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || a.n_spans <= 1) return e;

@@ -84,7 +84,10 @@ __global__ void __launch_bounds__(kTRows) k_spmm_tiles(TileSpmmArgs t) {
     uint64_t *bar = reinterpret_cast<uint64_t *>(sCF + kTCols);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 1);
 
-    const int g = blockIdx.x, f0 = blockIdx.y * kTFeat;
+    // feature blocks vary fastest: the CTAs of one group run close together,
+    // so each gathered feature row is fetched from DRAM once
+    const int nfb = t.F / kTFeat;
+    const int g = (int)(blockIdx.x / (unsigned)nfb), f0 = (int)(blockIdx.x % (unsigned)nfb) * kTFeat;
     const int tid = threadIdx.x, warp = tid >> 5;
     const int32_t row = g * kTRows + tid;
     const bool valid = row < t.n_rows;
@@ -314,8 +317,7 @@ extern "C" gnn_status gnn_spmm_blocksparse(const gnn_csr *g, const void *prep, c
         if (st != GNN_OK) return st;
     }
     if (bs->n_blocks == 0) return GNN_OK;
-    dim3 grid((unsigned)bs->n_groups, (unsigned)(F / kTFeat));
-    k_spmm_tiles<<<grid, kTRows, kTileSpmmSmem, s>>>(t);
+    k_spmm_tiles<<<(unsigned)((int64_t)bs->n_groups * (F / kTFeat)), kTRows, kTileSpmmSmem, s>>>(t);
     note_launch();
     GNN_LAUNCH_CHECK();
     return GNN_OK;

@@ -91,7 +91,11 @@ __global__ void __launch_bounds__(kRows) k_gt_tiles(TileArgs t) {
     uint64_t *bar = reinterpret_cast<uint64_t *>(sP + kRows * NCMAX * 2);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 1);
 
-    const int g = blockIdx.x, h = blockIdx.y;
+    // heads vary fastest: the CTAs of one group run close together, so each
+    // gathered K / V row is fetched from DRAM once and its other heads'
+    // slices are still in L2 when their CTAs read them (0.621 -> 0.586 ms on
+    // the clustered graph at fill 0)
+    const int h = (int)(blockIdx.x % (unsigned)t.heads), g = (int)(blockIdx.x / (unsigned)t.heads);
     const int tid = threadIdx.x, warp = tid >> 5;
     const int b0 = __ldg(t.grp_blk_offset + g), b1 = __ldg(t.grp_blk_offset + g + 1);
     const int64_t HD = (int64_t)t.heads * D;
@@ -346,8 +350,7 @@ cudaError_t launch_tiles(const TileArgs &t, int32_t n_groups, cudaStream_t s) {
         attr = cudaFuncSetAttribute(k_gt_tiles<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     });
     if (attr != cudaSuccess) return attr;
-    dim3 grid((unsigned)n_groups, (unsigned)t.heads);
-    k_gt_tiles<D><<<grid, kRows, tile_smem_bytes<D>(), s>>>(t);
+    k_gt_tiles<D><<<(unsigned)((int64_t)n_groups * t.heads), kRows, tile_smem_bytes<D>(), s>>>(t);
     return cudaGetLastError();
 }
 
