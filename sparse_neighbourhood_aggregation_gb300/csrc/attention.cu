@@ -27,6 +27,12 @@
 //   flight sits in shared memory, not registers, and the TMA engine does the
 //   address work.  A GATv2 record is the projected row r_j followed by its
 //   per-head linear parts A_r[j] (one copy); a GT record is K_j then V_j.
+//   (Filling the ring with 16-byte cp.async copies instead, 32/U lanes per
+//   record, issues ~8 fewer instructions per edge but measured 5-15% slower
+//   on GB300.)
+// * Softmax: the running maximum moves only when a score exceeds it by more
+//   than kLazy (base-2 units), so the rescale of the accumulator (a multiply
+//   per channel and an exp2) is rare; weights stay below 2^kLazy.
 // * Lanes: lane l owns CPL consecutive 16-byte chunks of a feature row (8
 //   bf16 or 4 fp32 channels per chunk); a head's channels sit on
 //   D / (CPL * chunk) adjacent lanes, whose partial scores are summed with
@@ -55,6 +61,10 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+// lazy-rescale margin of the online softmax (base-2 units); measured on
+// GB300 against a rescale at every new maximum: GATv2 attention at R-MAT
+// scale 20 2.064 -> 2.054 ms, GT on the clustered graph 2.107 -> 2.080 ms
+constexpr float kLazy = 8.f;
 // attention run = kAttnRunMul runs of the prepared graph's run table
 constexpr int kAttnRunMul = 4;
 constexpr int kAttnE = kRunEdges * kAttnRunMul;
@@ -204,12 +214,15 @@ __device__ __forceinline__ void fold_edges(const AttnArgs &a, const Lane<KIND, T
                                       : 0.f);
         mx = fmaxf(mx, part[g]);
     }
-    if (__any_sync(0xffffffffu, mx > st.m)) {
-        const float sc = (mx > st.m) ? exp2_approx(st.m - mx) : 1.f;
+    // lazy rescale: a new maximum is taken only kLazy above the current one
+    // (-inf + kLazy is -inf, so a head's first score always sets it)
+    if (__any_sync(0xffffffffu, mx > st.m + kLazy)) {
+        const bool up = mx > st.m + kLazy;
+        const float sc = up ? exp2_approx(st.m - mx) : 1.f;
         st.s *= sc;
 #pragma unroll
         for (int k = 0; k < NC; ++k) st.acc[k] *= sc;
-        st.m = mx;
+        if (up) st.m = mx;
     }
 #pragma unroll
     for (int g = 0; g < NG; ++g) {

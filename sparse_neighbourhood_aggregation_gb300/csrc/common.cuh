@@ -103,21 +103,6 @@ __device__ __forceinline__ uint4 ldcg16(const void *p) {
     return __ldcg(reinterpret_cast<const uint4 *>(p));
 }
 
-// 16-byte read-only loads with an L1 eviction priority: rows read many times
-// by the SM stay in L1 (evict_last); the others bypass it (no_allocate).
-__device__ __forceinline__ uint4 ldg16_l1_last(const void *p) {
-    uint4 r;
-    asm("ld.global.nc.L1::evict_last.v4.u32 {%0, %1, %2, %3}, [%4];"
-        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
-    return r;
-}
-__device__ __forceinline__ uint4 ldg16_l1_noalloc(const void *p) {
-    uint4 r;
-    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
-    return r;
-}
-
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
