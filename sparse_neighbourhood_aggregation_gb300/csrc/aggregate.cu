@@ -177,13 +177,6 @@ __device__ __forceinline__ float edge_weight(const AggArgs &a, int64_t e, int32_
 #define GNN_IDX_STREAM 1
 #endif
 
-// Source rows with d_out >= GNN_L1_HOT are gathered with L1 evict_last and
-// the others with L1 no_allocate (edge-span kernel), so the few rows that
-// most edges gather stay in the SM's L1; 0 = plain loads.
-#ifndef GNN_L1_HOT
-#define GNN_L1_HOT 0
-#endif
-
 __device__ __forceinline__ void st_out4(float *p, float4 v) {
 #if GNN_Y_STREAM
     __stcs(reinterpret_cast<float4 *>(p), v);
@@ -715,14 +708,9 @@ struct PieceVal {
 // WT = false: unit edge weights and row factor 1 (segment sum / mean / max);
 // WT = true: the SpMM's per-edge weights and row factors.
 template <int OP, class T, bool WT>
-__global__ void __launch_bounds__(kSpanBlock, ((!is_ext(OP) && sizeof(T) == 4) ? GNN_SPAN_MINB : GNN_SPAN_MINB - 1) * 256 / kSpanBlock)
-k_agg_span(AggArgs a) {
+__device__ __forceinline__ void agg_span_one(const AggArgs &a, const int32_t w, const int lane) {
     constexpr int U = GNN_SPAN_U;
     const unsigned FULL = 0xffffffffu;
-    // let the finalising kernel start its launch while this grid drains
-    asm volatile("griddepcontrol.launch_dependents;");
-    const int lane = threadIdx.x & 31;
-    const int32_t w = (int32_t)(((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5);
     if (w >= a.n_spans) {
         if (w - a.n_spans < (a.n_rows + kEmptyRowsPerWarp - 1) / kEmptyRowsPerWarp)
             write_empty_rows<OP>(a, w - a.n_spans, lane);
@@ -752,9 +740,6 @@ k_agg_span(AggArgs a) {
     int32_t rid = k0 + lane < a.n_rows ? __ldg(a.ne_rows + k0 + lane) : 0;
     float w_cur = (weighted && b0 + lane < b1) ? edge_weight(a, b0 + lane, c_cur) : 1.f;
     float rf = rsq ? __ldg(a.dinv_in + rid) : 1.f;
-#if GNN_L1_HOT > 0
-    uint32_t hotm = __ballot_sync(FULL, b0 + lane < b1 && __ldg(a.d_out + c_cur) >= GNN_L1_HOT);
-#endif
 
     Acc<OP, T, 1> acc;
     acc.reset();
@@ -774,13 +759,7 @@ k_agg_span(AggArgs a) {
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 jv[u] = __shfl_sync(FULL, c_cur, (u0 + u) & 31);
-#if GNN_L1_HOT > 0
-                if (u0 + u < n)
-                    xv[u] = ((hotm >> ((u0 + u) & 31)) & 1u) ? ldg16_l1_last(a.X + (size_t)jv[u] * 32 + lane)
-                                                               : ldg16_l1_noalloc(a.X + (size_t)jv[u] * 32 + lane);
-#else
                 if (u0 + u < n) xv[u] = ldg16(a.X + (size_t)jv[u] * 32 + lane);
-#endif
             }
             const uint32_t gb = (bits >> u0) & ((1u << U) - 1u);
             if (gb == 0 && u0 + U <= n) {
@@ -854,9 +833,6 @@ k_agg_span(AggArgs a) {
         const int32_t en = cb + 64 + lane;
         c_nxt = en < b1 ? ld_col(a.colidx + en) : 0;
         if (weighted) w_cur = cb + 32 + lane < b1 ? edge_weight(a, cb + 32 + lane, c_cur) : 1.f;
-#if GNN_L1_HOT > 0
-        hotm = __ballot_sync(FULL, cb + 32 + lane < b1 && __ldg(a.d_out + c_cur) >= GNN_L1_HOT);
-#endif
     }
     // a heavy row reaches past this span: leave its piece
     if (!last_closed) {
@@ -866,6 +842,28 @@ k_agg_span(AggArgs a) {
             store_piece<OP, T>(a, a.carry, 2 * (int64_t)w + (head ? 0 : 1), acc, lane);
         }
     }
+}
+
+// Work items of the span kernels: the spans, then the empty-row blocks.
+__device__ __forceinline__ int32_t span_items(const AggArgs &a) {
+    return a.n_spans + (a.n_rows + kEmptyRowsPerWarp - 1) / kEmptyRowsPerWarp;
+}
+
+// One warp per span (the grid covers every span).  The body is a device
+// function called from a loop: measured on GB300 with fp32 rows at R-MAT
+// scale 17, this form of the same code runs segment sum in 0.113 ms against
+// 0.121 for the body written inline in the kernel (one resident wave of
+// warps striding over the spans was no faster).
+template <int OP, class T, bool WT>
+__global__ void __launch_bounds__(kSpanBlock, ((!is_ext(OP) && sizeof(T) == 4) ? GNN_SPAN_MINB : GNN_SPAN_MINB - 1) * 256 / kSpanBlock)
+k_agg_span(AggArgs a) {
+    // let the finalising kernel start its launch while this grid drains
+    asm volatile("griddepcontrol.launch_dependents;");
+    const int lane = threadIdx.x & 31;
+    const int32_t nw = (int32_t)(((int64_t)gridDim.x * blockDim.x) >> 5);
+    const int32_t items = span_items(a);
+    for (int32_t w = (int32_t)(((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5); w < items; w += nw)
+        agg_span_one<OP, T, WT>(a, w, lane);
 }
 
 // Lean variant of k_agg_span for the sum-like ops (SpMM, sum, mean): the
@@ -886,6 +884,7 @@ k_agg_span(AggArgs a) {
 #ifndef GNN_SPAN_LEAN
 #define GNN_SPAN_LEAN 1
 #endif
+
 template <int OP, class T, bool WT>
 __global__ void __launch_bounds__(kSpanBlock, GNN_LEAN_MINB * 64 / kSpanBlock) k_agg_span_lean(AggArgs a) {
     static_assert(!is_ext(OP), "sum-like ops only");
@@ -1285,7 +1284,8 @@ static cudaError_t launch_span(const AggArgs &a, cudaStream_t s) {
     // bf16 rows: the lean kernel fits 32 warps per SM where k_agg_span's 72
     // registers fit 28 (R-MAT scale 22 SpMM 4.89 against 5.49 ms); fp32 rows
     // keep k_agg_span, which already fits 32 (scale 17: 0.136 against 0.146)
-    if (GNN_SPAN_LEAN && !is_ext(OP) && sizeof(T) == 2)
+    const bool lean = GNN_SPAN_LEAN && !is_ext(OP) && sizeof(T) == 2;
+    if (lean)
         k_agg_span_lean<(is_ext(OP) ? AGG_WSUM : OP), T, WT><<<span_blocks, kSpanBlock, 0, s>>>(a);
     else
         k_agg_span<OP, T, WT><<<span_blocks, kSpanBlock, 0, s>>>(a);
