@@ -801,7 +801,29 @@ def unfused_gatv2_peak(torch, gnn, args_tuple):
 def load_workload(synth, name, args):
     if name == "c4_clustered_spmm":
         return synth.workload("c4_clustered_gt", features=False)
+    if args.scale is not None:
+        return with_feature_width(synth, rescaled(synth, name, args.scale), args)
     return with_feature_width(synth, synth.workload(name), args)
+
+
+def rescaled(synth, name, scale):
+    """An R-MAT workload at another scale (same edge factor, a,b,c,d, seeds
+    and feature recipe): the small cases that ncu captures are sized on."""
+    if name not in ("c2_rmat17", "c3_rmat20_gatv2", "c5_rmat22"):
+        raise SystemExit(f"--scale applies to the R-MAT workloads, not {name}")
+    rp, ci = synth.rmat(scale, 16, *synth.RMAT_ABC)
+    n = 1 << scale
+    w = {"name": name, "rowptr": rp, "colidx": ci, "n": n}
+    if name == "c2_rmat17":
+        w["X"] = synth.normal_f32((n, 128), 1.0, synth.SEED_X)
+    elif name == "c3_rmat20_gatv2":
+        w["H"] = synth.normal_bf16((n, 256), 1.0, synth.SEED_X)
+        w["W"] = synth.normal_bf16((256, 256), 1.0 / 256, synth.SEED_W)
+        w["a"] = synth.normal_f32((4, 64), 1.0 / 64, synth.SEED_A)
+        w.update(heads=4, head_dim=64, slope=0.2)
+    else:
+        w["X"] = synth.normal_bf16((n, 256), 1.0, synth.SEED_X)
+    return w
 
 
 def setup_workload(torch, gnn, w, name, args, family=False):
@@ -909,6 +931,9 @@ def main():
                     help="vertex ordering applied before timing (c5_rmat22; prep timed apart)")
     ap.add_argument("--tiles", type=float, default=None,
                     help="c4 workloads: tensor-core tile path at this fill threshold")
+    ap.add_argument("--scale", type=int, default=None,
+                    help="R-MAT workloads at this scale instead of their own (small cases "
+                         "for profiling; the line's config names the scale)")
     ap.add_argument("--packing", default="id", choices=["id", "count"],
                     help="c4 tile paths: column order inside a row group (id, or descending "
                          "edge count)")
@@ -925,6 +950,8 @@ def main():
     if args.warmup < 3:
         args.warmup = 3
     suite = args.workload is None
+    if suite and args.scale is not None:
+        raise SystemExit("--scale needs --workload (one R-MAT workload)")
     if suite:
         args.workload = HEADLINE
     if args.impl == "reference":
@@ -957,6 +984,12 @@ def main():
     base = torch.cuda.memory_allocated()
     w = load_workload(synth, args.workload, args)
     W = setup_workload(torch, gnn, w, args.workload, args)
+    if args.scale is not None:
+        # a rescaled R-MAT graph: its own name, so no recorded figure of the
+        # full workload is attached to it
+        W.name = f"{W.name}_at_scale{args.scale}"
+        W.config["workload"] = W.name
+        W.config["graph"] = f"R-MAT scale {args.scale}, edge factor 16, dedup + self-loops"
 
     def barrier():
         if world > 1:
