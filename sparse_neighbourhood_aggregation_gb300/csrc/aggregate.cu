@@ -30,7 +30,9 @@
 // to the smaller id -- the paper's packed 64-bit atomic merge -- and is
 // exact and deterministic.
 #include <algorithm>
+#include <mutex>
 
+#include "async.cuh"
 #include "common.cuh"
 
 // Minimum resident 256-thread blocks per SM requested for the one-chunk-per-
@@ -978,6 +980,240 @@ __global__ void __launch_bounds__(kSpanBlock, GNN_LEAN_MINB * 64 / kSpanBlock) k
     if (!last_closed) store_piece<OP, T>(a, a.carry, 2 * (int64_t)w + (head ? 0 : 1), acc, lane);
 }
 
+// Ring variant of the span kernels: the same spans, row-end bits, row ranks
+// and piece slots as k_agg_span, but the feature rows travel global ->
+// shared memory by 16-byte cp.async copies into a per-warp ring of P groups
+// of GNN_RING_G edges, instead of into registers.  Lane l copies bytes
+// [16l, 16l+16) of every row and later reads back exactly those bytes, so its
+// own cp.async.wait_group orders the data (no barrier, no mbarrier).  Rows in
+// flight hold no registers: a warp keeps between (P-1)*G and P*G rows in
+// flight at all times, where the register-gather kernels drain their U rows
+// before each group is summed.  Measured on GB300 (G = 4): R-MAT scale 22
+// SpMM with bf16 rows 4.89 -> 3.81 ms at P = 3 (3.87 at P = 2, 3.88 at
+// P = 4 with 24 warps per SM, 3.96 for G = 2, P = 6); R-MAT scale 17 segment
+// sum with fp32 rows 0.115 -> 0.091 ms at P = 2 (0.093 at P = 3).
+#ifndef GNN_RING_G
+#define GNN_RING_G 4
+#endif
+#ifndef GNN_RING_P_BF16
+#define GNN_RING_P_BF16 3
+#endif
+#ifndef GNN_RING_P_F32
+#define GNN_RING_P_F32 2
+#endif
+#ifndef GNN_RING_MINB
+#define GNN_RING_MINB 16
+#endif
+#ifndef GNN_RING_EXT_MINB
+#define GNN_RING_EXT_MINB 16
+#endif
+// 0: off (register-gather span kernels); 1: on
+#ifndef GNN_SPAN_RING
+#define GNN_SPAN_RING 1
+#endif
+// L2 priority of gathered rows by source out-degree (SpMM with the GCN
+// column factor only, where the factor 1/sqrt(d_out) is at hand): rows of
+// d_out < GNN_RING_COLD_DOUT are copied evict_first, rows of d_out >=
+// GNN_RING_HOT_DOUT evict_last (0 = no such class)
+#ifndef GNN_RING_L2HINT
+#define GNN_RING_L2HINT 0
+#endif
+#ifndef GNN_RING_COLD_DOUT
+#define GNN_RING_COLD_DOUT 48
+#endif
+#ifndef GNN_RING_HOT_DOUT
+#define GNN_RING_HOT_DOUT 0
+#endif
+// max / min on the ring kernel (1) or on k_agg_span (0)
+#ifndef GNN_RING_EXT
+#define GNN_RING_EXT 1
+#endif
+template <class T>
+__host__ __device__ constexpr int ring_groups() { return sizeof(T) == 2 ? GNN_RING_P_BF16 : GNN_RING_P_F32; }
+template <class T>
+__host__ __device__ constexpr int ring_bytes_per_warp() { return GNN_RING_G * ring_groups<T>() * 512; }
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async16_pol(uint32_t dst, const void *src, uint64_t pol) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "l"(pol)
+                 : "memory");
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_normal() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ uint4 lds16(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+template <int OP, class T, bool WT>
+__global__ void __launch_bounds__(kSpanBlock, (is_ext(OP) ? GNN_RING_EXT_MINB : GNN_RING_MINB) * 64 / kSpanBlock)
+k_agg_span_ring(AggArgs a) {
+    constexpr int G = GNN_RING_G, P = ring_groups<T>();
+    static_assert(32 % G == 0 && 16 % G == 0 && P >= 2 && (P - 1) * G <= 32,
+                  "groups tile a window; issue runs at most one window ahead");
+    extern __shared__ __align__(16) uint4 ring_buf[];
+    const unsigned FULL = 0xffffffffu;
+    asm volatile("griddepcontrol.launch_dependents;");
+    const int lane = threadIdx.x & 31;
+    const int32_t w = (int32_t)(((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+    if (w >= a.n_spans) {
+        if (w - a.n_spans < (a.n_rows + kEmptyRowsPerWarp - 1) / kEmptyRowsPerWarp)
+            write_empty_rows<OP>(a, w - a.n_spans, lane);
+        return;
+    }
+    const int32_t b0 = __ldg(a.sp_begin + w), b1 = __ldg(a.sp_begin + w + 1);
+    if (b0 >= b1) return;
+    const int32_t len = b1 - b0;
+    const int32_t n_win = (int32_t)((a.nnz + 31) >> 5);
+    const bool weighted = WT && (a.values || a.col_mode != COL_ONE);
+    const bool rsq = WT && a.row_mode == ROW_RSQRT;
+    // this lane's 16 bytes of ring slot s: ring0 + 512 * s
+    const uint32_t ring0 = su32(ring_buf + (threadIdx.x >> 5) * (ring_bytes_per_warp<T>() / 16) + lane);
+    const uint4 *__restrict__ Xl = a.X + lane;
+
+    // column ids of the window being summed (c_cur) and of the next (c_nxt)
+    int32_t c_cur = lane < len ? ld_col(a.colidx + b0 + lane) : 0;
+    int32_t c_nxt = 32 + lane < len ? ld_col(a.colidx + b0 + 32 + lane) : 0;
+    float w_cur = 1.f, w_nxt = 1.f;
+    // L2 classes by out-degree (GCN column factor only)
+    const bool hint = GNN_RING_L2HINT && WT && !a.values && a.col_mode == COL_RSQRT;
+    uint64_t pol_cold = 0, pol_mid = 0, pol_hot = 0;
+    if (GNN_RING_L2HINT && hint) {
+        pol_cold = l2_policy_evict_first();
+        pol_mid = l2_policy_evict_normal();
+        pol_hot = GNN_RING_HOT_DOUT > 0 ? l2_policy_evict_last() : pol_mid;
+        w_cur = lane < len ? edge_weight(a, b0 + lane, c_cur) : 1.f;
+    }
+    // weight above which a row is cold, at or below which it is hot
+    const float w_cold = rsqrtf((float)GNN_RING_COLD_DOUT);
+    const float w_hot = GNN_RING_HOT_DOUT > 0 ? rsqrtf((float)GNN_RING_HOT_DOUT) : 0.f;
+    // copy the rows of group q (edges b0 + qG ..) into slot group qs; cw is
+    // the span offset of c_cur's window (the group lies in it or the next)
+    auto issue = [&](int32_t q, int qs, int32_t cw) {
+        const int32_t t0 = q * G;
+        const int32_t cols = t0 >= cw + 32 ? c_nxt : c_cur;
+        const float wsel = t0 >= cw + 32 ? w_nxt : w_cur;
+#pragma unroll
+        for (int u = 0; u < G; ++u) {
+            const int32_t j = __shfl_sync(FULL, cols, (t0 + u) & 31);
+            if (GNN_RING_L2HINT && hint) {
+                const float we = __shfl_sync(FULL, wsel, (t0 + u) & 31);
+                const uint64_t pol = we > w_cold ? pol_cold : (we <= w_hot ? pol_hot : pol_mid);
+                if (t0 + u < len) cp_async16_pol(ring0 + (uint32_t)(qs * G + u) * 512u, Xl + (size_t)j * 32, pol);
+            } else {
+                if (t0 + u < len) cp_async16(ring0 + (uint32_t)(qs * G + u) * 512u, Xl + (size_t)j * 32);
+            }
+        }
+        cp_async_commit();
+    };
+#pragma unroll
+    for (int q = 0; q < P - 1; ++q) issue(q, q, 0);
+
+    const uint32_t wb0 = __ldg(a.win_flags + (b0 >> 5));
+    const int32_t k0 = __ldg(a.win_rowbase + (b0 >> 5)) + __popc(wb0 & ((1u << (b0 & 31)) - 1u));
+    // a span that starts inside a row starts inside a heavy row; that row's
+    // piece here goes to slot 2w (max: every piece of a row is folded into
+    // the tail slot of the span the row starts in)
+    bool head = b0 > 0 && !((__ldg(a.win_flags + ((b0 - 1) >> 5)) >> ((b0 - 1) & 31)) & 1u);
+    const int64_t max_head_slot =
+        (is_ext(OP) && head) ? 2 * (int64_t)(__ldg(a.win_rowstart + (b0 >> 5)) >> a.span_shift) + 1 : 0;
+    int32_t kofs = 0;  // lane l holds the id (and row factor) of the row of rank k0 + kofs + l
+    int32_t rid = k0 + lane < a.n_rows ? __ldg(a.ne_rows + k0 + lane) : 0;
+    if (weighted && !(GNN_RING_L2HINT && hint)) w_cur = lane < len ? edge_weight(a, b0 + lane, c_cur) : 1.f;
+    float rf = rsq ? __ldg(a.dinv_in + rid) : 1.f;
+
+    Acc<OP, T, 1> acc;
+    acc.reset();
+    int32_t k = 0;    // rows closed so far in this span
+    int32_t rs = b0;  // first edge of the open row
+    uint32_t last_closed = 1u;
+    int32_t q = 0;    // group summed next
+    int qs_c = 0, qs_i = P - 1;
+#pragma unroll 1
+    for (int32_t cw = 0; cw < len; cw += 32) {
+        const int32_t cb = b0 + cw;
+        const int n = min(32, len - cw);
+        const uint32_t bits_all = end_bits(a.win_flags, n_win, cb);
+        last_closed = (bits_all >> (n - 1)) & 1u;
+#pragma unroll 1
+        for (int u0 = 0; u0 < n; u0 += G, ++q) {
+            issue(q + P - 1, qs_i, cw);
+            qs_i = qs_i + 1 == P ? 0 : qs_i + 1;
+            // the next window's weights, once its column ids have arrived
+            if (weighted && u0 == (GNN_RING_L2HINT ? 8 : 16))
+                w_nxt = cw + 32 + lane < len ? edge_weight(a, cb + 32 + lane, c_nxt) : 1.f;
+            cp_async_wait<P - 1>();
+            uint4 xv[G];
+#pragma unroll
+            for (int u = 0; u < G; ++u) xv[u] = lds16(ring0 + (uint32_t)(qs_c * G + u) * 512u);
+            qs_c = qs_c + 1 == P ? 0 : qs_c + 1;
+#pragma unroll
+            for (int u = 0; u < G; ++u) {
+                if (u0 + u >= n) break;
+                const float ww = weighted ? __shfl_sync(FULL, w_cur, (u0 + u) & 31) : 1.f;
+                const int32_t j = is_ext(OP) ? __shfl_sync(FULL, c_cur, (u0 + u) & 31) : 0;
+                acc.add(&xv[u], ww, j);
+                if ((bits_all >> (u0 + u)) & 1u) {
+                    const int32_t e = cb + u0 + u;
+                    if (head) {
+                        if constexpr (is_ext(OP)) fold_max_piece<OP, T>(a, max_head_slot, acc, lane);
+                        else store_piece<OP, T>(a, a.carry, 2 * (int64_t)w, acc, lane);
+                        head = false;
+                    } else {
+                        if (k - kofs == 32) {
+                            kofs += 32;
+                            rid = k0 + kofs + lane < a.n_rows ? __ldg(a.ne_rows + k0 + kofs + lane) : 0;
+                            if (rsq) rf = __ldg(a.dinv_in + rid);
+                        }
+                        const int32_t r = __shfl_sync(FULL, rid, k - kofs);
+                        const float f = rsq ? __shfl_sync(FULL, rf, k - kofs) : 1.f;
+                        store_row_f<OP, T, 1>(a, r, e - rs + 1, f, acc, lane);
+                    }
+                    acc.reset();
+                    ++k;
+                    rs = e + 1;
+                }
+            }
+        }
+        // advance the column window (a window too short to reach the weight
+        // fetch above has no successor within the span)
+        c_cur = c_nxt;
+        c_nxt = cw + 64 + lane < len ? ld_col(a.colidx + cb + 64 + lane) : 0;
+        w_cur = w_nxt;
+    }
+    // no copy may still target this warp's ring when the warp exits
+    cp_async_wait<0>();
+    // a heavy row reaches past this span: leave its piece
+    if (!last_closed) {
+        if constexpr (is_ext(OP)) fold_max_piece<OP, T>(a, head ? max_head_slot : 2 * (int64_t)w + 1, acc, lane);
+        else store_piece<OP, T>(a, a.carry, 2 * (int64_t)w + (head ? 0 : 1), acc, lane);
+    }
+}
+
 // Finalise heavy rows (degree > S).  Such a row's edges lie in spans
 // s0..s1 and it left one piece in each: the tail piece of span s0 (slot
 // 2*s0+1), then the head pieces of spans s0+1..s1 (slots 2*s), in edge order
@@ -1291,10 +1527,22 @@ static cudaError_t launch_span(const AggArgs &a, cudaStream_t s) {
     // registers fit 28 (R-MAT scale 22 SpMM 4.89 against 5.49 ms); fp32 rows
     // keep k_agg_span, which already fits 32 (scale 17: 0.136 against 0.146)
     const bool lean = GNN_SPAN_LEAN && !is_ext(OP) && sizeof(T) == 2;
-    if (lean)
+    if (GNN_SPAN_RING && (GNN_RING_EXT || !is_ext(OP))) {
+        static std::once_flag once;
+        static cudaError_t attr = cudaSuccess;
+        std::call_once(once, [] {
+            // the rings of GNN_RING_MINB blocks must fit one SM's shared memory
+            attr = cudaFuncSetAttribute(k_agg_span_ring<OP, T, WT>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                        cudaSharedmemCarveoutMaxShared);
+        });
+        if (attr != cudaSuccess) return attr;
+        const size_t smem = (size_t)(kSpanBlock / 32) * ring_bytes_per_warp<T>();
+        k_agg_span_ring<OP, T, WT><<<span_blocks, kSpanBlock, smem, s>>>(a);
+    } else if (lean) {
         k_agg_span_lean<(is_ext(OP) ? AGG_WSUM : OP), T, WT><<<span_blocks, kSpanBlock, 0, s>>>(a);
-    else
+    } else {
         k_agg_span<OP, T, WT><<<span_blocks, kSpanBlock, 0, s>>>(a);
+    }
     note_launch();
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || a.n_spans <= 1) return e;
