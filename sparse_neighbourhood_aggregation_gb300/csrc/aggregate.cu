@@ -1011,19 +1011,6 @@ __global__ void __launch_bounds__(kSpanBlock, GNN_LEAN_MINB * 64 / kSpanBlock) k
 #ifndef GNN_SPAN_RING
 #define GNN_SPAN_RING 1
 #endif
-// L2 priority of gathered rows by source out-degree (SpMM with the GCN
-// column factor only, where the factor 1/sqrt(d_out) is at hand): rows of
-// d_out < GNN_RING_COLD_DOUT are copied evict_first, rows of d_out >=
-// GNN_RING_HOT_DOUT evict_last (0 = no such class)
-#ifndef GNN_RING_L2HINT
-#define GNN_RING_L2HINT 0
-#endif
-#ifndef GNN_RING_COLD_DOUT
-#define GNN_RING_COLD_DOUT 48
-#endif
-#ifndef GNN_RING_HOT_DOUT
-#define GNN_RING_HOT_DOUT 0
-#endif
 // max / min on the ring kernel (1) or on k_agg_span (0)
 #ifndef GNN_RING_EXT
 #define GNN_RING_EXT 1
@@ -1033,27 +1020,13 @@ __host__ __device__ constexpr int ring_groups() { return sizeof(T) == 2 ? GNN_RI
 template <class T>
 __host__ __device__ constexpr int ring_bytes_per_warp() { return GNN_RING_G * ring_groups<T>() * 512; }
 
+// 16-byte copy global -> shared around L1 (.cg): copying through L1 (.ca)
+// measured slower on GB300 (R-MAT scale 22 SpMM 5.99 against 3.81 ms,
+// scale 17 sum 0.122 against 0.093 ms), and so did an L2 priority by source
+// out-degree through .L2::cache_hint (evict_first below d_out 16 or 48,
+// evict_last from 48, 64 or 128: 4.68-4.96 ms against 3.81)
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async16_pol(uint32_t dst, const void *src, uint64_t pol) {
-    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "l"(pol)
-                 : "memory");
-}
-__device__ __forceinline__ uint64_t l2_policy_evict_first() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-__device__ __forceinline__ uint64_t l2_policy_evict_normal() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-__device__ __forceinline__ uint64_t l2_policy_evict_last() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-    return p;
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
@@ -1098,35 +1071,15 @@ k_agg_span_ring(AggArgs a) {
     // column ids of the window being summed (c_cur) and of the next (c_nxt)
     int32_t c_cur = lane < len ? ld_col(a.colidx + b0 + lane) : 0;
     int32_t c_nxt = 32 + lane < len ? ld_col(a.colidx + b0 + 32 + lane) : 0;
-    float w_cur = 1.f, w_nxt = 1.f;
-    // L2 classes by out-degree (GCN column factor only)
-    const bool hint = GNN_RING_L2HINT && WT && !a.values && a.col_mode == COL_RSQRT;
-    uint64_t pol_cold = 0, pol_mid = 0, pol_hot = 0;
-    if (GNN_RING_L2HINT && hint) {
-        pol_cold = l2_policy_evict_first();
-        pol_mid = l2_policy_evict_normal();
-        pol_hot = GNN_RING_HOT_DOUT > 0 ? l2_policy_evict_last() : pol_mid;
-        w_cur = lane < len ? edge_weight(a, b0 + lane, c_cur) : 1.f;
-    }
-    // weight above which a row is cold, at or below which it is hot
-    const float w_cold = rsqrtf((float)GNN_RING_COLD_DOUT);
-    const float w_hot = GNN_RING_HOT_DOUT > 0 ? rsqrtf((float)GNN_RING_HOT_DOUT) : 0.f;
     // copy the rows of group q (edges b0 + qG ..) into slot group qs; cw is
     // the span offset of c_cur's window (the group lies in it or the next)
     auto issue = [&](int32_t q, int qs, int32_t cw) {
         const int32_t t0 = q * G;
         const int32_t cols = t0 >= cw + 32 ? c_nxt : c_cur;
-        const float wsel = t0 >= cw + 32 ? w_nxt : w_cur;
 #pragma unroll
         for (int u = 0; u < G; ++u) {
             const int32_t j = __shfl_sync(FULL, cols, (t0 + u) & 31);
-            if (GNN_RING_L2HINT && hint) {
-                const float we = __shfl_sync(FULL, wsel, (t0 + u) & 31);
-                const uint64_t pol = we > w_cold ? pol_cold : (we <= w_hot ? pol_hot : pol_mid);
-                if (t0 + u < len) cp_async16_pol(ring0 + (uint32_t)(qs * G + u) * 512u, Xl + (size_t)j * 32, pol);
-            } else {
-                if (t0 + u < len) cp_async16(ring0 + (uint32_t)(qs * G + u) * 512u, Xl + (size_t)j * 32);
-            }
+            if (t0 + u < len) cp_async16(ring0 + (uint32_t)(qs * G + u) * 512u, Xl + (size_t)j * 32);
         }
         cp_async_commit();
     };
@@ -1143,7 +1096,8 @@ k_agg_span_ring(AggArgs a) {
         (is_ext(OP) && head) ? 2 * (int64_t)(__ldg(a.win_rowstart + (b0 >> 5)) >> a.span_shift) + 1 : 0;
     int32_t kofs = 0;  // lane l holds the id (and row factor) of the row of rank k0 + kofs + l
     int32_t rid = k0 + lane < a.n_rows ? __ldg(a.ne_rows + k0 + lane) : 0;
-    if (weighted && !(GNN_RING_L2HINT && hint)) w_cur = lane < len ? edge_weight(a, b0 + lane, c_cur) : 1.f;
+    float w_cur = (weighted && lane < len) ? edge_weight(a, b0 + lane, c_cur) : 1.f;
+    float w_nxt = 1.f;
     float rf = rsq ? __ldg(a.dinv_in + rid) : 1.f;
 
     Acc<OP, T, 1> acc;
@@ -1164,7 +1118,7 @@ k_agg_span_ring(AggArgs a) {
             issue(q + P - 1, qs_i, cw);
             qs_i = qs_i + 1 == P ? 0 : qs_i + 1;
             // the next window's weights, once its column ids have arrived
-            if (weighted && u0 == (GNN_RING_L2HINT ? 8 : 16))
+            if (weighted && u0 == 16)
                 w_nxt = cw + 32 + lane < len ? edge_weight(a, cb + 32 + lane, c_nxt) : 1.f;
             cp_async_wait<P - 1>();
             uint4 xv[G];
@@ -1199,8 +1153,8 @@ k_agg_span_ring(AggArgs a) {
                 }
             }
         }
-        // advance the column window (a window too short to reach the weight
-        // fetch above has no successor within the span)
+        // advance the column window (a window of fewer than 17 edges never
+        // reached u0 == 16: its successor is past the span's end anyway)
         c_cur = c_nxt;
         c_nxt = cw + 64 + lane < len ? ld_col(a.colidx + cb + 64 + lane) : 0;
         w_cur = w_nxt;
