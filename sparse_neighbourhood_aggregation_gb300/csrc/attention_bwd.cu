@@ -91,32 +91,47 @@ __device__ __forceinline__ void st_f32(float *p, const float *f) {
     for (int c = 0; c < NC; c += 4) *reinterpret_cast<float4 *>(p + c) = make_float4(f[c], f[c + 1], f[c + 2], f[c + 3]);
 }
 
-// sum over the lph lanes of this lane's head (lph a power of two)
+// sum over the lph lanes of this lane's head (lph a power of two).  LPH > 0
+// fixes lph at compile time: the shuffles then unroll, where a loop with a
+// runtime trip count makes the compiler guard every shuffle against
+// divergence (measured on GB300 in the GATv2 backward: ~35 of its 210 warp
+// instructions per edge were those guards)
+template <int LPH>
 __device__ __forceinline__ float head_sum(float x, int lph) {
-    for (int o = lph >> 1; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    if constexpr (LPH > 0) {
+#pragma unroll
+        for (int o = LPH >> 1; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    } else {
+        for (int o = lph >> 1; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    }
     return x;
 }
 
-template <int NC>
+template <int NC, int LPH>
 __global__ void __launch_bounds__(256) k_gt_bwd_q(GtBwdArgs a) {
     const int lane = threadIdx.x & 31;
     const int32_t i = (int32_t)(((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5);
     if (i >= a.n) return;
-    const int lph = a.D / NC;
+    const int lph = LPH > 0 ? LPH : a.D / NC;
     const int h = (lane * NC) / a.D;
     const int64_t ro = (int64_t)i * a.HD + lane * NC;
     float q[NC], o[NC], g[NC], dq[NC];
     ld_bf16<NC>(a.Q + ro, q);
     ld_f32<NC>(a.O + ro, o);
     ld_f32<NC>(a.dO + ro, g);
-    float p = 0.f;
+    // Delta = <O_i, dO_i> in the same two-chain order as <dO_i, v_j> below,
+    // so a row whose only edge gives O_i = v_j gets ds = 0 exactly
+    uint64_t p2 = pk2(0.f, 0.f);
+#pragma unroll
+    for (int c = 0; c < NC; c += 2) p2 = fma2(pk2(g[c], g[c + 1]), pk2(o[c], o[c + 1]), p2);
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
-        p = fmaf(o[c], g[c], p);
         q[c] *= a.scale;
         dq[c] = 0.f;
     }
-    const float delta = head_sum(p, lph);
+    float p0, p1;
+    upk2(p2, p0, p1);
+    const float delta = head_sum<LPH>(p0 + p1, lph);
     const int32_t b = __ldg(a.rowptr + i), e = __ldg(a.rowptr + i + 1);
     const float L = e > b ? __ldg(a.lse + (int64_t)i * a.heads + h) : 0.f;
     for (int32_t cb = b; cb < e; cb += 32) {
@@ -135,17 +150,23 @@ __global__ void __launch_bounds__(256) k_gt_bwd_q(GtBwdArgs a) {
 #pragma unroll
             for (int u = 0; u < kBwdU; ++u) {
                 if (u0 + u >= n) break;
-                float s = 0.f, da = 0.f;
+                // <q_i, k_j> and <dO_i, v_j> on pairs of channels (f32x2)
+                uint64_t s2 = pk2(0.f, 0.f), d2 = pk2(0.f, 0.f);
 #pragma unroll
-                for (int c = 0; c < NC; ++c) {
-                    s = fmaf(q[c], kf[u][c], s);
-                    da = fmaf(g[c], vf[u][c], da);
+                for (int c = 0; c < NC; c += 2) {
+                    s2 = fma2(pk2(q[c], q[c + 1]), pk2(kf[u][c], kf[u][c + 1]), s2);
+                    d2 = fma2(pk2(g[c], g[c + 1]), pk2(vf[u][c], vf[u][c + 1]), d2);
                 }
-                s = head_sum(s, lph);
-                da = head_sum(da, lph);
+                float s0, s1, d0, d1;
+                upk2(s2, s0, s1);
+                upk2(d2, d0, d1);
+                const float s = head_sum<LPH>(s0 + s1, lph);
+                const float da = head_sum<LPH>(d0 + d1, lph);
                 const float ds = __expf(s - L) * (da - delta);
+                const uint64_t ds2 = pk2(ds, ds);
 #pragma unroll
-                for (int c = 0; c < NC; ++c) dq[c] = fmaf(ds, kf[u][c], dq[c]);
+                for (int c = 0; c < NC; c += 2)
+                    upk2(fma2(ds2, pk2(kf[u][c], kf[u][c + 1]), pk2(dq[c], dq[c + 1])), dq[c], dq[c + 1]);
             }
         }
     }
@@ -155,12 +176,12 @@ __global__ void __launch_bounds__(256) k_gt_bwd_q(GtBwdArgs a) {
     if (lane % lph == 0) a.delta[(int64_t)i * a.heads + h] = delta;
 }
 
-template <int NC>
+template <int NC, int LPH>
 __global__ void __launch_bounds__(256) k_gt_bwd_kv(GtBwdArgs a) {
     const int lane = threadIdx.x & 31;
     const int32_t j = (int32_t)(((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5);
     if (j >= a.n) return;
-    const int lph = a.D / NC;
+    const int lph = LPH > 0 ? LPH : a.D / NC;
     const int h = (lane * NC) / a.D;
     const int64_t ro = (int64_t)j * a.HD + lane * NC;
     float kf[NC], vf[NC], dk[NC], dv[NC];
@@ -192,20 +213,24 @@ __global__ void __launch_bounds__(256) k_gt_bwd_kv(GtBwdArgs a) {
 #pragma unroll
             for (int u = 0; u < kBwdU; ++u) {
                 if (u0 + u >= n) break;
-                float s = 0.f, da = 0.f;
+                uint64_t s2 = pk2(0.f, 0.f), d2 = pk2(0.f, 0.f);
 #pragma unroll
-                for (int c = 0; c < NC; ++c) {
-                    s = fmaf(qf[u][c], kf[c], s);
-                    da = fmaf(gf[u][c], vf[c], da);
+                for (int c = 0; c < NC; c += 2) {
+                    s2 = fma2(pk2(qf[u][c], qf[u][c + 1]), pk2(kf[c], kf[c + 1]), s2);
+                    d2 = fma2(pk2(gf[u][c], gf[u][c + 1]), pk2(vf[c], vf[c + 1]), d2);
                 }
-                s = head_sum(s, lph);
-                da = head_sum(da, lph);
+                float s0, s1, d0, d1;
+                upk2(s2, s0, s1);
+                upk2(d2, d0, d1);
+                const float s = head_sum<LPH>(s0 + s1, lph);
+                const float da = head_sum<LPH>(d0 + d1, lph);
                 const float al = __expf(s - Lh[u]);
                 const float ds = al * (da - Dh[u]);
+                const uint64_t al2 = pk2(al, al), ds2 = pk2(ds, ds);
 #pragma unroll
-                for (int c = 0; c < NC; ++c) {
-                    dv[c] = fmaf(al, gf[u][c], dv[c]);
-                    dk[c] = fmaf(ds, qf[u][c], dk[c]);
+                for (int c = 0; c < NC; c += 2) {
+                    upk2(fma2(al2, pk2(gf[u][c], gf[u][c + 1]), pk2(dv[c], dv[c + 1])), dv[c], dv[c + 1]);
+                    upk2(fma2(ds2, pk2(qf[u][c], qf[u][c + 1]), pk2(dk[c], dk[c + 1])), dk[c], dk[c + 1]);
                 }
             }
         }
@@ -296,7 +321,7 @@ struct GatRow {
     float L, G;      // AL: logsumexp and G of (i, head)
 };
 
-template <int SIDE, typename T, int NC>
+template <int SIDE, typename T, int NC, int LPH>
 __device__ __forceinline__ void gat_load_row(const GatBwdArgs &p, int32_t r, int ch, int hd, int lph,
                                              bool nonempty, GatRow<SIDE, NC> &R) {
     const int64_t ro = (int64_t)r * p.HD + ch;
@@ -305,10 +330,21 @@ __device__ __forceinline__ void gat_load_row(const GatBwdArgs &p, int32_t r, int
         float o[NC];
         ld_row<float, NC>(p.O, ro, o);
         ld_row<float, NC>(p.dO, ro, R.g);
+        // G = <O_i, dO_i> in the order the edge loop forms <dO_i, r_j> (two
+        // chains of channel pairs), so a row whose only edge gives O_i = r_j
+        // gets de = 0 exactly
         float s = 0.f;
+        if constexpr (NC == 1) {
+            s = R.g[0] * o[0];
+        } else {
+            uint64_t s2 = pk2(0.f, 0.f);
 #pragma unroll
-        for (int c = 0; c < NC; ++c) s = fmaf(o[c], R.g[c], s);
-        R.G = head_sum(s, lph);
+            for (int c = 0; c < NC; c += 2) s2 = fma2(pk2(R.g[c], R.g[c + 1]), pk2(o[c], o[c + 1]), s2);
+            float s0, s1;
+            upk2(s2, s0, s1);
+            s = s0 + s1;
+        }
+        R.G = head_sum<LPH>(s, lph);
         R.L = nonempty ? __ldg(p.lse + (int64_t)r * p.heads + hd) : 0.f;
     } else {
         ld_row<T, NC>(p.Cr, ro, R.own);
@@ -382,7 +418,7 @@ struct EdgeData {
 // Gradient contributions of the edges [eb, ee) of one row into acc (dl_i or
 // dr_j) and, on the AL side, ga (attention vector).  The gathers run one
 // edge ahead of the arithmetic.
-template <int SIDE, typename T, int NC>
+template <int SIDE, typename T, int NC, int LPH>
 __device__ __forceinline__ void gat_edges(const GatBwdArgs &p, const GatRow<SIDE, NC> &R, const float *av,
                                           int lane, int ch, int hd, int lph, int32_t eb, int32_t ee,
                                           float *acc, float *ga) {
@@ -405,36 +441,66 @@ __device__ __forceinline__ void gat_edges(const GatBwdArgs &p, const GatRow<SIDE
         if constexpr (SIDE == GAT_AL) {
             cur.v.unpack(rr);                    // r_j of neighbour j
 #pragma unroll
-            for (int c = 0; c < NC; ++c) { x[c] = R.own[c] + rr[c]; gg[c] = R.g[c]; }
+            for (int c = 0; c < NC; ++c) gg[c] = R.g[c];
             L = R.L;
             G = R.G;
         } else {
-            float lk[NC];
-            cur.v.unpack(lk);                    // l_i of destination i
+            cur.v.unpack(x);                     // l_i of destination i (x = l_i + r_j below)
             cur.g.unpack(gg);                    // dO_i
             L = cur.L;
             G = cur.G;
 #pragma unroll
-            for (int c = 0; c < NC; ++c) { rr[c] = R.own[c]; x[c] = lk[c] + rr[c]; }
+            for (int c = 0; c < NC; ++c) rr[c] = R.own[c];
         }
-        float ev = 0.f, pr = 0.f;
+        // x = l_i + r_j; lr = LeakyReLU(x); the score and <dO_i, r_j> on
+        // pairs of channels (f32x2), two chains each
+        float lr[NC];
+        uint64_t ev2 = pk2(0.f, 0.f), pr2 = pk2(0.f, 0.f);
 #pragma unroll
-        for (int c = 0; c < NC; ++c) {
-            ev = fmaf(av[c], x[c] > 0.f ? x[c] : p.slope * x[c], ev);
-            pr = fmaf(gg[c], rr[c], pr);
+        for (int c = 0; c < NC; c += 2) {
+            if constexpr (NC == 1) {
+                x[0] = (SIDE == GAT_AL ? R.own[0] : x[0]) + rr[0];
+                lr[0] = x[0] > 0.f ? x[0] : p.slope * x[0];
+                ev2 = pk2(av[0] * lr[0], 0.f);
+                pr2 = pk2(gg[0] * rr[0], 0.f);
+            } else {
+                const uint64_t a2 = SIDE == GAT_AL ? pk2(R.own[c], R.own[c + 1]) : pk2(x[c], x[c + 1]);
+                upk2(add2(a2, pk2(rr[c], rr[c + 1])), x[c], x[c + 1]);
+                lr[c] = x[c] > 0.f ? x[c] : p.slope * x[c];
+                lr[c + 1] = x[c + 1] > 0.f ? x[c + 1] : p.slope * x[c + 1];
+                ev2 = fma2(pk2(av[c], av[c + 1]), pk2(lr[c], lr[c + 1]), ev2);
+                pr2 = fma2(pk2(gg[c], gg[c + 1]), pk2(rr[c], rr[c + 1]), pr2);
+            }
         }
-        ev = head_sum(ev, lph);
-        pr = head_sum(pr, lph);
+        float e0, e1, p0, p1;
+        upk2(ev2, e0, e1);
+        upk2(pr2, p0, p1);
+        const float ev = head_sum<LPH>(e0 + e1, lph);
+        const float pr = head_sum<LPH>(p0 + p1, lph);
         const float al = __expf(ev - L);
         const float de = al * (pr - G);
+        // sigma'(x) a = a or slope a, so de sigma'(x) is de or de slope; and
+        // sigma'(x) x is LeakyReLU(x), already at hand
+        const float ds = de * p.slope;
 #pragma unroll
-        for (int c = 0; c < NC; ++c) {
-            const float d1 = x[c] > 0.f ? 1.f : p.slope;
-            if constexpr (SIDE == GAT_AL) {
-                acc[c] = fmaf(de * d1, av[c], acc[c]);
-                ga[c] = fmaf(de, d1 * x[c], ga[c]);
+        for (int c = 0; c < NC; c += 2) {
+            if constexpr (NC == 1) {
+                const float d = x[0] > 0.f ? de : ds;
+                if constexpr (SIDE == GAT_AL) {
+                    acc[0] = fmaf(d, av[0], acc[0]);
+                    ga[0] = fmaf(de, lr[0], ga[0]);
+                } else {
+                    acc[0] = fmaf(al, gg[0], fmaf(d, av[0], acc[0]));
+                }
             } else {
-                acc[c] = fmaf(al, gg[c], fmaf(de * d1, av[c], acc[c]));
+                const uint64_t d2 = pk2(x[c] > 0.f ? de : ds, x[c + 1] > 0.f ? de : ds);
+                uint64_t a2 = fma2(d2, pk2(av[c], av[c + 1]), pk2(acc[c], acc[c + 1]));
+                if constexpr (SIDE == GAT_AL) {
+                    upk2(fma2(pk2(de, de), pk2(lr[c], lr[c + 1]), pk2(ga[c], ga[c + 1])), ga[c], ga[c + 1]);
+                } else {
+                    a2 = fma2(pk2(al, al), pk2(gg[c], gg[c + 1]), a2);
+                }
+                upk2(a2, acc[c], acc[c + 1]);
             }
         }
     }
@@ -474,11 +540,11 @@ __device__ __forceinline__ void gat_flush_piece(const GatBwdArgs &p, int64_t w, 
 // the compiler's 94 registers; the edge loop waits on gathers, so resident
 // warps matter more than the few values spilled.
 constexpr int kGatMinBlocks = 3;
-template <int SIDE, typename T, int NC>
+template <int SIDE, typename T, int NC, int LPH>
 __global__ void __launch_bounds__(kGatWarps * 32, kGatMinBlocks) k_gatv2_bwd(GatBwdArgs p) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t w = (int64_t)blockIdx.x * kGatWarps + warp;
-    const int lph = p.D / NC;
+    const int lph = LPH > 0 ? LPH : p.D / NC;
     const int ch = (int)blockIdx.y * 32 * NC + lane * NC;  // this lane's first channel
     const int hd = ch / p.D;
     float av[NC], ga[NC];
@@ -493,11 +559,11 @@ __global__ void __launch_bounds__(kGatWarps * 32, kGatMinBlocks) k_gatv2_bwd(Gat
             const int32_t lo_beg = __ldg(p.rowptr + lo);
             if (lo_beg > e0 && lo_beg - __ldg(p.rowptr + lo - 1) > kGatE) {
                 GatRow<SIDE, NC> R;
-                gat_load_row<SIDE, T, NC>(p, lo - 1, ch, hd, lph, true, R);
+                gat_load_row<SIDE, T, NC, LPH>(p, lo - 1, ch, hd, lph, true, R);
                 float acc[NC];
 #pragma unroll
                 for (int c = 0; c < NC; ++c) acc[c] = 0.f;
-                gat_edges<SIDE, T, NC>(p, R, av, lane, ch, hd, lph, (int32_t)e0,
+                gat_edges<SIDE, T, NC, LPH>(p, R, av, lane, ch, hd, lph, (int32_t)e0,
                                        (int32_t)min((int64_t)lo_beg, e1), acc, ga);
                 gat_flush_piece<NC>(p, w, lo - 1, lane, ch, acc);
             }
@@ -515,7 +581,7 @@ __global__ void __launch_bounds__(kGatWarps * 32, kGatMinBlocks) k_gatv2_bwd(Gat
                 const int32_t r = rbase + k;
                 const int32_t rb = __shfl_sync(0xffffffffu, my_b, k), re = __shfl_sync(0xffffffffu, my_e, k);
                 GatRow<SIDE, NC> R;
-                gat_load_row<SIDE, T, NC>(p, r, ch, hd, lph, re > rb, R);
+                gat_load_row<SIDE, T, NC, LPH>(p, r, ch, hd, lph, re > rb, R);
                 if constexpr (SIDE == GAT_AL) {
                     if (lane % lph == 0) p.G[(int64_t)r * p.heads + hd] = R.G;
                 }
@@ -523,10 +589,10 @@ __global__ void __launch_bounds__(kGatWarps * 32, kGatMinBlocks) k_gatv2_bwd(Gat
 #pragma unroll
                 for (int c = 0; c < NC; ++c) acc[c] = 0.f;
                 if (re - rb > kGatE) {  // heavy: its first piece (the last owned row)
-                    gat_edges<SIDE, T, NC>(p, R, av, lane, ch, hd, lph, rb, (int32_t)e1, acc, ga);
+                    gat_edges<SIDE, T, NC, LPH>(p, R, av, lane, ch, hd, lph, rb, (int32_t)e1, acc, ga);
                     gat_flush_piece<NC>(p, w, r, lane, ch, acc);
                 } else {
-                    gat_edges<SIDE, T, NC>(p, R, av, lane, ch, hd, lph, rb, re, acc, ga);
+                    gat_edges<SIDE, T, NC, LPH>(p, R, av, lane, ch, hd, lph, rb, re, acc, ga);
                     st_row<NC>(p.grad + (int64_t)r * p.HD + ch, acc);
                 }
             }
@@ -649,16 +715,36 @@ void launch_gatv2_bwd(const GatBwdArgs &al, const GatBwdArgs &r, const GatBwdWs 
     k_gatv2_bwd_runs<<<(unsigned)((nt + 255) / 256), 256, 0, s>>>(al.rowptr, r.rowptr, al.n, al.n_runs, W.run_rows,
                                                                    W.run_rows_t, W.tickets,
                                                                    al.n_runs * gat_groups(al.HD), W.da_ticket);
-    k_gatv2_bwd<GAT_AL, T, NC><<<grid, kGatWarps * 32, 0, s>>>(al);
-    k_gatv2_bwd<GAT_R, T, NC><<<grid, kGatWarps * 32, 0, s>>>(r);
+    // lanes per head fixed at compile time for the 8-channel shapes (4 or 8
+    // lanes: 32- or 64-dimensional heads), a runtime value otherwise
+    const int lph = al.D / NC;
+    if (NC == 8 && lph == 8) {
+        k_gatv2_bwd<GAT_AL, T, NC, 8><<<grid, kGatWarps * 32, 0, s>>>(al);
+        k_gatv2_bwd<GAT_R, T, NC, 8><<<grid, kGatWarps * 32, 0, s>>>(r);
+    } else if (NC == 8 && lph == 4) {
+        k_gatv2_bwd<GAT_AL, T, NC, 4><<<grid, kGatWarps * 32, 0, s>>>(al);
+        k_gatv2_bwd<GAT_R, T, NC, 4><<<grid, kGatWarps * 32, 0, s>>>(r);
+    } else {
+        k_gatv2_bwd<GAT_AL, T, NC, 0><<<grid, kGatWarps * 32, 0, s>>>(al);
+        k_gatv2_bwd<GAT_R, T, NC, 0><<<grid, kGatWarps * 32, 0, s>>>(r);
+    }
     k_gatv2_bwd_da<<<kDaBlocks, 256, 0, s>>>(W.da_part, blocks, al.HD, W.da_part2, W.da_ticket, da);
 }
 
 template <int NC>
 void launch_gt_bwd(GtBwdArgs q, GtBwdArgs kv, cudaStream_t s) {
     const int blocks = (int)(((int64_t)q.n * 32 + 255) / 256);
-    k_gt_bwd_q<NC><<<blocks, 256, 0, s>>>(q);
-    k_gt_bwd_kv<NC><<<blocks, 256, 0, s>>>(kv);
+    const int lph = q.D / NC;
+    if (NC == 8 && lph == 4) {
+        k_gt_bwd_q<NC, 4><<<blocks, 256, 0, s>>>(q);
+        k_gt_bwd_kv<NC, 4><<<blocks, 256, 0, s>>>(kv);
+    } else if (NC == 8 && lph == 8) {
+        k_gt_bwd_q<NC, 8><<<blocks, 256, 0, s>>>(q);
+        k_gt_bwd_kv<NC, 8><<<blocks, 256, 0, s>>>(kv);
+    } else {
+        k_gt_bwd_q<NC, 0><<<blocks, 256, 0, s>>>(q);
+        k_gt_bwd_kv<NC, 0><<<blocks, 256, 0, s>>>(kv);
+    }
 }
 
 }  // namespace
