@@ -50,7 +50,10 @@ namespace {
 // backward, against 6.0-7.5 ms with 2, 7.5 with 4 and 13.7 with 8, and
 // asking for more resident blocks made it slower still; the gathered rows
 // thrash L1 before they are reused, so fewer rows in flight win.
-constexpr int kBwdU = 1;
+#ifndef GNN_GT_BWD_U
+#define GNN_GT_BWD_U 1
+#endif
+constexpr int kBwdU = GNN_GT_BWD_U;
 
 struct GtBwdArgs {
     const int32_t *rowptr, *colidx;      // CSR (destination rows) or CSR^T (source rows)

@@ -58,6 +58,8 @@ __host__ __device__ constexpr int o_col(int D) { return chunk_blocks(D) * 16; }
 __host__ __device__ constexpr int tmem_cols_for(int n) { return n <= 32 ? 32 : n <= 64 ? 64 : n <= 128 ? 128 : 256; }
 constexpr float kLog2eT = 1.4426950408889634f;
 constexpr float kLn2T = 0.6931471805599453f;
+// lazy-rescale margin of the tile softmax (base-2 units), as in the CSR kernels
+constexpr float kLazyT = 8.f;
 
 struct TileArgs {
     const int32_t *grp_blk_offset;
@@ -217,50 +219,82 @@ __global__ void __launch_bounds__(kRows) k_gt_tiles(TileArgs t) {
         }
         phase ^= 1u;
         tc_fence_after();
-        // pass 1: masked row maximum of this chunk (scores in base-2 units)
         const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-        float cm = -INFINITY;
+        // P = exp2(s - m) (0 where masked) into shared memory, its rounded
+        // weights summed into l; with track, also the chunk's masked maximum
+        // (scores in base-2 units) in cm
+        auto exp_pass = [&](bool write, bool track, float &cm) {
 #pragma unroll
-        for (int cc = 0; cc < NCMAX; cc += 32) {
-            if (cc >= NC) break;
-            uint32_t v[32];
-            tmem_ld32(lane_base + (uint32_t)cc, v);
-            const uint32_t mkc = (cc + 16 < NC) ? mk[cc / 32] : (mk[cc / 32] & 0xFFFFu);
+            for (int cc = 0; cc < NCMAX; cc += 32) {
+                if (cc >= NC) break;
+                uint32_t v[32];
+                tmem_ld32(lane_base + (uint32_t)cc, v);
+                const uint32_t mkc = (cc + 16 < NC) ? mk[cc / 32] : (mk[cc / 32] & 0xFFFFu);
+                const int nq = min(32, NC - cc);
 #pragma unroll
-            for (int q = 0; q < 32; ++q)
-                if ((mkc >> q) & 1u) cm = fmaxf(cm, __uint_as_float(v[q]) * t.qscale);
-        }
-        const float mn = fmaxf(m, cm);
-        const float sc = (m == -INFINITY) ? 0.f : exp2_approx(m - mn);
-        l *= sc;
+                for (int g8 = 0; g8 < 4; ++g8) {
+                    if (g8 * 8 >= nq) break;
+                    uint32_t pk[4];
 #pragma unroll
-        for (int d = 0; d < D; ++d) o[d] *= sc;
-        m = mn;
-        // pass 2: P = exp2(s - m) (0 where masked), into shared memory
-#pragma unroll
-        for (int cc = 0; cc < NCMAX; cc += 32) {
-            if (cc >= NC) break;
-            uint32_t v[32];
-            tmem_ld32(lane_base + (uint32_t)cc, v);
-            const uint32_t mkc = (cc + 16 < NC) ? mk[cc / 32] : (mk[cc / 32] & 0xFFFFu);
-            const int nq = min(32, NC - cc);
-#pragma unroll
-            for (int g8 = 0; g8 < 4; ++g8) {
-                if (g8 * 8 >= nq) break;
-                uint32_t pk[4];
-#pragma unroll
-                for (int q2 = 0; q2 < 4; ++q2) {
-                    const int q = g8 * 8 + 2 * q2;
-                    const float p0 = ((mkc >> q) & 1u) ? exp2_approx(__uint_as_float(v[q]) * t.qscale - m) : 0.f;
-                    const float p1 = ((mkc >> (q + 1)) & 1u) ? exp2_approx(__uint_as_float(v[q + 1]) * t.qscale - m) : 0.f;
-                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
-                    // the sum uses the rounded weights, the ones the product uses
-                    l += __low2float(b2) + __high2float(b2);
-                    pk[q2] = *reinterpret_cast<const uint32_t *>(&b2);
+                    for (int q2 = 0; q2 < 4; ++q2) {
+                        const int q = g8 * 8 + 2 * q2;
+                        const bool b0 = (mkc >> q) & 1u, b1 = (mkc >> (q + 1)) & 1u;
+                        const float s0 = __uint_as_float(v[q]) * t.qscale;
+                        const float s1 = __uint_as_float(v[q + 1]) * t.qscale;
+                        if (track) {
+                            if (b0) cm = fmaxf(cm, s0);
+                            if (b1) cm = fmaxf(cm, s1);
+                        }
+                        const float p0 = b0 ? exp2_approx(s0 - m) : 0.f;
+                        const float p1 = b1 ? exp2_approx(s1 - m) : 0.f;
+                        const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
+                        // the sum uses the rounded weights, the ones the product uses
+                        if (write) l += __low2float(b2) + __high2float(b2);
+                        pk[q2] = *reinterpret_cast<const uint32_t *>(&b2);
+                    }
+                    const int c = cc + g8 * 8;
+                    if (write)
+                        st16s(sP + ((tid / 8) * (NC / 8) + c / 8) * 128 + (tid % 8) * 16,
+                              make_uint4(pk[0], pk[1], pk[2], pk[3]));
                 }
-                const int c = cc + g8 * 8;
-                st16s(sP + ((tid / 8) * (NC / 8) + c / 8) * 128 + (tid % 8) * 16, make_uint4(pk[0], pk[1], pk[2], pk[3]));
             }
+        };
+        // One pass when every row of the warp has a running maximum: P is
+        // formed against it while the chunk maximum is taken alongside, and a
+        // row keeps that P unless its chunk maximum passes the running one by
+        // more than kLazyT (weights then stay below 2^kLazyT).  Such rows, and
+        // every row in its first chunk, take two passes: the masked maximum,
+        // the rescale of l and o, then P.
+        bool redo = true;
+        if (__all_sync(0xffffffffu, m != -INFINITY)) {
+            float cm = -INFINITY;
+            const float l0 = l;
+            exp_pass(true, true, cm);
+            redo = cm > m + kLazyT;
+            if (redo) l = l0;
+        }
+        if (__any_sync(0xffffffffu, redo)) {
+            float cm = -INFINITY;
+#pragma unroll
+            for (int cc = 0; cc < NCMAX; cc += 32) {
+                if (cc >= NC) break;
+                uint32_t v[32];
+                tmem_ld32(lane_base + (uint32_t)cc, v);
+                const uint32_t mkc = (cc + 16 < NC) ? mk[cc / 32] : (mk[cc / 32] & 0xFFFFu);
+#pragma unroll
+                for (int q = 0; q < 32; ++q)
+                    if ((mkc >> q) & 1u) cm = fmaxf(cm, __uint_as_float(v[q]) * t.qscale);
+            }
+            if (redo) {
+                const float mn = fmaxf(m, cm);
+                const float sc = (m == -INFINITY) ? 0.f : exp2_approx(m - mn);
+                l *= sc;
+#pragma unroll
+                for (int d = 0; d < D; ++d) o[d] *= sc;
+                m = mn;
+            }
+            float unused = -INFINITY;
+            exp_pass(redo, false, unused);
         }
         fence_proxy_async_smem();
         tc_fence_before();
