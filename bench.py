@@ -347,6 +347,22 @@ def setup_c3(torch, gnn, w):
         lambda: gnn.gnn_gatv2_attn_bwd(g, gtr, C, None, a, heads, D, out, lse, dout, w["slope"]),
         b_bwd, "dl and da over CSR, dr over CSR^T, from the forward's out and lse (one projection: "
                "dC = dl + dr); timed apart, cold")}
+    # the Graph Transformer backward on this power-law graph (8 heads x 32,
+    # bf16 Q, K, V N(0,1) from the GT seeds): the edge-run schedule its mean
+    # degree selects, hub rows of ~40K edges cut into 256-edge pieces
+    gh, gd = 8, 32
+    gq, gk, gv = (_dev(torch, synth_mod().normal_bf16((n, gh * gd), 1.0, s)) for s in (4, 5, 6))
+    gout = torch.empty((n, gh * gd), dtype=torch.float32, device="cuda")
+    glse = torch.empty((n, gh), dtype=torch.float32, device="cuda")
+    gscale = 1.0 / float(np.sqrt(gd))
+    gnn.gnn_gt_attn_fwd(g, gq, gk, gv, gh, gd, gscale, out=gout, lse=glse)
+    gdout = torch.randn((n, gh * gd), dtype=torch.float32, device="cuda")
+    b_gt = 3 * n * gh * gd * 2 + 2 * n * gh * gd * 4 + 3 * n * gh * gd * 4 + 2 * idx
+    timed["gt_backward_rmat20"] = (
+        lambda: gnn.gnn_gt_attn_bwd(g, gtr, gq, gk, gv, gh, gd, gscale, gout, glse, gdout),
+        b_gt, "Graph Transformer backward on this graph (8 heads x 32, bf16 Q, K, V): dQ over CSR, "
+              "dK and dV over CSR^T on 256-edge runs (hub rows cut and summed in edge order); timed "
+              "apart, cold")
     cfg = {"workload": "c3_rmat20_gatv2", "graph": "R-MAT scale 20, edge factor 16, dedup + "
            "self-loops", "nodes": n, "edges": M, "heads": heads, "head_dim": D, "f_in": 256,
            "dtype": "bf16 H, W and C; fp32 softmax and accumulation; fp32 out",

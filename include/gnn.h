@@ -356,7 +356,10 @@ gnn_status gnn_gt_attn_fwd(const gnn_csr *g, const void *prep, const gnn_blocksp
 /* Backward of gnn_gt_attn_fwd on the CSR path (IO-aware GNN layers,
  * Appendix D.2: Delta = <O, dO> per destination and head, then the weights
  * recomputed from the stored logsumexp, dQ over the CSR and dK, dV over
- * CSR^T, each gradient row owned by one warp: no atomics, deterministic).
+ * CSR^T; no atomics on gradients, deterministic).  Graphs of mean degree 32
+ * or more give each gradient row one warp; sparser (power-law) graphs run
+ * warps over 256-edge runs, a row longer than a run cut into pieces that the
+ * last to finish sums in edge order.
  * g square; gt its transpose from gnn_csr_transpose (rows = sources).
  * Q, K, V bf16 [n, heads*head_dim] as in the forward; out, lse (natural
  * log) from the forward; dout fp32 [n, heads*head_dim]; dQ, dK, dV fp32

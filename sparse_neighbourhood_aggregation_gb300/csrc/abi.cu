@@ -12,7 +12,7 @@ size_t apply_perm_workspace_bytes(const gnn_csr *g);
 size_t blocksparse_workspace_bytes(const gnn_csr *g);
 size_t tile_spmm_workspace_bytes(const gnn_csr *g, int32_t F);
 size_t transpose_workspace_bytes(const gnn_csr *g);
-size_t gt_bwd_workspace_bytes(const gnn_csr *g, int32_t heads);
+size_t gt_bwd_workspace_bytes(const gnn_csr *g, int32_t heads, int32_t head_dim);
 size_t gatv2_bwd_workspace_bytes(const gnn_csr *g, int32_t heads, int32_t head_dim);
 size_t graph_stats_workspace_bytes(const gnn_csr *g);
 gnn_status check_csr_args(const gnn_csr *g);
@@ -46,7 +46,7 @@ extern "C" size_t gnn_workspace_size(int32_t op, const gnn_csr *g, int32_t F, in
         case GNN_OP_TRANSPOSE:
             return transpose_workspace_bytes(g);
         case GNN_OP_GT_BACKWARD:
-            return gt_bwd_workspace_bytes(g, heads);
+            return gt_bwd_workspace_bytes(g, heads, head_dim);
         case GNN_OP_GATV2_BACKWARD:
             return gatv2_bwd_workspace_bytes(g, heads, head_dim);
         case GNN_OP_GRAPH_STATS:

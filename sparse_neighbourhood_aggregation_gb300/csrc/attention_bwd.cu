@@ -5,9 +5,11 @@
 // CSR^T that recompute the weights from the stored logsumexp L).  For row i,
 // head h, edge j in N(i), with s_ij = scale <q_i, k_j>:
 //   alpha_ij = exp(s_ij - L_i),  ds_ij = alpha_ij (<dO_i, v_j> - Delta_i)
-//   dQ_i = scale sum_j ds_ij k_j          (k_gt_bwd_q, a warp per row of CSR)
-//   dK_j = scale sum_i ds_ij q_i,  dV_j = sum_i alpha_ij dO_i
-//                                        (k_gt_bwd_kv, a warp per row of CSR^T)
+//   dQ_i = scale sum_j ds_ij k_j          (over the CSR)
+//   dK_j = scale sum_i ds_ij q_i,  dV_j = sum_i alpha_ij dO_i   (over CSR^T)
+// Two schedules: a warp per row (k_gt_bwd_q, k_gt_bwd_kv) on graphs of long,
+// even rows, and the GATv2 backward's edge runs (k_gt_bwd_run) on power-law
+// graphs, chosen by the mean degree.
 // Each gradient row is owned by one warp, so there are no atomics and the
 // sums are deterministic.  Lane l holds channels [l*NC, (l+1)*NC) of the
 // HD = 32 NC channels; the D / NC lanes of a head reduce its dot products
@@ -672,6 +674,254 @@ __global__ void __launch_bounds__(256) k_gatv2_bwd_da(const float *__restrict__ 
     if (threadIdx.x == 0) *ticket = 0;
 }
 
+// ---------------------------------------------------------------- GT on edge runs
+
+// The GT backward on the GATv2 backward's schedule: a warp per run of kGatE
+// edges, owning the rows whose first edge lies in its run, a heavy row cut at
+// run boundaries and its pieces summed in edge order by the last to finish.
+// Q side over CSR (rows = destinations i): Delta_i = <O_i, dO_i>, then for
+// every edge j: s = <q_i, k_j> scale, alpha = exp(s - L_i), ds = alpha
+// (<dO_i, v_j> - Delta_i), dQ_i += scale ds k_j.  KV side over CSR^T (rows
+// = sources j): for every edge i: dV_j += alpha dO_i, dK_j += scale ds q_i.
+// Delta_i is formed by every warp that holds a piece of row i (a few
+// multiply-adds) and stored by the row's owner for the KV side.
+enum GtSide { GT_Q = 0, GT_KV = 1 };
+
+struct GtRunArgs {
+    const int32_t *rowptr, *colidx;  // Q: CSR; KV: CSR^T
+    const int32_t *run_rows;         // [n_runs + 1]
+    const __nv_bfloat16 *Q, *K, *V;
+    const float *O, *lse, *dO;
+    float *delta;                    // [n, heads]: Q writes, KV reads
+    float *dA, *dB;                  // Q: dQ; KV: dK, dV  [n, HD]
+    float *slots;                    // [2 n_runs, 2 HD] partial rows of heavy-row pieces
+    int32_t *tickets;                // [n_runs], zero on entry and on exit
+    int64_t nnz, n_runs;
+    int32_t n, heads, D, HD;
+    float scale;
+};
+
+// The row-side data of row r: Q side q_i (scaled), dO_i, L_i, Delta_i;
+// KV side k_j (scaled) and v_j.
+template <int SIDE, int NC, int LPH>
+struct GtRow {
+    float a[NC], b[NC];  // Q: q, dO;  KV: k, v
+    float L, Dl;
+    __device__ __forceinline__ void load(const GtRunArgs &p, int32_t r, int ch, int hd, int lph, bool nonempty) {
+        const int64_t ro = (int64_t)r * p.HD + ch;
+        if constexpr (SIDE == GT_Q) {
+            ld_bf16<NC>(p.Q + ro, a);
+            float o[NC];
+            ld_f32<NC>(p.O + ro, o);
+            ld_f32<NC>(p.dO + ro, b);
+            // Delta in the two-chain order of <dO_i, v_j> below: a row whose
+            // only edge gives O_i = v_j gets ds = 0 exactly
+            uint64_t p2 = pk2(0.f, 0.f);
+#pragma unroll
+            for (int c = 0; c < NC; c += 2) p2 = fma2(pk2(b[c], b[c + 1]), pk2(o[c], o[c + 1]), p2);
+            float p0, p1;
+            upk2(p2, p0, p1);
+            Dl = head_sum<LPH>(p0 + p1, lph);
+            L = nonempty ? __ldg(p.lse + (int64_t)r * p.heads + hd) : 0.f;
+#pragma unroll
+            for (int c = 0; c < NC; ++c) a[c] *= p.scale;
+        } else {
+            ld_bf16<NC>(p.K + ro, a);
+            ld_bf16<NC>(p.V + ro, b);
+#pragma unroll
+            for (int c = 0; c < NC; ++c) a[c] *= p.scale;
+        }
+    }
+};
+
+// What one edge gathers: Q side k_j, v_j; KV side q_i, dO_i, L_i, Delta_i.
+template <int SIDE, int NC>
+struct GtEdge {
+    Raw<__nv_bfloat16, NC> u;   // Q: k_j; KV: q_i
+    Raw<__nv_bfloat16, NC> v;   // Q: v_j
+    Raw<float, NC> g;           // KV: dO_i
+    float L, Dl;
+    __device__ __forceinline__ void load(const GtRunArgs &p, int32_t k, int ch, int hd) {
+        const int64_t ko = (int64_t)k * p.HD + ch;
+        if constexpr (SIDE == GT_Q) {
+            u.load(p.K, ko);
+            v.load(p.V, ko);
+        } else {
+            u.load(p.Q, ko);
+            g.load(p.dO, ko);
+            L = __ldg(p.lse + (int64_t)k * p.heads + hd);
+            Dl = __ldg(p.delta + (int64_t)k * p.heads + hd);
+        }
+    }
+};
+
+// The edges [eb, ee) of one row (gathers one edge ahead of the arithmetic);
+// acc holds W = NC (Q: dQ) or 2 NC (KV: dK then dV) floats.
+template <int SIDE, int NC, int LPH>
+__device__ __forceinline__ void gt_edges(const GtRunArgs &p, const GtRow<SIDE, NC, LPH> &R, int lane, int ch,
+                                         int hd, int lph, int32_t eb, int32_t ee, float *acc) {
+    if (eb >= ee) return;
+    int32_t base = eb;
+    int32_t cn = base + lane < ee ? __ldg(p.colidx + base + lane) : 0;
+    GtEdge<SIDE, NC> nxt;
+    nxt.load(p, __shfl_sync(0xffffffffu, cn, 0), ch, hd);
+    for (int32_t e = eb; e < ee; ++e) {
+        const GtEdge<SIDE, NC> cur = nxt;
+        if (e + 1 < ee) {
+            if (e + 1 - base == 32) {
+                base = e + 1;
+                cn = base + lane < ee ? __ldg(p.colidx + base + lane) : 0;
+            }
+            nxt.load(p, __shfl_sync(0xffffffffu, cn, e + 1 - base), ch, hd);
+        }
+        float x[NC], y[NC];
+        cur.u.unpack(x);  // Q: k_j; KV: q_i
+        if constexpr (SIDE == GT_Q) cur.v.unpack(y);  // v_j
+        else cur.g.unpack(y);                         // dO_i
+        // s = <q, k> (the scale sits in the row's q or k); da = <dO_i, v_j>
+        uint64_t s2 = pk2(0.f, 0.f), d2 = pk2(0.f, 0.f);
+#pragma unroll
+        for (int c = 0; c < NC; c += 2) {
+            s2 = fma2(pk2(R.a[c], R.a[c + 1]), pk2(x[c], x[c + 1]), s2);
+            if constexpr (SIDE == GT_Q) d2 = fma2(pk2(R.b[c], R.b[c + 1]), pk2(y[c], y[c + 1]), d2);
+            else d2 = fma2(pk2(y[c], y[c + 1]), pk2(R.b[c], R.b[c + 1]), d2);
+        }
+        float s0, s1, d0, d1;
+        upk2(s2, s0, s1);
+        upk2(d2, d0, d1);
+        const float sc = head_sum<LPH>(s0 + s1, lph);
+        const float da = head_sum<LPH>(d0 + d1, lph);
+        if constexpr (SIDE == GT_Q) {
+            const float ds = __expf(sc - R.L) * (da - R.Dl);
+            const uint64_t ds2 = pk2(ds, ds);
+#pragma unroll
+            for (int c = 0; c < NC; c += 2)
+                upk2(fma2(ds2, pk2(x[c], x[c + 1]), pk2(acc[c], acc[c + 1])), acc[c], acc[c + 1]);
+        } else {
+            const float al = __expf(sc - cur.L);
+            const float ds = al * (da - cur.Dl);
+            const uint64_t al2 = pk2(al, al), ds2 = pk2(ds, ds);
+#pragma unroll
+            for (int c = 0; c < NC; c += 2) {
+                upk2(fma2(ds2, pk2(x[c], x[c + 1]), pk2(acc[c], acc[c + 1])), acc[c], acc[c + 1]);
+                upk2(fma2(al2, pk2(y[c], y[c + 1]), pk2(acc[NC + c], acc[NC + c + 1])), acc[NC + c],
+                     acc[NC + c + 1]);
+            }
+        }
+    }
+}
+
+// Store a finished gradient row: Q dQ = scale acc; KV dK = scale acc[0:NC],
+// dV = acc[NC:2NC].
+template <int SIDE, int NC>
+__device__ __forceinline__ void gt_store(const GtRunArgs &p, int32_t r, int ch, const float *acc) {
+    const int64_t ro = (int64_t)r * p.HD + ch;
+    float t[NC];
+#pragma unroll
+    for (int c = 0; c < NC; ++c) t[c] = acc[c] * p.scale;
+    st_f32<NC>(p.dA + ro, t);
+    if constexpr (SIDE == GT_KV) st_f32<NC>(p.dB + ro, acc + NC);
+}
+
+// A piece of heavy row r leaves its W floats a lane in its slot; the last of
+// the row's pieces to arrive sums them in edge order and stores the row.
+template <int SIDE, int NC>
+__device__ __forceinline__ void gt_flush_piece(const GtRunArgs &p, int64_t w, int32_t r, int lane, int ch,
+                                               const float *acc) {
+    constexpr int W = SIDE == GT_Q ? NC : 2 * NC;
+    const int64_t stride = 2 * (int64_t)p.HD;
+    const int32_t rb = __ldg(p.rowptr + r), re = __ldg(p.rowptr + r + 1);
+    const int64_t wa = rb / kGatE, wb = ((int64_t)re - 1) / kGatE;
+    float *slot = p.slots + (2 * w + (w == wa ? 1 : 0)) * stride + (int64_t)lane * W;
+#pragma unroll
+    for (int c = 0; c < W; ++c) __stcg(slot + c, acc[c]);
+    __threadfence();
+    __syncwarp();
+    int t = 0;
+    if (lane == 0) t = atomicAdd(p.tickets + wa, 1);
+    t = __shfl_sync(0xffffffffu, t, 0);
+    if (t != (int)(wb - wa)) return;
+    __threadfence();
+    float sum[W];
+#pragma unroll
+    for (int c = 0; c < W; ++c) sum[c] = 0.f;
+    for (int64_t k = wa; k <= wb; ++k) {
+        const float *sk = p.slots + (2 * k + (k == wa ? 1 : 0)) * stride + (int64_t)lane * W;
+#pragma unroll
+        for (int c = 0; c < W; ++c) sum[c] += __ldcg(sk + c);
+    }
+    gt_store<SIDE, NC>(p, r, ch, sum);
+    __syncwarp();
+    if (lane == 0) p.tickets[wa] = 0;
+}
+
+// resident 256-thread blocks per SM asked of the compiler, per side (the KV
+// side holds dK and dV, 16 accumulators a lane at 8 channels: at 3 blocks it
+// spills 128 bytes yet runs the R-MAT scale 20 backward in 8.28 ms against
+// 9.70 at 2 blocks)
+#ifndef GNN_GT_RUN_MINB
+#define GNN_GT_RUN_MINB 3
+#endif
+#ifndef GNN_GT_RUN_MINB_KV
+#define GNN_GT_RUN_MINB_KV 3
+#endif
+
+template <int SIDE, int NC, int LPH>
+__global__ void __launch_bounds__(kGatWarps * 32, SIDE == GT_Q ? GNN_GT_RUN_MINB : GNN_GT_RUN_MINB_KV)
+k_gt_bwd_run(GtRunArgs p) {
+    constexpr int W = SIDE == GT_Q ? NC : 2 * NC;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t w = (int64_t)blockIdx.x * kGatWarps + warp;
+    if (w >= p.n_runs) return;
+    const int lph = LPH > 0 ? LPH : p.D / NC;
+    const int ch = lane * NC;
+    const int hd = ch / p.D;
+    const int64_t e0 = w * kGatE, e1 = min(e0 + kGatE, p.nnz);
+    const int32_t lo = __ldg(p.run_rows + w), lo_end = __ldg(p.run_rows + w + 1);
+    // a heavy row that started in an earlier run and reaches into this one
+    if (lo > 0 && e0 < p.nnz) {
+        const int32_t lo_beg = __ldg(p.rowptr + lo);
+        if (lo_beg > e0 && lo_beg - __ldg(p.rowptr + lo - 1) > kGatE) {
+            GtRow<SIDE, NC, LPH> R;
+            R.load(p, lo - 1, ch, hd, lph, true);
+            float acc[W];
+#pragma unroll
+            for (int c = 0; c < W; ++c) acc[c] = 0.f;
+            gt_edges<SIDE, NC, LPH>(p, R, lane, ch, hd, lph, (int32_t)e0, (int32_t)min((int64_t)lo_beg, e1), acc);
+            gt_flush_piece<SIDE, NC>(p, w, lo - 1, lane, ch, acc);
+        }
+    }
+    // owned rows, bounds read 32 at a time
+    for (int32_t rbase = lo; rbase < lo_end; rbase += 32) {
+        const int32_t rr = rbase + lane;
+        int32_t my_b = 0, my_e = 0;
+        if (rr < lo_end) {
+            my_b = __ldg(p.rowptr + rr);
+            my_e = __ldg(p.rowptr + rr + 1);
+        }
+        const int cnt = min(32, lo_end - rbase);
+        for (int k = 0; k < cnt; ++k) {
+            const int32_t r = rbase + k;
+            const int32_t rb = __shfl_sync(0xffffffffu, my_b, k), re = __shfl_sync(0xffffffffu, my_e, k);
+            GtRow<SIDE, NC, LPH> R;
+            R.load(p, r, ch, hd, lph, re > rb);
+            if constexpr (SIDE == GT_Q) {
+                if (lane % lph == 0) p.delta[(int64_t)r * p.heads + hd] = R.Dl;
+            }
+            float acc[W];
+#pragma unroll
+            for (int c = 0; c < W; ++c) acc[c] = 0.f;
+            if (re - rb > kGatE) {  // heavy: its first piece (the last owned row)
+                gt_edges<SIDE, NC, LPH>(p, R, lane, ch, hd, lph, rb, (int32_t)e1, acc);
+                gt_flush_piece<SIDE, NC>(p, w, r, lane, ch, acc);
+            } else {
+                gt_edges<SIDE, NC, LPH>(p, R, lane, ch, hd, lph, rb, re, acc);
+                gt_store<SIDE, NC>(p, r, ch, acc);
+            }
+        }
+    }
+}
+
 struct GatBwdWs {
     float *G, *slots, *da_part, *da_part2;
     int32_t *run_rows, *run_rows_t, *tickets, *da_ticket;
@@ -734,8 +984,48 @@ void launch_gatv2_bwd(const GatBwdArgs &al, const GatBwdArgs &r, const GatBwdWs 
     k_gatv2_bwd_da<<<kDaBlocks, 256, 0, s>>>(W.da_part, blocks, al.HD, W.da_part2, W.da_ticket, da);
 }
 
+// Schedule of the GT backward: 1 = a warp per row, 2 = edge runs, 0 = by
+// the graph's mean degree (runs below GNN_GT_RUNS_BELOW_DEGREE: power-law
+// graphs, whose hub rows would leave one warp with tens of thousands of
+// edges; a warp per row where rows are long and even).  Measured on GB300
+// (8 heads x 32, bf16): R-MAT scale 20 (mean degree 16, max 39,472) 43.0 ms
+// per row against 8.3 ms on runs; the clustered 262K-node graph (mean 77)
+// 4.04 ms per row against 4.96 ms on runs.
+#ifndef GNN_GT_BWD_SCHEDULE
+#define GNN_GT_BWD_SCHEDULE 0
+#endif
+#ifndef GNN_GT_RUNS_BELOW_DEGREE
+#define GNN_GT_RUNS_BELOW_DEGREE 32
+#endif
+inline bool gt_bwd_use_runs(const gnn_csr *g) {
+    if (GNN_GT_BWD_SCHEDULE == 1) return false;
+    if (GNN_GT_BWD_SCHEDULE == 2) return true;
+    return g->nnz < (int64_t)GNN_GT_RUNS_BELOW_DEGREE * g->n_rows;
+}
+
+struct GtBwdWs {
+    float *delta, *slots;
+    int32_t *run_rows, *run_rows_t, *tickets, *spare;
+    size_t bytes;
+};
+
+GtBwdWs gt_bwd_layout(const gnn_csr *g, int32_t heads, int32_t HD, void *base) {
+    const int64_t nr = n_runs(g->nnz, (int32_t)kGatE);
+    Carver cv(base);
+    GtBwdWs W{};
+    W.delta = cv.take<float>((size_t)std::max<int64_t>((int64_t)g->n_rows * heads, 1));
+    W.slots = cv.take<float>((size_t)(2 * nr) * 2 * HD);
+    W.run_rows = cv.take<int32_t>((size_t)(nr + 1));
+    W.run_rows_t = cv.take<int32_t>((size_t)(nr + 1));
+    W.tickets = cv.take<int32_t>((size_t)nr);
+    W.spare = cv.take<int32_t>(1);
+    W.bytes = cv.used;
+    return W;
+}
+
+// Warp per row: dQ and Delta over the CSR, then dK and dV over CSR^T.
 template <int NC>
-void launch_gt_bwd(GtBwdArgs q, GtBwdArgs kv, cudaStream_t s) {
+void launch_gt_bwd_rows(const GtBwdArgs &q, const GtBwdArgs &kv, cudaStream_t s) {
     const int blocks = (int)(((int64_t)q.n * 32 + 255) / 256);
     const int lph = q.D / NC;
     if (NC == 8 && lph == 4) {
@@ -750,10 +1040,23 @@ void launch_gt_bwd(GtBwdArgs q, GtBwdArgs kv, cudaStream_t s) {
     }
 }
 
+// Edge runs: run tables of CSR and CSR^T (and the tickets cleared), then dQ
+// and Delta over the CSR, then dK and dV over CSR^T
+template <int NC, int LPH>
+void launch_gt_bwd(const GtRunArgs &q, const GtRunArgs &kv, const GtBwdWs &W, cudaStream_t s) {
+    const int64_t nt = (int64_t)q.n + 1;
+    k_gatv2_bwd_runs<<<(unsigned)((nt + 255) / 256), 256, 0, s>>>(q.rowptr, kv.rowptr, q.n, q.n_runs, W.run_rows,
+                                                                   W.run_rows_t, W.tickets, q.n_runs, W.spare);
+    const int blocks = (int)((q.n_runs + kGatWarps - 1) / kGatWarps);
+    k_gt_bwd_run<GT_Q, NC, LPH><<<blocks, kGatWarps * 32, 0, s>>>(q);
+    k_gt_bwd_run<GT_KV, NC, LPH><<<blocks, kGatWarps * 32, 0, s>>>(kv);
+}
+
 }  // namespace
 
-size_t gt_bwd_workspace_bytes(const gnn_csr *g, int32_t heads) {
-    return round_up(sizeof(float) * (size_t)std::max<int64_t>((int64_t)g->n_rows * heads, 1), 256);
+size_t gt_bwd_workspace_bytes(const gnn_csr *g, int32_t heads, int32_t head_dim) {
+    if (heads <= 0 || head_dim <= 0) return 0;
+    return gt_bwd_layout(g, heads, heads * head_dim, nullptr).bytes;
 }
 
 size_t gatv2_bwd_workspace_bytes(const gnn_csr *g, int32_t heads, int32_t head_dim) {
@@ -786,34 +1089,71 @@ extern "C" gnn_status gnn_gt_attn_bwd(const gnn_csr *g, const gnn_csr *gt, const
     if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(out) || !aligned16(dout) ||
         !aligned16(dQ) || !aligned16(dK) || !aligned16(dV))
         return GNN_ERR_INVALID_ARG;
-    if (!ws || ws_bytes < gt_bwd_workspace_bytes(g, heads)) return GNN_ERR_WORKSPACE;
+    if (!ws || ws_bytes < gt_bwd_workspace_bytes(g, heads, head_dim)) return GNN_ERR_WORKSPACE;
     if (g->n_rows == 0) return GNN_OK;
 
-    GtBwdArgs q{};
+    const GtBwdWs W = gt_bwd_layout(g, heads, HD, ws);
+    GtRunArgs q{};
     q.rowptr = g->rowptr;
     q.colidx = g->colidx;
+    q.run_rows = W.run_rows;
     q.Q = static_cast<const __nv_bfloat16 *>(Q);
     q.K = static_cast<const __nv_bfloat16 *>(K);
     q.V = static_cast<const __nv_bfloat16 *>(V);
     q.O = out;
     q.lse = lse;
     q.dO = dout;
-    q.delta = static_cast<float *>(ws);
+    q.delta = W.delta;
     q.dA = dQ;
+    q.slots = W.slots;
+    q.tickets = W.tickets;
+    q.nnz = g->nnz;
+    q.n_runs = n_runs(g->nnz, (int32_t)kGatE);
     q.n = g->n_rows;
     q.heads = heads;
     q.D = head_dim;
     q.HD = HD;
     q.scale = scale;
-    GtBwdArgs kv = q;
+    GtRunArgs kv = q;
     kv.rowptr = gt->rowptr;
     kv.colidx = gt->colidx;
+    kv.run_rows = W.run_rows_t;
     kv.dA = dK;
     kv.dB = dV;
     cudaStream_t s = as_stream(stream);
-    if (NC == 4) launch_gt_bwd<4>(q, kv, s);
-    else launch_gt_bwd<8>(q, kv, s);
-    note_launch(2);
+    if (!gt_bwd_use_runs(g)) {
+        GtBwdArgs qr{};
+        qr.rowptr = g->rowptr;
+        qr.colidx = g->colidx;
+        qr.Q = q.Q;
+        qr.K = q.K;
+        qr.V = q.V;
+        qr.O = out;
+        qr.lse = lse;
+        qr.dO = dout;
+        qr.delta = W.delta;
+        qr.dA = dQ;
+        qr.n = g->n_rows;
+        qr.heads = heads;
+        qr.D = head_dim;
+        qr.HD = HD;
+        qr.scale = scale;
+        GtBwdArgs kvr = qr;
+        kvr.rowptr = gt->rowptr;
+        kvr.colidx = gt->colidx;
+        kvr.dA = dK;
+        kvr.dB = dV;
+        if (NC == 4) launch_gt_bwd_rows<4>(qr, kvr, s);
+        else launch_gt_bwd_rows<8>(qr, kvr, s);
+        note_launch(2);
+        GNN_LAUNCH_CHECK();
+        return GNN_OK;
+    }
+    if (NC == 8 && lph == 4) launch_gt_bwd<8, 4>(q, kv, W, s);
+    else if (NC == 8 && lph == 8) launch_gt_bwd<8, 8>(q, kv, W, s);
+    else if (NC == 8) launch_gt_bwd<8, 0>(q, kv, W, s);
+    else launch_gt_bwd<4, 0>(q, kv, W, s);
+    note_launch(3);
     GNN_LAUNCH_CHECK();
     return GNN_OK;
 }
