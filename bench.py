@@ -30,7 +30,8 @@ Metric: aggregation Gedge*feat/s = edges x features aggregated per second
 launching stream around every layer, an L2 flush (a 512 MB write, outside
 the events) before EVERY timed layer ("cold"); median, min and mean over the
 K steps; "warm" = the same layer K times back to back with no flush (the
-second-pass cache mode).  Max over ranks.  The roofline object describes
+second-pass cache mode); for the scale-17 layers also "warm_graph", 20
+back-to-back calls captured in one CUDA graph and replayed, per call.  Max over ranks.  The roofline object describes
 the headline step's dominant kernel: achieved = its compulsory bytes
 (indices read once, every feature row read once, every output written
 once) / its mean event-timed duration; traffic = the DRAM bytes of an ncu
@@ -701,6 +702,38 @@ def time_warm(torch, fn, steps, stream):
     return [e0.elapsed_time(e1) for e0, e1 in evs]
 
 
+def time_warm_graph(torch, fn, steps, stream, reps=20):
+    """fn() `reps` times back to back captured in one CUDA graph, replayed
+    `steps` times: the warm per-call time without per-launch host overhead
+    (the layers of the scale-17 workload are tens of microseconds).  Returns
+    (per-call ms list, None) or (None, the capture error)."""
+    try:
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            fn()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for _ in range(reps):
+                fn()
+        graph.replay()
+        torch.cuda.synchronize()
+        evs = [_ev(torch) for _ in range(steps)]
+        for e0, e1 in evs:
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        out = [e0.elapsed_time(e1) / reps for e0, e1 in evs]
+        del graph
+        return out, None
+    except Exception as e:  # reported in the line, the cold and warm figures stand
+        torch.cuda.synchronize()
+        return None, f"{type(e).__name__}: {str(e)[:160]}"
+
+
 def summary(ms):
     return {"ms_median": float(np.median(ms)), "ms_min": float(np.min(ms)),
             "ms_mean": float(np.mean(ms))}
@@ -870,6 +903,12 @@ def measure(torch, gnn, W, args, flush, stream, hbm, base_bytes):
     for L in W.layers:
         warm = time_warm(torch, lambda: L.fn(W.inputs), args.steps, stream)
         layers[L.name] = layer_report(torch, W, L, per[L.name], warm, hbm)
+        if W.name == "c2_rmat17":
+            g_ms, g_err = time_warm_graph(torch, lambda: L.fn(W.inputs), args.steps, stream)
+            if g_ms is not None:
+                layers[L.name]["warm_graph_ms_median"] = float(np.median(g_ms))
+            else:
+                layers[L.name]["warm_graph_error"] = g_err
     return step_ms, layers, launches, peak_mem
 
 
