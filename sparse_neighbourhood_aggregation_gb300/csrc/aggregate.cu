@@ -1011,6 +1011,10 @@ __global__ void __launch_bounds__(kSpanBlock, GNN_LEAN_MINB * 64 / kSpanBlock) k
 #ifndef GNN_SPAN_RING
 #define GNN_SPAN_RING 1
 #endif
+// groups of G edges without a row end summed on a path without per-edge tests
+#ifndef GNN_RING_FAST
+#define GNN_RING_FAST 1
+#endif
 // max / min on the ring kernel (1) or on k_agg_span (0)
 #ifndef GNN_RING_EXT
 #define GNN_RING_EXT 1
@@ -1125,6 +1129,16 @@ k_agg_span_ring(AggArgs a) {
 #pragma unroll
             for (int u = 0; u < G; ++u) xv[u] = lds16(ring0 + (uint32_t)(qs_c * G + u) * 512u);
             qs_c = qs_c + 1 == P ? 0 : qs_c + 1;
+            if (GNN_RING_FAST && u0 + G <= n && ((bits_all >> u0) & ((1u << G) - 1u)) == 0u) {
+                // no row ends among these G edges: sum them without the tests
+#pragma unroll
+                for (int u = 0; u < G; ++u) {
+                    const float ww = weighted ? __shfl_sync(FULL, w_cur, (u0 + u) & 31) : 1.f;
+                    const int32_t j = is_ext(OP) ? __shfl_sync(FULL, c_cur, (u0 + u) & 31) : 0;
+                    acc.add(&xv[u], ww, j);
+                }
+                continue;
+            }
 #pragma unroll
             for (int u = 0; u < G; ++u) {
                 if (u0 + u >= n) break;
@@ -1183,7 +1197,10 @@ __device__ __forceinline__ int64_t piece_slot(int32_t s0, int32_t p) {
     return p == 0 ? 2 * (int64_t)s0 + 1 : 2 * ((int64_t)s0 + p);
 }
 
-constexpr int kFixBlocksPerSm = 4;
+#ifndef GNN_FIX_BLOCKS
+#define GNN_FIX_BLOCKS 4
+#endif
+constexpr int kFixBlocksPerSm = GNN_FIX_BLOCKS;
 #ifndef GNN_FIX_WORDS
 #define GNN_FIX_WORDS 4
 #endif
