@@ -1499,13 +1499,10 @@ static cudaError_t launch_span(const AggArgs &a, cudaStream_t s) {
     // keep k_agg_span, which already fits 32 (scale 17: 0.136 against 0.146)
     const bool lean = GNN_SPAN_LEAN && !is_ext(OP) && sizeof(T) == 2;
     if (GNN_SPAN_RING && (GNN_RING_EXT || !is_ext(OP))) {
-        static std::once_flag once;
-        static cudaError_t attr = cudaSuccess;
-        std::call_once(once, [] {
-            // the rings of GNN_RING_MINB blocks must fit one SM's shared memory
-            attr = cudaFuncSetAttribute(k_agg_span_ring<OP, T, WT>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                        cudaSharedmemCarveoutMaxShared);
-        });
+        // the rings of GNN_RING_MINB blocks must fit one SM's shared memory
+        const cudaError_t attr = func_attr(reinterpret_cast<const void *>(k_agg_span_ring<OP, T, WT>),
+                                           cudaFuncAttributePreferredSharedMemoryCarveout,
+                                           cudaSharedmemCarveoutMaxShared);
         if (attr != cudaSuccess) return attr;
         const size_t smem = (size_t)(kSpanBlock / 32) * ring_bytes_per_warp<T>();
         k_agg_span_ring<OP, T, WT><<<span_blocks, kSpanBlock, smem, s>>>(a);

@@ -755,12 +755,8 @@ static void ring_shape(AttnArgs &a) {
 
 template <int KIND, class T, int CPL, int LPH>
 static cudaError_t launch_attn_lph(const AttnArgs &a, cudaStream_t s) {
-    static std::once_flag once;
-    static cudaError_t attr = cudaSuccess;
-    std::call_once(once, [] {
-        attr = cudaFuncSetAttribute(k_attn<KIND, T, CPL, LPH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    227 * 1024);
-    });
+    const cudaError_t attr = func_attr(reinterpret_cast<const void *>(k_attn<KIND, T, CPL, LPH>),
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (attr != cudaSuccess) return attr;
     if (!Geo<KIND, T, CPL, LPH>::agrees(a)) return cudaErrorInvalidValue;
     const size_t smem = (size_t)kAttnWarps * a.ring_bytes;

@@ -68,6 +68,11 @@ int32_t *device_error_word();
 // Number of SMs of the current device (cached).
 int sm_count();
 
+// cudaFuncSetAttribute(fn, attr, value) once per (kernel, current device,
+// attribute, value): a kernel attribute belongs to a device's context, so a
+// process that drives several GPUs sets it on each before launching there.
+cudaError_t func_attr(const void *fn, cudaFuncAttribute attr, int value);
+
 #define GNN_LAUNCH_CHECK()                                        \
     do {                                                          \
         cudaError_t e__ = cudaGetLastError();                     \

@@ -351,11 +351,8 @@ gnn_status projection_tc_lin(const void *H, int64_t n, int32_t Fi, const void *W
     p.stages = stages;
     const size_t smem = fixed + (size_t)stages * kStageBytes;
 
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(k_proj_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    });
+    const cudaError_t attr_err = func_attr(reinterpret_cast<const void *>(k_proj_tc),
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (attr_err != cudaSuccess) return cuda_status(attr_err);
     const int64_t n_tiles = (n + kBM - 1) / kBM;
     const int grid = (int)std::min<int64_t>(n_tiles, sm_count());

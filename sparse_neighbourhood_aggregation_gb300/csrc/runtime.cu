@@ -5,6 +5,8 @@
 
 #include <cub/device/device_scan.cuh>
 
+#include <set>
+#include <tuple>
 #include "common.cuh"
 
 namespace gnn {
@@ -29,6 +31,20 @@ int32_t *device_error_word() {
         ptrs[dev] = static_cast<int32_t *>(p);
     }
     return ptrs[dev];
+}
+
+cudaError_t func_attr(const void *fn, cudaFuncAttribute attr, int value) {
+    static std::mutex mu;
+    static std::set<std::tuple<const void *, int, int, int>> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const auto key = std::make_tuple(fn, dev, (int)attr, value);
+    std::lock_guard<std::mutex> lk(mu);
+    if (done.count(key)) return cudaSuccess;
+    e = cudaFuncSetAttribute(fn, attr, value);
+    if (e == cudaSuccess) done.insert(key);
+    return e;
 }
 
 int sm_count() {

@@ -378,11 +378,8 @@ size_t tile_smem_bytes() {
 
 template <int D>
 cudaError_t launch_tiles(const TileArgs &t, int32_t n_groups, cudaStream_t s) {
-    static std::once_flag once;
-    static cudaError_t attr = cudaSuccess;
-    std::call_once(once, [] {
-        attr = cudaFuncSetAttribute(k_gt_tiles<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    });
+    const cudaError_t attr = func_attr(reinterpret_cast<const void *>(k_gt_tiles<D>),
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (attr != cudaSuccess) return attr;
     k_gt_tiles<D><<<(unsigned)((int64_t)n_groups * t.heads), kRows, tile_smem_bytes<D>(), s>>>(t);
     return cudaGetLastError();
