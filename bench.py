@@ -31,7 +31,12 @@ launching stream around every layer, an L2 flush (a 512 MB write, outside
 the events) before EVERY timed layer ("cold"); median, min and mean over the
 K steps; "warm" = the same layer K times back to back with no flush (the
 second-pass cache mode); for the scale-17 layers also "warm_graph", 20
-back-to-back calls captured in one CUDA graph and replayed, per call.  Max over ranks.  The roofline object describes
+back-to-back calls captured in one CUDA graph and replayed, per call.  Max
+over ranks.  e2e: the headline step through the same API starting from
+pinned host buffers, every step copying its inputs in and reading its
+results back inside the timed region, steps pipelined over three streams
+(copy in, compute, read back; the sequential per-step figure beside it).
+The roofline object describes
 the headline step's dominant kernel: achieved = its compulsory bytes
 (indices read once, every feature row read once, every output written
 once) / its mean event-timed duration; traffic = the DRAM bytes of an ncu
@@ -690,6 +695,81 @@ def time_cold(torch, fn, steps, flush, stream):
     return [e0.elapsed_time(e1) for e0, e1 in evs]
 
 
+def time_e2e_sequential(torch, W, steps, flush, stream, ins_h, outs_h):
+    """One step at a time through the public API: copy the inputs in from
+    pinned host memory, run the layers, read the results back; one untimed
+    step first, then `steps` steps, each in its own events (L2 flushed before
+    each, outside the events).  Per-step ms."""
+    ins_d = [torch.empty_like(x, device="cuda") for x in ins_h]
+
+    def one():
+        for xd, xh in zip(ins_d, ins_h):
+            xd.copy_(xh, non_blocking=True)
+        W.step(ins=ins_d)
+        for oh, od in zip(outs_h[0], W.outputs):
+            oh.copy_(od, non_blocking=True)
+
+    one()
+    ms = time_cold(torch, one, steps, flush, stream)
+    del ins_d
+    return ms
+
+
+def time_e2e_pipelined(torch, W, steps, warmup, stream, ins_h, outs_h, runs=3):
+    """Steps as a serving loop runs them: three streams (copy in, compute,
+    copy out) and two buffers of each kind, so that step k+1's input copy and
+    step k-1's read-back overlap step k's kernels.  Every step still copies
+    its own inputs from pinned host memory and reads its own results back
+    into pinned host memory inside the timed region; a step's results are
+    first copied on the device into a staging buffer of their own, so the
+    next step's kernels can overwrite the outputs while the read-back runs.
+    `warmup` untimed steps, then `runs` timed runs of `steps` steps each (the
+    host link is shared with the rest of the machine, so a single run can
+    catch a stall); returns each run's ms per step."""
+    ins_d = [[torch.empty_like(x, device="cuda") for x in ins_h] for _ in range(2)]
+    stage = [[torch.empty_like(o) for o in W.outputs] for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def run(K, timed):
+        ev_in = [torch.cuda.Event() for _ in range(K)]
+        ev_c = [torch.cuda.Event() for _ in range(K)]
+        ev_out = [torch.cuda.Event() for _ in range(K)]
+        t0, t1 = _ev(torch)
+        torch.cuda.synchronize()
+        t0.record(stream)
+        s_in.wait_event(t0)
+        s_out.wait_event(t0)
+        for k in range(K):
+            b = k & 1
+            with torch.cuda.stream(s_in):
+                if k >= 2:  # buffer b is free once step k-2's kernels have read it
+                    s_in.wait_event(ev_c[k - 2])
+                for xd, xh in zip(ins_d[b], ins_h):
+                    xd.copy_(xh, non_blocking=True)
+                ev_in[k].record(s_in)
+            stream.wait_event(ev_in[k])
+            W.step(ins=ins_d[b])
+            if k >= 2:  # staging buffer b is free once step k-2's read-back is done
+                stream.wait_event(ev_out[k - 2])
+            for sd, od in zip(stage[b], W.outputs):
+                sd.copy_(od, non_blocking=True)
+            ev_c[k].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_c[k])
+                for oh, sd in zip(outs_h[b], stage[b]):
+                    oh.copy_(sd, non_blocking=True)
+                ev_out[k].record(s_out)
+        stream.wait_event(ev_out[K - 1])
+        t1.record(stream)
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1) / K if timed else None
+
+    run(max(2, warmup), False)
+    ms = [run(steps, True) for _ in range(runs)]
+    del ins_d, stage
+    return ms
+
+
 def time_warm(torch, fn, steps, stream):
     """fn() K times back to back (the caches keep what the last call left)."""
     fn()
@@ -1086,25 +1166,26 @@ def main():
     e2e = None
     if not args.no_e2e:
         ins_h = [x.cpu().pin_memory() for x in W.inputs]
-        outs_h = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in W.outputs]
-        ins_d = [torch.empty_like(x) for x in W.inputs]
-        e2e_ev = [_ev(torch) for _ in range(max(3, args.steps // 4))]
-        for k, (e0, e1) in enumerate(e2e_ev):
-            flush.fill_(float(k))
-            e0.record(stream)
-            for xd, xh in zip(ins_d, ins_h):
-                xd.copy_(xh, non_blocking=True)
-            W.step(ins=ins_d)
-            for oh, od in zip(outs_h, W.outputs):
-                oh.copy_(od, non_blocking=True)
-            e1.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms = max_over_ranks(torch, float(np.mean([a.elapsed_time(b) for a, b in e2e_ev])), world)
-        e2e = {"value": job_rate(world, units, 1, e2e_ms), "unit": UNIT,
+        outs_h = [[torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in W.outputs]
+                  for _ in range(2)]
+        k_e2e = max(4, args.steps // 2)
+        pipe = time_e2e_pipelined(torch, W, k_e2e, args.warmup, stream, ins_h, outs_h)
+        pipe_ms = max_over_ranks(torch, float(np.median(pipe)), world)
+        seq = time_e2e_sequential(torch, W, max(3, args.steps // 4), flush, stream, ins_h, outs_h)
+        seq_ms = max_over_ranks(torch, float(np.median(seq)), world)
+        e2e = {"value": job_rate(world, units, 1, pipe_ms), "unit": UNIT,
                "h2d_bytes_per_step": sum(x.numel() * x.element_size() for x in ins_h),
-               "d2h_bytes_per_step": sum(o.numel() * o.element_size() for o in outs_h),
-               "ms_per_step": e2e_ms}
-        del ins_h, outs_h, ins_d
+               "d2h_bytes_per_step": sum(o.numel() * o.element_size() for o in outs_h[0]),
+               "ms_per_step": pipe_ms, "steps": k_e2e,
+               "runs_ms_per_step": [round(x, 4) for x in pipe],
+               "schedule": "pipelined: copy-in, compute and read-back streams, two buffers "
+                           "each; every step's copies inside the timed run; median of "
+                           f"{len(pipe)} runs of {k_e2e} steps",
+               "sequential": {"value": job_rate(world, units, 1, seq_ms),
+                              "ms_per_step_median": seq_ms,
+                              "ms_per_step_min": float(np.min(seq)),
+                              "ms_per_step_mean": float(np.mean(seq))}}
+        del ins_h, outs_h
 
     families = {}
     if suite and not args.no_families:
