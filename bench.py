@@ -720,14 +720,16 @@ def time_e2e_pipelined(torch, W, steps, warmup, stream, ins_h, outs_h, runs=3):
     copy out) and two buffers of each kind, so that step k+1's input copy and
     step k-1's read-back overlap step k's kernels.  Every step still copies
     its own inputs from pinned host memory and reads its own results back
-    into pinned host memory inside the timed region; a step's results are
-    first copied on the device into a staging buffer of their own, so the
-    next step's kernels can overwrite the outputs while the read-back runs.
-    `warmup` untimed steps, then `runs` timed runs of `steps` steps each (the
-    host link is shared with the rest of the machine, so a single run can
-    catch a stall); returns each run's ms per step."""
+    into pinned host memory inside the timed region.  The step's output
+    tensors are pointed (Tensor.set_) at one of two device buffers before
+    each step, so the kernels write straight into the buffer whose previous
+    read-back has finished, with no staging copy.  `warmup` untimed steps,
+    then `runs` timed runs of `steps` steps each (the host link is shared
+    with the rest of the machine, so a single run can catch a stall); returns
+    each run's ms per step."""
     ins_d = [[torch.empty_like(x, device="cuda") for x in ins_h] for _ in range(2)]
-    stage = [[torch.empty_like(o) for o in W.outputs] for _ in range(2)]
+    outs_d = [[torch.empty_like(o) for o in W.outputs] for _ in range(2)]
+    keep = [o.detach() for o in W.outputs]  # the outputs' own storage, restored after
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
 
     def run(K, timed):
@@ -742,31 +744,36 @@ def time_e2e_pipelined(torch, W, steps, warmup, stream, ins_h, outs_h, runs=3):
         for k in range(K):
             b = k & 1
             with torch.cuda.stream(s_in):
-                if k >= 2:  # buffer b is free once step k-2's kernels have read it
+                if k >= 2:  # input buffer b is free once step k-2's kernels have read it
                     s_in.wait_event(ev_c[k - 2])
                 for xd, xh in zip(ins_d[b], ins_h):
                     xd.copy_(xh, non_blocking=True)
                 ev_in[k].record(s_in)
             stream.wait_event(ev_in[k])
-            W.step(ins=ins_d[b])
-            if k >= 2:  # staging buffer b is free once step k-2's read-back is done
+            if k >= 2:  # output buffer b is free once step k-2's read-back is done
                 stream.wait_event(ev_out[k - 2])
-            for sd, od in zip(stage[b], W.outputs):
-                sd.copy_(od, non_blocking=True)
+            for o, od in zip(W.outputs, outs_d[b]):
+                o.set_(od)
+            W.step(ins=ins_d[b])
             ev_c[k].record(stream)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(ev_c[k])
-                for oh, sd in zip(outs_h[b], stage[b]):
-                    oh.copy_(sd, non_blocking=True)
+                for oh, od in zip(outs_h[b], outs_d[b]):
+                    oh.copy_(od, non_blocking=True)
                 ev_out[k].record(s_out)
         stream.wait_event(ev_out[K - 1])
         t1.record(stream)
         torch.cuda.synchronize()
         return t0.elapsed_time(t1) / K if timed else None
 
-    run(max(2, warmup), False)
-    ms = [run(steps, True) for _ in range(runs)]
-    del ins_d, stage
+    try:
+        run(max(2, warmup), False)
+        ms = [run(steps, True) for _ in range(runs)]
+    finally:
+        torch.cuda.synchronize()
+        for o, k0 in zip(W.outputs, keep):
+            o.set_(k0)
+    del ins_d, outs_d
     return ms
 
 
@@ -1168,8 +1175,8 @@ def main():
         ins_h = [x.cpu().pin_memory() for x in W.inputs]
         outs_h = [[torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in W.outputs]
                   for _ in range(2)]
-        k_e2e = max(4, args.steps // 2)
-        pipe = time_e2e_pipelined(torch, W, k_e2e, args.warmup, stream, ins_h, outs_h)
+        k_e2e = max(4, args.steps // 4)
+        pipe = time_e2e_pipelined(torch, W, k_e2e, args.warmup, stream, ins_h, outs_h, runs=5)
         pipe_ms = max_over_ranks(torch, float(np.median(pipe)), world)
         seq = time_e2e_sequential(torch, W, max(3, args.steps // 4), flush, stream, ins_h, outs_h)
         seq_ms = max_over_ranks(torch, float(np.median(seq)), world)
